@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the eighth-shell halo exchange on one GB300 (or N replicas).
+
+One step = one coordinate exchange (halo_exchange_x) followed by one force
+reduction (halo_exchange_f) over a resident synthetic system: the whole hot
+path, all pulses, through the C ABI.  Metric: halo atoms (slots) per second of
+coordinate+force exchange; also microseconds per exchange and the HBM roofline
+fraction of the dominant kernel.
+
+  python bench.py [--gpus N --steps K --warmup W --workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
+
+Timing: CUDA events on the launching stream around every step; the L2 is
+flushed between steps (a write of 2x L2 bytes, then a read of another 2x L2
+buffer so the flush's dirty lines are written back before the next step);
+warm-up steps are untimed.  N > 1: one process per GPU (torchrun), each an
+independent replica of the workload (the path has no cross-GPU exchange on one
+box), barrier + synchronize around the timed loop, max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "halo atoms/s & µs per coord+force exchange; HBM GB/s as % of GB300 peak"
+UNIT = "halo atoms/s"
+DEFAULT_WORKLOAD = "water1M_4x4x4"
+LATENCY_WORKLOAD = "water24k_2x4x8"
+# algorithmic bytes per halo slot: x = 4 (index) + 12 (gather) + 12 (store);
+# f = 4 (index) + 12 (halo force) + 12 (owner read) + 12 (owner write)
+BYTES_X, BYTES_F = 28, 40
+HBM_FALLBACK_GBS = 6800.0
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "domain_decomposition_halo_build_gb300", "csrc",
+                           "halo_exchange.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    with open(path) as f:
+        for line in f:
+            v = line.split()
+            if len(v) >= 4 and not line.startswith("#") and v[0] == kernel and v[1] == workload \
+                    and v[2] == digest:
+                return int(float(v[3]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.p = None
+        self.path = os.path.join("/tmp", "halo_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                v = [x.strip() for x in line.split(",")]
+                if len(v) >= 9:
+                    rows.append(v)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def gpu_index(local_rank):
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in cvd.split(",") if p.strip()]
+    if parts and all(p.strip().isdigit() for p in parts) and local_rank < len(parts):
+        return int(parts[local_rank])
+    return local_rank
+
+
+def setup_workload(name, device):
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo, synth
+    w = synth.WORKLOADS[name]
+    xyz, dom = synth.system(w)
+    x = torch.from_numpy(xyz).to(device)
+    d = torch.from_numpy(dom).to(device)
+    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d)
+    loc = plan.load_home(x)
+    f0 = torch.from_numpy(synth.forces(plan.n_local_total, seed=1)).to(device)
+    return w, xyz, dom, x, plan, loc, f0
+
+
+def time_steps(plan, loc, f, steps, warmup, flush, stream, sampler=None, barrier=None):
+    """Per-step CUDA-event timing of x and f; returns lists of (x_ms, f_ms)."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        plan.exchange_x(loc, stream)
+        plan.exchange_f(f, stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    lx0, lf0 = plan.launch_counts()
+    t0 = time.perf_counter()
+    for a, b, c in ev:
+        flush()
+        a.record(stream)
+        plan.exchange_x(loc, stream)
+        b.record(stream)
+        plan.exchange_f(f, stream)
+        c.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if barrier:
+        barrier()
+    clocks = sampler.stop() if sampler else None
+    lx1, lf1 = plan.launch_counts()
+    xs = [a.elapsed_time(b) for a, b, c in ev]
+    fs = [b.elapsed_time(c) for a, b, c in ev]
+    return xs, fs, wall, clocks, (lx1 - lx0) + (lf1 - lf0)
+
+
+def make_flush(device):
+    import torch
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    n = max(2 * l2, 64 << 20) // 4
+    wbuf = torch.empty(n, dtype=torch.float32, device=device)
+    rbuf = torch.ones(n, dtype=torch.float32, device=device)
+    sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush():
+        wbuf.zero_()
+        torch.amax(rbuf, dim=0, out=sink)
+    return flush, 2 * n * 4
+
+
+def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
+    """Public API with host buffers: H2D of the step's positions and forces
+    (pinned), load_home, exchange_x, exchange_f, D2H of the forces."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import synth
+    h_xyz = torch.from_numpy(xyz).pin_memory()
+    h_f = torch.from_numpy(synth.forces(plan.n_local_total, seed=2)).pin_memory()
+    h_out = torch.empty_like(h_f).pin_memory()
+    d_xyz = torch.empty_like(h_xyz, device=device)
+    d_f = torch.empty_like(h_f, device=device)
+    loc = torch.empty((plan.n_local_total, 3), dtype=torch.float32, device=device)
+
+    def step():
+        with torch.cuda.stream(stream):
+            d_xyz.copy_(h_xyz, non_blocking=True)
+            plan.load_home(d_xyz, loc, stream)
+            plan.exchange_x(loc, stream)
+            d_f.copy_(h_f, non_blocking=True)
+            plan.exchange_f(d_f, stream)
+            h_out.copy_(d_f, non_blocking=True)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = h_xyz.numel() * 4 + h_f.numel() * 4
+    d2h = h_out.numel() * 4
+    return ms, h2d, d2h
+
+
+def cpu_baseline(name, budget_s=10.0):
+    """The CPU oracle as it stands, single-threaded, on a bounded sample."""
+    import oracle
+    from domain_decomposition_halo_build_gb300 import synth
+    w = synth.WORKLOADS[name]
+    xyz, dom = synth.system(w)
+    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+    loc = o.load_home(xyz)
+    f = synth.forces(o.n_local_total, seed=1)
+    halo_slots = o.n_local_total - o.n_atoms
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        o.exchange_x(loc)
+        o.exchange_f(f)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": halo_slots * n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d full coord+force exchanges of %s (%d halo slots each), %.1f s, "
+                      "single-threaded C oracle" % (n, name, halo_slots, el),
+            "us_per_exchange": 1e6 * el / n}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from domain_decomposition_halo_build_gb300 import synth
+    oracle.build_oracle()
+    w = synth.WORKLOADS[args.workload]
+    xyz, dom = synth.system(w)
+    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+    loc = o.load_home(xyz)
+    f = synth.forces(o.n_local_total, seed=1)
+    halo_slots = o.n_local_total - o.n_atoms
+    for _ in range(args.warmup):
+        o.exchange_x(loc)
+        o.exchange_f(f)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.exchange_x(loc)
+        o.exchange_f(f)
+    el = time.perf_counter() - t0
+    value = halo_slots * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "n_atoms": w.n_atoms, "grid": list(w.grid),
+                   "rc_nm": w.rc, "halo_slots": halo_slots},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d full coord+force exchanges (single-threaded C oracle)"
+                                   % args.steps},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if args.steps == 2000 and "--steps" not in sys.argv:
+            args.steps = 200
+        return run_reference(args)
+
+    import torch
+    import __graft_entry__
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+        __graft_entry__.build()
+    stream = torch.cuda.current_stream(device)
+    barrier = (lambda: dist.barrier()) if dist else None
+
+    w, xyz, dom, x, plan, loc, f0 = setup_workload(args.workload, device)
+    flush, flush_bytes = make_flush(device)
+    f = f0.clone()
+    sampler = ClockSampler(gpu_index(local))
+    xs, fs, wall, clocks, launches = time_steps(plan, loc, f, args.steps, args.warmup, flush,
+                                                stream, sampler, barrier)
+    code = plan.status()
+    if code != 0:
+        raise SystemExit("device error %d during the timed region" % code)
+    step_ms = statistics.fmean(a + b for a, b in zip(xs, fs))
+    x_ms, f_ms = statistics.fmean(xs), statistics.fmean(fs)
+    if dist:
+        t = torch.tensor([step_ms, x_ms, f_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, x_ms, f_ms = [float(v) for v in t.tolist()]
+    halo_slots = plan.n_halo_total
+    value = world * halo_slots / (step_ms * 1e-3)
+    peak, peak_kind = measured_peak()
+    dom_kernel, dom_ms, per_slot = (("unpack_f_kernel", f_ms, BYTES_F) if f_ms >= x_ms
+                                    else ("pack_x_kernel", x_ms, BYTES_X))
+    achieved = per_slot * halo_slots / (dom_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(dom_kernel, args.workload)
+    alg_gbs = (BYTES_X + BYTES_F) * halo_slots / (step_ms * 1e-3) / 1e9
+
+    # latency case: the multi-pulse system, one launch per direction
+    lw, lxyz, ldom, lx, lplan, lloc, lf0 = setup_workload(LATENCY_WORKLOAD, device)
+    lf = lf0.clone()
+    lxs, lfs, _, _, llaunch = time_steps(lplan, lloc, lf, min(args.steps, 1000), args.warmup,
+                                         flush, stream)
+    assert lplan.status() == 0
+    lat_us = 1e3 * statistics.fmean(a + b for a, b in zip(lxs, lfs))
+    lat = {"workload": LATENCY_WORKLOAD, "us_per_exchange": lat_us,
+           "us_x": 1e3 * statistics.fmean(lxs), "us_f": 1e3 * statistics.fmean(lfs),
+           "launches_per_direction": llaunch / (2 * min(args.steps, 1000)),
+           "halo_slots": lplan.n_halo_total, "pulses": lplan.n_pulses}
+    lplan.close()
+
+    # end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = e2e_steps(w, xyz, plan, max(20, min(args.steps, 200)), 5, device, stream)
+    assert plan.status() == 0
+    e2e_value = world * halo_slots / (e2e_ms * 1e-3)
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_value = world * halo_slots / (float(t.item()) * 1e-3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "n_atoms": w.n_atoms, "grid": list(w.grid),
+                       "box_nm": list(w.box), "rc_nm": w.rc, "pulses": plan.n_pulses,
+                       "halo_slots": halo_slots, "parallelism": "replicas" if world > 1 else "1 GPU",
+                       "l2": "flushed between steps (%d MB written+read)" % (flush_bytes >> 20)},
+            "us_per_exchange": 1e3 * step_ms, "us_x": 1e3 * x_ms, "us_f": 1e3 * f_ms,
+            "algorithmic_gbs": alg_gbs, "hbm_frac": alg_gbs / peak,
+            "hbm_frac_nominal_8tbs": alg_gbs / 8000.0,
+            "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": per_slot * halo_slots},
+            "latency_case": lat,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line))
+    plan.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,642 @@
+// halo_build.cu -- device-side construction of the per-pulse index maps.
+//
+// Page "Redesigning GROMACS Halo Exchange: Improving Strong Scaling with
+// GPU-initiated NVSHMEM" (review), section 3 and Algorithm 1: every domain owns
+// its home atoms; for each pulse, the atoms of a sender domain that lie within
+// the cut-off of its lower face are listed in an index map (PulseData.indexMap,
+// sendSize), which the receiver appends to its halo at atomOffset, shifted by
+// coordShift across the periodic boundary.  Forwarding (eighth shell): pulse 0
+// of a dim selects among home atoms plus all halo received in earlier dims,
+// pulse k >= 1 only among the slots received in pulse k-1 of the same dim.
+// Algorithm 4: depOffset splits each map into entries that are home atoms
+// (independent) and entries that arrived in earlier pulses (dependent).
+//
+// Device pipeline (one stream, one host synchronisation at the end):
+//   1. home partition: per-warp-tile histogram of domain ids, exclusive scan,
+//      stable scatter (warp match + running per-domain counters) -> every
+//      domain's home atoms in input order, in a home-compact region;
+//   2. per pulse: count kernel (predicate per candidate), scan kernel (block
+//      offsets, sizes, receiver offsets), write kernel (stable block-wide
+//      ballot compaction -> ascending index map + the new halo coordinates);
+//   3. finalize: dense bases, home slot -> dense slot map; one D2H copy of the
+//      metadata.
+// Index maps hold domain-relative local indices, so the dense relayout touches
+// none of them.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "halo_internal.cuh"
+
+namespace halo {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---- packed metadata (int64 entries) -----------------------------------------
+struct Meta {
+    int64_t* flags;     // [0] capacity overflow, [1] bad domain id
+    int64_t* n_home;    // n_dom
+    int64_t* hstart;    // n_dom: first home-compact slot of each domain
+    int64_t* base;      // n_dom: first dense slot of each domain
+    int64_t* own_off;   // n_dom*(P+1): first local index of each received slice; [P] = n_local
+    int64_t* recv_pos;  // n_dom*P: build-buffer slot of each received slice
+    int64_t* send;      // n_dom*P
+    int64_t* split;     // n_dom*P
+    int64_t* map_pos;   // n_dom*P: build-buffer slot of the sender's output
+    int64_t* region;    // P+1: first build-buffer slot of each pulse's output region
+};
+
+size_t meta_count(int nd, int P) {
+    return 4 + 3 * (size_t)nd + (size_t)nd * (P + 1) + 4 * (size_t)nd * P + (P + 1);
+}
+
+Meta meta_ptrs(void* m, int nd, int P) {
+    int64_t* q = (int64_t*)m;
+    Meta r;
+    r.flags = q;
+    q += 4;
+    r.n_home = q;
+    q += nd;
+    r.hstart = q;
+    q += nd;
+    r.base = q;
+    q += nd;
+    r.own_off = q;
+    q += (size_t)nd * (P + 1);
+    r.recv_pos = q;
+    q += (size_t)nd * P;
+    r.send = q;
+    q += (size_t)nd * P;
+    r.split = q;
+    q += (size_t)nd * P;
+    r.map_pos = q;
+    q += (size_t)nd * P;
+    r.region = q;
+    return r;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ int cell_of(int D, int d, int nx, int ny) {
+    return d == 0 ? D % nx : (d == 1 ? (D / nx) % ny : D / (nx * ny));
+}
+
+// Exclusive scan across a block of NT threads (NT a multiple of 32, <= 1024).
+template <int NT>
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
+    __shared__ int64_t ws[NT / 32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int64_t t = lane < NT / 32 ? ws[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(kFull, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < NT / 32) ws[lane] = t;
+    }
+    __syncthreads();
+    int64_t pre = (w > 0 ? ws[w - 1] : 0) + x - v;
+    *total = ws[NT / 32 - 1];
+    __syncthreads();
+    return pre;
+}
+
+// ---- 1. home partition ------------------------------------------------------------
+// Warp tile t covers atoms [t*kHistTile, (t+1)*kHistTile).  counts is domain-major:
+// counts[D*ntiles + t], so one exclusive scan gives every (domain, tile) start.
+__global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int nd,
+                                 int64_t ntiles, int32_t* __restrict__ counts,
+                                 int64_t* __restrict__ flags) {
+    extern __shared__ int32_t sh[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wpb = blockDim.x >> 5;
+    int32_t* h = sh + (size_t)warp * nd;
+    for (int i = lane; i < nd; i += 32) h[i] = 0;
+    __syncwarp();
+    const int64_t tile = (int64_t)blockIdx.x * wpb + warp;
+    if (tile >= ntiles) return;
+    const int64_t a0 = tile * kHistTile;
+    bool bad = false;
+    for (int it = 0; it < kHistTile / 32; it++) {
+        const int64_t a = a0 + it * 32 + lane;
+        int d = -1;
+        if (a < n) {
+            d = __ldg(dom + a);
+            if (d < 0 || d >= nd) {
+                bad = true;
+                d = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(kFull, d);
+        if (d >= 0 && lane == __ffs(peers) - 1) h[d] += __popc(peers);
+        __syncwarp();
+    }
+    if (bad) flags[1] = 1;
+    for (int i = lane; i < nd; i += 32) counts[(int64_t)i * ntiles + tile] = h[i];
+}
+
+// Stable scatter: atoms of each tile are visited in input order; within 32
+// atoms the rank among equal domain ids comes from the warp match mask.
+__global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t* __restrict__ dom,
+                                    int64_t n, int nd, int64_t ntiles,
+                                    const int32_t* __restrict__ offs,
+                                    int32_t* __restrict__ home_gid, float* __restrict__ bxyz) {
+    extern __shared__ int32_t sh[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wpb = blockDim.x >> 5;
+    int32_t* run = sh + (size_t)warp * nd;
+    const int64_t tile = (int64_t)blockIdx.x * wpb + warp;
+    if (tile >= ntiles) return;
+    for (int i = lane; i < nd; i += 32) run[i] = offs[(int64_t)i * ntiles + tile];
+    __syncwarp();
+    const int64_t a0 = tile * kHistTile;
+    const unsigned lt = lanemask_lt();
+    for (int it = 0; it < kHistTile / 32; it++) {
+        const int64_t a = a0 + it * 32 + lane;
+        int d = -1;
+        if (a < n) {
+            d = __ldg(dom + a);
+            if (d < 0 || d >= nd) d = -1;
+        }
+        const unsigned peers = __match_any_sync(kFull, d);
+        if (d >= 0) {
+            const int64_t pos = (int64_t)run[d] + __popc(peers & lt);
+            home_gid[pos] = (int32_t)a;
+            bxyz[3 * pos + 0] = __ldg(xyz + 3 * a + 0);
+            bxyz[3 * pos + 1] = __ldg(xyz + 3 * a + 1);
+            bxyz[3 * pos + 2] = __ldg(xyz + 3 * a + 2);
+        }
+        __syncwarp();
+        if (d >= 0 && lane == __ffs(peers) - 1) run[d] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// ---- generic int32 exclusive scan (three launches) ---------------------------------
+__global__ void scan_reduce_kernel(const int32_t* __restrict__ in, int64_t n,
+                                   int32_t* __restrict__ sums) {
+    const int64_t b0 = (int64_t)blockIdx.x * kScanTile;
+    int64_t s = 0;
+    for (int j = threadIdx.x; j < kScanTile; j += kThreads) {
+        const int64_t i = b0 + j;
+        if (i < n) s += in[i];
+    }
+    int64_t tot;
+    block_exclusive_scan<kThreads>(s, &tot);
+    if (threadIdx.x == 0) sums[blockIdx.x] = (int32_t)tot;
+}
+
+__global__ void scan_top_kernel(int32_t* __restrict__ sums, int64_t nb) {
+    int64_t carry = 0;
+    for (int64_t b = 0; b < nb; b += 1024) {
+        const int64_t i = b + threadIdx.x;
+        const int64_t v = i < nb ? sums[i] : 0;
+        int64_t tot;
+        const int64_t pre = block_exclusive_scan<1024>(v, &tot);
+        if (i < nb) sums[i] = (int32_t)(carry + pre);
+        carry += tot;
+    }
+}
+
+__global__ void scan_down_kernel(const int32_t* __restrict__ in, int32_t* __restrict__ out,
+                                 int64_t n, const int32_t* __restrict__ sums) {
+    constexpr int E = kScanTile / kThreads;
+    const int64_t b0 = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * E;
+    int32_t v[E];
+    int64_t s = 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        v[e] = (b0 + e < n) ? in[b0 + e] : 0;
+        s += v[e];
+    }
+    int64_t tot;
+    int64_t pre = block_exclusive_scan<kThreads>(s, &tot) + sums[blockIdx.x];
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        if (b0 + e < n) out[b0 + e] = (int32_t)pre;
+        pre += v[e];
+    }
+}
+
+int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
+                          cudaStream_t st) {
+    const int64_t nb = (n + kScanTile - 1) / kScanTile;
+    if (nb == 0) return HALO_OK;
+    scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, n, tmp);
+    scan_top_kernel<<<1, 1024, 0, st>>>(tmp, nb);
+    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp);
+    return cuda_code(cudaGetLastError());
+}
+
+// Per-domain home counts and starts from the scanned tile offsets; pulse state init.
+__global__ void home_meta_kernel(const int32_t* __restrict__ offs, int64_t ntiles, int64_t n,
+                                 int nd, int P, Meta m) {
+    for (int D = blockIdx.x * blockDim.x + threadIdx.x; D < nd; D += gridDim.x * blockDim.x) {
+        const int64_t h0 = offs[(int64_t)D * ntiles];
+        const int64_t h1 = (D + 1 < nd) ? offs[(int64_t)(D + 1) * ntiles] : n;
+        m.hstart[D] = h0;
+        m.n_home[D] = h1 - h0;
+        m.own_off[(int64_t)D * (P + 1)] = h1 - h0;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        m.region[0] = n;
+        m.flags[0] = 0;
+    }
+}
+
+// ---- 2. one pulse ---------------------------------------------------------------
+struct PulseArgs {
+    float* bxyz;
+    int32_t* maps;  // maps[slot - N]
+    int64_t N;
+    int64_t cap;    // slots of bxyz
+    Meta m;
+    int32_t* cnt;
+    int32_t* cnt_home;
+    int32_t* blk_off;
+    const float* thr;  // thresholds of this pulse, by sender cell along d
+    int nd, P, p, d, k, B;
+    int nx, ny, nz;
+    float Ld;
+};
+
+struct Locator {
+    int64_t oo[HALO_MAX_PULSES + 1];
+    int64_t rp[HALO_MAX_PULSES];
+    int64_t hstart;
+};
+
+// Build-buffer slot of local index i of the block's sender (i < oo[p]).
+__device__ __forceinline__ int64_t locate(const Locator& L, int p, int64_t i) {
+    if (i < L.oo[0]) return L.hstart + i;
+    int q = p - 1;
+    while (q > 0 && i < L.oo[q]) q--;
+    return L.rp[q] + (i - L.oo[q]);
+}
+
+__device__ __forceinline__ void load_locator(Locator& L, const PulseArgs& a, int s) {
+    const int64_t* oo = a.m.own_off + (int64_t)s * (a.P + 1);
+    const int64_t* rp = a.m.recv_pos + (int64_t)s * a.P;
+    for (int q = threadIdx.x; q <= a.p; q += blockDim.x) L.oo[q] = oo[q];
+    for (int q = threadIdx.x; q < a.p; q += blockDim.x) L.rp[q] = rp[q];
+    if (threadIdx.x == 0) L.hstart = a.m.hstart[s];
+    __syncthreads();
+}
+
+__device__ __forceinline__ void sub_range(const Locator& L, const PulseArgs& a, int b,
+                                          int64_t* lo, int64_t* hi) {
+    const int64_t c0 = (a.k == 0) ? 0 : L.oo[a.p - 1];
+    const int64_t c1 = L.oo[a.p];
+    const int64_t len = c1 - c0;
+    *lo = c0 + len * b / a.B;
+    *hi = c0 + len * (b + 1) / a.B;
+}
+
+__global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
+    __shared__ Locator L;
+    const int s = blockIdx.y, b = blockIdx.x;
+    load_locator(L, a, s);
+    const int cs = cell_of(s, a.d, a.nx, a.ny);
+    const float thr = a.thr[cs];
+    int64_t lo, hi;
+    sub_range(L, a, b, &lo, &hi);
+    const int64_t nh = L.oo[0];
+    int64_t c = 0, ch = 0;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
+        const int64_t pos = locate(L, a.p, i);
+        if (pos >= 0 && pos < a.cap && a.bxyz[3 * pos + a.d] < thr) {
+            c++;
+            if (i < nh) ch++;
+        }
+    }
+    int64_t tc, th;
+    block_exclusive_scan<kThreads>(c, &tc);
+    block_exclusive_scan<kThreads>(ch, &th);
+    if (threadIdx.x == 0) {
+        a.cnt[(int64_t)s * a.B + b] = (int32_t)tc;
+        a.cnt_home[(int64_t)s * a.B + b] = (int32_t)th;
+    }
+}
+
+__global__ void __launch_bounds__(1024) pulse_scan_kernel(PulseArgs a) {
+    const int64_t M = (int64_t)a.nd * a.B;
+    int64_t carry = 0;
+    for (int64_t b0 = 0; b0 < M; b0 += 1024) {
+        const int64_t i = b0 + threadIdx.x;
+        const int64_t v = i < M ? a.cnt[i] : 0;
+        int64_t tot;
+        const int64_t pre = block_exclusive_scan<1024>(v, &tot);
+        if (i < M) a.blk_off[i] = (int32_t)(carry + pre);
+        carry += tot;
+    }
+    __syncthreads();
+    const int64_t R = a.m.region[a.p];
+    for (int s = threadIdx.x; s < a.nd; s += blockDim.x) {
+        int64_t snd = 0, spl = 0;
+        for (int b = 0; b < a.B; b++) {
+            snd += a.cnt[(int64_t)s * a.B + b];
+            spl += a.cnt_home[(int64_t)s * a.B + b];
+        }
+        const int64_t G = a.blk_off[(int64_t)s * a.B];
+        const int64_t sp = (int64_t)s * a.P + a.p;
+        a.m.send[sp] = snd;
+        a.m.split[sp] = spl;
+        a.m.map_pos[sp] = R + G;
+        int c[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
+        const int nd_d = a.d == 0 ? a.nx : (a.d == 1 ? a.ny : a.nz);
+        c[a.d] = (c[a.d] - 1 + nd_d) % nd_d;
+        const int r = c[0] + a.nx * (c[1] + a.ny * c[2]);
+        a.m.recv_pos[(int64_t)r * a.P + a.p] = R + G;
+        a.m.own_off[(int64_t)r * (a.P + 1) + a.p + 1] =
+            a.m.own_off[(int64_t)r * (a.P + 1) + a.p] + snd;
+    }
+    if (threadIdx.x == 0) {
+        a.m.region[a.p + 1] = R + carry;
+        if (R + carry > a.cap) a.m.flags[0] = 1;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
+    __shared__ Locator L;
+    __shared__ int wcnt[kThreads / 32];
+    const int s = blockIdx.y, b = blockIdx.x;
+    load_locator(L, a, s);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cs = cell_of(s, a.d, a.nx, a.ny);
+    const float thr = a.thr[cs];
+    float sh[3] = {0.0f, 0.0f, 0.0f};
+    if (cs == 0) sh[a.d] = a.Ld;
+    int64_t lo, hi;
+    sub_range(L, a, b, &lo, &hi);
+    int64_t out = a.m.region[a.p] + a.blk_off[(int64_t)s * a.B + b];
+    const unsigned lt = lanemask_lt();
+    for (int64_t t0 = lo; t0 < hi; t0 += kThreads) {
+        const int64_t i = t0 + threadIdx.x;
+        bool sel = false;
+        float v0 = 0, v1 = 0, v2 = 0;
+        if (i < hi) {
+            const int64_t pos = locate(L, a.p, i);
+            if (pos >= 0 && pos < a.cap) {
+                v0 = a.bxyz[3 * pos + 0];
+                v1 = a.bxyz[3 * pos + 1];
+                v2 = a.bxyz[3 * pos + 2];
+                const float vd = a.d == 0 ? v0 : (a.d == 1 ? v1 : v2);
+                sel = vd < thr;
+            }
+        }
+        const unsigned bal = __ballot_sync(kFull, sel);
+        if (lane == 0) wcnt[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; w++) {
+            const int c = wcnt[w];
+            before += (w < warp) ? c : 0;
+            total += c;
+        }
+        if (sel) {
+            const int64_t o = out + before + __popc(bal & lt);
+            if (o >= a.N && o < a.cap) {
+                a.maps[o - a.N] = (int32_t)i;
+                a.bxyz[3 * o + 0] = v0 + sh[0];
+                a.bxyz[3 * o + 1] = v1 + sh[1];
+                a.bxyz[3 * o + 2] = v2 + sh[2];
+            }
+        }
+        out += total;
+        __syncthreads();
+    }
+}
+
+// ---- 3. finalize -----------------------------------------------------------------
+__global__ void __launch_bounds__(1024) finalize_kernel(Meta m, int nd, int P) {
+    int64_t carry = 0;
+    for (int D0 = 0; D0 < nd; D0 += 1024) {
+        const int D = D0 + threadIdx.x;
+        const int64_t v = D < nd ? m.own_off[(int64_t)D * (P + 1) + P] : 0;
+        int64_t tot;
+        const int64_t pre = block_exclusive_scan<1024>(v, &tot);
+        if (D < nd) m.base[D] = carry + pre;
+        carry += tot;
+    }
+}
+
+__global__ void home_dst_kernel(Meta m, int64_t* __restrict__ home_dst) {
+    const int D = blockIdx.x;
+    const int64_t h0 = m.hstart[D], nh = m.n_home[D], b = m.base[D];
+    for (int64_t j = threadIdx.x; j < nh; j += blockDim.x) home_dst[h0 + j] = b + j;
+}
+
+int grow(float** p, int64_t* cap_have, int64_t need_slots) {
+    if (*p && *cap_have >= need_slots) return HALO_OK;
+    dev_free(*p);
+    *cap_have = 0;
+    HALO_TRY(dev_alloc(p, (size_t)need_slots * 3));
+    *cap_have = need_slots;
+    return HALO_OK;
+}
+
+}  // namespace
+
+void free_build(halo_plan* pl) {
+    dev_free(pl->d_bxyz);
+    dev_free(pl->d_maps);
+    dev_free(pl->d_home_gid);
+    dev_free(pl->d_home_dst);
+    dev_free(pl->d_counts);
+    dev_free(pl->d_scan_tmp);
+    dev_free(pl->d_meta);
+    dev_free(pl->d_pulse_scratch);
+    dev_free(pl->d_thr);
+    pl->cap_slots = 0;
+    pl->n_alloc_atoms = 0;
+    pl->counts_cap = 0;
+    pl->scan_tmp_cap = 0;
+    pl->meta_bytes = 0;
+}
+
+int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n,
+               cudaStream_t st) {
+    const int nd = pl->n_dom, P = pl->P;
+    const int64_t ntiles = (n + kHistTile - 1) / kHistTile;
+
+    // --- buffers that depend on N
+    if (n > pl->n_alloc_atoms) {
+        dev_free(pl->d_home_gid);
+        dev_free(pl->d_home_dst);
+        pl->n_alloc_atoms = 0;
+        HALO_TRY(dev_alloc(&pl->d_home_gid, (size_t)n));
+        HALO_TRY(dev_alloc(&pl->d_home_dst, (size_t)n));
+        pl->n_alloc_atoms = n;
+    }
+    const int64_t ncount = (int64_t)nd * ntiles;
+    if (ncount > pl->counts_cap) {
+        dev_free(pl->d_counts);
+        pl->counts_cap = 0;
+        HALO_TRY(dev_alloc(&pl->d_counts, (size_t)ncount * 2));  // counts + scanned offsets
+        pl->counts_cap = ncount;
+    }
+    const int64_t nsum = std::max<int64_t>((ncount + kScanTile - 1) / kScanTile, 1);
+    if (nsum > pl->scan_tmp_cap) {
+        dev_free(pl->d_scan_tmp);
+        pl->scan_tmp_cap = 0;
+        HALO_TRY(dev_alloc(&pl->d_scan_tmp, (size_t)nsum));
+        pl->scan_tmp_cap = nsum;
+    }
+    const size_t mbytes = meta_count(nd, P) * sizeof(int64_t);
+    if (mbytes > pl->meta_bytes) {
+        dev_free(pl->d_meta);
+        pl->meta_bytes = 0;
+        HALO_TRY(dev_alloc((char**)&pl->d_meta, mbytes));
+        pl->meta_bytes = mbytes;
+    }
+    // blocks per sender domain in the pulse kernels: enough blocks to fill the
+    // GPU, but at least ~256 candidates per block
+    {
+        const int64_t per_dom = n / nd + 1;
+        int64_t B = std::max<int64_t>(1, (int64_t)8 * pl->num_sms / nd);
+        B = std::min<int64_t>(B, std::max<int64_t>(1, per_dom / 256));
+        B = std::min<int64_t>(B, 64);
+        if (B != pl->build_blocks_per_domain || !pl->d_pulse_scratch) {
+            dev_free(pl->d_pulse_scratch);
+            HALO_TRY(dev_alloc(&pl->d_pulse_scratch, (size_t)3 * nd * B));
+            pl->build_blocks_per_domain = (int)B;
+        }
+    }
+    const int B = pl->build_blocks_per_domain;
+    // thresholds: fl32(c * L_d / n_d + rc), evaluated in double, per pulse and sender cell
+    if (!pl->d_thr && P > 0) {
+        const int nmax = std::max(pl->grid[0], std::max(pl->grid[1], pl->grid[2]));
+        std::vector<float> thr((size_t)P * nmax, 0.0f);
+        for (int p = 0; p < P; p++) {
+            const int d = pl->pulse_dim[p];
+            for (int c = 0; c < pl->grid[d]; c++)
+                thr[(size_t)p * nmax + c] =
+                    (float)((double)c * (double)pl->box[d] / (double)pl->grid[d] + (double)pl->rc);
+        }
+        HALO_TRY(dev_alloc(&pl->d_thr, thr.size()));
+        HALO_CUDA(cudaMemcpy(pl->d_thr, thr.data(), thr.size() * sizeof(float),
+                             cudaMemcpyHostToDevice));
+    }
+    const int nmax = std::max(pl->grid[0], std::max(pl->grid[1], pl->grid[2]));
+
+    // capacity estimate: each decomposed dim widens a domain by rc
+    double grow_f = 1.0;
+    for (int d = 0; d < 3; d++)
+        if (pl->grid[d] > 1) grow_f *= 1.0 + (double)pl->rc / ((double)pl->box[d] / pl->grid[d]);
+    int64_t want = n + (int64_t)ceil((double)n * (grow_f - 1.0) * 1.15) + (int64_t)256 * nd * P + 1024;
+    want = std::max(want, pl->cap_slots);
+
+    const Meta m = meta_ptrs(pl->d_meta, nd, P);
+    std::vector<int64_t> hm(meta_count(nd, P));
+    const Meta h = meta_ptrs(hm.data(), nd, P);
+
+    int wpb = (int)std::min<int64_t>(8, std::max<int64_t>(1, (48 * 1024) / ((int64_t)nd * 4)));
+    const size_t hist_smem = (size_t)wpb * nd * sizeof(int32_t);
+    const unsigned hist_blocks = (unsigned)((ntiles + wpb - 1) / wpb);
+
+    for (int attempt = 0; attempt < 6; attempt++) {
+        if (want > pl->cap_slots) {
+            int64_t have = pl->cap_slots;
+            HALO_TRY(grow(&pl->d_bxyz, &have, want));
+            // maps[slot - N] for slots in [N, cap): sized by cap so that any N fits
+            dev_free(pl->d_maps);
+            HALO_TRY(dev_alloc(&pl->d_maps, (size_t)want));
+            pl->cap_slots = want;
+        } else if (!pl->d_maps) {
+            HALO_TRY(dev_alloc(&pl->d_maps, (size_t)pl->cap_slots));
+        }
+        HALO_CUDA(cudaMemsetAsync(pl->d_meta, 0, mbytes, st));
+        // 1. home partition
+        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(dom, n, nd, ntiles,
+                                                                  pl->d_counts, m.flags);
+        int32_t* offs = pl->d_counts + ncount;
+        HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
+        home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
+            coords, dom, n, nd, ntiles, offs, pl->d_home_gid, pl->d_bxyz);
+        home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, ntiles, n, nd, P, m);
+        HALO_CUDA(cudaGetLastError());
+        // 2. pulses in global order
+        for (int p = 0; p < P; p++) {
+            PulseArgs a;
+            a.bxyz = pl->d_bxyz;
+            a.maps = pl->d_maps;
+            a.N = n;
+            a.cap = pl->cap_slots;
+            a.m = m;
+            a.cnt = pl->d_pulse_scratch;
+            a.cnt_home = pl->d_pulse_scratch + (size_t)nd * B;
+            a.blk_off = pl->d_pulse_scratch + (size_t)2 * nd * B;
+            a.thr = pl->d_thr + (size_t)p * nmax;
+            a.nd = nd;
+            a.P = P;
+            a.p = p;
+            a.d = pl->pulse_dim[p];
+            a.k = pl->pulse_k[p];
+            a.B = B;
+            a.nx = pl->grid[0];
+            a.ny = pl->grid[1];
+            a.nz = pl->grid[2];
+            a.Ld = pl->box[a.d];
+            dim3 g((unsigned)B, (unsigned)nd);
+            pulse_count_kernel<<<g, kThreads, 0, st>>>(a);
+            pulse_scan_kernel<<<1, 1024, 0, st>>>(a);
+            pulse_write_kernel<<<g, kThreads, 0, st>>>(a);
+        }
+        // 3. dense layout
+        finalize_kernel<<<1, 1024, 0, st>>>(m, nd, P);
+        home_dst_kernel<<<nd, 256, 0, st>>>(m, pl->d_home_dst);
+        HALO_CUDA(cudaGetLastError());
+        HALO_CUDA(cudaMemcpyAsync(hm.data(), pl->d_meta, mbytes, cudaMemcpyDeviceToHost, st));
+        HALO_CUDA(cudaStreamSynchronize(st));
+        if (h.flags[1]) return HALO_EDOMAIN;
+        if (!h.flags[0]) break;
+        if (attempt == 5) return HALO_ECAPACITY;
+        want = std::max<int64_t>(2 * pl->cap_slots, h.region[P] + h.region[P] / 4);
+    }
+
+    // host copy of the plan
+    pl->n_atoms = n;
+    pl->n_home.assign(nd, 0);
+    pl->n_local.assign(nd, 0);
+    pl->base.assign(nd, 0);
+    pl->own_off.assign((size_t)nd * (P + 1), 0);
+    pl->send.assign((size_t)nd * P, 0);
+    pl->split.assign((size_t)nd * P, 0);
+    pl->map_off.assign((size_t)nd * P, 0);
+    int64_t tot = 0;
+    for (int D = 0; D < nd; D++) {
+        pl->n_home[D] = (int32_t)h.n_home[D];
+        pl->n_local[D] = (int32_t)h.own_off[(size_t)D * (P + 1) + P];
+        pl->base[D] = h.base[D];
+        for (int q = 0; q <= P; q++)
+            pl->own_off[(size_t)D * (P + 1) + q] = (int32_t)h.own_off[(size_t)D * (P + 1) + q];
+        tot += pl->n_local[D];
+    }
+    for (size_t i = 0; i < (size_t)nd * P; i++) {
+        pl->send[i] = (int32_t)h.send[i];
+        pl->split[i] = (int32_t)h.split[i];
+        pl->map_off[i] = h.map_pos[i] - n;
+    }
+    pl->n_local_total = tot;
+    pl->n_halo_total = tot - n;
+    if (P > 0 && h.region[P] - n != pl->n_halo_total) return HALO_ECAPACITY;
+    return HALO_OK;
+}
+
+}  // namespace halo

@@ -1,0 +1,161 @@
+// halo_internal.cuh -- plan structure, device-side helpers and the internal
+// entry points shared by the translation units of libhalo.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "halo.h"
+
+namespace halo {
+
+constexpr int kThreads = 256;          // threads per block of every kernel here
+constexpr int kHistTile = 1024;        // atoms per warp tile of the home partition
+constexpr int kScanTile = 2048;        // elements per block of the device scan
+
+// Per (sender s, pulse p) description used by both exchange kernels.
+struct SPDesc {
+    int64_t map_off;   // first entry of the index map in the plan's map array
+    int64_t src_base;  // base[s]: first dense slot of the sender
+    int64_t dst;       // base[r] + atomOffset: first dense slot of the halo slice in r
+    int32_t send;      // entries
+    int32_t split;     // entries below depOffset
+    int32_t s, r, p, pad;
+    float shift[3];
+    float pad2;
+};
+
+// One unit of exchange work: a chunk of one (s, p) index map.
+struct WorkItem {
+    int32_t sp;     // s * P + p
+    int32_t start;  // first entry
+    int32_t len;    // entries
+    int32_t pad;
+};
+
+// Where a bounded wait gave up (debug record, read by tests through halo_status).
+struct ErrInfo {
+    int32_t code;
+    int32_t kernel;  // 1 = exchange_x, 2 = exchange_f
+    int32_t sp;
+    int32_t waited_on;
+};
+
+struct DevBuf {
+    void* p = nullptr;
+    size_t bytes = 0;
+};
+
+}  // namespace halo
+
+struct halo_plan {
+    int dev = 0;
+    int num_sms = 0;
+    int grid[3] = {1, 1, 1};
+    float box[3] = {0, 0, 0};
+    float rc = 0;
+    int n_dom = 0;
+    int P = 0;
+    int pulses_per_dim[3] = {0, 0, 0};
+    int pulse_dim[HALO_MAX_PULSES] = {};
+    int pulse_k[HALO_MAX_PULSES] = {};
+    int64_t n_atoms = 0;
+    int64_t n_local_total = 0;
+    int64_t n_halo_total = 0;
+
+    // host copies of the plan (filled after each build)
+    std::vector<int32_t> n_home, n_local, send, split, own_off;  // own_off: n_dom*(P+1)
+    std::vector<int64_t> base, map_off;                           // map_off: n_dom*P
+    std::vector<halo::SPDesc> sp;
+    std::vector<int64_t> x_pulse_item_begin;  // first x item of each pulse (P+1)
+
+    // device memory owned by the plan
+    float* d_bxyz = nullptr;        // build buffer: home-compact region + halo regions
+    int64_t cap_slots = 0;          // capacity of d_bxyz in slots (and of d_maps + N)
+    int32_t* d_maps = nullptr;      // index maps, (pulse, sender) order
+    int32_t* d_home_gid = nullptr;  // global id of each home-compact slot
+    int64_t* d_home_dst = nullptr;  // dense slot of each home-compact slot
+    int64_t n_alloc_atoms = 0;
+    int32_t* d_counts = nullptr;    // home partition tile counts (and scan output)
+    int64_t counts_cap = 0;
+    int32_t* d_scan_tmp = nullptr;
+    int64_t scan_tmp_cap = 0;
+    void* d_meta = nullptr;         // packed per-domain / per-pulse metadata (see build)
+    size_t meta_bytes = 0;
+    int32_t* d_pulse_scratch = nullptr;  // per-pulse block counts (3 * n_dom * B)
+    int build_blocks_per_domain = 1;
+    float* d_thr = nullptr;         // thresholds per pulse and sender cell
+
+    // exchange
+    halo::SPDesc* d_sp = nullptr;
+    halo::WorkItem* d_items_x = nullptr;
+    halo::WorkItem* d_items_f = nullptr;
+    int n_items = 0;
+    int chunk = 256;                // entries per work item
+    int entries_per_thread = 1;
+    uint32_t* d_nch = nullptr;       // chunks of (s, p): n_dom*P
+    uint32_t* d_nch_in = nullptr;    // chunks delivered into (r, p): n_dom*P
+    int32_t* d_own_off = nullptr;    // n_dom*(P+1)
+    uint64_t* d_fmask = nullptr;     // 2*P: force-wait masks on s and on r
+    uint32_t* d_flags = nullptr;     // arrived[n_dom*P] | done[n_dom*P]
+    unsigned long long* d_tickets = nullptr;  // [0] x, [1] f
+    int* d_err = nullptr;            // sticky error word + ErrInfo
+    int grid_x = 0, grid_f = 0;
+    long long wait_timeout_ns = 1000000000LL;
+    int drop_sp = -1;
+    int64_t launches_x = 0, launches_f = 0;
+};
+
+namespace halo {
+
+// halo_build.cu
+int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n_atoms,
+               cudaStream_t st);
+
+// halo_exchange.cu
+int prepare_exchange(halo_plan* pl, cudaStream_t st);
+int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st);
+int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st);
+int launch_load_home(const halo_plan* pl, const float* g, float* local, cudaStream_t st);
+int launch_local_to_global(const halo_plan* pl, int32_t* out, cudaStream_t st);
+void free_exchange(halo_plan* pl);
+int reset_flags(halo_plan* pl, cudaStream_t st);
+
+void free_build(halo_plan* pl);
+
+inline int cuda_code(cudaError_t e) { return e == cudaSuccess ? HALO_OK : HALO_ECUDA; }
+
+template <class T>
+inline int dev_alloc(T** p, size_t count) {
+    *p = nullptr;
+    if (count == 0) count = 1;
+    cudaError_t e = cudaMalloc((void**)p, count * sizeof(T));
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        *p = nullptr;
+        return e == cudaErrorMemoryAllocation ? HALO_ENOMEM : HALO_ECUDA;
+    }
+    return HALO_OK;
+}
+
+template <class T>
+inline void dev_free(T*& p) {
+    if (p) cudaFree((void*)p);
+    p = nullptr;
+}
+
+}  // namespace halo
+
+#define HALO_TRY(x)                      \
+    do {                                 \
+        int _rc = (x);                   \
+        if (_rc != HALO_OK) return _rc;  \
+    } while (0)
+
+#define HALO_CUDA(x)                              \
+    do {                                          \
+        cudaError_t _e = (x);                     \
+        if (_e != cudaSuccess) return HALO_ECUDA; \
+    } while (0)

@@ -1,0 +1,284 @@
+"""ctypes binding of libhalo.so (include/halo.h), argument marshalling only.
+
+Every step of the halo build and of both exchanges runs in the library's CUDA
+kernels; PyTorch only provides device memory and streams.  There is no CPU
+fallback: importing this module on a machine without the compiled library, or
+calling it without a CUDA device, raises.
+
+The C functions keep their names (``halo_setup``, ``halo_exchange_x`` ...);
+``HaloPlan`` wraps one plan for convenience.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_PKG, "libhalo.so")
+
+OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM = (
+    0, -1, -2, -3, -4, -5, -6, -7, -8)
+MAX_PULSES = 64
+
+
+class HaloError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__("%s failed: %s (%d)" % (where, strerror(code), code))
+        self.code = code
+
+
+class halo_info(ctypes.Structure):
+    _fields_ = [("n_domains", ctypes.c_int32), ("n_pulses", ctypes.c_int32),
+                ("pulses_per_dim", ctypes.c_int32 * 3),
+                ("pulse_dim", ctypes.c_int32 * MAX_PULSES),
+                ("n_atoms", ctypes.c_int64), ("n_local_total", ctypes.c_int64),
+                ("n_halo_total", ctypes.c_int64)]
+
+
+class halo_pulse_info(ctypes.Structure):
+    _fields_ = [("send_domain", ctypes.c_int32), ("recv_domain", ctypes.c_int32),
+                ("send_size", ctypes.c_int32), ("split", ctypes.c_int32),
+                ("dep_offset", ctypes.c_int32), ("atom_offset", ctypes.c_int32),
+                ("coord_shift", ctypes.c_float * 3)]
+
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_P = ctypes.POINTER
+
+SIGNATURES = {
+    "halo_setup": (ctypes.c_int, [_P(ctypes.c_float), _P(_i32), ctypes.c_float, _vp, _vp, _i64,
+                                  _vp, _P(_vp)]),
+    "halo_rebuild": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
+    "halo_query": (ctypes.c_int, [_vp, _P(halo_info)]),
+    "halo_domain_layout": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "halo_get_pulse": (ctypes.c_int, [_vp, _i32, _i32, _P(halo_pulse_info), _vp]),
+    "halo_get_index_maps": (ctypes.c_int, [_vp, _vp, _vp]),
+    "halo_local_to_global": (ctypes.c_int, [_vp, _vp, _vp]),
+    "halo_load_home": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "halo_exchange_x": (ctypes.c_int, [_vp, _vp, _vp]),
+    "halo_exchange_f": (ctypes.c_int, [_vp, _vp, _vp]),
+    "halo_status": (ctypes.c_int, [_vp, _vp]),
+    "halo_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_double]),
+    "halo_debug_drop_signal": (ctypes.c_int, [_vp, _i32, _i32]),
+    "halo_launch_counts": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
+    "halo_destroy": (None, [_vp]),
+    "halo_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def load_library(path: str = LIBRARY):
+    """Load libhalo.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError("libhalo.so not built: run __graft_entry__.build() "
+                              "(there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return load_library().halo_strerror(code).decode()
+
+
+def _check(code, where):
+    if code != OK:
+        raise HaloError(code, where)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(getattr(stream, "cuda_stream", stream)))
+
+
+def _dev_ptr(t, dtype=None, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("expected a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("expected dtype %s, got %s" % (dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("expected shape %s, got %s" % (tuple(shape), tuple(t.shape)))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# --------------------------------------------------------------------------- #
+# C names
+# --------------------------------------------------------------------------- #
+def halo_setup(box, grid, rc, coords, domain_of_atom, stream=None):
+    """Build a plan on the device; returns the raw handle (c_void_p)."""
+    import torch
+    lib = load_library()
+    n = int(coords.shape[0])
+    boxa = (ctypes.c_float * 3)(*[float(v) for v in box])
+    grida = (_i32 * 3)(*[int(v) for v in grid])
+    h = ctypes.c_void_p()
+    code = lib.halo_setup(boxa, grida, ctypes.c_float(float(rc)),
+                          _dev_ptr(coords, torch.float32, (n, 3)),
+                          _dev_ptr(domain_of_atom, torch.int32, (n,)),
+                          _i64(n), _stream_handle(stream), ctypes.byref(h))
+    _check(code, "halo_setup")
+    return h
+
+
+def halo_rebuild(plan, coords, domain_of_atom, stream=None):
+    import torch
+    n = int(coords.shape[0])
+    _check(load_library().halo_rebuild(plan, _dev_ptr(coords, torch.float32, (n, 3)),
+                                       _dev_ptr(domain_of_atom, torch.int32, (n,)), _i64(n),
+                                       _stream_handle(stream)), "halo_rebuild")
+
+
+def halo_query(plan) -> halo_info:
+    out = halo_info()
+    _check(load_library().halo_query(plan, ctypes.byref(out)), "halo_query")
+    return out
+
+
+def halo_exchange_x(plan, local_coords, stream=None):
+    _check(load_library().halo_exchange_x(plan, ctypes.c_void_p(local_coords.data_ptr()),
+                                          _stream_handle(stream)), "halo_exchange_x")
+
+
+def halo_exchange_f(plan, local_forces, stream=None):
+    _check(load_library().halo_exchange_f(plan, ctypes.c_void_p(local_forces.data_ptr()),
+                                          _stream_handle(stream)), "halo_exchange_f")
+
+
+def halo_status(plan, stream=None) -> int:
+    return load_library().halo_status(plan, _stream_handle(stream))
+
+
+def halo_destroy(plan):
+    load_library().halo_destroy(plan)
+
+
+# --------------------------------------------------------------------------- #
+# convenience wrapper
+# --------------------------------------------------------------------------- #
+class HaloPlan:
+    """One plan.  Tensors are torch CUDA tensors; host results are numpy."""
+
+    def __init__(self, box, grid, rc, coords, domain_of_atom, stream=None):
+        self.box = np.asarray(box, np.float32)
+        self.grid = np.asarray(grid, np.int32)
+        self.rc = float(np.float32(rc))
+        self._lib = load_library()
+        self._h = halo_setup(box, grid, rc, coords, domain_of_atom, stream)
+        self._refresh()
+
+    def _refresh(self):
+        info = halo_query(self._h)
+        self.n_domains = info.n_domains
+        self.n_pulses = info.n_pulses
+        self.pulses_per_dim = np.asarray(list(info.pulses_per_dim), np.int32)
+        self.pulse_dim = np.asarray(list(info.pulse_dim)[: info.n_pulses], np.int32)
+        self.n_atoms = info.n_atoms
+        self.n_local_total = info.n_local_total
+        self.n_halo_total = info.n_halo_total
+        nd = self.n_domains
+        self.base = np.zeros(nd, np.int64)
+        self.n_home = np.zeros(nd, np.int32)
+        self.n_local = np.zeros(nd, np.int32)
+        _check(self._lib.halo_domain_layout(self._h, self.base.ctypes.data_as(_vp),
+                                            self.n_home.ctypes.data_as(_vp),
+                                            self.n_local.ctypes.data_as(_vp)), "layout")
+
+    @property
+    def handle(self):
+        return self._h
+
+    def rebuild(self, coords, domain_of_atom, stream=None):
+        halo_rebuild(self._h, coords, domain_of_atom, stream)
+        self._refresh()
+
+    def pulse(self, s: int, p: int):
+        out = halo_pulse_info()
+        _check(self._lib.halo_get_pulse(self._h, s, p, ctypes.byref(out), None), "halo_get_pulse")
+        return out
+
+    def index_map(self, s: int, p: int) -> np.ndarray:
+        info = self.pulse(s, p)
+        m = np.zeros(max(info.send_size, 1), np.int32)
+        _check(self._lib.halo_get_pulse(self._h, s, p, ctypes.byref(info), m.ctypes.data_as(_vp)),
+               "halo_get_pulse")
+        return m[: info.send_size].copy()
+
+    def index_maps(self):
+        maps = np.zeros(max(self.n_halo_total, 1), np.int32)
+        offs = np.zeros(self.n_pulses * self.n_domains + 1, np.int64)
+        _check(self._lib.halo_get_index_maps(self._h, maps.ctypes.data_as(_vp),
+                                             offs.ctypes.data_as(_vp)), "halo_get_index_maps")
+        return maps[: self.n_halo_total], offs
+
+    def local_to_global(self, stream=None):
+        import torch
+        out = torch.empty(self.n_local_total, dtype=torch.int32, device="cuda")
+        _check(self._lib.halo_local_to_global(self._h, _dev_ptr(out), _stream_handle(stream)),
+               "halo_local_to_global")
+        return out
+
+    def load_home(self, global_xyz, local_xyz=None, stream=None):
+        import torch
+        if local_xyz is None:
+            local_xyz = torch.zeros((self.n_local_total, 3), dtype=torch.float32, device="cuda")
+        _check(self._lib.halo_load_home(
+            self._h, _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)),
+            _dev_ptr(local_xyz, torch.float32, (self.n_local_total, 3)), _stream_handle(stream)),
+            "halo_load_home")
+        return local_xyz
+
+    def exchange_x(self, local_xyz, stream=None):
+        import torch
+        _check(self._lib.halo_exchange_x(
+            self._h, _dev_ptr(local_xyz, torch.float32, (self.n_local_total, 3)),
+            _stream_handle(stream)), "halo_exchange_x")
+        return local_xyz
+
+    def exchange_f(self, local_f, stream=None):
+        import torch
+        _check(self._lib.halo_exchange_f(
+            self._h, _dev_ptr(local_f, torch.float32, (self.n_local_total, 3)),
+            _stream_handle(stream)), "halo_exchange_f")
+        return local_f
+
+    def status(self, stream=None) -> int:
+        return halo_status(self._h, stream)
+
+    def set_wait_timeout(self, seconds: float):
+        _check(self._lib.halo_set_wait_timeout(self._h, float(seconds)), "halo_set_wait_timeout")
+
+    def debug_drop_signal(self, domain: int, pulse: int):
+        _check(self._lib.halo_debug_drop_signal(self._h, domain, pulse), "halo_debug_drop_signal")
+
+    def launch_counts(self):
+        x, f = _i64(), _i64()
+        _check(self._lib.halo_launch_counts(self._h, ctypes.byref(x), ctypes.byref(f)),
+               "halo_launch_counts")
+        return x.value, f.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            halo_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,171 @@
+/*
+ * halo.h -- C ABI of libhalo.so: the eighth-shell domain-decomposition halo
+ * exchange of a molecular-dynamics code, with every domain of the periodic box
+ * resident in one GPU's memory (GB300, sm_103a).
+ *
+ * What it computes (page "Redesigning GROMACS Halo Exchange: Improving Strong
+ * Scaling with GPU-initiated NVSHMEM", review):
+ *   - section 3 "GROMACS domain-decomposition halo exchange": the box is split
+ *     into n = (nx, ny, nz) domains, each owning its home atoms; atoms within
+ *     the cut-off rc of a domain face are sent to the neighbour and forwarded
+ *     through intermediate domains (eighth shell), np(z) pulses in z, then
+ *     np(y) in y, then np(x) in x;
+ *   - Algorithm 1: per pulse an index map (sendSize entries), the receiver's
+ *     atomOffset and a periodic coordShift;
+ *   - Algorithms 3/4 (FusedPackCommX, packWithDeps): one launch packs every
+ *     pulse; entries below depOffset are independent, the others wait for the
+ *     pulse that delivered them;
+ *   - Algorithm 6 (FusedCommUnpackF): one launch adds every halo force back to
+ *     its owner, pulses from the last to the first.
+ *
+ * Conventions (fixed by this library where the page is silent):
+ *   - domain id D = ix + nx*(iy + ny*iz);
+ *   - p_d = ceil(rc / (L_d/n_d)) pulses in each dim with n_d > 1, 0 otherwise;
+ *     global pulse order z0..z(pz-1), y0.., x0..; P = pz + py + px <= 64;
+ *   - coordinates flow from sender s to receiver r = s - e_d (periodic), so a
+ *     domain's halo lies above its upper faces; forces flow back from r to s;
+ *   - an atom of s is selected for a pulse of dim d iff x_d < thr, one fp32
+ *     compare with thr = fl32(s_d*L_d/n_d + rc) evaluated in double; pulse 0 of
+ *     a dim selects among s's home atoms and all halo of earlier dims, pulse
+ *     k >= 1 only among the slots s received in pulse k-1 of the same dim;
+ *   - index maps are ascending local indices; depOffset = n_home[s]; split =
+ *     number of entries < depOffset;
+ *   - coordShift = +L_d on component d iff s_d == 0, else 0;
+ *   - local layout of domain D: [home atoms in input order | halo of pulse 0 |
+ *     ... | halo of pulse P-1]; the dense buffers hold all domains back to
+ *     back, domain D starting at slot base[D] = sum of n_local of lower ids;
+ *   - coordinates and forces are fp32 AoS xyz (12 bytes per slot).
+ *
+ * Pointers are DEVICE pointers unless marked (host).  `stream` is a
+ * cudaStream_t passed as void* (NULL = legacy default stream).  Exchanges are
+ * asynchronous on `stream`; halo_setup / halo_rebuild synchronise `stream` once
+ * to read the sizes back.  A plan is used by one stream at a time.  Every call
+ * returns HALO_OK or a negative error code; no exception crosses the ABI.
+ * Errors met by a kernel (a bounded wait that gave up) are sticky in the plan
+ * and are returned, and cleared, by halo_status().
+ */
+#ifndef HALO_H
+#define HALO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HALO_OK 0
+#define HALO_EINVAL (-1)    /* null pointer, non-positive L / rc / n, n_atoms <= 0 */
+#define HALO_EPULSES (-2)   /* p_d >= n_d: the halo would wrap onto its own domain */
+#define HALO_EDOMAIN (-3)   /* a domain id outside [0, nx*ny*nz) */
+#define HALO_ECAPACITY (-4) /* build buffers could not be sized (internal retries exhausted) */
+#define HALO_ECUDA (-5)     /* a CUDA runtime call failed */
+#define HALO_ETIMEOUT (-6)  /* a device-side wait gave up after the plan's time limit */
+#define HALO_EBOUNDS (-7)   /* an index outside its buffer was met and skipped */
+#define HALO_ENOMEM (-8)    /* device or host allocation failed */
+
+#define HALO_MAX_PULSES 64
+#define HALO_MAX_DOMAINS 4096
+
+typedef struct halo_plan halo_plan; /* opaque; owns maps, metadata, flags, build buffers */
+
+typedef struct {
+    int32_t n_domains;
+    int32_t n_pulses;
+    int32_t pulses_per_dim[3];              /* p_x, p_y, p_z */
+    int32_t pulse_dim[HALO_MAX_PULSES];     /* dim (0=x,1=y,2=z) of each global pulse */
+    int64_t n_atoms;
+    int64_t n_local_total;                  /* home + halo slots of all domains */
+    int64_t n_halo_total;
+} halo_info;
+
+typedef struct {
+    int32_t send_domain;   /* s */
+    int32_t recv_domain;   /* r = s - e_d (periodic) */
+    int32_t send_size;     /* index-map entries (= halo slots the receiver gets) */
+    int32_t split;         /* entries < dep_offset: independent of earlier pulses */
+    int32_t dep_offset;    /* = n_home[s] */
+    int32_t atom_offset;   /* first halo slot of this pulse in the receiver's local range */
+    float coord_shift[3];  /* added to every packed coordinate */
+} halo_pulse_info;
+
+/* Build a plan: pulses, home partition and every pulse's index map, on the
+ * device (Algorithm 1's PulseData for all domains).
+ *   box (host, 3 floats, nm), grid (host, 3 ints), rc (nm);
+ *   coords: n_atoms x 3 fp32 positions in [0, L) (device);
+ *   domain_of_atom: n_atoms int32 domain ids (device; trusted, range-checked).
+ * Synchronises `stream` once.  On success *out_plan owns device memory until
+ * halo_destroy().  Errors: HALO_EINVAL, HALO_EPULSES, HALO_EDOMAIN,
+ * HALO_ENOMEM, HALO_ECUDA. */
+int halo_setup(const float box[3], const int32_t grid[3], float rc, const float* coords,
+               const int32_t* domain_of_atom, int64_t n_atoms, void* stream,
+               halo_plan** out_plan);
+
+/* Rebuild the plan's maps for new positions / domain ids (same box, grid and
+ * cut-off; n_atoms may change).  Synchronises `stream` once.  Sizes and
+ * layout change: query them again and re-size the caller's buffers. */
+int halo_rebuild(halo_plan* plan, const float* coords, const int32_t* domain_of_atom,
+                 int64_t n_atoms, void* stream);
+
+/* Sizes of the plan (host struct). */
+int halo_query(const halo_plan* plan, halo_info* out);
+
+/* Dense layout (host arrays of n_domains entries each; any may be NULL). */
+int halo_domain_layout(const halo_plan* plan, int64_t* base, int32_t* n_home, int32_t* n_local);
+
+/* One pulse of one sender domain (host struct); if index_map (host) is not
+ * NULL it receives send_size int32 entries.  Synchronous copy. */
+int halo_get_pulse(const halo_plan* plan, int32_t domain, int32_t pulse, halo_pulse_info* out,
+                   int32_t* index_map);
+
+/* All index maps (host): maps receives n_halo_total int32 entries; the map of
+ * (sender s, pulse p) is maps[offsets[p*n_domains + s] .. offsets[p*n_domains
+ * + s + 1]); offsets (host) has n_pulses*n_domains + 1 entries.  Synchronous. */
+int halo_get_index_maps(const halo_plan* plan, int32_t* maps, int64_t* offsets);
+
+/* Global atom id of the owner of every local slot: out has n_local_total
+ * int32 (device).  Asynchronous on stream. */
+int halo_local_to_global(const halo_plan* plan, int32_t* out, void* stream);
+
+/* Copy the home atoms' coordinates from the global array (n_atoms x 3) into
+ * the dense local layout (n_local_total x 3); halo slots are not touched. */
+int halo_load_home(const halo_plan* plan, const float* global_xyz, float* local_xyz,
+                   void* stream);
+
+/* Coordinate halo exchange (FusedPackCommX, Algorithms 3/4), one kernel
+ * launch for all pulses: for every pulse p and sender s,
+ *   local_coords[base[r] + atom_offset + i] = local_coords[base[s] + map[i]] + coord_shift,
+ * i in [0, send_size).  local_coords: n_local_total x 3 fp32, caller-owned,
+ * home slots filled.  Asynchronous. */
+int halo_exchange_x(halo_plan* plan, float* local_coords, void* stream);
+
+/* Force halo reduction (FusedCommUnpackF, Algorithm 6), one kernel launch for
+ * all pulses: for p = P-1 .. 0 and every sender s,
+ *   local_forces[base[s] + map[i]] += local_forces[base[r] + atom_offset + i].
+ * Halo slots keep their (possibly forwarded-into) values.  Bit-identical to
+ * the sequential order.  Asynchronous. */
+int halo_exchange_f(halo_plan* plan, float* local_forces, void* stream);
+
+/* Synchronise `stream`, return the plan's sticky device error (HALO_OK if
+ * none) and clear it, resetting the plan's flags. */
+int halo_status(halo_plan* plan, void* stream);
+
+/* Time limit of every device-side wait (default 1 s).  seconds > 0. */
+int halo_set_wait_timeout(halo_plan* plan, double seconds);
+
+/* Test hook: in the next halo_exchange_x, the producer of (domain, pulse)
+ * skips its completion signal, so its consumers' waits run out and the kernel
+ * reports HALO_ETIMEOUT through halo_status().  (-1, -1) disarms. */
+int halo_debug_drop_signal(halo_plan* plan, int32_t domain, int32_t pulse);
+
+/* Kernel launches made so far by halo_exchange_x and halo_exchange_f (host). */
+int halo_launch_counts(const halo_plan* plan, int64_t* x_launches, int64_t* f_launches);
+
+void halo_destroy(halo_plan* plan);
+
+const char* halo_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HALO_H */

@@ -1,0 +1,60 @@
+"""Failure detection without a GPU fault: a producer's completion signal is
+suppressed on the host side (test hook), its consumers' bounded waits run out
+after a short limit, the kernel returns, and the plan reports HALO_ETIMEOUT
+through halo_status(); the context stays usable and the next exchange is
+correct."""
+import numpy as np
+import pytest
+
+import oracle
+from domain_decomposition_halo_build_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def test_dropped_signal_times_out_and_recovers():
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    w = synth.WORKLOADS["water24k_2x4x8"]
+    xyz, dom = synth.system(w)
+    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d)
+    try:
+        plan.set_wait_timeout(0.05)
+        # pulse 0 (z0) of domain 0 feeds the whole z1 pulse of its receiver
+        plan.debug_drop_signal(0, 0)
+        loc = plan.load_home(x)
+        plan.exchange_x(loc)
+        assert plan.status() == halo.ETIMEOUT
+        assert plan.status() == halo.OK          # cleared
+        want = o.load_home(xyz)
+        o.exchange_x(want)
+        for _ in range(3):                       # flags were reset: exchanges work again
+            loc = plan.load_home(x)
+            plan.exchange_x(loc)
+            assert plan.status() == halo.OK
+            np.testing.assert_array_equal(loc.cpu().numpy(), want)
+    finally:
+        plan.close()
+
+
+def test_bad_arguments_return_codes():
+    import ctypes
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    assert lib.halo_exchange_x(None, None, None) == halo.EINVAL
+    assert lib.halo_status(None, None) == halo.EINVAL
+    assert lib.halo_set_wait_timeout(None, 1.0) == halo.EINVAL
+    h = ctypes.c_void_p()
+    box = (ctypes.c_float * 3)(1, 1, 1)
+    grid = (ctypes.c_int32 * 3)(1, 1, 1)
+    assert lib.halo_setup(box, grid, ctypes.c_float(0.1), None, None, 10, None,
+                          ctypes.byref(h)) == halo.EINVAL

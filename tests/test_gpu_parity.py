@@ -1,0 +1,221 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar: index maps, splits, sizes, offsets, shifts, local-to-global ids and
+exchanged coordinates bit-exact; forces bit-exact (the kernel keeps the
+oracle's per-slot add order), and in any case within 1e-6 relative per fp32
+component.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import pins
+from domain_decomposition_halo_build_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+FORCE_RTOL = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def gpu_plan(box, grid, rc, xyz, dom):
+    from gpu_adaptor import GpuPlan
+    return GpuPlan(box, grid, rc, xyz, dom)
+
+
+def bits(a):
+    return np.ascontiguousarray(a, np.float32).view(np.uint32)
+
+
+def compare_plans(g, o):
+    assert g.n_pulses == o.n_pulses
+    np.testing.assert_array_equal(g.pulse_dim, o.pulse_dim)
+    np.testing.assert_array_equal(g.pulses_per_dim, o.pulses_per_dim)
+    np.testing.assert_array_equal(g.n_home, o.n_home)
+    np.testing.assert_array_equal(g.n_local, o.n_local)
+    np.testing.assert_array_equal(g.base, o.base)
+    assert g.n_local_total == o.n_local_total
+    maps, offs = g.plan.index_maps()
+    nd = o.n_domains
+    for p in range(o.n_pulses):
+        for s in range(nd):
+            gi, oi = g.pulse(s, p), o.pulse(s, p)
+            for k in ("recv_domain", "send_size", "split", "dep_offset", "atom_offset"):
+                assert getattr(gi, k) == getattr(oi, k), ((s, p), k)
+            np.testing.assert_array_equal(bits(gi.coord_shift), bits(oi.coord_shift))
+            want = o.index_map(s, p)
+            got = maps[offs[p * nd + s]:offs[p * nd + s + 1]]
+            np.testing.assert_array_equal(got, want, err_msg=str((s, p)))
+    np.testing.assert_array_equal(g.local_to_global(), o.local_to_global())
+
+
+def compare_exchanges(g, o, xyz, reps=2, seed=1):
+    want_x = o.load_home(xyz)
+    o.exchange_x(want_x)
+    for _ in range(reps):
+        got = g.load_home(xyz)
+        g.exchange_x(got)
+        np.testing.assert_array_equal(bits(got), bits(want_x), err_msg="coordinates")
+    f0 = synth.forces(o.n_local_total, seed=seed)
+    want = f0.copy()
+    got = f0.copy()
+    for r in range(reps):
+        o.exchange_f(want)
+        g.exchange_f(got)
+        rel = np.abs(got.astype(np.float64) - want) / np.maximum(np.abs(want.astype(np.float64)), 1e-30)
+        assert float(rel.max()) <= FORCE_RTOL, ("force rel err", float(rel.max()), r)
+        np.testing.assert_array_equal(bits(got), bits(want), err_msg="forces (bit-exact)")
+
+
+WORKLOADS = list(synth.WORKLOADS)
+
+
+@pytest.fixture(scope="module")
+def cases():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            w = synth.WORKLOADS[name]
+            xyz, dom = synth.system(w)
+            o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+            cache[name] = (w, xyz, dom, o, gpu_plan(w.box, w.grid, w.rc, xyz, dom))
+        return cache[name]
+
+    yield get
+    for v in cache.values():
+        v[4].close()
+
+
+@pytest.mark.parametrize("name", pins.EXAMPLES)
+def test_golden_examples_on_gpu(name):
+    """The hand-worked examples, run through the library."""
+    pins.check_example(gpu_plan, pins.load_example(name))
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_plan_parity(cases, name):
+    w, xyz, dom, o, g = cases(name)
+    compare_plans(g, o)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_exchange_parity(cases, name):
+    w, xyz, dom, o, g = cases(name)
+    compare_exchanges(g, o, xyz)
+
+
+@pytest.mark.parametrize("name", ["water24k_2x4x8", "water1M_4x4x4"])
+def test_gpu_forces_integer_closed_form(cases, name):
+    w, xyz, dom, o, g = cases(name)
+    pins.check_forces_integer(g)
+
+
+def test_rebuild_after_displacement(cases):
+    """3M-atom system: displace by N(0, 0.01 nm), rebuild, compare again."""
+    w, xyz, dom, o, g = cases("water3M_8x8x8")
+    x1, d1 = synth.displaced(xyz, w.box, w.grid, k=1)
+    g.rebuild(x1, d1)
+    o1 = oracle.Oracle(w.box, w.grid, w.rc, x1, d1)
+    compare_plans(g, o1)
+    compare_exchanges(g, o1, x1, reps=1)
+
+
+EDGE = [
+    # (box, grid, rc, n_atoms, seed)
+    ((2.0, 2.0, 2.0), (1, 1, 1), 0.5, 37, 0),        # one domain, no pulses
+    ((3.0, 3.0, 3.0), (2, 1, 1), 0.5, 1, 0),         # a single atom
+    ((2.4, 2.4, 2.4), (3, 3, 3), 1.0, 3000, 3),      # two pulses in every dim
+    ((3.2, 3.2, 3.2), (4, 1, 1), 1.0, 777, 4),       # 1D, two pulses, ragged
+    ((4.0, 4.0, 4.0), (1, 2, 5), 1.1, 1500, 5),      # x undecomposed
+    ((5.0, 4.0, 3.0), (5, 4, 3), 0.9, 20000, 6),     # rectangular box, odd grid
+    ((6.0, 6.0, 6.0), (3, 3, 3), 0.05, 2000, 7),     # almost nothing sent
+    ((8.0, 8.0, 8.0), (16, 16, 16), 1.4, 40000, 8),  # 4096 domains, 3 pulses per dim
+]
+
+
+@pytest.mark.parametrize("box,grid,rc,n,seed", EDGE)
+def test_edge_cases(box, grid, rc, n, seed):
+    xyz, dom = synth.custom_system(n, box, grid, seed=seed)
+    o = oracle.Oracle(box, grid, rc, xyz, dom)
+    g = gpu_plan(box, grid, rc, xyz, dom)
+    try:
+        compare_plans(g, o)
+        compare_exchanges(g, o, xyz)
+    finally:
+        g.close()
+
+
+def test_empty_domains_and_skewed_load():
+    """All atoms in two of 27 domains: most senders send nothing."""
+    box, grid, rc = (3.0, 3.0, 3.0), (3, 3, 3), 0.7
+    rng = np.random.default_rng(9)
+    xyz = (rng.random((5000, 3)) * np.array([0.9, 0.9, 2.9])).astype(np.float32)
+    dom = synth.assign_domains(xyz, box, grid)
+    o = oracle.Oracle(box, grid, rc, xyz, dom)
+    g = gpu_plan(box, grid, rc, xyz, dom)
+    try:
+        assert (o.n_home == 0).sum() >= 20
+        compare_plans(g, o)
+        compare_exchanges(g, o, xyz)
+    finally:
+        g.close()
+
+
+def test_setup_errors():
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    xyz, dom = synth.custom_system(100, (3, 3, 3), (3, 1, 1), seed=1)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    with pytest.raises(halo.HaloError) as e:
+        halo.HaloPlan((3, 3, 3), (3, 1, 1), 2.5, x, d)
+    assert e.value.code == halo.EPULSES
+    bad = d.clone()
+    bad[7] = 3
+    with pytest.raises(halo.HaloError) as e:
+        halo.HaloPlan((3, 3, 3), (3, 1, 1), 0.5, x, bad)
+    assert e.value.code == halo.EDOMAIN
+    with pytest.raises(halo.HaloError) as e:
+        halo.HaloPlan((3, 3, 3), (3, 1, 1), 0.0, x, d)
+    assert e.value.code == halo.EINVAL
+    with pytest.raises(halo.HaloError) as e:
+        halo.HaloPlan((3, 3, 3), (0, 1, 1), 0.5, x, d)
+    assert e.value.code == halo.EINVAL
+
+
+def test_one_launch_per_direction(cases):
+    w, xyz, dom, o, g = cases("water24k_2x4x8")
+    x0, f0 = g.plan.launch_counts()
+    loc = g.plan.load_home(g.xyz_d)
+    g.plan.exchange_x(loc)
+    g.plan.exchange_f(loc)
+    assert g.plan.status() == 0
+    x1, f1 = g.plan.launch_counts()
+    assert (x1 - x0, f1 - f0) == (1, 1)
+
+
+def test_determinism_repeated(cases):
+    """Twenty back-to-back x+f exchanges give bitwise identical results (a race
+    would show up as run-to-run variance)."""
+    import torch
+    w, xyz, dom, o, g = cases("water48k_2x2x2")
+    f0 = torch.from_numpy(synth.forces(g.n_local_total, seed=3)).cuda()
+    ref = None
+    for _ in range(20):
+        loc = g.plan.load_home(g.xyz_d)
+        g.plan.exchange_x(loc)
+        f = f0.clone()
+        g.plan.exchange_f(f)
+        out = (loc.cpu().numpy().view(np.uint32).copy(), f.cpu().numpy().view(np.uint32).copy())
+        if ref is None:
+            ref = out
+        else:
+            np.testing.assert_array_equal(out[0], ref[0])
+            np.testing.assert_array_equal(out[1], ref[1])
+    assert g.plan.status() == 0
