@@ -86,6 +86,8 @@ void destroy_plan(halo_plan* pl) {
 
 int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, void* stream) {
     const cudaStream_t st = as_stream(stream);
+    pl->trace = nullptr;  // item counts change with the plan: the caller re-arms tracing
+    pl->trace_cap = 0;
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
     return halo::prepare_exchange(pl, st);
 }
@@ -246,11 +248,33 @@ int halo_set_wait_timeout(halo_plan* pl, double seconds) {
 int halo_debug_drop_signal(halo_plan* pl, int32_t domain, int32_t pulse) {
     if (!pl) return HALO_EINVAL;
     if (domain == -1 && pulse == -1) {
-        pl->drop_sp = -1;
+        pl->drop_flag = -1;
         return HALO_OK;
     }
     if (domain < 0 || domain >= pl->n_dom || pulse < 0 || pulse >= pl->P) return HALO_EINVAL;
-    pl->drop_sp = domain * pl->P + pulse;
+    // the counter the producer (domain, pulse) releases: arrived[r*P + pulse]
+    pl->drop_flag = pl->sp[(size_t)domain * pl->P + pulse].r * pl->P + pulse;
+    return HALO_OK;
+}
+
+int halo_set_trace(halo_plan* pl, uint64_t* trace, int64_t capacity_items) {
+    if (!pl) return HALO_EINVAL;
+    if (!trace) {
+        pl->trace = nullptr;
+        pl->trace_cap = 0;
+        return HALO_OK;
+    }
+    if (capacity_items < (int64_t)pl->n_items_x + pl->n_items_f) return HALO_EINVAL;
+    pl->trace = reinterpret_cast<unsigned long long*>(trace);
+    pl->trace_cap = capacity_items;
+    return HALO_OK;
+}
+
+int halo_work_items(const halo_plan* pl, int32_t* x_items, int32_t* f_items, int32_t* chunk) {
+    if (!pl) return HALO_EINVAL;
+    if (x_items) *x_items = pl->n_items_x;
+    if (f_items) *f_items = pl->n_items_f;
+    if (chunk) *chunk = pl->chunk;
     return HALO_OK;
 }
 

@@ -20,13 +20,24 @@
 // epoch * chunks; the epoch is the call number, recovered from a monotonically
 // increasing work ticket, so no counter is ever reset between calls.
 //
-// Forward progress: blocks take work items from one atomic ticket counter, in
-// pulse order (ascending for coordinates, descending for forces), and a work
-// item only waits on items of earlier pulses.  The earliest unfinished item was
-// taken by a block that is running, and everything it waits on has an earlier
-// ticket, so by induction every wait ends -- whatever the grid size and
-// however the hardware schedules blocks.  Every wait is still bounded in time
-// and reports HALO_ETIMEOUT through the plan's error word instead of hanging.
+// Work order.  Coordinates: the independent chunks (entries below depOffset)
+// of every pulse come first, then the dependent chunks in pulse order, so the
+// bulk of the traffic streams with no wait and only the forwarded entries form
+// the z -> y -> x chain.  Forces: the build classifies every entry; an entry is
+// independent when no later pulse adds into its destination slot and its halo
+// source slot was never forwarded; independent chunks come first, dependent
+// chunks follow in reverse pulse order and wait for the later pulses that touch
+// their destination domain or their source slice.  Each destination slot still
+// receives its adds in reverse pulse order, so the result is bit-identical to
+// the sequential reduction.
+//
+// Forward progress: blocks take work items from one atomic ticket counter in
+// that order, and an item only waits on items with earlier tickets.  The
+// earliest unfinished item was taken by a block that is running (a block holds
+// at most the item it works on and one prefetched ticket), and everything it
+// waits on has an earlier ticket, so by induction every wait ends -- whatever
+// the grid size and however blocks are scheduled.  Every wait is still bounded
+// in time and reports HALO_ETIMEOUT through the plan's error word.
 #include <string.h>
 
 #include <algorithm>
@@ -35,6 +46,8 @@
 
 namespace halo {
 namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
@@ -58,108 +71,99 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ unsigned smid() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
+// Trace record of one work item: ticket time, time the waits ended, release
+// time (global timer, ns) and the SM that ran it.
+__device__ __forceinline__ void trace_item(unsigned long long* trace, int item, uint64_t t0,
+                                           uint64_t t1) {
+    unsigned long long* r = trace + 4 * (int64_t)item;
+    r[0] = t0;
+    r[1] = t1;
+    r[2] = global_timer_ns();
+    r[3] = smid();
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
 // Bounded wait until *c has reached target (modulo 2^32).  On timeout the
 // first waiter records where it gave up; every waiter gives up as soon as the
 // plan's error word is set.
 __device__ bool wait_count(const uint32_t* c, uint32_t target, int* err, long long timeout_ns,
-                           int kernel, int sp, int q) {
+                           int kernel, int flag) {
     if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) return true;
     const uint64_t t0 = global_timer_ns();
-    unsigned ns = 16;
+    unsigned ns = 8;
     for (;;) {
         __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
+        if (ns < 128) ns <<= 1;
         if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) return true;
         if (ld_relaxed_gpu(err) != 0) return false;
         if ((long long)(global_timer_ns() - t0) > timeout_ns) {
             if (atomicCAS(err, 0, HALO_ETIMEOUT) == 0) {
                 err[1] = kernel;
-                err[2] = sp;
-                err[3] = q;
+                err[2] = flag;
             }
             return false;
         }
     }
 }
 
-// Largest pulse q < p whose received slice (starting at oo[q]) holds local index i.
-__device__ __forceinline__ int pulse_of(const int32_t* oo, int p, int i) {
-    int q = p - 1;
-    while (q > 0 && i < __ldg(oo + q)) q--;
-    return q < 0 ? 0 : q;
-}
-
 struct XArgs {
     float* xyz;
     const int32_t* maps;
-    const SPDesc* sp;
-    const WorkItem* items;
-    const int32_t* own_off;
-    const uint32_t* nch_in;
+    const XItem* items;
+    const uint32_t* target;  // chunks delivered into each (r, p)
     uint32_t* arrived;
     unsigned long long* ticket;
     int* err;
     int n_items;
-    int P;
     long long timeout_ns;
-    int drop_sp;
+    int drop_flag;
+    unsigned long long* trace;  // optional: 4 words per item (see halo_set_trace)
 };
 
 struct FArgs {
     float* f;
-    const int32_t* maps;
-    const SPDesc* sp;
-    const WorkItem* items;
-    const uint32_t* nch;
-    const uint64_t* fmask;
+    const int2* pairs;
+    const FItem* items;
+    const uint32_t* target;  // chunks reduced into each (s, p)
     uint32_t* done;
     unsigned long long* ticket;
     int* err;
     int n_items;
-    int P;
     long long timeout_ns;
+    unsigned long long* trace;
 };
 
-// dst[i] = src[map[i]] + shift for i in [i0, i1).  CG: the source slots may
-// have been written by other blocks of this launch, so they are read through
-// L2 (ld.global.cg); otherwise they are read-only for the launch (ld.global.nc).
-template <int E, bool CG>
-__device__ __forceinline__ void gather_shift(const int32_t* map, const float* src, float* dst,
-                                             int i0, int i1, float s0, float s1, float s2) {
-    for (int b = i0; b < i1; b += kThreads * E) {
-        int idx[E];
-#pragma unroll
-        for (int e = 0; e < E; e++) {
-            const int i = b + threadIdx.x + e * kThreads;
-            idx[e] = i < i1 ? __ldg(map + i) : -1;
-        }
-        float v[E][3];
-#pragma unroll
-        for (int e = 0; e < E; e++) {
-            if (idx[e] >= 0) {
-                const float* p = src + 3 * (int64_t)idx[e];
-                if (CG) {
-                    v[e][0] = __ldcg(p);
-                    v[e][1] = __ldcg(p + 1);
-                    v[e][2] = __ldcg(p + 2);
-                } else {
-                    v[e][0] = __ldg(p);
-                    v[e][1] = __ldg(p + 1);
-                    v[e][2] = __ldg(p + 2);
-                }
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < E; e++) {
-            const int i = b + threadIdx.x + e * kThreads;
-            if (i < i1) {
-                float* q = dst + 3 * (int64_t)i;
-                q[0] = v[e][0] + s0;
-                q[1] = v[e][1] + s1;
-                q[2] = v[e][2] + s2;
-            }
-        }
-    }
+// Ticket handling shared by both kernels: thread 0 decodes the held ticket into
+// (item, epoch) and prefetches the next one.
+struct TicketState {
+    unsigned long long next;
+};
+
+__device__ __forceinline__ void take_ticket(TicketState& ts, unsigned long long* ticket, int n_items,
+                                            unsigned long long T, const int* err, int* s_item,
+                                            uint32_t* s_epoch, int* s_abort) {
+    const unsigned long long k = ts.next / T;
+    int item = (int)(ts.next - k * T);
+    if (item < n_items && ld_relaxed_gpu(err) != 0) item = n_items;
+    *s_item = item;
+    *s_epoch = (uint32_t)(k + 1);
+    *s_abort = 0;
+    if (item < n_items) ts.next = atomicAdd(ticket, 1ull);
 }
 
 template <int E>
@@ -168,52 +172,74 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
     __shared__ uint32_t s_epoch;
     __shared__ int s_abort;
     const unsigned long long T = (unsigned long long)a.n_items + gridDim.x;
+    TicketState ts;
+    if (threadIdx.x == 0) ts.next = atomicAdd(a.ticket, 1ull);
     for (;;) {
-        if (threadIdx.x == 0) {
-            const unsigned long long t = atomicAdd(a.ticket, 1ull);
-            const unsigned long long k = t / T;
-            int item = (int)(t - k * T);
-            if (item < a.n_items && ld_relaxed_gpu(a.err) != 0) item = a.n_items;
-            s_item = item;
-            s_epoch = (uint32_t)(k + 1);
-            s_abort = 0;
-        }
+        if (threadIdx.x == 0)
+            take_ticket(ts, a.ticket, a.n_items, T, a.err, &s_item, &s_epoch, &s_abort);
         __syncthreads();
         const int item = s_item;
-        const uint32_t epoch = s_epoch;
         if (item >= a.n_items) return;
-        const WorkItem w = a.items[item];
-        const SPDesc d = a.sp[w.sp];
-        const int i0 = w.start, i1 = w.start + w.len;
-        const int32_t* map = a.maps + d.map_off;
-        const float* src = a.xyz + 3 * d.src_base;
-        float* dst = a.xyz + 3 * d.dst;
-        // independent entries: home atoms of the sender (Algorithm 4, first loop)
-        const int ie = min(i1, d.split);
-        if (i0 < ie) gather_shift<E, false>(map, src, dst, i0, ie, d.shift[0], d.shift[1], d.shift[2]);
-        // dependent entries: wait for the pulses that delivered them
-        if (i1 > d.split) {
-            const int j0 = max(i0, d.split);
+        const uint64_t t_take = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
+        const XItem w = a.items[item];
+        const bool dependent = w.wait_mask != 0;
+        const int32_t* map = a.maps + w.map_off;
+        const float* src = a.xyz + 3 * w.src_base;
+        float* dst = a.xyz + 3 * w.dst;
+        // a chunk holds at most kThreads*E entries: the index loads are issued
+        // before any wait, so only the forwarded coordinates remain after it
+        int idx[E];
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int i = threadIdx.x + e * kThreads;
+            idx[e] = i < w.len ? __ldg(map + i) : -1;
+        }
+        if (dependent) {
+            // packWithDeps: one thread waits for the pulses that delivered the
+            // slots this chunk forwards, then the block goes on
             if (threadIdx.x == 0) {
-                const int32_t* oo = a.own_off + (int64_t)d.s * (a.P + 1);
-                const int qlo = pulse_of(oo, d.p, __ldg(map + j0));
-                const int qhi = pulse_of(oo, d.p, __ldg(map + i1 - 1));
+                const uint32_t epoch = s_epoch;
                 bool ok = true;
-                for (int q = qlo; q <= qhi && ok; q++) {
-                    const int sq = d.s * a.P + q;
-                    ok = wait_count(a.arrived + sq, epoch * __ldg(a.nch_in + sq), a.err,
-                                    a.timeout_ns, 1, w.sp, q);
+                for (uint64_t m = w.wait_mask; m && ok; m &= m - 1) {
+                    const int c = w.wait_base + __ffsll((long long)m) - 1;
+                    ok = wait_count(a.arrived + c, epoch * __ldg(a.target + c), a.err,
+                                    a.timeout_ns, 1, c);
                 }
                 s_abort = ok ? 0 : 1;
             }
             __syncthreads();
             if (s_abort) return;
-            gather_shift<E, true>(map, src, dst, j0, i1, d.shift[0], d.shift[1], d.shift[2]);
+        }
+        const uint64_t t_wait = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
+        float v[E][3];
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            if (idx[e] >= 0) {
+                const float* p = src + 3 * (int64_t)idx[e];
+                if (dependent) {  // slots written by this launch: read through L2
+                    v[e][0] = __ldcg(p);
+                    v[e][1] = __ldcg(p + 1);
+                    v[e][2] = __ldcg(p + 2);
+                } else {          // home slots: read-only for the launch
+                    v[e][0] = __ldg(p);
+                    v[e][1] = __ldg(p + 1);
+                    v[e][2] = __ldg(p + 2);
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            if (idx[e] >= 0) {
+                float* q = dst + 3 * (int64_t)(threadIdx.x + e * kThreads);
+                q[0] = v[e][0] + w.shift[0];
+                q[1] = v[e][1] + w.shift[1];
+                q[2] = v[e][2] + w.shift[2];
+            }
         }
         // all stores of the block, then one gpu-scope release (Algorithm 5)
         __syncthreads();
-        if (threadIdx.x == 0 && w.sp != a.drop_sp)
-            red_release_gpu_add(a.arrived + (int64_t)d.r * a.P + d.p, 1u);
+        if (threadIdx.x == 0 && w.flag != a.drop_flag) red_release_gpu_add(a.arrived + w.flag, 1u);
+        if (a.trace && threadIdx.x == 0) trace_item(a.trace, item, t_take, t_wait);
     }
 }
 
@@ -223,80 +249,154 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
     __shared__ uint32_t s_epoch;
     __shared__ int s_abort;
     const unsigned long long T = (unsigned long long)a.n_items + gridDim.x;
+    TicketState ts;
+    if (threadIdx.x == 0) ts.next = atomicAdd(a.ticket, 1ull);
     for (;;) {
-        if (threadIdx.x == 0) {
-            const unsigned long long t = atomicAdd(a.ticket, 1ull);
-            const unsigned long long k = t / T;
-            int item = (int)(t - k * T);
-            if (item < a.n_items && ld_relaxed_gpu(a.err) != 0) item = a.n_items;
-            s_item = item;
-            s_epoch = (uint32_t)(k + 1);
-            s_abort = 0;
-        }
+        if (threadIdx.x == 0)
+            take_ticket(ts, a.ticket, a.n_items, T, a.err, &s_item, &s_epoch, &s_abort);
         __syncthreads();
         const int item = s_item;
-        const uint32_t epoch = s_epoch;
         if (item >= a.n_items) return;
-        const WorkItem w = a.items[item];
-        const SPDesc d = a.sp[w.sp];
-        // wait for every later pulse that writes into s's slots or into the
-        // slice of r this pulse reads
-        const uint64_t ms = __ldg(a.fmask + 2 * d.p), mr = __ldg(a.fmask + 2 * d.p + 1);
-        if (threadIdx.x == 0 && (ms | mr)) {
-            bool ok = true;
-            for (uint64_t m = ms; m && ok; m &= m - 1) {
-                const int q = __ffsll((long long)m) - 1;
-                const int sq = d.s * a.P + q;
-                ok = wait_count(a.done + sq, epoch * __ldg(a.nch + sq), a.err, a.timeout_ns, 2,
-                                w.sp, q);
-            }
-            for (uint64_t m = mr; m && ok; m &= m - 1) {
-                const int q = __ffsll((long long)m) - 1;
-                const int rq = d.r * a.P + q;
-                ok = wait_count(a.done + rq, epoch * __ldg(a.nch + rq), a.err, a.timeout_ns, 2,
-                                w.sp, q);
-            }
-            s_abort = ok ? 0 : 1;
+        const uint64_t t_take = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
+        const FItem w = a.items[item];
+        const int2* pr = a.pairs + w.off;
+        int2 sd[E];
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int i = threadIdx.x + e * kThreads;
+            sd[e] = i < w.len ? __ldg(pr + i) : make_int2(-1, -1);
         }
-        __syncthreads();
-        if (s_abort) return;
-        const int32_t* map = a.maps + d.map_off;
-        const float* halo = a.f + 3 * d.dst;
-        float* own = a.f + 3 * d.src_base;
-        const int i1 = w.start + w.len;
-        for (int b = w.start; b < i1; b += kThreads * E) {
-            int idx[E];
+        if (w.ms | w.mr) {
+            // warm L2 with the lines read after the wait (L2 is coherent, so
+            // the loads that follow the acquire still see the latest values)
 #pragma unroll
             for (int e = 0; e < E; e++) {
-                const int i = b + threadIdx.x + e * kThreads;
-                idx[e] = i < i1 ? __ldg(map + i) : -1;
-            }
-            float h[E][3], o[E][3];
-#pragma unroll
-            for (int e = 0; e < E; e++) {
-                if (idx[e] >= 0) {
-                    const float* hp = halo + 3 * (int64_t)(b + threadIdx.x + e * kThreads);
-                    const float* op = own + 3 * (int64_t)idx[e];
-                    h[e][0] = __ldcg(hp);
-                    h[e][1] = __ldcg(hp + 1);
-                    h[e][2] = __ldcg(hp + 2);
-                    o[e][0] = __ldcg(op);
-                    o[e][1] = __ldcg(op + 1);
-                    o[e][2] = __ldcg(op + 2);
+                if (sd[e].x >= 0) {
+                    prefetch_l2(a.f + 3 * (int64_t)sd[e].x);
+                    prefetch_l2(a.f + 3 * (int64_t)sd[e].y);
                 }
             }
-#pragma unroll
-            for (int e = 0; e < E; e++) {
-                if (idx[e] >= 0) {
-                    float* op = own + 3 * (int64_t)idx[e];
-                    op[0] = o[e][0] + h[e][0];
-                    op[1] = o[e][1] + h[e][1];
-                    op[2] = o[e][2] + h[e][2];
+            if (threadIdx.x == 0) {
+                const uint32_t epoch = s_epoch;
+                bool ok = true;
+                for (uint64_t m = w.ms; m && ok; m &= m - 1) {
+                    const int c = w.s_base + __ffsll((long long)m) - 1;
+                    ok = wait_count(a.done + c, epoch * __ldg(a.target + c), a.err, a.timeout_ns,
+                                    2, c);
                 }
+                for (uint64_t m = w.mr; m && ok; m &= m - 1) {
+                    const int c = w.r_base + __ffsll((long long)m) - 1;
+                    ok = wait_count(a.done + c, epoch * __ldg(a.target + c), a.err, a.timeout_ns,
+                                    2, c);
+                }
+                s_abort = ok ? 0 : 1;
+            }
+            __syncthreads();
+            if (s_abort) return;
+        }
+        const uint64_t t_wait = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
+        float h[E][3], o[E][3];
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            if (sd[e].x >= 0) {
+                const float* hp = a.f + 3 * (int64_t)sd[e].x;
+                const float* op = a.f + 3 * (int64_t)sd[e].y;
+                h[e][0] = __ldcg(hp);
+                h[e][1] = __ldcg(hp + 1);
+                h[e][2] = __ldcg(hp + 2);
+                o[e][0] = __ldcg(op);
+                o[e][1] = __ldcg(op + 1);
+                o[e][2] = __ldcg(op + 2);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            if (sd[e].x >= 0) {
+                float* op = a.f + 3 * (int64_t)sd[e].y;
+                op[0] = o[e][0] + h[e][0];
+                op[1] = o[e][1] + h[e][1];
+                op[2] = o[e][2] + h[e][2];
             }
         }
         __syncthreads();
-        if (threadIdx.x == 0) red_release_gpu_add(a.done + (int64_t)d.s * a.P + d.p, 1u);
+        if (threadIdx.x == 0) red_release_gpu_add(a.done + w.flag, 1u);
+        if (a.trace && threadIdx.x == 0) trace_item(a.trace, item, t_take, t_wait);
+    }
+}
+
+// ---- build-time kernels of the exchange plan --------------------------------------
+
+// wmax[dense slot] = last pulse whose index map names the slot (pulses are
+// launched in ascending order; within one pulse a slot appears at most once).
+__global__ void mark_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
+                            int8_t* __restrict__ wmax, int P, int p) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x)
+        wmax[d.src_base + maps[d.map_off + i]] = (int8_t)p;
+}
+
+// Stable partition of the force entries of one (s, p) into independent then
+// dependent, written as (source halo slot, destination slot) pairs.
+__global__ void __launch_bounds__(kThreads) classify_kernel(const SPDesc* __restrict__ sp,
+                                                            const int32_t* __restrict__ maps,
+                                                            const int8_t* __restrict__ wmax,
+                                                            int2* __restrict__ pairs,
+                                                            int32_t* __restrict__ nindep) {
+    __shared__ int wi[kThreads / 32], wd[kThreads / 32];
+    __shared__ int s_tot;
+    const SPDesc d = sp[blockIdx.x];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned lt = lanemask_lt();
+    int cnt = 0;
+    for (int i = threadIdx.x; i < d.send; i += kThreads) {
+        const int64_t dst = d.src_base + maps[d.map_off + i];
+        const int64_t src = d.dst + i;
+        cnt += (wmax[dst] == d.p && wmax[src] < 0) ? 1 : 0;
+    }
+    cnt = __reduce_add_sync(kFull, cnt);
+    if (lane == 0) wi[warp] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = 0;
+        for (int w = 0; w < kThreads / 32; w++) t += wi[w];
+        s_tot = t;
+        nindep[blockIdx.x] = t;
+    }
+    __syncthreads();
+    int oi = 0, od = s_tot;
+    for (int b = 0; b < d.send; b += kThreads) {
+        const int i = b + threadIdx.x;
+        bool ind = false;
+        int2 v = make_int2(0, 0);
+        const bool valid = i < d.send;
+        if (valid) {
+            const int64_t dst = d.src_base + maps[d.map_off + i];
+            const int64_t src = d.dst + i;
+            ind = wmax[dst] == d.p && wmax[src] < 0;
+            v = make_int2((int)src, (int)dst);
+        }
+        const unsigned bi = __ballot_sync(kFull, valid && ind);
+        const unsigned bd = __ballot_sync(kFull, valid && !ind);
+        __syncthreads();
+        if (lane == 0) {
+            wi[warp] = __popc(bi);
+            wd[warp] = __popc(bd);
+        }
+        __syncthreads();
+        int pi = 0, pd = 0, ti = 0, td = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; w++) {
+            pi += w < warp ? wi[w] : 0;
+            pd += w < warp ? wd[w] : 0;
+            ti += wi[w];
+            td += wd[w];
+        }
+        if (valid) {
+            const int pos = ind ? oi + pi + __popc(bi & lt) : od + pd + __popc(bd & lt);
+            pairs[d.map_off + pos] = v;
+        }
+        oi += ti;
+        od += td;
     }
 }
 
@@ -320,12 +420,11 @@ __global__ void home_gid_kernel(const int64_t* __restrict__ home_dst,
         out[home_dst[i]] = home_gid[i];
 }
 
-// Owner id of every halo slot of one pulse (items of that pulse only).
-__global__ void halo_gid_kernel(const WorkItem* __restrict__ items, const SPDesc* __restrict__ sp,
-                                const int32_t* __restrict__ maps, int32_t* out) {
-    const WorkItem w = items[blockIdx.x];
-    const SPDesc d = sp[w.sp];
-    for (int i = w.start + threadIdx.x; i < w.start + w.len; i += blockDim.x)
+// Owner id of every halo slot of one pulse.
+__global__ void halo_gid_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
+                                int32_t* out, int P, int p) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x)
         out[d.dst + i] = out[d.src_base + maps[d.map_off + i]];
 }
 
@@ -358,13 +457,15 @@ void free_exchange(halo_plan* pl) {
     dev_free(pl->d_sp);
     dev_free(pl->d_items_x);
     dev_free(pl->d_items_f);
-    dev_free(pl->d_nch);
-    dev_free(pl->d_nch_in);
-    dev_free(pl->d_own_off);
-    dev_free(pl->d_fmask);
+    dev_free(pl->d_fpairs);
+    dev_free(pl->d_wmax);
+    dev_free(pl->d_nindep);
+    dev_free(pl->d_target);
     dev_free(pl->d_flags);
     dev_free(pl->d_tickets);
     dev_free(pl->d_err);
+    pl->fpairs_cap = 0;
+    pl->wmax_cap = 0;
 }
 
 int reset_flags(halo_plan* pl, cudaStream_t st) {
@@ -378,21 +479,23 @@ int reset_flags(halo_plan* pl, cudaStream_t st) {
 
 int prepare_exchange(halo_plan* pl, cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
-    // chunk size: large chunks (more independent loads per thread) when there
-    // are enough of them to give every resident block several items
+    const size_t nsp = (size_t)nd * std::max(P, 1);
+    if (pl->n_local_total >= ((int64_t)1 << 31)) return HALO_ECAPACITY;  // int32 dense slots
+    // chunk size: large chunks (more loads in flight per thread) when there
+    // are enough of them to give every SM several items
     const int64_t H = pl->n_halo_total;
-    const int64_t resident = (int64_t)pl->num_sms * (2048 / kThreads);
     int E = 1;
-    if (H / (kThreads * 4) >= 2 * resident)
+    if (H / (kThreads * 4) >= 4 * (int64_t)pl->num_sms)
         E = 4;
-    else if (H / (kThreads * 2) >= resident)
+    else if (H / (kThreads * 2) >= 4 * (int64_t)pl->num_sms)
         E = 2;
     pl->entries_per_thread = E;
     pl->chunk = kThreads * E;
     const int CH = pl->chunk;
 
+    // per (s, p) descriptors
     pl->sp.assign((size_t)nd * P, SPDesc{});
-    std::vector<uint32_t> nch((size_t)nd * std::max(P, 1), 0), nch_in((size_t)nd * std::max(P, 1), 0);
+    pl->max_chunks.assign((size_t)std::max(P, 1), 0);
     for (int s = 0; s < nd; s++) {
         int c[3];
         grid_cells(pl, s, c);
@@ -413,57 +516,124 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
             x.p = p;
             x.shift[0] = x.shift[1] = x.shift[2] = 0.0f;
             if (c[d] == 0) x.shift[d] = pl->box[d];
-            nch[sp] = (uint32_t)((x.send + CH - 1) / CH);
-            nch_in[(size_t)r * P + p] = nch[sp];
+            pl->max_chunks[p] = std::max(pl->max_chunks[p], (x.send + kThreads - 1) / kThreads);
         }
-    }
-    std::vector<WorkItem> ix, iff;
-    pl->x_pulse_item_begin.assign((size_t)P + 1, 0);
-    for (int p = 0; p < P; p++) {
-        pl->x_pulse_item_begin[p] = (int64_t)ix.size();
-        for (int s = 0; s < nd; s++) {
-            const int sp = s * P + p;
-            for (int st0 = 0; st0 < pl->send[sp]; st0 += CH)
-                ix.push_back(WorkItem{sp, st0, std::min(CH, pl->send[sp] - st0), 0});
-        }
-    }
-    pl->x_pulse_item_begin[P] = (int64_t)ix.size();
-    for (int p = P - 1; p >= 0; p--)
-        for (int s = 0; s < nd; s++) {
-            const int sp = s * P + p;
-            for (int st0 = 0; st0 < pl->send[sp]; st0 += CH)
-                iff.push_back(WorkItem{sp, st0, std::min(CH, pl->send[sp] - st0), 0});
-        }
-    pl->n_items = (int)ix.size();
-    // force waits: (s, p) waits for (s, q) and (r, q), q > p, whose index maps
-    // can touch the same slots: pulse 0 of a later dim (its candidates include
-    // every earlier slot), and, for r, the next pulse of the same dim (its
-    // candidates are exactly this pulse's slice)
-    std::vector<uint64_t> fmask((size_t)2 * std::max(P, 1), 0);
-    for (int p = 0; p < P; p++) {
-        uint64_t ms = 0, mr = 0;
-        for (int q = p + 1; q < P; q++) {
-            if (pl->pulse_k[q] == 0) {
-                ms |= 1ull << q;
-                mr |= 1ull << q;
-            } else if (q == p + 1) {
-                mr |= 1ull << q;
-            }
-        }
-        fmask[2 * p] = ms;
-        fmask[2 * p + 1] = mr;
     }
     HALO_TRY(upload(&pl->d_sp, pl->sp));
+
+    // force-entry classification on the device: last pulse adding into each
+    // slot, then a stable independent/dependent partition per (s, p)
+    std::vector<int32_t> nindep(nsp, 0);
+    if (P > 0) {
+        if (pl->n_local_total > pl->wmax_cap) {
+            dev_free(pl->d_wmax);
+            HALO_TRY(dev_alloc(&pl->d_wmax, (size_t)pl->n_local_total));
+            pl->wmax_cap = pl->n_local_total;
+        }
+        if (pl->n_halo_total > pl->fpairs_cap || !pl->d_fpairs) {
+            dev_free(pl->d_fpairs);
+            HALO_TRY(dev_alloc(&pl->d_fpairs, (size_t)std::max<int64_t>(pl->n_halo_total, 1)));
+            pl->fpairs_cap = pl->n_halo_total;
+        }
+        dev_free(pl->d_nindep);
+        HALO_TRY(dev_alloc(&pl->d_nindep, nsp));
+        HALO_CUDA(cudaMemsetAsync(pl->d_wmax, 0xff, (size_t)pl->n_local_total, st));
+        for (int p = 0; p < P; p++) {
+            const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+            mark_kernel<<<dim3(gx, nd), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, pl->d_wmax, P, p);
+        }
+        classify_kernel<<<(unsigned)(nd * P), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, pl->d_wmax,
+                                                                  pl->d_fpairs, pl->d_nindep);
+        HALO_CUDA(cudaGetLastError());
+        HALO_CUDA(cudaMemcpyAsync(nindep.data(), pl->d_nindep, sizeof(int32_t) * nsp,
+                                  cudaMemcpyDeviceToHost, st));
+        HALO_CUDA(cudaStreamSynchronize(st));
+    }
+
+    // coordinate items: independent chunks of all pulses, then dependent ones
+    std::vector<uint32_t> target((size_t)2 * nsp, 0);
+    std::vector<XItem> ix;
+    for (int pass = 0; pass < 2; pass++)
+        for (int p = 0; p < P; p++)
+            for (int s = 0; s < nd; s++) {
+                const size_t sp = (size_t)s * P + p;
+                const SPDesc& d = pl->sp[sp];
+                const int lo = pass == 0 ? 0 : d.split, hi = pass == 0 ? d.split : d.send;
+                uint64_t mask = 0;
+                if (pass == 1)
+                    for (int q = 0; q < p; q++)
+                        if (pl->own_off[(size_t)s * (P + 1) + q + 1] > pl->own_off[(size_t)s * (P + 1) + q])
+                            mask |= 1ull << q;
+                for (int st0 = lo; st0 < hi; st0 += CH) {
+                    XItem w{};
+                    w.map_off = d.map_off + st0;
+                    w.src_base = d.src_base;
+                    w.dst = d.dst + st0;
+                    w.len = std::min(CH, hi - st0);
+                    w.flag = d.r * P + p;
+                    w.wait_base = s * P;
+                    w.wait_mask = mask;
+                    w.pad = pass;
+                    for (int e = 0; e < 3; e++) w.shift[e] = d.shift[e];
+                    ix.push_back(w);
+                    target[(size_t)d.r * P + p]++;
+                }
+            }
+    // force items: independent chunks first, then dependent ones, pulses from
+    // the last to the first.  Dependent (s, p) waits for (s, q) and (r, q), q > p,
+    // whose index maps can touch the same slots: pulse 0 of a later dim (its
+    // candidates include every earlier slot) and, on r, the next pulse of the
+    // same dim (its candidates are exactly this pulse's slice).
+    std::vector<FItem> iff;
+    std::vector<uint64_t> fms((size_t)std::max(P, 1), 0), fmr((size_t)std::max(P, 1), 0);
+    for (int p = 0; p < P; p++)
+        for (int q = p + 1; q < P; q++) {
+            if (pl->pulse_k[q] == 0) {
+                fms[p] |= 1ull << q;
+                fmr[p] |= 1ull << q;
+            } else if (q == p + 1) {
+                fmr[p] |= 1ull << q;
+            }
+        }
+    // level 0: chunks that wait for nothing (independent entries, and the
+    // dependent entries of the last pulse); then dependent chunks by pulse,
+    // last to first
+    for (int level = 0; level < 2; level++)
+        for (int p = P - 1; p >= 0; p--) {
+            const bool no_wait = (fms[p] | fmr[p]) == 0;
+            for (int s = 0; s < nd; s++) {
+                const size_t sp = (size_t)s * P + p;
+                const SPDesc& d = pl->sp[sp];
+                int lo, hi;
+                if (level == 0) {
+                    lo = 0;
+                    hi = no_wait ? d.send : nindep[sp];
+                } else {
+                    if (no_wait) continue;
+                    lo = nindep[sp];
+                    hi = d.send;
+                }
+                for (int st0 = lo; st0 < hi; st0 += CH) {
+                    FItem w{};
+                    w.off = d.map_off + st0;
+                    w.len = std::min(CH, hi - st0);
+                    w.flag = s * P + p;
+                    w.s_base = s * P;
+                    w.r_base = d.r * P;
+                    w.ms = level == 0 ? 0 : fms[p];
+                    w.mr = level == 0 ? 0 : fmr[p];
+                    iff.push_back(w);
+                    target[nsp + (size_t)s * P + p]++;
+                }
+            }
+        }
+    pl->n_items_x = (int)ix.size();
+    pl->n_items_f = (int)iff.size();
     HALO_TRY(upload(&pl->d_items_x, ix));
     HALO_TRY(upload(&pl->d_items_f, iff));
-    HALO_TRY(upload(&pl->d_nch, nch));
-    HALO_TRY(upload(&pl->d_nch_in, nch_in));
-    HALO_TRY(upload(&pl->d_own_off, pl->own_off));
-    HALO_TRY(upload(&pl->d_fmask, fmask));
-    if (!pl->d_flags || true) {
-        dev_free(pl->d_flags);
-        HALO_TRY(dev_alloc(&pl->d_flags, (size_t)2 * nd * std::max(P, 1)));
-    }
+    HALO_TRY(upload(&pl->d_target, target));
+    dev_free(pl->d_flags);
+    HALO_TRY(dev_alloc(&pl->d_flags, 2 * nsp));
     if (!pl->d_tickets) HALO_TRY(dev_alloc(&pl->d_tickets, 2));
     if (!pl->d_err) HALO_TRY(dev_alloc(&pl->d_err, 8));
     int bx = 1, bf = 1;
@@ -473,29 +643,27 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
         HALO_TRY(occupancy<2>(&bx, &bf));
     else
         HALO_TRY(occupancy<1>(&bx, &bf));
-    pl->grid_x = (int)std::min<int64_t>(pl->n_items, (int64_t)pl->num_sms * std::max(bx, 1));
-    pl->grid_f = (int)std::min<int64_t>(pl->n_items, (int64_t)pl->num_sms * std::max(bf, 1));
+    pl->grid_x = (int)std::min<int64_t>(pl->n_items_x, (int64_t)pl->num_sms * std::max(bx, 1));
+    pl->grid_f = (int)std::min<int64_t>(pl->n_items_f, (int64_t)pl->num_sms * std::max(bf, 1));
     HALO_TRY(reset_flags(pl, st));
     return cuda_code(cudaStreamSynchronize(st));
 }
 
 int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
-    if (pl->n_items == 0) return HALO_OK;
+    if (pl->n_items_x == 0) return HALO_OK;
     XArgs a;
     a.xyz = xyz;
     a.maps = pl->d_maps;
-    a.sp = pl->d_sp;
     a.items = pl->d_items_x;
-    a.own_off = pl->d_own_off;
-    a.nch_in = pl->d_nch_in;
+    a.target = pl->d_target;
     a.arrived = pl->d_flags;
     a.ticket = pl->d_tickets;
     a.err = pl->d_err;
-    a.n_items = pl->n_items;
-    a.P = pl->P;
+    a.n_items = pl->n_items_x;
     a.timeout_ns = pl->wait_timeout_ns;
-    a.drop_sp = pl->drop_sp;
-    pl->drop_sp = -1;
+    a.drop_flag = pl->drop_flag;
+    a.trace = pl->trace;
+    pl->drop_flag = -1;
     switch (pl->entries_per_thread) {
         case 4: pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a); break;
         case 2: pack_x_kernel<2><<<pl->grid_x, kThreads, 0, st>>>(a); break;
@@ -506,20 +674,19 @@ int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
 }
 
 int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
-    if (pl->n_items == 0) return HALO_OK;
+    if (pl->n_items_f == 0) return HALO_OK;
+    const size_t nsp = (size_t)pl->n_dom * std::max(pl->P, 1);
     FArgs a;
     a.f = f;
-    a.maps = pl->d_maps;
-    a.sp = pl->d_sp;
+    a.pairs = pl->d_fpairs;
     a.items = pl->d_items_f;
-    a.nch = pl->d_nch;
-    a.fmask = pl->d_fmask;
-    a.done = pl->d_flags + (size_t)pl->n_dom * pl->P;
+    a.target = pl->d_target + nsp;
+    a.done = pl->d_flags + nsp;
     a.ticket = pl->d_tickets + 1;
     a.err = pl->d_err;
-    a.n_items = pl->n_items;
-    a.P = pl->P;
+    a.n_items = pl->n_items_f;
     a.timeout_ns = pl->wait_timeout_ns;
+    a.trace = pl->trace ? pl->trace + 4 * (size_t)pl->n_items_x : nullptr;
     switch (pl->entries_per_thread) {
         case 4: unpack_f_kernel<4><<<pl->grid_f, kThreads, 0, st>>>(a); break;
         case 2: unpack_f_kernel<2><<<pl->grid_f, kThreads, 0, st>>>(a); break;
@@ -541,10 +708,9 @@ int launch_local_to_global(const halo_plan* pl, int32_t* out, cudaStream_t st) {
     const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
     home_gid_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, out);
     for (int p = 0; p < pl->P; p++) {
-        const int64_t b = pl->x_pulse_item_begin[p], e = pl->x_pulse_item_begin[p + 1];
-        if (e > b)
-            halo_gid_kernel<<<(unsigned)(e - b), 256, 0, st>>>(pl->d_items_x + b, pl->d_sp,
-                                                                pl->d_maps, out);
+        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+        halo_gid_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, out,
+                                                                   pl->P, p);
     }
     return cuda_code(cudaGetLastError());
 }

@@ -1,5 +1,5 @@
-// halo_internal.cuh -- plan structure, device-side helpers and the internal
-// entry points shared by the translation units of libhalo.so.
+// halo_internal.cuh -- plan structure and the internal entry points shared by
+// the translation units of libhalo.so.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -15,7 +15,7 @@ constexpr int kThreads = 256;          // threads per block of every kernel here
 constexpr int kHistTile = 1024;        // atoms per warp tile of the home partition
 constexpr int kScanTile = 2048;        // elements per block of the device scan
 
-// Per (sender s, pulse p) description used by both exchange kernels.
+// Per (sender s, pulse p) description (host side, and the build-time kernels).
 struct SPDesc {
     int64_t map_off;   // first entry of the index map in the plan's map array
     int64_t src_base;  // base[s]: first dense slot of the sender
@@ -27,25 +27,31 @@ struct SPDesc {
     float pad2;
 };
 
-// One unit of exchange work: a chunk of one (s, p) index map.
-struct WorkItem {
-    int32_t sp;     // s * P + p
-    int32_t start;  // first entry
-    int32_t len;    // entries
+// One chunk of coordinate work: entries [start, start+len) of one (s, p) map,
+// all independent (below depOffset) or all dependent.  Self-contained, so a
+// block needs one descriptor load per item.
+struct XItem {
+    int64_t map_off;     // index of the chunk's first map entry
+    int64_t src_base;    // dense slot of the sender's local index 0
+    int64_t dst;         // dense slot written by the chunk's first entry
+    int32_t len;
+    int32_t flag;        // counter released when done: arrived[r*P + p]
+    int32_t wait_base;   // s*P: counters of the slices s received
     int32_t pad;
+    uint64_t wait_mask;  // pulses q < p whose slices into s the entries reference
+    float shift[3];
+    int32_t pad2;
 };
 
-// Where a bounded wait gave up (debug record, read by tests through halo_status).
-struct ErrInfo {
-    int32_t code;
-    int32_t kernel;  // 1 = exchange_x, 2 = exchange_f
-    int32_t sp;
-    int32_t waited_on;
-};
-
-struct DevBuf {
-    void* p = nullptr;
-    size_t bytes = 0;
+// One chunk of force work: pairs [off, off+len) of the reordered (src, dst)
+// list; independent chunks wait for nothing.
+struct FItem {
+    int64_t off;
+    int32_t len;
+    int32_t flag;        // done[s*P + p]
+    int32_t s_base;      // s*P
+    int32_t r_base;      // r*P
+    uint64_t ms, mr;     // later pulses to wait for, on s and on r (0 for independent)
 };
 
 }  // namespace halo
@@ -69,11 +75,10 @@ struct halo_plan {
     std::vector<int32_t> n_home, n_local, send, split, own_off;  // own_off: n_dom*(P+1)
     std::vector<int64_t> base, map_off;                           // map_off: n_dom*P
     std::vector<halo::SPDesc> sp;
-    std::vector<int64_t> x_pulse_item_begin;  // first x item of each pulse (P+1)
 
-    // device memory owned by the plan
+    // device memory owned by the plan: build
     float* d_bxyz = nullptr;        // build buffer: home-compact region + halo regions
-    int64_t cap_slots = 0;          // capacity of d_bxyz in slots (and of d_maps + N)
+    int64_t cap_slots = 0;          // capacity of d_bxyz in slots (and of d_maps)
     int32_t* d_maps = nullptr;      // index maps, (pulse, sender) order
     int32_t* d_home_gid = nullptr;  // global id of each home-compact slot
     int64_t* d_home_dst = nullptr;  // dense slot of each home-compact slot
@@ -88,23 +93,28 @@ struct halo_plan {
     int build_blocks_per_domain = 1;
     float* d_thr = nullptr;         // thresholds per pulse and sender cell
 
-    // exchange
+    // device memory owned by the plan: exchange
     halo::SPDesc* d_sp = nullptr;
-    halo::WorkItem* d_items_x = nullptr;
-    halo::WorkItem* d_items_f = nullptr;
-    int n_items = 0;
+    halo::XItem* d_items_x = nullptr;
+    halo::FItem* d_items_f = nullptr;
+    int n_items_x = 0, n_items_f = 0;
+    std::vector<int32_t> max_chunks;  // per pulse: most chunks of one sender (utility grids)
     int chunk = 256;                // entries per work item
     int entries_per_thread = 1;
-    uint32_t* d_nch = nullptr;       // chunks of (s, p): n_dom*P
-    uint32_t* d_nch_in = nullptr;    // chunks delivered into (r, p): n_dom*P
-    int32_t* d_own_off = nullptr;    // n_dom*(P+1)
-    uint64_t* d_fmask = nullptr;     // 2*P: force-wait masks on s and on r
+    int2* d_fpairs = nullptr;        // (src dense slot, dst dense slot) per force entry
+    int64_t fpairs_cap = 0;
+    int8_t* d_wmax = nullptr;        // last pulse adding into each dense slot (build time)
+    int64_t wmax_cap = 0;
+    int32_t* d_nindep = nullptr;     // independent force entries of each (s, p)
+    uint32_t* d_target = nullptr;    // chunks per counter: arrived[n_dom*P] | done[n_dom*P]
     uint32_t* d_flags = nullptr;     // arrived[n_dom*P] | done[n_dom*P]
     unsigned long long* d_tickets = nullptr;  // [0] x, [1] f
-    int* d_err = nullptr;            // sticky error word + ErrInfo
+    int* d_err = nullptr;            // sticky error word + where a wait gave up
     int grid_x = 0, grid_f = 0;
     long long wait_timeout_ns = 1000000000LL;
-    int drop_sp = -1;
+    int drop_flag = -1;              // test hook: arrived counter whose release is skipped
+    unsigned long long* trace = nullptr;  // caller's trace buffer (device), or null
+    int64_t trace_cap = 0;                // its size in items
     int64_t launches_x = 0, launches_f = 0;
 };
 

@@ -65,6 +65,8 @@ SIGNATURES = {
     "halo_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_double]),
     "halo_debug_drop_signal": (ctypes.c_int, [_vp, _i32, _i32]),
     "halo_launch_counts": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
+    "halo_set_trace": (ctypes.c_int, [_vp, _vp, _i64]),
+    "halo_work_items": (ctypes.c_int, [_vp, _P(_i32), _P(_i32), _P(_i32)]),
     "halo_destroy": (None, [_vp]),
     "halo_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -271,6 +273,19 @@ class HaloPlan:
         _check(self._lib.halo_launch_counts(self._h, ctypes.byref(x), ctypes.byref(f)),
                "halo_launch_counts")
         return x.value, f.value
+
+    def work_items(self):
+        x, f, c = _i32(), _i32(), _i32()
+        _check(self._lib.halo_work_items(self._h, ctypes.byref(x), ctypes.byref(f), ctypes.byref(c)),
+               "halo_work_items")
+        return x.value, f.value, c.value
+
+    def set_trace(self, buf=None):
+        """Arm (buf: int64 CUDA tensor of 4*(x_items+f_items) words) or disarm tracing."""
+        if buf is None:
+            _check(self._lib.halo_set_trace(self._h, None, 0), "halo_set_trace")
+            return
+        _check(self._lib.halo_set_trace(self._h, _dev_ptr(buf), buf.numel() // 4), "halo_set_trace")
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -157,6 +157,17 @@ int halo_set_wait_timeout(halo_plan* plan, double seconds);
  * reports HALO_ETIMEOUT through halo_status().  (-1, -1) disarms. */
 int halo_debug_drop_signal(halo_plan* plan, int32_t domain, int32_t pulse);
 
+/* Tracing (optional).  trace: device buffer of 4 * capacity_items uint64
+ * words, caller-owned; capacity_items >= x_items + f_items of
+ * halo_work_items().  While armed, every work item of both exchange kernels
+ * records {time it was taken, time its waits ended, time it released its
+ * signal (global timer, ns), SM id}: coordinate items at [0, x_items), force
+ * items after them.  NULL disarms; a rebuild disarms.  For diagnosis only. */
+int halo_set_trace(halo_plan* plan, uint64_t* trace, int64_t capacity_items);
+
+/* Work decomposition of the exchanges (host): items per kernel, entries per item. */
+int halo_work_items(const halo_plan* plan, int32_t* x_items, int32_t* f_items, int32_t* chunk);
+
 /* Kernel launches made so far by halo_exchange_x and halo_exchange_f (host). */
 int halo_launch_counts(const halo_plan* plan, int64_t* x_launches, int64_t* f_launches);
 
