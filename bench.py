@@ -305,6 +305,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mode", default="fused", choices=["fused", "stepwise", "flat"],
+                    help="exchange mode of the headline value; every mode is also reported")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -334,13 +336,22 @@ def main():
 
     w, xyz, dom, x, plan, loc, f0 = setup_workload(args.workload, device)
     flush, flush_bytes = make_flush(device)
-    f = f0.clone()
-    sampler = ClockSampler(gpu_index(local))
-    xs, fs, wall, clocks, launches = time_steps(plan, loc, f, args.steps, args.warmup, flush,
-                                                stream, sampler, barrier)
-    code = plan.status()
-    if code != 0:
-        raise SystemExit("device error %d during the timed region" % code)
+    modes = ["fused", "stepwise", "flat"]
+    others = {}
+    for mode in [m for m in modes if m != args.mode] + [args.mode]:
+        plan.set_mode(mode)
+        f = f0.clone()
+        sampler = ClockSampler(gpu_index(local)) if mode == args.mode else None
+        steps = args.steps if mode == args.mode else min(args.steps, 500)
+        xs, fs, wall, clocks, launches = time_steps(plan, loc, f, steps, args.warmup, flush,
+                                                    stream, sampler, barrier)
+        code = plan.status()
+        if code != 0:
+            raise SystemExit("device error %d during the timed region" % code)
+        if mode != args.mode:
+            others[mode] = {"us_per_exchange": 1e3 * statistics.fmean(a + b for a, b in zip(xs, fs)),
+                            "us_x": 1e3 * statistics.fmean(xs), "us_f": 1e3 * statistics.fmean(fs),
+                            "launches_per_step": launches / steps}
     step_ms = statistics.fmean(a + b for a, b in zip(xs, fs))
     x_ms, f_ms = statistics.fmean(xs), statistics.fmean(fs)
     if dist:
@@ -349,25 +360,33 @@ def main():
         step_ms, x_ms, f_ms = [float(v) for v in t.tolist()]
     halo_slots = plan.n_halo_total
     value = world * halo_slots / (step_ms * 1e-3)
+    for m in others.values():
+        m["value"] = world * halo_slots / (m["us_per_exchange"] * 1e-6)
+        m["hbm_frac"] = (BYTES_X + BYTES_F) * halo_slots / (m["us_per_exchange"] * 1e-6) / 1e9 \
+            / measured_peak()[0]
     peak, peak_kind = measured_peak()
-    dom_kernel, dom_ms, per_slot = (("unpack_f_kernel", f_ms, BYTES_F) if f_ms >= x_ms
-                                    else ("pack_x_kernel", x_ms, BYTES_X))
+    kname = {"fused": ("unpack_f_kernel", "pack_x_kernel"), "stepwise": ("step_f_kernel", "step_x_kernel"),
+             "flat": ("flat_f_kernel", "flat_x_kernel")}[args.mode]
+    dom_kernel, dom_ms, per_slot = ((kname[0], f_ms, BYTES_F) if f_ms >= x_ms
+                                    else (kname[1], x_ms, BYTES_X))
     achieved = per_slot * halo_slots / (dom_ms * 1e-3) / 1e9
     traffic = recorded_traffic(dom_kernel, args.workload)
     alg_gbs = (BYTES_X + BYTES_F) * halo_slots / (step_ms * 1e-3) / 1e9
 
-    # latency case: the multi-pulse system, one launch per direction
+    # latency case: the multi-pulse system, every mode
     lw, lxyz, ldom, lx, lplan, lloc, lf0 = setup_workload(LATENCY_WORKLOAD, device)
-    lf = lf0.clone()
-    lxs, lfs, _, _, llaunch = time_steps(lplan, lloc, lf, min(args.steps, 1000), args.warmup,
-                                         flush, stream)
-    assert lplan.status() == 0
-    lat_us = 1e3 * statistics.fmean(a + b for a, b in zip(lxs, lfs))
-    lat = {"workload": LATENCY_WORKLOAD, "us_per_exchange": lat_us,
-           "us_x": 1e3 * statistics.fmean(lxs), "us_f": 1e3 * statistics.fmean(lfs),
-           "launches_per_direction": llaunch / (2 * min(args.steps, 1000)),
-           "halo_slots": lplan.n_halo_total, "pulses": lplan.n_pulses}
+    lat = {"workload": LATENCY_WORKLOAD, "halo_slots": lplan.n_halo_total, "pulses": lplan.n_pulses}
+    lsteps = min(args.steps, 1000)
+    for mode in modes:
+        lplan.set_mode(mode)
+        lf = lf0.clone()
+        lxs, lfs, _, _, llaunch = time_steps(lplan, lloc, lf, lsteps, args.warmup, flush, stream)
+        assert lplan.status() == 0
+        lat[mode] = {"us_per_exchange": 1e3 * statistics.fmean(a + b for a, b in zip(lxs, lfs)),
+                     "us_x": 1e3 * statistics.fmean(lxs), "us_f": 1e3 * statistics.fmean(lfs),
+                     "launches_per_direction": llaunch / (2 * lsteps)}
     lplan.close()
+    plan.set_mode(args.mode)
 
     # end to end through the public API with host buffers
     e2e_ms, h2d, d2h = e2e_steps(w, xyz, plan, max(20, min(args.steps, 200)), 5, device, stream)
@@ -388,7 +407,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": args.workload, "n_atoms": w.n_atoms, "grid": list(w.grid),
+            "config": {"workload": args.workload, "mode": args.mode, "n_atoms": w.n_atoms,
+                       "grid": list(w.grid),
                        "box_nm": list(w.box), "rc_nm": w.rc, "pulses": plan.n_pulses,
                        "halo_slots": halo_slots, "parallelism": "replicas" if world > 1 else "1 GPU",
                        "l2": "flushed between steps (%d MB written+read)" % (flush_bytes >> 20)},
@@ -399,6 +419,7 @@ def main():
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": per_slot * halo_slots},
+            "other_modes": others,
             "latency_case": lat,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms},

@@ -79,6 +79,7 @@ void destroy_plan(halo_plan* pl) {
     {
         DeviceGuard g(pl->dev);
         halo::free_exchange(pl);
+        halo::free_flat(pl);
         halo::free_build(pl);
     }
     delete pl;
@@ -88,8 +89,11 @@ int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, 
     const cudaStream_t st = as_stream(stream);
     pl->trace = nullptr;  // item counts change with the plan: the caller re-arms tracing
     pl->trace_cap = 0;
+    halo::free_flat(pl);  // the flattened tables describe the previous plan
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
-    return halo::prepare_exchange(pl, st);
+    HALO_TRY(halo::prepare_exchange(pl, st));
+    if (pl->mode == HALO_MODE_FLAT) return halo::prepare_flat(pl, st);
+    return HALO_OK;
 }
 
 }  // namespace
@@ -215,13 +219,21 @@ int halo_load_home(const halo_plan* pl, const float* global_xyz, float* local_xy
 int halo_exchange_x(halo_plan* pl, float* local_coords, void* stream) {
     if (!pl || !local_coords) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
-    return halo::launch_exchange_x(pl, local_coords, as_stream(stream));
+    switch (pl->mode) {
+        case HALO_MODE_STEPWISE: return halo::launch_stepwise_x(pl, local_coords, as_stream(stream));
+        case HALO_MODE_FLAT: return halo::launch_flat_x(pl, local_coords, as_stream(stream));
+        default: return halo::launch_exchange_x(pl, local_coords, as_stream(stream));
+    }
 }
 
 int halo_exchange_f(halo_plan* pl, float* local_forces, void* stream) {
     if (!pl || !local_forces) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
-    return halo::launch_exchange_f(pl, local_forces, as_stream(stream));
+    switch (pl->mode) {
+        case HALO_MODE_STEPWISE: return halo::launch_stepwise_f(pl, local_forces, as_stream(stream));
+        case HALO_MODE_FLAT: return halo::launch_flat_f(pl, local_forces, as_stream(stream));
+        default: return halo::launch_exchange_f(pl, local_forces, as_stream(stream));
+    }
 }
 
 int halo_status(halo_plan* pl, void* stream) {
@@ -254,6 +266,28 @@ int halo_debug_drop_signal(halo_plan* pl, int32_t domain, int32_t pulse) {
     if (domain < 0 || domain >= pl->n_dom || pulse < 0 || pulse >= pl->P) return HALO_EINVAL;
     // the counter the producer (domain, pulse) releases: arrived[r*P + pulse]
     pl->drop_flag = pl->sp[(size_t)domain * pl->P + pulse].r * pl->P + pulse;
+    return HALO_OK;
+}
+
+int halo_set_mode(halo_plan* pl, int32_t mode, void* stream) {
+    if (!pl) return HALO_EINVAL;
+    if (mode != HALO_MODE_FUSED && mode != HALO_MODE_STEPWISE && mode != HALO_MODE_FLAT)
+        return HALO_EINVAL;
+    DeviceGuard g(pl->dev);
+    if (mode == HALO_MODE_FLAT && !pl->flat_ready) {
+        try {
+            HALO_TRY(halo::prepare_flat(pl, as_stream(stream)));
+        } catch (const std::bad_alloc&) {
+            return HALO_ENOMEM;
+        }
+    }
+    pl->mode = mode;
+    return HALO_OK;
+}
+
+int halo_get_mode(const halo_plan* pl, int32_t* mode) {
+    if (!pl || !mode) return HALO_EINVAL;
+    *mode = pl->mode;
     return HALO_OK;
 }
 

@@ -233,16 +233,6 @@ __global__ void scan_down_kernel(const int32_t* __restrict__ in, int32_t* __rest
     }
 }
 
-int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
-                          cudaStream_t st) {
-    const int64_t nb = (n + kScanTile - 1) / kScanTile;
-    if (nb == 0) return HALO_OK;
-    scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, n, tmp);
-    scan_top_kernel<<<1, 1024, 0, st>>>(tmp, nb);
-    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp);
-    return cuda_code(cudaGetLastError());
-}
-
 // Per-domain home counts and starts from the scanned tile offsets; pulse state init.
 __global__ void home_meta_kernel(const int32_t* __restrict__ offs, int64_t ntiles, int64_t n,
                                  int nd, int P, Meta m) {
@@ -452,6 +442,16 @@ int grow(float** p, int64_t* cap_have, int64_t need_slots) {
 }
 
 }  // namespace
+
+int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
+                          cudaStream_t st) {
+    const int64_t nb = (n + kScanTile - 1) / kScanTile;
+    if (nb == 0) return HALO_OK;
+    scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, n, tmp);
+    scan_top_kernel<<<1, 1024, 0, st>>>(tmp, nb);
+    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp);
+    return cuda_code(cudaGetLastError());
+}
 
 void free_build(halo_plan* pl) {
     dev_free(pl->d_bxyz);

@@ -116,6 +116,18 @@ struct halo_plan {
     unsigned long long* trace = nullptr;  // caller's trace buffer (device), or null
     int64_t trace_cap = 0;                // its size in items
     int64_t launches_x = 0, launches_f = 0;
+
+    // exchange mode (HALO_MODE_*) and the flattened exchange's tables
+    int mode = 0;
+    bool flat_ready = false;
+    int32_t* d_xflat = nullptr;      // per halo slot: owner dense slot | shift bits << 29
+    int4* d_xflat_items = nullptr;   // {flat halo index, dense slot, len, 0} per chunk
+    int n_xflat_items = 0;
+    int32_t* d_fown = nullptr;       // owners with copies: home dense slot
+    int32_t* d_fstart = nullptr;     // n_owners + 1 entry offsets
+    int32_t* d_fent = nullptr;       // per copy, in reduction order: node slot | parent << 26
+    int64_t n_owners = 0;
+    int max_copies = 0;
 };
 
 namespace halo {
@@ -123,6 +135,17 @@ namespace halo {
 // halo_build.cu
 int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n_atoms,
                cudaStream_t st);
+
+int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
+                          cudaStream_t st);  // scratch tmp: ceil(n / kScanTile) ints
+
+// halo_modes.cu: one launch per pulse, and the flattened exchange
+int prepare_flat(halo_plan* pl, cudaStream_t st);
+void free_flat(halo_plan* pl);
+int launch_stepwise_x(halo_plan* pl, float* xyz, cudaStream_t st);
+int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st);
+int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st);
+int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st);
 
 // halo_exchange.cu
 int prepare_exchange(halo_plan* pl, cudaStream_t st);

@@ -1,0 +1,480 @@
+// halo_modes.cu -- two more ways to run the same exchange on one GPU.
+//
+// STEPWISE: one kernel launch per pulse and direction, in pulse order for
+// coordinates and reverse pulse order for forces, ordered by the stream alone.
+// This is the shape of the GPU-aware-MPI schedule the page "GPU-Initiated Halo
+// Exchange Cuts CPU Bottlenecks in GROMACS" describes (section "The CPU
+// bottleneck in halo exchange": a pack kernel per pulse, pulses chained Z -> Y
+// -> X) and of the first fused design ("Fusing pack, put, and wait into one
+// kernel": one kernel per pulse, stream-ordered), without the MPI transfers that
+// one GPU does not need.
+//
+// FLAT: because every domain lives in the same HBM, each halo slot's forwarding
+// chain (page "Redesigning GROMACS Halo Exchange ...", section 3: eighth-shell
+// forwarding through intermediate domains) can be composed once at build time:
+//   coordinates: slot = owner's home coordinate + (L_d on every component d
+//     whose chain crossed the periodic boundary) -- one fp32 add per
+//     component, as in the chained exchange, because a chain crosses each
+//     boundary at most once (p_d < n_d) and adds 0 to the other components;
+//   forces: the copies of one owner atom form a tree (each copy's parent is the
+//     slot it was received from); the chained reduction (Algorithm 6, last
+//     pulse first) adds every child into its parent after the child has
+//     received all of its own children, children of one parent in decreasing
+//     pulse order.  Visiting an owner's copies in decreasing order of the pulse
+//     that created them, and adding each into its parent, performs exactly the
+//     same fp32 additions in the same order, so the results (owners and
+//     intermediate halo slots) are bit-identical.
+// Both passes then have no waits and no cross-block dependencies.
+#include <algorithm>
+#include <vector>
+
+#include "halo_internal.cuh"
+
+namespace halo {
+namespace {
+
+constexpr int kFlatChunk = 1024;          // halo slots per coordinate item
+constexpr int kNodeBits = 26;             // entry = node slot | parent position << 26
+constexpr int32_t kNodeMask = (1 << kNodeBits) - 1;
+constexpr int kMaxCopies = 63;            // parent positions fit in 6 bits
+
+// ---- stepwise ----------------------------------------------------------------
+__global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
+                              float* xyz, int P, int p) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
+        const float* s = xyz + 3 * (d.src_base + maps[d.map_off + i]);
+        float* q = xyz + 3 * (d.dst + i);
+        const float v0 = s[0], v1 = s[1], v2 = s[2];
+        q[0] = v0 + d.shift[0];
+        q[1] = v1 + d.shift[1];
+        q[2] = v2 + d.shift[2];
+    }
+}
+
+__global__ void step_f_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
+                              float* f, int P, int p) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
+        const float* h = f + 3 * (d.dst + i);
+        float* o = f + 3 * (d.src_base + maps[d.map_off + i]);
+        const float h0 = h[0], h1 = h[1], h2 = h[2];
+        o[0] = o[0] + h0;
+        o[1] = o[1] + h1;
+        o[2] = o[2] + h2;
+    }
+}
+
+// ---- flat: build-time composition of the chains -------------------------------
+__global__ void chain_init_kernel(int32_t* owner, int32_t* parent, int8_t* hop, int8_t* code,
+                                  int64_t n) {
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        owner[j] = (int32_t)j;
+        parent[j] = -1;
+        hop[j] = -1;
+        code[j] = 0;
+    }
+}
+
+// Pulse p, in ascending order: every received slot inherits its source's owner
+// and boundary crossings, and remembers its source (parent) and pulse.
+__global__ void chain_pulse_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
+                                   int32_t* owner, int32_t* parent, int8_t* hop, int8_t* code,
+                                   int P, int p, int dim) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    const int8_t bit = d.shift[dim] != 0.0f ? (int8_t)(1 << dim) : (int8_t)0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
+        const int64_t h = d.dst + i;
+        const int64_t src = d.src_base + maps[d.map_off + i];
+        owner[h] = owner[src];
+        parent[h] = (int32_t)src;
+        hop[h] = (int8_t)p;
+        code[h] = (int8_t)(code[src] | bit);
+    }
+}
+
+// Coordinate table over halo slots; also counts the copies of every owner.
+__global__ void xflat_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
+                             const int8_t* __restrict__ code, int32_t* __restrict__ xflat,
+                             int32_t* __restrict__ ncopies) {
+    const int4 it = items[blockIdx.x];
+    for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
+        const int64_t j = (int64_t)it.y + i;
+        const int32_t o = owner[j];
+        xflat[(int64_t)it.x + i] = o | ((int32_t)code[j] << 29);
+        atomicAdd(ncopies + o, 1);
+    }
+}
+
+__global__ void owner_flag_kernel(const int32_t* __restrict__ ncopies, int32_t* __restrict__ flag,
+                                  int64_t n) {
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x)
+        flag[j] = ncopies[j] > 0 ? 1 : 0;
+}
+
+__global__ void owner_list_kernel(const int32_t* __restrict__ ncopies,
+                                  const int32_t* __restrict__ entry_pos,
+                                  const int32_t* __restrict__ owner_idx, int64_t n, int32_t* fown,
+                                  int32_t* fstart) {
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x)
+        if (ncopies[j] > 0) {
+            fown[owner_idx[j]] = (int32_t)j;
+            fstart[owner_idx[j]] = entry_pos[j];
+        }
+}
+
+__global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
+                                  const int32_t* __restrict__ entry_pos, int32_t* fillc,
+                                  int32_t* __restrict__ tmp) {
+    const int4 it = items[blockIdx.x];
+    for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
+        const int64_t j = (int64_t)it.y + i;
+        const int32_t o = owner[j];
+        tmp[entry_pos[o] + atomicAdd(fillc + o, 1)] = (int32_t)j;
+    }
+}
+
+// Per owner: order its copies by decreasing creating pulse (ties by slot) and
+// replace each copy's parent slot by the parent's position (0 = the owner).
+__global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
+                                  const int32_t* __restrict__ tmp, const int32_t* __restrict__ parent,
+                                  const int8_t* __restrict__ hop, int64_t n_owners,
+                                  int32_t* __restrict__ fent, int* max_copies, int* err) {
+    __shared__ int block_max;
+    if (threadIdx.x == 0) block_max = 0;
+    __syncthreads();
+    int my_max = 0;
+    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
+         m += (int64_t)gridDim.x * blockDim.x) {
+        const int s0 = fstart[m], k = fstart[m + 1] - s0;
+        my_max = max(my_max, k);
+        if (k > kMaxCopies) {
+            atomicCAS(err, 0, HALO_ECAPACITY);
+            continue;
+        }
+        int32_t node[kMaxCopies];
+        int8_t hp[kMaxCopies];
+        for (int j = 0; j < k; j++) {
+            const int32_t v = tmp[s0 + j];
+            int8_t hv = hop[v];
+            int i = j;
+            while (i > 0 && (hp[i - 1] < hv || (hp[i - 1] == hv && node[i - 1] > v))) {
+                node[i] = node[i - 1];
+                hp[i] = hp[i - 1];
+                i--;
+            }
+            node[i] = v;
+            hp[i] = hv;
+        }
+        const int32_t home = fown[m];
+        for (int j = 0; j < k; j++) {
+            const int32_t ps = parent[node[j]];
+            int pos = 0;
+            if (ps != home) {
+                for (int q = j + 1; q < k; q++)
+                    if (node[q] == ps) {
+                        pos = q + 1;
+                        break;
+                    }
+                if (pos == 0) atomicCAS(err, 0, HALO_ECAPACITY);  // parent not among the copies
+            }
+            fent[s0 + j] = node[j] | (pos << kNodeBits);
+        }
+    }
+    atomicMax(&block_max, my_max);
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(max_copies, block_max);
+}
+
+// ---- flat: the exchanges ------------------------------------------------------------
+template <int E>
+__global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int32_t* __restrict__ xflat,
+                                                          const int4* __restrict__ items, float L0,
+                                                          float L1, float L2) {
+    const int4 it = items[blockIdx.x];
+    int32_t v[E];
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        const int i = threadIdx.x + e * kThreads;
+        v[e] = i < it.z ? __ldg(xflat + it.x + i) : 0;
+    }
+    float a[E][3];
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        if (threadIdx.x + e * kThreads < it.z) {
+            // owners are home slots, never written by this kernel
+            const float* s = xyz + 3 * (int64_t)(v[e] & ((1 << 29) - 1));
+            a[e][0] = __ldg(s);
+            a[e][1] = __ldg(s + 1);
+            a[e][2] = __ldg(s + 2);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        const int i = threadIdx.x + e * kThreads;
+        if (i < it.z) {
+            const unsigned c = (unsigned)v[e] >> 29;
+            float* q = xyz + 3 * ((int64_t)it.y + i);
+            q[0] = a[e][0] + ((c & 1u) ? L0 : 0.0f);
+            q[1] = a[e][1] + ((c & 2u) ? L1 : 0.0f);
+            q[2] = a[e][2] + ((c & 4u) ? L2 : 0.0f);
+        }
+    }
+}
+
+// One thread per owner with copies.  KR: copies kept in registers; owners
+// with more copies take the sequential path through memory (same order).
+template <int KR>
+__global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int32_t* __restrict__ fown,
+                                                          const int32_t* __restrict__ fstart,
+                                                          const int32_t* __restrict__ fent,
+                                                          int64_t n_owners) {
+    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
+         m += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t home = __ldg(fown + m);
+        const int s0 = __ldg(fstart + m), k = __ldg(fstart + m + 1) - s0;
+        float* fh = f + 3 * (int64_t)home;
+        if (k <= KR) {
+            int32_t ent[KR];
+#pragma unroll
+            for (int j = 0; j < KR; j++) ent[j] = j < k ? __ldg(fent + s0 + j) : 0;
+            float c0[3] = {fh[0], fh[1], fh[2]};
+            float c[KR][3];
+#pragma unroll
+            for (int j = 0; j < KR; j++) {
+                if (j < k) {
+                    const float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
+                    c[j][0] = fn[0];
+                    c[j][1] = fn[1];
+                    c[j][2] = fn[2];
+                }
+            }
+            // finalize the copies in order: copy q receives its children (all
+            // earlier in the order) in ascending position, then the owner
+            // receives its children; every accumulator sees the same adds in
+            // the same order as the chained reduction
+            int par[KR];
+#pragma unroll
+            for (int j = 0; j < KR; j++) par[j] = j < k ? (int)((unsigned)ent[j] >> kNodeBits) : -1;
+            unsigned has_child = 0;
+#pragma unroll
+            for (int q = 1; q < KR; q++) {
+#pragma unroll
+                for (int j = 0; j < q; j++) {
+                    if (par[j] == q + 1) {
+                        c[q][0] = c[q][0] + c[j][0];
+                        c[q][1] = c[q][1] + c[j][1];
+                        c[q][2] = c[q][2] + c[j][2];
+                        has_child |= 1u << q;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < KR; j++) {
+                if (par[j] == 0) {
+                    c0[0] = c0[0] + c[j][0];
+                    c0[1] = c0[1] + c[j][1];
+                    c0[2] = c0[2] + c[j][2];
+                }
+            }
+            fh[0] = c0[0];
+            fh[1] = c0[1];
+            fh[2] = c0[2];
+#pragma unroll
+            for (int j = 0; j < KR; j++) {
+                if (j < k && (has_child >> j & 1u)) {
+                    float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
+                    fn[0] = c[j][0];
+                    fn[1] = c[j][1];
+                    fn[2] = c[j][2];
+                }
+            }
+        } else {
+            // every slot of this tree belongs to this thread alone: plain
+            // sequential read-modify-write in the same order
+            for (int j = 0; j < k; j++) {
+                const int32_t e = __ldg(fent + s0 + j);
+                const int par = (int)((unsigned)e >> kNodeBits);
+                const float* fn = f + 3 * (int64_t)(e & kNodeMask);
+                float* fp = par == 0 ? fh : f + 3 * (int64_t)(__ldg(fent + s0 + par - 1) & kNodeMask);
+                const float n0 = __ldcg(fn), n1 = __ldcg(fn + 1), n2 = __ldcg(fn + 2);
+                __stcg(fp, __ldcg(fp) + n0);
+                __stcg(fp + 1, __ldcg(fp + 1) + n1);
+                __stcg(fp + 2, __ldcg(fp + 2) + n2);
+            }
+        }
+    }
+}
+
+int blocks_for(int64_t n, int num_sms) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>((n + kThreads - 1) / kThreads,
+                                                       (int64_t)num_sms * 16));
+}
+
+}  // namespace
+
+void free_flat(halo_plan* pl) {
+    dev_free(pl->d_xflat);
+    dev_free(pl->d_xflat_items);
+    dev_free(pl->d_fown);
+    dev_free(pl->d_fstart);
+    dev_free(pl->d_fent);
+    pl->flat_ready = false;
+    pl->n_xflat_items = 0;
+    pl->n_owners = 0;
+    pl->max_copies = 0;
+}
+
+int prepare_flat(halo_plan* pl, cudaStream_t st) {
+    free_flat(pl);
+    const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
+    const int nd = pl->n_dom, P = pl->P;
+    if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
+    // coordinate items: halo range of every domain, in chunks
+    std::vector<int4> items;
+    int64_t k = 0;
+    for (int D = 0; D < nd; D++) {
+        const int64_t d0 = pl->base[D] + pl->n_home[D];
+        const int64_t nh = (int64_t)pl->n_local[D] - pl->n_home[D];
+        for (int64_t i = 0; i < nh; i += kFlatChunk)
+            items.push_back(make_int4((int)(k + i), (int)(d0 + i),
+                                      (int)std::min<int64_t>(kFlatChunk, nh - i), 0));
+        k += nh;
+    }
+    pl->n_xflat_items = (int)items.size();
+    HALO_TRY(dev_alloc(&pl->d_xflat_items, items.size()));
+    if (!items.empty())
+        HALO_CUDA(cudaMemcpy(pl->d_xflat_items, items.data(), items.size() * sizeof(int4),
+                             cudaMemcpyHostToDevice));
+    HALO_TRY(dev_alloc(&pl->d_xflat, (size_t)std::max<int64_t>(H, 1)));
+    HALO_TRY(dev_alloc(&pl->d_fent, (size_t)std::max<int64_t>(H, 1)));
+
+    // scratch for the build of the tables
+    int32_t *owner = nullptr, *parent = nullptr, *ncopies = nullptr, *entry_pos = nullptr,
+            *flag = nullptr, *owner_idx = nullptr, *tmp = nullptr, *scan_tmp = nullptr, *misc = nullptr;
+    int8_t *hop = nullptr, *code = nullptr;
+    int rc = HALO_OK;
+    auto cleanup = [&]() {
+        dev_free(owner);
+        dev_free(parent);
+        dev_free(ncopies);
+        dev_free(entry_pos);
+        dev_free(flag);
+        dev_free(owner_idx);
+        dev_free(tmp);
+        dev_free(scan_tmp);
+        dev_free(misc);
+        dev_free(hop);
+        dev_free(code);
+    };
+    do {
+        if ((rc = dev_alloc(&owner, (size_t)nl)) != HALO_OK) break;
+        if ((rc = dev_alloc(&parent, (size_t)nl)) != HALO_OK) break;
+        if ((rc = dev_alloc(&ncopies, (size_t)nl)) != HALO_OK) break;
+        if ((rc = dev_alloc(&entry_pos, (size_t)nl)) != HALO_OK) break;
+        if ((rc = dev_alloc(&flag, (size_t)nl)) != HALO_OK) break;
+        if ((rc = dev_alloc(&owner_idx, (size_t)nl)) != HALO_OK) break;
+        if ((rc = dev_alloc(&tmp, (size_t)std::max<int64_t>(H, 1))) != HALO_OK) break;
+        if ((rc = dev_alloc(&scan_tmp, (size_t)(nl / kScanTile + 2))) != HALO_OK) break;
+        if ((rc = dev_alloc(&misc, 4)) != HALO_OK) break;
+        if ((rc = dev_alloc(&hop, (size_t)nl)) != HALO_OK) break;
+        if ((rc = dev_alloc(&code, (size_t)nl)) != HALO_OK) break;
+        const int gb = blocks_for(nl, pl->num_sms);
+        chain_init_kernel<<<gb, kThreads, 0, st>>>(owner, parent, hop, code, nl);
+        for (int p = 0; p < P; p++) {
+            const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+            chain_pulse_kernel<<<dim3(gx, nd), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, owner, parent,
+                                                                  hop, code, P, p, pl->pulse_dim[p]);
+        }
+        if ((rc = cuda_code(cudaMemsetAsync(ncopies, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
+        if (!items.empty())
+            xflat_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
+                                                                       pl->d_xflat, ncopies);
+        if ((rc = device_exclusive_scan(ncopies, entry_pos, nl, scan_tmp, st)) != HALO_OK) break;
+        owner_flag_kernel<<<gb, kThreads, 0, st>>>(ncopies, flag, nl);
+        if ((rc = device_exclusive_scan(flag, owner_idx, nl, scan_tmp, st)) != HALO_OK) break;
+        int32_t last[4] = {0, 0, 0, 0};
+        if ((rc = cuda_code(cudaMemcpyAsync(last, owner_idx + nl - 1, sizeof(int32_t),
+                                            cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
+        if ((rc = cuda_code(cudaMemcpyAsync(last + 1, flag + nl - 1, sizeof(int32_t),
+                                            cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
+        if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
+        const int64_t n_owners = (int64_t)last[0] + last[1];
+        pl->n_owners = n_owners;
+        if ((rc = dev_alloc(&pl->d_fown, (size_t)std::max<int64_t>(n_owners, 1))) != HALO_OK) break;
+        if ((rc = dev_alloc(&pl->d_fstart, (size_t)n_owners + 1)) != HALO_OK) break;
+        owner_list_kernel<<<gb, kThreads, 0, st>>>(ncopies, entry_pos, owner_idx, nl, pl->d_fown,
+                                                   pl->d_fstart);
+        const int32_t Hi = (int32_t)H;
+        if ((rc = cuda_code(cudaMemcpyAsync(pl->d_fstart + n_owners, &Hi, sizeof(int32_t),
+                                            cudaMemcpyHostToDevice, st))) != HALO_OK) break;
+        if ((rc = cuda_code(cudaMemsetAsync(flag, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
+        if (!items.empty())
+            owner_fill_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner,
+                                                                            entry_pos, flag, tmp);
+        if ((rc = cuda_code(cudaMemsetAsync(misc, 0, sizeof(int32_t) * 4, st))) != HALO_OK) break;
+        if (n_owners > 0)
+            owner_sort_kernel<<<blocks_for(n_owners, pl->num_sms), kThreads, 0, st>>>(
+                pl->d_fown, pl->d_fstart, tmp, parent, hop, n_owners, pl->d_fent, misc, misc + 1);
+        int32_t info[2] = {0, 0};
+        if ((rc = cuda_code(cudaMemcpyAsync(info, misc, sizeof(info), cudaMemcpyDeviceToHost, st))) !=
+            HALO_OK)
+            break;
+        if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
+        if ((rc = cuda_code(cudaGetLastError())) != HALO_OK) break;
+        if (info[1] != 0) {
+            rc = HALO_ECAPACITY;
+            break;
+        }
+        pl->max_copies = info[0];
+    } while (false);
+    cleanup();
+    if (rc != HALO_OK) {
+        free_flat(pl);
+        return rc;
+    }
+    pl->flat_ready = true;
+    return HALO_OK;
+}
+
+int launch_stepwise_x(halo_plan* pl, float* xyz, cudaStream_t st) {
+    for (int p = 0; p < pl->P; p++) {
+        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+        step_x_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, xyz, pl->P, p);
+        pl->launches_x++;
+    }
+    return cuda_code(cudaGetLastError());
+}
+
+int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st) {
+    for (int p = pl->P - 1; p >= 0; p--) {
+        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+        step_f_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, f, pl->P, p);
+        pl->launches_f++;
+    }
+    return cuda_code(cudaGetLastError());
+}
+
+int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
+    if (pl->n_xflat_items == 0) return HALO_OK;
+    flat_x_kernel<kFlatChunk / kThreads><<<pl->n_xflat_items, kThreads, 0, st>>>(
+        xyz, pl->d_xflat, pl->d_xflat_items, pl->box[0], pl->box[1], pl->box[2]);
+    pl->launches_x++;
+    return cuda_code(cudaGetLastError());
+}
+
+int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
+    if (pl->n_owners == 0) return HALO_OK;
+    const int gb = blocks_for(pl->n_owners, pl->num_sms);
+    if (pl->max_copies <= 8)
+        flat_f_kernel<8><<<gb, kThreads, 0, st>>>(f, pl->d_fown, pl->d_fstart, pl->d_fent, pl->n_owners);
+    else
+        flat_f_kernel<16><<<gb, kThreads, 0, st>>>(f, pl->d_fown, pl->d_fstart, pl->d_fent, pl->n_owners);
+    pl->launches_f++;
+    return cuda_code(cudaGetLastError());
+}
+
+}  // namespace halo

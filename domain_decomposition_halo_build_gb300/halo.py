@@ -21,6 +21,8 @@ LIBRARY = os.path.join(_PKG, "libhalo.so")
 OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM = (
     0, -1, -2, -3, -4, -5, -6, -7, -8)
 MAX_PULSES = 64
+MODE_FUSED, MODE_STEPWISE, MODE_FLAT = 0, 1, 2
+MODES = {"fused": MODE_FUSED, "stepwise": MODE_STEPWISE, "flat": MODE_FLAT}
 
 
 class HaloError(RuntimeError):
@@ -66,6 +68,8 @@ SIGNATURES = {
     "halo_debug_drop_signal": (ctypes.c_int, [_vp, _i32, _i32]),
     "halo_launch_counts": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
     "halo_set_trace": (ctypes.c_int, [_vp, _vp, _i64]),
+    "halo_set_mode": (ctypes.c_int, [_vp, _i32, _vp]),
+    "halo_get_mode": (ctypes.c_int, [_vp, _P(_i32)]),
     "halo_work_items": (ctypes.c_int, [_vp, _P(_i32), _P(_i32), _P(_i32)]),
     "halo_destroy": (None, [_vp]),
     "halo_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -273,6 +277,17 @@ class HaloPlan:
         _check(self._lib.halo_launch_counts(self._h, ctypes.byref(x), ctypes.byref(f)),
                "halo_launch_counts")
         return x.value, f.value
+
+    def set_mode(self, mode, stream=None):
+        """'fused' (default), 'stepwise' or 'flat' (or a MODE_* value)."""
+        m = MODES[mode] if isinstance(mode, str) else int(mode)
+        _check(self._lib.halo_set_mode(self._h, m, _stream_handle(stream)), "halo_set_mode")
+
+    @property
+    def mode(self):
+        m = _i32()
+        _check(self._lib.halo_get_mode(self._h, ctypes.byref(m)), "halo_get_mode")
+        return {v: k for k, v in MODES.items()}[m.value]
 
     def work_items(self):
         x, f, c = _i32(), _i32(), _i32()

@@ -63,6 +63,11 @@ extern "C" {
 #define HALO_EBOUNDS (-7)   /* an index outside its buffer was met and skipped */
 #define HALO_ENOMEM (-8)    /* device or host allocation failed */
 
+/* Exchange modes (halo_set_mode).  All three compute bit-identical results. */
+#define HALO_MODE_FUSED 0    /* one launch per direction, per-(domain, pulse) signals (default) */
+#define HALO_MODE_STEPWISE 1 /* one launch per pulse and direction, ordered by the stream */
+#define HALO_MODE_FLAT 2     /* forwarding chains composed at build time, one wait-free pass */
+
 #define HALO_MAX_PULSES 64
 #define HALO_MAX_DOMAINS 4096
 
@@ -144,6 +149,22 @@ int halo_exchange_x(halo_plan* plan, float* local_coords, void* stream);
  * Halo slots keep their (possibly forwarded-into) values.  Bit-identical to
  * the sequential order.  Asynchronous. */
 int halo_exchange_f(halo_plan* plan, float* local_forces, void* stream);
+
+/* Select how halo_exchange_x / halo_exchange_f run (HALO_MODE_*).
+ *   FUSED: the pages' design (Algorithms 3-6): one launch per direction; the
+ *     entries below depOffset stream at once, forwarded entries wait on
+ *     per-(domain, pulse) release/acquire counters.
+ *   STEPWISE: one launch per pulse and direction (the MPI-era schedule without
+ *     the transfers); P launches per call.
+ *   FLAT: every halo slot's forwarding chain composed at build time (owner,
+ *     periodic shift; per owner the tree of its copies in reverse creation
+ *     order); one launch per direction with no waits.  Needs extra tables
+ *     (built here, synchronising `stream`; rebuilt by halo_rebuild) and
+ *     n_local_total < 2^26, at most 63 copies per atom (HALO_ECAPACITY
+ *     otherwise).
+ * The mode is kept across halo_rebuild. */
+int halo_set_mode(halo_plan* plan, int32_t mode, void* stream);
+int halo_get_mode(const halo_plan* plan, int32_t* mode);
 
 /* Synchronise `stream`, return the plan's sticky device error (HALO_OK if
  * none) and clear it, resetting the plan's flags. */

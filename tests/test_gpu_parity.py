@@ -104,10 +104,19 @@ def test_plan_parity(cases, name):
     compare_plans(g, o)
 
 
+MODES = ["fused", "stepwise", "flat"]
+
+
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", WORKLOADS)
-def test_exchange_parity(cases, name):
+def test_exchange_parity(cases, name, mode):
     w, xyz, dom, o, g = cases(name)
-    compare_exchanges(g, o, xyz)
+    g.plan.set_mode(mode)
+    try:
+        assert g.plan.mode == mode
+        compare_exchanges(g, o, xyz)
+    finally:
+        g.plan.set_mode("fused")
 
 
 @pytest.mark.parametrize("name", ["water24k_2x4x8", "water1M_4x4x4"])
@@ -117,13 +126,18 @@ def test_gpu_forces_integer_closed_form(cases, name):
 
 
 def test_rebuild_after_displacement(cases):
-    """3M-atom system: displace by N(0, 0.01 nm), rebuild, compare again."""
+    """3M-atom system: displace by N(0, 0.01 nm), rebuild (twice, the second time
+    with the flat mode active, whose tables are rebuilt too), compare again."""
     w, xyz, dom, o, g = cases("water3M_8x8x8")
-    x1, d1 = synth.displaced(xyz, w.box, w.grid, k=1)
-    g.rebuild(x1, d1)
-    o1 = oracle.Oracle(w.box, w.grid, w.rc, x1, d1)
-    compare_plans(g, o1)
-    compare_exchanges(g, o1, x1, reps=1)
+    for k, mode in ((1, "fused"), (2, "flat")):
+        g.plan.set_mode(mode)
+        xk, dk = synth.displaced(xyz, w.box, w.grid, k=k)
+        g.rebuild(xk, dk)
+        assert g.plan.mode == mode
+        ok = oracle.Oracle(w.box, w.grid, w.rc, xk, dk)
+        compare_plans(g, ok)
+        compare_exchanges(g, ok, xk, reps=1)
+    g.plan.set_mode("fused")
 
 
 EDGE = [
@@ -146,7 +160,9 @@ def test_edge_cases(box, grid, rc, n, seed):
     g = gpu_plan(box, grid, rc, xyz, dom)
     try:
         compare_plans(g, o)
-        compare_exchanges(g, o, xyz)
+        for mode in MODES:
+            g.plan.set_mode(mode)
+            compare_exchanges(g, o, xyz)
     finally:
         g.close()
 
@@ -162,7 +178,9 @@ def test_empty_domains_and_skewed_load():
     try:
         assert (o.n_home == 0).sum() >= 20
         compare_plans(g, o)
-        compare_exchanges(g, o, xyz)
+        for mode in MODES:
+            g.plan.set_mode(mode)
+            compare_exchanges(g, o, xyz)
     finally:
         g.close()
 
@@ -189,15 +207,22 @@ def test_setup_errors():
     assert e.value.code == halo.EINVAL
 
 
-def test_one_launch_per_direction(cases):
+@pytest.mark.parametrize("mode", MODES)
+def test_launches_per_direction(cases, mode):
+    """fused and flat: one launch per direction; stepwise: one per pulse."""
     w, xyz, dom, o, g = cases("water24k_2x4x8")
-    x0, f0 = g.plan.launch_counts()
-    loc = g.plan.load_home(g.xyz_d)
-    g.plan.exchange_x(loc)
-    g.plan.exchange_f(loc)
-    assert g.plan.status() == 0
-    x1, f1 = g.plan.launch_counts()
-    assert (x1 - x0, f1 - f0) == (1, 1)
+    g.plan.set_mode(mode)
+    try:
+        x0, f0 = g.plan.launch_counts()
+        loc = g.plan.load_home(g.xyz_d)
+        g.plan.exchange_x(loc)
+        g.plan.exchange_f(loc)
+        assert g.plan.status() == 0
+        x1, f1 = g.plan.launch_counts()
+        want = g.n_pulses if mode == "stepwise" else 1
+        assert (x1 - x0, f1 - f0) == (want, want)
+    finally:
+        g.plan.set_mode("fused")
 
 
 def test_determinism_repeated(cases):
