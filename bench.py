@@ -130,6 +130,23 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def max_over_ranks(values, device, dist=None):
+    """Element-wise maximum of a list of floats over all ranks (identity for one
+    process).  Used for the per-rank times: the slowest rank sets the pace."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(units_per_rank, world, seconds_max):
+    """Units processed by all ranks (weak scaling: each rank a full replica)
+    divided by the slowest rank's time."""
+    return world * units_per_rank / seconds_max
+
+
 def gpu_index(local_rank):
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     parts = [p for p in cvd.split(",") if p.strip()]
@@ -354,12 +371,9 @@ def main():
                             "launches_per_step": launches / steps}
     step_ms = statistics.fmean(a + b for a, b in zip(xs, fs))
     x_ms, f_ms = statistics.fmean(xs), statistics.fmean(fs)
-    if dist:
-        t = torch.tensor([step_ms, x_ms, f_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, x_ms, f_ms = [float(v) for v in t.tolist()]
+    step_ms, x_ms, f_ms = max_over_ranks([step_ms, x_ms, f_ms], device, dist)
     halo_slots = plan.n_halo_total
-    value = world * halo_slots / (step_ms * 1e-3)
+    value = whole_job_rate(halo_slots, world, step_ms * 1e-3)
     for m in others.values():
         m["value"] = world * halo_slots / (m["us_per_exchange"] * 1e-6)
         m["hbm_frac"] = (BYTES_X + BYTES_F) * halo_slots / (m["us_per_exchange"] * 1e-6) / 1e9 \
@@ -391,11 +405,8 @@ def main():
     # end to end through the public API with host buffers
     e2e_ms, h2d, d2h = e2e_steps(w, xyz, plan, max(20, min(args.steps, 200)), 5, device, stream)
     assert plan.status() == 0
-    e2e_value = world * halo_slots / (e2e_ms * 1e-3)
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_value = world * halo_slots / (float(t.item()) * 1e-3)
+    (e2e_ms,) = max_over_ranks([e2e_ms], device, dist)
+    e2e_value = whole_job_rate(halo_slots, world, e2e_ms * 1e-3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
