@@ -332,6 +332,7 @@ const char* halo_strerror(int code) {
         case HALO_ETIMEOUT: return "device-side wait timed out";
         case HALO_EBOUNDS: return "index out of bounds";
         case HALO_ENOMEM: return "out of memory";
+        case HALO_ESCRATCH: return "plan too large for the fixed scratch of halo_exchange_x_noalloc";
         default: return "unknown error";
     }
 }

@@ -673,6 +673,31 @@ int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     return cuda_code(cudaGetLastError());
 }
 
+int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
+                              unsigned long long* ticket, cudaStream_t st) {
+    if (pl->n_items_x == 0) return HALO_OK;
+    XArgs a;
+    a.xyz = xyz;
+    a.maps = pl->d_maps;
+    a.items = pl->d_items_x;
+    a.target = pl->d_target;
+    a.arrived = arrived;
+    a.ticket = ticket;
+    a.err = pl->d_err;
+    a.n_items = pl->n_items_x;
+    a.timeout_ns = pl->wait_timeout_ns;
+    a.drop_flag = pl->drop_flag;
+    a.trace = pl->trace;
+    pl->drop_flag = -1;
+    switch (pl->entries_per_thread) {
+        case 4: pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a); break;
+        case 2: pack_x_kernel<2><<<pl->grid_x, kThreads, 0, st>>>(a); break;
+        default: pack_x_kernel<1><<<pl->grid_x, kThreads, 0, st>>>(a); break;
+    }
+    pl->launches_x++;
+    return cuda_code(cudaGetLastError());
+}
+
 int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
     if (pl->n_items_f == 0) return HALO_OK;
     const size_t nsp = (size_t)pl->n_dom * std::max(pl->P, 1);

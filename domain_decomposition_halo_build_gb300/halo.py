@@ -18,8 +18,9 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_PKG, "libhalo.so")
 
-OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM = (
-    0, -1, -2, -3, -4, -5, -6, -7, -8)
+OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM, ESCRATCH = (
+    0, -1, -2, -3, -4, -5, -6, -7, -8, -9)
+NOALLOC_MAX_COUNTERS = 16384
 MAX_PULSES = 64
 MODE_FUSED, MODE_STEPWISE, MODE_FLAT = 0, 1, 2
 MODES = {"fused": MODE_FUSED, "stepwise": MODE_STEPWISE, "flat": MODE_FLAT}
@@ -63,6 +64,7 @@ SIGNATURES = {
     "halo_load_home": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "halo_exchange_x": (ctypes.c_int, [_vp, _vp, _vp]),
     "halo_exchange_f": (ctypes.c_int, [_vp, _vp, _vp]),
+    "halo_exchange_x_noalloc": (ctypes.c_int, [_vp, _vp, _vp]),
     "halo_status": (ctypes.c_int, [_vp, _vp]),
     "halo_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_double]),
     "halo_debug_drop_signal": (ctypes.c_int, [_vp, _i32, _i32]),
@@ -254,6 +256,15 @@ class HaloPlan:
         _check(self._lib.halo_exchange_x(
             self._h, _dev_ptr(local_xyz, torch.float32, (self.n_local_total, 3)),
             _stream_handle(stream)), "halo_exchange_x")
+        return local_xyz
+
+    def exchange_x_noalloc(self, local_xyz, stream=None):
+        """halo_exchange_x_noalloc: the fused coordinate exchange with its
+        scratch in the library's fixed array (no device allocation)."""
+        import torch
+        _check(self._lib.halo_exchange_x_noalloc(
+            self._h, _dev_ptr(local_xyz, torch.float32, (self.n_local_total, 3)),
+            _stream_handle(stream)), "halo_exchange_x_noalloc")
         return local_xyz
 
     def exchange_f(self, local_f, stream=None):

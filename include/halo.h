@@ -62,6 +62,7 @@ extern "C" {
 #define HALO_ETIMEOUT (-6)  /* a device-side wait gave up after the plan's time limit */
 #define HALO_EBOUNDS (-7)   /* an index outside its buffer was met and skipped */
 #define HALO_ENOMEM (-8)    /* device or host allocation failed */
+#define HALO_ESCRATCH (-9)  /* the plan needs more counters than halo_exchange_x_noalloc's fixed array */
 
 /* Exchange modes (halo_set_mode).  All three compute bit-identical results. */
 #define HALO_MODE_FUSED 0    /* one launch per direction, per-(domain, pulse) signals (default) */
@@ -142,6 +143,28 @@ int halo_load_home(const halo_plan* plan, const float* global_xyz, float* local_
  * i in [0, send_size).  local_coords: n_local_total x 3 fp32, caller-owned,
  * home slots filled.  Asynchronous. */
 int halo_exchange_x(halo_plan* plan, float* local_coords, void* stream);
+
+/* Coordinate exchange that allocates no device memory.  The page has no
+ * counterpart: this call exists for callers that may not allocate device
+ * memory when they call in (a host framework whose pool allocator owns all
+ * device memory, or a latency-critical loop where a cudaMalloc / cudaFree,
+ * which can synchronise the whole device, is not acceptable).
+ * Same result as halo_exchange_x in HALO_MODE_FUSED, whatever the plan's mode:
+ * the same kernel, with its arrival counters and work ticket taken from a
+ * fixed array compiled into the library (HALO_NOALLOC_MAX_COUNTERS counters,
+ * 64 KiB, held by every GPU that loads the library until exit) instead of the
+ * plan's memory.  The plan itself comes from halo_setup.
+ *   - n_domains * n_pulses must be <= HALO_NOALLOC_MAX_COUNTERS, else
+ *     HALO_ESCRATCH and nothing runs.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Each call clears the part of the array it uses (an asynchronous memset
+ *     on `stream`) before its launch.  All calls share the array: calls whose
+ *     kernels overlap on the GPU race and give wrong results.
+ * Asynchronous; a timed-out wait is reported by halo_status() as usual. */
+#define HALO_NOALLOC_MAX_COUNTERS 16384
+int halo_exchange_x_noalloc(halo_plan* plan, float* local_coords, void* stream);
 
 /* Force halo reduction (FusedCommUnpackF, Algorithm 6), one kernel launch for
  * all pulses: for p = P-1 .. 0 and every sender s,

@@ -1,0 +1,102 @@
+"""halo_exchange_x_noalloc: the coordinate exchange for callers that may not
+allocate device memory when they call in (a host framework whose pool
+allocator owns all device memory, or a latency-critical loop where cudaMalloc
+/ cudaFree and the device-wide synchronisation they can cause are not
+acceptable).  Its scratch is a fixed array inside the library.
+
+Checked through the C ABI: two calls in a row give the same coordinates as
+halo_exchange_x (bit-exact, the tolerance of every coordinate test here), a
+plan too large for the fixed array is refused with HALO_ESCRATCH, and the
+calls leave the device's free memory unchanged.  This file is collected last
+and builds everything it needs, so it runs alone or after the other tests."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from domain_decomposition_halo_build_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _plan(name):
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    w = synth.WORKLOADS[name]
+    xyz, dom = synth.system(w)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    return halo.HaloPlan(w.box, w.grid, w.rc, x, d), x
+
+
+@pytest.mark.parametrize("name", ["water24k_2x4x8", "water1M_4x4x4"])
+def test_noalloc_matches_exchange_x_twice(name):
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    plan, x = _plan(name)
+    try:
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        want = plan.load_home(x)
+        assert lib.halo_exchange_x(plan.handle, ctypes.c_void_p(want.data_ptr()), stream) == 0
+        assert plan.status() == 0
+        want = want.cpu().numpy()
+        for call in range(2):
+            got = plan.load_home(x)
+            got_ptr = ctypes.c_void_p(got.data_ptr())
+            assert lib.halo_exchange_x_noalloc(plan.handle, got_ptr, stream) == halo.OK
+            assert plan.status() == halo.OK
+            np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32), want.view(np.uint32),
+                                          err_msg="call %d" % call)
+    finally:
+        plan.close()
+
+
+def test_noalloc_leaves_free_memory_unchanged():
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    plan, x = _plan("water24k_2x4x8")
+    try:
+        loc = plan.load_home(x)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        ptr = ctypes.c_void_p(loc.data_ptr())
+        assert lib.halo_exchange_x_noalloc(plan.handle, ptr, stream) == 0   # first call: set-up
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        for _ in range(5):
+            assert lib.halo_exchange_x_noalloc(plan.handle, ptr, stream) == 0
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert plan.status() == 0
+    finally:
+        plan.close()
+
+
+def test_noalloc_refuses_plans_beyond_the_fixed_array():
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    box, grid, rc = (8.0, 8.0, 8.0), (16, 16, 16), 1.4      # 4096 domains x 9 pulses
+    xyz, dom = synth.custom_system(40000, box, grid, seed=8)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    plan = halo.HaloPlan(box, grid, rc, x, d)
+    try:
+        assert plan.n_domains * plan.n_pulses > halo.NOALLOC_MAX_COUNTERS
+        loc = plan.load_home(x)
+        before = loc.clone()
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        code = lib.halo_exchange_x_noalloc(plan.handle, ctypes.c_void_p(loc.data_ptr()), stream)
+        assert code == halo.ESCRATCH
+        assert "fixed scratch" in halo.strerror(code)
+        torch.cuda.synchronize()
+        assert torch.equal(loc, before)                       # nothing ran
+    finally:
+        plan.close()
