@@ -322,7 +322,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--mode", default="fused", choices=["fused", "stepwise", "flat"],
+    ap.add_argument("--mode", default="flat", choices=["fused", "stepwise", "flat"],
                     help="exchange mode of the headline value; every mode is also reported")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

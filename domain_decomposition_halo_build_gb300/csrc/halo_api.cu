@@ -217,7 +217,7 @@ int halo_load_home(const halo_plan* pl, const float* global_xyz, float* local_xy
 }
 
 int halo_exchange_x(halo_plan* pl, float* local_coords, void* stream) {
-    if (!pl || !local_coords) return HALO_EINVAL;
+    if (!pl || !local_coords || ((uintptr_t)local_coords & 3u)) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
     switch (pl->mode) {
         case HALO_MODE_STEPWISE: return halo::launch_stepwise_x(pl, local_coords, as_stream(stream));

@@ -1,0 +1,61 @@
+// halo_device.cuh -- device helpers shared by the exchange kernels.
+#pragma once
+
+#include <stdint.h>
+
+namespace halo {
+
+// A block's chunk of halo coordinates is one contiguous range of 12-byte
+// slots in the destination domain.  The block stages it in shared memory and
+// one thread writes it back with a bulk asynchronous copy (cp.async.bulk,
+// shared -> global), which needs 16-byte aligned addresses and a multiple of
+// 16 bytes: the 16-byte aligned middle goes by bulk copy, the at most three
+// leading and three trailing floats by ordinary stores.
+//
+// Staging convention: the float that belongs at gdst[j] sits at
+// stage[stage_shift(gdst) + j], so that global and shared addresses agree
+// modulo 16.
+__device__ __forceinline__ int stage_shift(const float* gdst) {
+    return (int)(((uintptr_t)gdst & 15u) >> 2);
+}
+
+// Make this thread's generic-proxy writes to shared memory visible to the
+// asynchronous proxy (every writing thread, before the block barrier).
+__device__ __forceinline__ void fence_smem_to_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Called by one thread after the (warp or block) barrier.  complete = true:
+// returns once the data is in global memory and ordered before this thread's
+// later (release) operations; false: returns once the shared source has been
+// read (enough before the block exits: kernel completion makes it visible).
+__device__ __forceinline__ void bulk_store_floats(float* gdst, const float* stage, int nfloats,
+                                                  bool complete) {
+    const uintptr_t B = (uintptr_t)gdst;
+    const int a = stage_shift(gdst);
+    const uintptr_t Bend = B + 4 * (uintptr_t)nfloats;
+    const uintptr_t Bup = (B + 15) & ~(uintptr_t)15;
+    const uintptr_t Bdn = Bend & ~(uintptr_t)15;
+    if (Bdn > Bup) {
+        uint64_t g;
+        asm("cvta.to.global.u64 %0, %1;" : "=l"(g) : "l"((uint64_t)Bup));
+        const uint32_t s = (uint32_t)__cvta_generic_to_shared(stage + a) + (uint32_t)(Bup - B);
+        const uint32_t size = (uint32_t)(Bdn - Bup);
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g), "r"(s),
+                     "r"(size)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        for (uintptr_t x = B; x < Bup; x += 4) gdst[(x - B) >> 2] = stage[a + ((x - B) >> 2)];
+        for (uintptr_t x = Bdn; x < Bend; x += 4) gdst[(x - B) >> 2] = stage[a + ((x - B) >> 2)];
+        if (complete) {
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        } else {
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+    } else {
+        for (int j = 0; j < nfloats; j++) gdst[j] = stage[a + j];
+    }
+}
+
+}  // namespace halo

@@ -20,20 +20,20 @@
 // epoch * chunks; the epoch is the call number, recovered from a monotonically
 // increasing work ticket, so no counter is ever reset between calls.
 //
-// Work order.  Coordinates: the independent chunks (entries below depOffset)
-// of every pulse come first, then the dependent chunks in pulse order, so the
-// bulk of the traffic streams with no wait and only the forwarded entries form
-// the z -> y -> x chain.  Forces: the build classifies every entry; an entry is
-// independent when no later pulse adds into its destination slot and its halo
-// source slot was never forwarded; independent chunks come first, dependent
-// chunks follow in reverse pulse order and wait for the later pulses that touch
-// their destination domain or their source slice.  Each destination slot still
-// receives its adds in reverse pulse order, so the result is bit-identical to
-// the sequential reduction.
+// Work order.  Items are listed pulse by pulse (ascending for coordinates,
+// descending for forces) and, within a pulse, the dependent chunks first: the
+// forwarding chain is served first and the bulk of independent traffic
+// streams behind it.  Coordinates: a chunk is independent when all its
+// entries lie below depOffset.  Forces: the build classifies every entry; an
+// entry is independent when no later pulse adds into its destination slot and
+// its halo source slot was never forwarded.  Dependent force chunks wait for
+// the later pulses that touch their destination domain or their source
+// slice.  Each destination slot still receives its adds in reverse pulse
+// order, so the result is bit-identical to the sequential reduction.
 //
-// Forward progress: blocks take work items from one atomic ticket counter in
+// Forward progress: warps take work items from one atomic ticket counter in
 // that order, and an item only waits on items with earlier tickets.  The
-// earliest unfinished item was taken by a block that is running (a block holds
+// earliest unfinished item was taken by a warp that is running (a warp holds
 // at most the item it works on and one prefetched ticket), and everything it
 // waits on has an earlier ticket, so by induction every wait ends -- whatever
 // the grid size and however blocks are scheduled.  Every wait is still bounded
@@ -42,6 +42,7 @@
 
 #include <algorithm>
 
+#include "halo_device.cuh"
 #include "halo_internal.cuh"
 
 namespace halo {
@@ -148,46 +149,52 @@ struct FArgs {
     unsigned long long* trace;
 };
 
-// Ticket handling shared by both kernels: thread 0 decodes the held ticket into
-// (item, epoch) and prefetches the next one.
-struct TicketState {
-    unsigned long long next;
+constexpr int kWarps = kThreads / 32;
+
+// Work items are warp-granular: every warp takes its own tickets (lane 0
+// draws, the value is broadcast), so a warp that waits for a pulse holds up
+// no other warp -- the pages' NVLink path, where each warp packs its own chunk
+// and its leader issues the bulk store (Algorithm 3).  A warp's ticket t
+// decodes to call number t / T and item t mod T, with T = items + warps in
+// the grid: every warp ends by drawing exactly one ticket past the items.
+struct WarpTicket {
+    int item;
+    uint32_t epoch;
 };
 
-__device__ __forceinline__ void take_ticket(TicketState& ts, unsigned long long* ticket, int n_items,
-                                            unsigned long long T, const int* err, int* s_item,
-                                            uint32_t* s_epoch, int* s_abort) {
-    const unsigned long long k = ts.next / T;
-    int item = (int)(ts.next - k * T);
-    if (item < n_items && ld_relaxed_gpu(err) != 0) item = n_items;
-    *s_item = item;
-    *s_epoch = (uint32_t)(k + 1);
-    *s_abort = 0;
-    if (item < n_items) ts.next = atomicAdd(ticket, 1ull);
+__device__ __forceinline__ WarpTicket decode_ticket(unsigned long long t, unsigned long long T) {
+    const unsigned long long k = t / T;
+    return WarpTicket{(int)(t - k * T), (uint32_t)(k + 1)};
 }
 
+// Coordinates: block-granular items of up to kThreads * E entries whose
+// destination is one contiguous halo range; the block stages it in shared
+// memory and one thread writes it with a single bulk copy.
 template <int E>
 __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
-    __shared__ int s_item;
-    __shared__ uint32_t s_epoch;
-    __shared__ int s_abort;
+    __shared__ __align__(128) float stage[3 * kThreads * E + 4];
+    __shared__ unsigned long long s_ticket;
+    __shared__ int s_go;
     const unsigned long long T = (unsigned long long)a.n_items + gridDim.x;
-    TicketState ts;
-    if (threadIdx.x == 0) ts.next = atomicAdd(a.ticket, 1ull);
+    unsigned long long next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(a.ticket, 1ull);
     for (;;) {
-        if (threadIdx.x == 0)
-            take_ticket(ts, a.ticket, a.n_items, T, a.err, &s_item, &s_epoch, &s_abort);
+        if (threadIdx.x == 0) {
+            s_ticket = next;
+            const WarpTicket tk0 = decode_ticket(next, T);
+            s_go = tk0.item < a.n_items && ld_relaxed_gpu(a.err) == 0;
+            if (s_go) next = atomicAdd(a.ticket, 1ull);  // prefetch the next ticket
+        }
         __syncthreads();
-        const int item = s_item;
-        if (item >= a.n_items) return;
+        if (!s_go) return;
+        const WarpTicket tk = decode_ticket(s_ticket, T);
         const uint64_t t_take = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
-        const XItem w = a.items[item];
+        const XItem w = a.items[tk.item];
         const bool dependent = w.wait_mask != 0;
         const int32_t* map = a.maps + w.map_off;
         const float* src = a.xyz + 3 * w.src_base;
         float* dst = a.xyz + 3 * w.dst;
-        // a chunk holds at most kThreads*E entries: the index loads are issued
-        // before any wait, so only the forwarded coordinates remain after it
+        // index loads first: only the forwarded coordinates remain after a wait
         int idx[E];
 #pragma unroll
         for (int e = 0; e < E; e++) {
@@ -196,19 +203,19 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
         }
         if (dependent) {
             // packWithDeps: one thread waits for the pulses that delivered the
-            // slots this chunk forwards, then the block goes on
+            // slots this chunk forwards (Algorithm 4), then the block goes on
+            __syncthreads();  // every thread has read s_go / s_ticket
             if (threadIdx.x == 0) {
-                const uint32_t epoch = s_epoch;
-                bool ok = true;
+                int ok = 1;
                 for (uint64_t m = w.wait_mask; m && ok; m &= m - 1) {
                     const int c = w.wait_base + __ffsll((long long)m) - 1;
-                    ok = wait_count(a.arrived + c, epoch * __ldg(a.target + c), a.err,
+                    ok = wait_count(a.arrived + c, tk.epoch * __ldg(a.target + c), a.err,
                                     a.timeout_ns, 1, c);
                 }
-                s_abort = ok ? 0 : 1;
+                s_go = ok;
             }
             __syncthreads();
-            if (s_abort) return;
+            if (!s_go) return;
         }
         const uint64_t t_wait = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
         float v[E][3];
@@ -227,43 +234,54 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
                 }
             }
         }
+        // stage the chunk's contiguous destination range; one thread writes
+        // it with a bulk asynchronous copy (the pages' TMA store of a packed
+        // chunk, Algorithm 3), then signals with a gpu-scope release
+        // (Algorithm 5)
+        const int sh = stage_shift(dst);
 #pragma unroll
         for (int e = 0; e < E; e++) {
             if (idx[e] >= 0) {
-                float* q = dst + 3 * (int64_t)(threadIdx.x + e * kThreads);
+                float* q = stage + sh + 3 * (threadIdx.x + e * kThreads);
                 q[0] = v[e][0] + w.shift[0];
                 q[1] = v[e][1] + w.shift[1];
                 q[2] = v[e][2] + w.shift[2];
             }
         }
-        // all stores of the block, then one gpu-scope release (Algorithm 5)
+        fence_smem_to_async();
         __syncthreads();
-        if (threadIdx.x == 0 && w.flag != a.drop_flag) red_release_gpu_add(a.arrived + w.flag, 1u);
-        if (a.trace && threadIdx.x == 0) trace_item(a.trace, item, t_take, t_wait);
+        if (threadIdx.x == 0) {
+            bulk_store_floats(dst, stage, 3 * w.len, true);
+            if (w.flag != a.drop_flag) red_release_gpu_add(a.arrived + w.flag, 1u);
+            if (a.trace) trace_item(a.trace, tk.item, t_take, t_wait);
+        }
+        // the next iteration's barrier keeps the stage until the copy has read it
     }
 }
 
 template <int E>
 __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
-    __shared__ int s_item;
-    __shared__ uint32_t s_epoch;
-    __shared__ int s_abort;
-    const unsigned long long T = (unsigned long long)a.n_items + gridDim.x;
-    TicketState ts;
-    if (threadIdx.x == 0) ts.next = atomicAdd(a.ticket, 1ull);
+    const int lane = threadIdx.x & 31;
+    const unsigned long long T = (unsigned long long)a.n_items + (unsigned long long)gridDim.x * kWarps;
+    unsigned long long next = 0;
+    if (lane == 0) next = atomicAdd(a.ticket, 1ull);
+    next = __shfl_sync(kFull, next, 0);
     for (;;) {
-        if (threadIdx.x == 0)
-            take_ticket(ts, a.ticket, a.n_items, T, a.err, &s_item, &s_epoch, &s_abort);
-        __syncthreads();
-        const int item = s_item;
-        if (item >= a.n_items) return;
-        const uint64_t t_take = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
-        const FItem w = a.items[item];
+        const WarpTicket tk = decode_ticket(next, T);
+        if (tk.item >= a.n_items) return;
+        int stop = 0;
+        if (lane == 0) {
+            stop = ld_relaxed_gpu(a.err) != 0;
+            if (!stop) next = atomicAdd(a.ticket, 1ull);
+        }
+        if (__shfl_sync(kFull, stop, 0)) return;
+        const uint64_t t_take = a.trace && lane == 0 ? global_timer_ns() : 0;
+        const FItem w = a.items[tk.item];
         const int2* pr = a.pairs + w.off;
         int2 sd[E];
 #pragma unroll
         for (int e = 0; e < E; e++) {
-            const int i = threadIdx.x + e * kThreads;
+            const int i = lane + 32 * e;
             sd[e] = i < w.len ? __ldg(pr + i) : make_int2(-1, -1);
         }
         if (w.ms | w.mr) {
@@ -276,25 +294,22 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
                     prefetch_l2(a.f + 3 * (int64_t)sd[e].y);
                 }
             }
-            if (threadIdx.x == 0) {
-                const uint32_t epoch = s_epoch;
-                bool ok = true;
+            int ok = 1;
+            if (lane == 0) {
                 for (uint64_t m = w.ms; m && ok; m &= m - 1) {
                     const int c = w.s_base + __ffsll((long long)m) - 1;
-                    ok = wait_count(a.done + c, epoch * __ldg(a.target + c), a.err, a.timeout_ns,
-                                    2, c);
+                    ok = wait_count(a.done + c, tk.epoch * __ldg(a.target + c), a.err,
+                                    a.timeout_ns, 2, c);
                 }
                 for (uint64_t m = w.mr; m && ok; m &= m - 1) {
                     const int c = w.r_base + __ffsll((long long)m) - 1;
-                    ok = wait_count(a.done + c, epoch * __ldg(a.target + c), a.err, a.timeout_ns,
-                                    2, c);
+                    ok = wait_count(a.done + c, tk.epoch * __ldg(a.target + c), a.err,
+                                    a.timeout_ns, 2, c);
                 }
-                s_abort = ok ? 0 : 1;
             }
-            __syncthreads();
-            if (s_abort) return;
+            if (!__shfl_sync(kFull, ok, 0)) return;
         }
-        const uint64_t t_wait = a.trace && threadIdx.x == 0 ? global_timer_ns() : 0;
+        const uint64_t t_wait = a.trace && lane == 0 ? global_timer_ns() : 0;
         float h[E][3], o[E][3];
 #pragma unroll
         for (int e = 0; e < E; e++) {
@@ -318,9 +333,13 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
                 op[2] = o[e][2] + h[e][2];
             }
         }
-        __syncthreads();
-        if (threadIdx.x == 0) red_release_gpu_add(a.done + w.flag, 1u);
-        if (a.trace && threadIdx.x == 0) trace_item(a.trace, item, t_take, t_wait);
+        // the warp's stores, then one gpu-scope release by the leader
+        __syncwarp();
+        if (lane == 0) {
+            red_release_gpu_add(a.done + w.flag, 1u);
+            if (a.trace) trace_item(a.trace, tk.item, t_take, t_wait);
+        }
+        next = __shfl_sync(kFull, next, 0);
     }
 }
 
@@ -481,16 +500,12 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
     const size_t nsp = (size_t)nd * std::max(P, 1);
     if (pl->n_local_total >= ((int64_t)1 << 31)) return HALO_ECAPACITY;  // int32 dense slots
-    // chunk size: large chunks (more loads in flight per thread) when there
-    // are enough of them to give every SM several items
-    const int64_t H = pl->n_halo_total;
-    int E = 1;
-    if (H / (kThreads * 4) >= 4 * (int64_t)pl->num_sms)
-        E = 4;
-    else if (H / (kThreads * 2) >= 4 * (int64_t)pl->num_sms)
-        E = 2;
+    // coordinate items: one block, kThreads * E entries; force items: one
+    // warp, 32 * E entries
+    const int E = 4;
     pl->entries_per_thread = E;
     pl->chunk = kThreads * E;
+    const int CHF = 32 * E;
     const int CH = pl->chunk;
 
     // per (s, p) descriptors
@@ -550,11 +565,14 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
         HALO_CUDA(cudaStreamSynchronize(st));
     }
 
-    // coordinate items: independent chunks of all pulses, then dependent ones
+    // coordinate items, pulse by pulse; within a pulse the dependent chunks
+    // (the forwarding chain) come before the independent ones, so the chain
+    // is served first and the rest streams behind it.  Dependent chunks wait
+    // only on earlier pulses, i.e. on earlier tickets.
     std::vector<uint32_t> target((size_t)2 * nsp, 0);
     std::vector<XItem> ix;
-    for (int pass = 0; pass < 2; pass++)
-        for (int p = 0; p < P; p++)
+    for (int p = 0; p < P; p++)
+        for (int pass = 1; pass >= 0; pass--)
             for (int s = 0; s < nd; s++) {
                 const size_t sp = (size_t)s * P + p;
                 const SPDesc& d = pl->sp[sp];
@@ -595,38 +613,30 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
                 fmr[p] |= 1ull << q;
             }
         }
-    // level 0: chunks that wait for nothing (independent entries, and the
-    // dependent entries of the last pulse); then dependent chunks by pulse,
-    // last to first
-    for (int level = 0; level < 2; level++)
-        for (int p = P - 1; p >= 0; p--) {
-            const bool no_wait = (fms[p] | fmr[p]) == 0;
+    // pulses from the last to the first; within a pulse the dependent chunks
+    // (the reverse chain) come first
+    for (int p = P - 1; p >= 0; p--) {
+        const bool no_wait = (fms[p] | fmr[p]) == 0;
+        for (int level = 1; level >= 0; level--)
             for (int s = 0; s < nd; s++) {
                 const size_t sp = (size_t)s * P + p;
                 const SPDesc& d = pl->sp[sp];
-                int lo, hi;
-                if (level == 0) {
-                    lo = 0;
-                    hi = no_wait ? d.send : nindep[sp];
-                } else {
-                    if (no_wait) continue;
-                    lo = nindep[sp];
-                    hi = d.send;
-                }
-                for (int st0 = lo; st0 < hi; st0 += CH) {
+                const int lo = level == 0 ? 0 : nindep[sp];
+                const int hi = level == 0 ? nindep[sp] : d.send;
+                for (int st0 = lo; st0 < hi; st0 += CHF) {
                     FItem w{};
                     w.off = d.map_off + st0;
-                    w.len = std::min(CH, hi - st0);
+                    w.len = std::min(CHF, hi - st0);
                     w.flag = s * P + p;
                     w.s_base = s * P;
                     w.r_base = d.r * P;
-                    w.ms = level == 0 ? 0 : fms[p];
-                    w.mr = level == 0 ? 0 : fmr[p];
+                    w.ms = (level == 0 || no_wait) ? 0 : fms[p];
+                    w.mr = (level == 0 || no_wait) ? 0 : fmr[p];
                     iff.push_back(w);
                     target[nsp + (size_t)s * P + p]++;
                 }
             }
-        }
+    }
     pl->n_items_x = (int)ix.size();
     pl->n_items_f = (int)iff.size();
     HALO_TRY(upload(&pl->d_items_x, ix));
@@ -637,14 +647,11 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
     if (!pl->d_tickets) HALO_TRY(dev_alloc(&pl->d_tickets, 2));
     if (!pl->d_err) HALO_TRY(dev_alloc(&pl->d_err, 8));
     int bx = 1, bf = 1;
-    if (E == 4)
-        HALO_TRY(occupancy<4>(&bx, &bf));
-    else if (E == 2)
-        HALO_TRY(occupancy<2>(&bx, &bf));
-    else
-        HALO_TRY(occupancy<1>(&bx, &bf));
-    pl->grid_x = (int)std::min<int64_t>(pl->n_items_x, (int64_t)pl->num_sms * std::max(bx, 1));
-    pl->grid_f = (int)std::min<int64_t>(pl->n_items_f, (int64_t)pl->num_sms * std::max(bf, 1));
+    HALO_TRY(occupancy<4>(&bx, &bf));
+    pl->grid_x = (int)std::max<int64_t>(1, std::min<int64_t>(pl->n_items_x,
+                                                              (int64_t)pl->num_sms * std::max(bx, 1)));
+    pl->grid_f = (int)std::max<int64_t>(1, std::min<int64_t>((pl->n_items_f + kWarps - 1) / kWarps,
+                                                              (int64_t)pl->num_sms * std::max(bf, 1)));
     HALO_TRY(reset_flags(pl, st));
     return cuda_code(cudaStreamSynchronize(st));
 }
@@ -664,11 +671,7 @@ int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
-    switch (pl->entries_per_thread) {
-        case 4: pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a); break;
-        case 2: pack_x_kernel<2><<<pl->grid_x, kThreads, 0, st>>>(a); break;
-        default: pack_x_kernel<1><<<pl->grid_x, kThreads, 0, st>>>(a); break;
-    }
+    pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a);
     pl->launches_x++;
     return cuda_code(cudaGetLastError());
 }
@@ -689,11 +692,7 @@ int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
-    switch (pl->entries_per_thread) {
-        case 4: pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a); break;
-        case 2: pack_x_kernel<2><<<pl->grid_x, kThreads, 0, st>>>(a); break;
-        default: pack_x_kernel<1><<<pl->grid_x, kThreads, 0, st>>>(a); break;
-    }
+    pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a);
     pl->launches_x++;
     return cuda_code(cudaGetLastError());
 }
@@ -712,11 +711,7 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
     a.n_items = pl->n_items_f;
     a.timeout_ns = pl->wait_timeout_ns;
     a.trace = pl->trace ? pl->trace + 4 * (size_t)pl->n_items_x : nullptr;
-    switch (pl->entries_per_thread) {
-        case 4: unpack_f_kernel<4><<<pl->grid_f, kThreads, 0, st>>>(a); break;
-        case 2: unpack_f_kernel<2><<<pl->grid_f, kThreads, 0, st>>>(a); break;
-        default: unpack_f_kernel<1><<<pl->grid_f, kThreads, 0, st>>>(a); break;
-    }
+    unpack_f_kernel<4><<<pl->grid_f, kThreads, 0, st>>>(a);
     pl->launches_f++;
     return cuda_code(cudaGetLastError());
 }

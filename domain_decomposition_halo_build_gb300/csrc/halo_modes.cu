@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <vector>
 
+#include "halo_device.cuh"
 #include "halo_internal.cuh"
 
 namespace halo {
@@ -212,17 +213,24 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
             a[e][2] = __ldg(s + 2);
         }
     }
+    // the chunk's halo slots are contiguous: stage them, one bulk copy out
+    __shared__ __align__(128) float stage[3 * kThreads * E + 4];
+    float* dst = xyz + 3 * (int64_t)it.y;
+    const int sh = stage_shift(dst);
 #pragma unroll
     for (int e = 0; e < E; e++) {
         const int i = threadIdx.x + e * kThreads;
         if (i < it.z) {
             const unsigned c = (unsigned)v[e] >> 29;
-            float* q = xyz + 3 * ((int64_t)it.y + i);
+            float* q = stage + sh + 3 * i;
             q[0] = a[e][0] + ((c & 1u) ? L0 : 0.0f);
             q[1] = a[e][1] + ((c & 2u) ? L1 : 0.0f);
             q[2] = a[e][2] + ((c & 4u) ? L2 : 0.0f);
         }
     }
+    fence_smem_to_async();
+    __syncthreads();
+    if (threadIdx.x == 0) bulk_store_floats(dst, stage, 3 * it.z, false);
 }
 
 // One thread per owner with copies.  KR: copies kept in registers; owners
