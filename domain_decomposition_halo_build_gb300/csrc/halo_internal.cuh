@@ -128,6 +128,8 @@ struct halo_plan {
     int32_t* d_fent = nullptr;       // per copy, in reduction order: node slot | parent << 26
     int64_t n_owners = 0;
     int max_copies = 0;
+    int4* d_frec[3] = {nullptr, nullptr, nullptr};  // owner records: A (<=3), B (<=7), C (more)
+    int64_t n_rec[3] = {0, 0, 0};
 };
 
 namespace halo {

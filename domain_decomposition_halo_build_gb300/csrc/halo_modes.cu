@@ -233,76 +233,100 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
     if (threadIdx.x == 0) bulk_store_floats(dst, stage, 3 * it.z, false);
 }
 
-// One thread per owner with copies.  KR: copies kept in registers; owners
-// with more copies take the sequential path through memory (same order).
-template <int KR>
-__global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int32_t* __restrict__ fown,
-                                                          const int32_t* __restrict__ fstart,
-                                                          const int32_t* __restrict__ fent,
-                                                          int64_t n_owners) {
-    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
+// Reduction of one owner's copy tree held in registers (k <= K copies).
+// Copy q receives its children (all earlier in the order) in ascending
+// position, then the owner receives its children: every accumulator sees the
+// same adds in the same order as the chained reduction.
+template <int K>
+__device__ __forceinline__ void reduce_tree(float* f, int32_t home, int k, const int32_t (&ent)[K]) {
+    float* fh = f + 3 * (int64_t)home;
+    float c0[3] = {fh[0], fh[1], fh[2]};
+    float c[K][3];
+    int par[K];
+#pragma unroll
+    for (int j = 0; j < K; j++) {
+        par[j] = -1;
+        if (j < k) {
+            const float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
+            c[j][0] = fn[0];
+            c[j][1] = fn[1];
+            c[j][2] = fn[2];
+            par[j] = (int)((unsigned)ent[j] >> kNodeBits);
+        }
+    }
+    unsigned has_child = 0;
+#pragma unroll
+    for (int q = 1; q < K; q++) {
+#pragma unroll
+        for (int j = 0; j < q; j++) {
+            if (par[j] == q + 1) {
+                c[q][0] = c[q][0] + c[j][0];
+                c[q][1] = c[q][1] + c[j][1];
+                c[q][2] = c[q][2] + c[j][2];
+                has_child |= 1u << q;
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < K; j++) {
+        if (par[j] == 0) {
+            c0[0] = c0[0] + c[j][0];
+            c0[1] = c0[1] + c[j][1];
+            c0[2] = c0[2] + c[j][2];
+        }
+    }
+    fh[0] = c0[0];
+    fh[1] = c0[1];
+    fh[2] = c0[2];
+#pragma unroll
+    for (int j = 0; j < K; j++) {
+        if (has_child >> j & 1u) {
+            float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
+            fn[0] = c[j][0];
+            fn[1] = c[j][1];
+            fn[2] = c[j][2];
+        }
+    }
+}
+
+// One thread per owner with copies.  Owners come in three record classes
+// (sorted by class, then by home slot): A -- up to 3 copies, one 16-byte
+// record {home | k << 26, three entries}; B -- up to 7 copies, two 16-byte
+// records; C -- more copies, {header, first entry} into the entry list,
+// reduced sequentially through memory in the same order.  A record is one
+// load, so the forces follow after a single dependent round trip.
+template <bool WIDE>
+__global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* __restrict__ recA,
+                                                          int64_t nA, const int4* __restrict__ recB,
+                                                          int64_t nB, const int4* __restrict__ recC,
+                                                          int64_t nC, const int32_t* __restrict__ fent) {
+    const int64_t n = nA + nB + nC;
+    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n;
          m += (int64_t)gridDim.x * blockDim.x) {
-        const int32_t home = __ldg(fown + m);
-        const int s0 = __ldg(fstart + m), k = __ldg(fstart + m + 1) - s0;
-        float* fh = f + 3 * (int64_t)home;
-        if (k <= KR) {
-            int32_t ent[KR];
-#pragma unroll
-            for (int j = 0; j < KR; j++) ent[j] = j < k ? __ldg(fent + s0 + j) : 0;
-            float c0[3] = {fh[0], fh[1], fh[2]};
-            float c[KR][3];
-#pragma unroll
-            for (int j = 0; j < KR; j++) {
-                if (j < k) {
-                    const float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
-                    c[j][0] = fn[0];
-                    c[j][1] = fn[1];
-                    c[j][2] = fn[2];
-                }
-            }
-            // finalize the copies in order: copy q receives its children (all
-            // earlier in the order) in ascending position, then the owner
-            // receives its children; every accumulator sees the same adds in
-            // the same order as the chained reduction
-            int par[KR];
-#pragma unroll
-            for (int j = 0; j < KR; j++) par[j] = j < k ? (int)((unsigned)ent[j] >> kNodeBits) : -1;
-            unsigned has_child = 0;
-#pragma unroll
-            for (int q = 1; q < KR; q++) {
-#pragma unroll
-                for (int j = 0; j < q; j++) {
-                    if (par[j] == q + 1) {
-                        c[q][0] = c[q][0] + c[j][0];
-                        c[q][1] = c[q][1] + c[j][1];
-                        c[q][2] = c[q][2] + c[j][2];
-                        has_child |= 1u << q;
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < KR; j++) {
-                if (par[j] == 0) {
-                    c0[0] = c0[0] + c[j][0];
-                    c0[1] = c0[1] + c[j][1];
-                    c0[2] = c0[2] + c[j][2];
-                }
-            }
-            fh[0] = c0[0];
-            fh[1] = c0[1];
-            fh[2] = c0[2];
-#pragma unroll
-            for (int j = 0; j < KR; j++) {
-                if (j < k && (has_child >> j & 1u)) {
-                    float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
-                    fn[0] = c[j][0];
-                    fn[1] = c[j][1];
-                    fn[2] = c[j][2];
-                }
-            }
+        if (m < nA) {
+            const int4 r = __ldg(recA + m);
+            const int32_t ent[3] = {r.y, r.z, r.w};
+            reduce_tree<3>(f, r.x & kNodeMask, (int)((unsigned)r.x >> kNodeBits), ent);
+        } else if (m < nA + nB) {
+            const int4 r0 = __ldg(recB + 2 * (m - nA)), r1 = __ldg(recB + 2 * (m - nA) + 1);
+            const int32_t ent[7] = {r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            reduce_tree<7>(f, r0.x & kNodeMask, (int)((unsigned)r0.x >> kNodeBits), ent);
         } else {
+            const int4 r = __ldg(recC + (m - nA - nB));
+            if (WIDE && ((unsigned)r.x >> kNodeBits) <= 16) {
+                // plans with deeper trees (several pulses per dim): up to 16
+                // copies in registers
+                const int k = (int)((unsigned)r.x >> kNodeBits);
+                int32_t ent[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) ent[j] = j < k ? __ldg(fent + r.y + j) : 0;
+                reduce_tree<16>(f, r.x & kNodeMask, k, ent);
+                continue;
+            }
             // every slot of this tree belongs to this thread alone: plain
-            // sequential read-modify-write in the same order
+            // sequential read-modify-write in the same order, through L2
+            float* fh = f + 3 * (int64_t)(r.x & kNodeMask);
+            const int k = (int)((unsigned)r.x >> kNodeBits), s0 = r.y;
             for (int j = 0; j < k; j++) {
                 const int32_t e = __ldg(fent + s0 + j);
                 const int par = (int)((unsigned)e >> kNodeBits);
@@ -313,6 +337,40 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int32_
                 __stcg(fp + 1, __ldcg(fp + 1) + n1);
                 __stcg(fp + 2, __ldcg(fp + 2) + n2);
             }
+        }
+    }
+}
+
+// Record classes of the owners (A: k <= 3, B: k <= 7, C: more).
+__global__ void owner_class_kernel(const int32_t* __restrict__ fstart, int64_t n_owners,
+                                   int32_t* __restrict__ isA, int32_t* __restrict__ isB) {
+    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
+         m += (int64_t)gridDim.x * blockDim.x) {
+        const int k = fstart[m + 1] - fstart[m];
+        isA[m] = k <= 3 ? 1 : 0;
+        isB[m] = (k > 3 && k <= 7) ? 1 : 0;
+    }
+}
+
+__global__ void owner_record_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
+                                    const int32_t* __restrict__ fent, const int32_t* __restrict__ posA,
+                                    const int32_t* __restrict__ posB, int64_t n_owners,
+                                    int4* __restrict__ recA, int4* __restrict__ recB,
+                                    int4* __restrict__ recC) {
+    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
+         m += (int64_t)gridDim.x * blockDim.x) {
+        const int s0 = fstart[m], k = fstart[m + 1] - s0;
+        const int32_t hdr = fown[m] | (k << kNodeBits);
+        int32_t e[7] = {0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < k && j < 7; j++) e[j] = fent[s0 + j];
+        if (k <= 3) {
+            recA[posA[m]] = make_int4(hdr, e[0], e[1], e[2]);
+        } else if (k <= 7) {
+            recB[2 * (int64_t)posB[m]] = make_int4(hdr, e[0], e[1], e[2]);
+            recB[2 * (int64_t)posB[m] + 1] = make_int4(e[3], e[4], e[5], e[6]);
+        } else {
+            const int64_t c = m - posA[m] - posB[m];  // class-C owners before m
+            recC[c] = make_int4(hdr, s0, 0, 0);
         }
     }
 }
@@ -330,6 +388,10 @@ void free_flat(halo_plan* pl) {
     dev_free(pl->d_fown);
     dev_free(pl->d_fstart);
     dev_free(pl->d_fent);
+    for (int c = 0; c < 3; c++) {
+        dev_free(pl->d_frec[c]);
+        pl->n_rec[c] = 0;
+    }
     pl->flat_ready = false;
     pl->n_xflat_items = 0;
     pl->n_owners = 0;
@@ -438,6 +500,34 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             break;
         }
         pl->max_copies = info[0];
+        // record classes: indicator scans give every owner's slot in its class
+        if (n_owners > 0) {
+            int32_t* isA = owner_idx;  // scratch reuse: n_owners <= nl
+            int32_t* isB = flag;
+            int32_t* posA = entry_pos;
+            int32_t* posB = ncopies;
+            const int gbo = blocks_for(n_owners, pl->num_sms);
+            owner_class_kernel<<<gbo, kThreads, 0, st>>>(pl->d_fstart, n_owners, isA, isB);
+            if ((rc = device_exclusive_scan(isA, posA, n_owners, scan_tmp, st)) != HALO_OK) break;
+            if ((rc = device_exclusive_scan(isB, posB, n_owners, scan_tmp, st)) != HALO_OK) break;
+            int32_t tail[4] = {0, 0, 0, 0};
+            if ((rc = cuda_code(cudaMemcpyAsync(tail, posA + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
+            if ((rc = cuda_code(cudaMemcpyAsync(tail + 1, isA + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
+            if ((rc = cuda_code(cudaMemcpyAsync(tail + 2, posB + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
+            if ((rc = cuda_code(cudaMemcpyAsync(tail + 3, isB + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
+            if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
+            pl->n_rec[0] = (int64_t)tail[0] + tail[1];
+            pl->n_rec[1] = (int64_t)tail[2] + tail[3];
+            pl->n_rec[2] = n_owners - pl->n_rec[0] - pl->n_rec[1];
+            if ((rc = dev_alloc(&pl->d_frec[0], (size_t)std::max<int64_t>(pl->n_rec[0], 1))) != HALO_OK) break;
+            if ((rc = dev_alloc(&pl->d_frec[1], (size_t)std::max<int64_t>(2 * pl->n_rec[1], 1))) != HALO_OK) break;
+            if ((rc = dev_alloc(&pl->d_frec[2], (size_t)std::max<int64_t>(pl->n_rec[2], 1))) != HALO_OK) break;
+            owner_record_kernel<<<gbo, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB,
+                                                          n_owners, pl->d_frec[0], pl->d_frec[1],
+                                                          pl->d_frec[2]);
+            if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
+            if ((rc = cuda_code(cudaGetLastError())) != HALO_OK) break;
+        }
     } while (false);
     cleanup();
     if (rc != HALO_OK) {
@@ -477,10 +567,12 @@ int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
 int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
     if (pl->n_owners == 0) return HALO_OK;
     const int gb = blocks_for(pl->n_owners, pl->num_sms);
-    if (pl->max_copies <= 8)
-        flat_f_kernel<8><<<gb, kThreads, 0, st>>>(f, pl->d_fown, pl->d_fstart, pl->d_fent, pl->n_owners);
+    if (pl->max_copies > 7)
+        flat_f_kernel<true><<<gb, kThreads, 0, st>>>(f, pl->d_frec[0], pl->n_rec[0], pl->d_frec[1],
+                                                     pl->n_rec[1], pl->d_frec[2], pl->n_rec[2], pl->d_fent);
     else
-        flat_f_kernel<16><<<gb, kThreads, 0, st>>>(f, pl->d_fown, pl->d_fstart, pl->d_fent, pl->n_owners);
+        flat_f_kernel<false><<<gb, kThreads, 0, st>>>(f, pl->d_frec[0], pl->n_rec[0], pl->d_frec[1],
+                                                      pl->n_rec[1], pl->d_frec[2], pl->n_rec[2], pl->d_fent);
     pl->launches_f++;
     return cuda_code(cudaGetLastError());
 }
