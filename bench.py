@@ -50,11 +50,20 @@ def measured_peak():
         return HBM_FALLBACK_GBS, "fallback"
 
 
-def source_digest():
+KERNEL_SOURCE = {"pack_x_kernel": "halo_exchange.cu", "unpack_f_kernel": "halo_exchange.cu",
+                 "step_x_kernel": "halo_modes.cu", "step_f_kernel": "halo_modes.cu",
+                 "flat_x_kernel": "halo_modes.cu", "flat_f_kernel": "halo_modes.cu"}
+
+
+def source_digest(kernel):
+    """First 16 hex digits of the sha256 of the source file defining `kernel`
+    (and of the shared device header), so recorded counters go stale when the
+    kernel changes."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "domain_decomposition_halo_build_gb300", "csrc",
-                           "halo_exchange.cu"), "rb") as f:
-        h.update(f.read())
+    csrc = os.path.join(ROOT, "domain_decomposition_halo_build_gb300", "csrc")
+    for name in (KERNEL_SOURCE[kernel], "halo_device.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -64,7 +73,7 @@ def recorded_traffic(kernel, workload):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = source_digest()
+    digest = source_digest(kernel)
     with open(path) as f:
         for line in f:
             v = line.split()
@@ -252,6 +261,46 @@ def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
     return ms, h2d, d2h
 
 
+REBUILD_WORKLOAD = "water3M_8x8x8"
+
+
+def rebuild_case(device, stream, flush, steps, warmup, reps=5):
+    """The 3M-atom system: exchanges per step, and halo_rebuild (home
+    partition + every pulse's index map on the device, one host sync) after
+    N(0, 0.01 nm) displacements, in the headline mode."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import synth
+    w, xyz, dom, x, plan, loc, f0 = setup_workload(REBUILD_WORKLOAD, device)
+    out = {"workload": REBUILD_WORKLOAD, "halo_slots": plan.n_halo_total,
+           "rebuild_every": w.rebuild_every}
+    res = {}
+    for mode in ("fused", "flat"):
+        plan.set_mode(mode)
+        f = f0.clone()
+        xs, fs, _, _, _ = time_steps(plan, loc, f, steps, warmup, flush, stream)
+        assert plan.status() == 0
+        ex_us = 1e3 * statistics.fmean(a + b for a, b in zip(xs, fs))
+        times = []
+        for k in range(1, reps + 1):
+            xk, dk = synth.displaced(xyz, w.box, w.grid, k)
+            xt = torch.from_numpy(xk).to(device)
+            dt = torch.from_numpy(dk).to(device)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            plan.rebuild(xt, dt, stream)
+            torch.cuda.synchronize()
+            times.append(time.perf_counter() - t0)
+        rb_ms = 1e3 * statistics.median(times[1:] if len(times) > 1 else times)
+        # back to the original positions: the layout (and `loc`) match again
+        plan.rebuild(x, torch.from_numpy(dom).to(device), stream)
+        torch.cuda.synchronize()
+        res[mode] = {"us_per_exchange": ex_us, "rebuild_ms": rb_ms,
+                     "us_per_exchange_with_rebuild": ex_us + 1e3 * rb_ms / w.rebuild_every}
+    out.update(res)
+    plan.close()
+    return out
+
+
 def cpu_baseline(name, budget_s=10.0):
     """The CPU oracle as it stands, single-threaded, on a bounded sample."""
     import oracle
@@ -402,6 +451,8 @@ def main():
     lplan.close()
     plan.set_mode(args.mode)
 
+    rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
+
     # end to end through the public API with host buffers
     e2e_ms, h2d, d2h = e2e_steps(w, xyz, plan, max(20, min(args.steps, 200)), 5, device, stream)
     assert plan.status() == 0
@@ -432,6 +483,7 @@ def main():
                          "algorithmic_bytes_per_launch": per_slot * halo_slots},
             "other_modes": others,
             "latency_case": lat,
+            "rebuild_case": rebuild,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms},
             "gpu_launches": launches,

@@ -130,6 +130,7 @@ struct halo_plan {
     int max_copies = 0;
     int4* d_frec[3] = {nullptr, nullptr, nullptr};  // owner records: A (<=3), B (<=7), C (more)
     int64_t n_rec[3] = {0, 0, 0};
+    int flat_x_e = 4;                // entries per thread of the flat coordinate kernel
 };
 
 namespace halo {

@@ -34,7 +34,7 @@
 namespace halo {
 namespace {
 
-constexpr int kFlatChunk = 1024;          // halo slots per coordinate item
+constexpr int kFlatChunkMax = 4 * kThreads;  // halo slots per coordinate item (at most)
 constexpr int kNodeBits = 26;             // entry = node slot | parent position << 26
 constexpr int32_t kNodeMask = (1 << kNodeBits) - 1;
 constexpr int kMaxCopies = 63;            // parent positions fit in 6 bits
@@ -213,6 +213,21 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
             a[e][2] = __ldg(s + 2);
         }
     }
+    if (E < 4) {
+        // small chunks: direct stores (a bulk copy's round trip does not pay)
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int i = threadIdx.x + e * kThreads;
+            if (i < it.z) {
+                const unsigned c = (unsigned)v[e] >> 29;
+                float* q = xyz + 3 * ((int64_t)it.y + i);
+                q[0] = a[e][0] + ((c & 1u) ? L0 : 0.0f);
+                q[1] = a[e][1] + ((c & 2u) ? L1 : 0.0f);
+                q[2] = a[e][2] + ((c & 4u) ? L2 : 0.0f);
+            }
+        }
+        return;
+    }
     // the chunk's halo slots are contiguous: stage them, one bulk copy out
     __shared__ __align__(128) float stage[3 * kThreads * E + 4];
     float* dst = xyz + 3 * (int64_t)it.y;
@@ -233,95 +248,143 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
     if (threadIdx.x == 0) bulk_store_floats(dst, stage, 3 * it.z, false);
 }
 
-// Reduction of one owner's copy tree held in registers (k <= K copies).
-// Copy q receives its children (all earlier in the order) in ascending
-// position, then the owner receives its children: every accumulator sees the
-// same adds in the same order as the chained reduction.
-template <int K>
-__device__ __forceinline__ void reduce_tree(float* f, int32_t home, int k, const int32_t (&ent)[K]) {
-    float* fh = f + 3 * (int64_t)home;
-    float c0[3] = {fh[0], fh[1], fh[2]};
-    float c[K][3];
-    int par[K];
+// Reduction of N owners' copy trees held in registers (k <= K copies each).
+// All loads of the N trees are issued before any arithmetic (their slots never
+// overlap, which the compiler cannot know), so a thread keeps N trees' worth of
+// loads in flight.  Copy q receives its children (all earlier in the order) in
+// ascending position, then the owner receives its children: every accumulator
+// sees the same adds in the same order as the chained reduction.
+template <int K, int N>
+__device__ __forceinline__ void reduce_trees(float* f, const int32_t (&home)[N], const int (&kk)[N],
+                                             const int32_t (&ent)[N][K]) {
+    float c0[N][3], c[N][K][3];
+    int par[N][K];
 #pragma unroll
-    for (int j = 0; j < K; j++) {
-        par[j] = -1;
-        if (j < k) {
-            const float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
-            c[j][0] = fn[0];
-            c[j][1] = fn[1];
-            c[j][2] = fn[2];
-            par[j] = (int)((unsigned)ent[j] >> kNodeBits);
+    for (int o = 0; o < N; o++) {
+        if (kk[o] > 0) {
+            const float* fh = f + 3 * (int64_t)home[o];
+            c0[o][0] = fh[0];
+            c0[o][1] = fh[1];
+            c0[o][2] = fh[2];
         }
-    }
-    unsigned has_child = 0;
 #pragma unroll
-    for (int q = 1; q < K; q++) {
-#pragma unroll
-        for (int j = 0; j < q; j++) {
-            if (par[j] == q + 1) {
-                c[q][0] = c[q][0] + c[j][0];
-                c[q][1] = c[q][1] + c[j][1];
-                c[q][2] = c[q][2] + c[j][2];
-                has_child |= 1u << q;
+        for (int j = 0; j < K; j++) {
+            par[o][j] = -1;
+            if (j < kk[o]) {
+                const float* fn = f + 3 * (int64_t)(ent[o][j] & kNodeMask);
+                c[o][j][0] = fn[0];
+                c[o][j][1] = fn[1];
+                c[o][j][2] = fn[2];
+                par[o][j] = (int)((unsigned)ent[o][j] >> kNodeBits);
             }
         }
     }
 #pragma unroll
-    for (int j = 0; j < K; j++) {
-        if (par[j] == 0) {
-            c0[0] = c0[0] + c[j][0];
-            c0[1] = c0[1] + c[j][1];
-            c0[2] = c0[2] + c[j][2];
-        }
-    }
-    fh[0] = c0[0];
-    fh[1] = c0[1];
-    fh[2] = c0[2];
+    for (int o = 0; o < N; o++) {
+        if (kk[o] <= 0) continue;
+        unsigned has_child = 0;
 #pragma unroll
-    for (int j = 0; j < K; j++) {
-        if (has_child >> j & 1u) {
-            float* fn = f + 3 * (int64_t)(ent[j] & kNodeMask);
-            fn[0] = c[j][0];
-            fn[1] = c[j][1];
-            fn[2] = c[j][2];
+        for (int q = 1; q < K; q++) {
+#pragma unroll
+            for (int j = 0; j < q; j++) {
+                if (par[o][j] == q + 1) {
+                    c[o][q][0] = c[o][q][0] + c[o][j][0];
+                    c[o][q][1] = c[o][q][1] + c[o][j][1];
+                    c[o][q][2] = c[o][q][2] + c[o][j][2];
+                    has_child |= 1u << q;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < K; j++) {
+            if (par[o][j] == 0) {
+                c0[o][0] = c0[o][0] + c[o][j][0];
+                c0[o][1] = c0[o][1] + c[o][j][1];
+                c0[o][2] = c0[o][2] + c[o][j][2];
+            }
+        }
+        float* fh = f + 3 * (int64_t)home[o];
+        fh[0] = c0[o][0];
+        fh[1] = c0[o][1];
+        fh[2] = c0[o][2];
+#pragma unroll
+        for (int j = 0; j < K; j++) {
+            if (has_child >> j & 1u) {
+                float* fn = f + 3 * (int64_t)(ent[o][j] & kNodeMask);
+                fn[0] = c[o][j][0];
+                fn[1] = c[o][j][1];
+                fn[2] = c[o][j][2];
+            }
         }
     }
 }
 
+template <int K>
+__device__ __forceinline__ void reduce_tree(float* f, int32_t home, int k, const int32_t (&ent)[K]) {
+    const int32_t h[1] = {home};
+    const int kk[1] = {k};
+    int32_t e[1][K];
+#pragma unroll
+    for (int j = 0; j < K; j++) e[0][j] = ent[j];
+    reduce_trees<K, 1>(f, h, kk, e);
+}
+
 // One thread per owner with copies.  Owners come in three record classes
 // (sorted by class, then by home slot): A -- up to 3 copies, one 16-byte
-// record {home | k << 26, three entries}; B -- up to 7 copies, two 16-byte
-// records; C -- more copies, {header, first entry} into the entry list,
-// reduced sequentially through memory in the same order.  A record is one
-// load, so the forces follow after a single dependent round trip.
-template <bool WIDE>
+// record {home | k << 26, three entries}; B -- up to 11 copies, three 16-byte
+// records; C -- more copies, {header, first entry} into the entry list.  A
+// record is one load, so the forces follow after a single dependent round
+// trip.  KB: copies held in registers for class B (7 or 11, the plan's
+// largest tree); KW: class C trees of up to KW copies in registers (0: none),
+// larger ones reduced sequentially through memory in the same order.
+template <int KB, int KW>
 __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* __restrict__ recA,
                                                           int64_t nA, const int4* __restrict__ recB,
                                                           int64_t nB, const int4* __restrict__ recC,
                                                           int64_t nC, const int32_t* __restrict__ fent) {
+    // blocks [0, tilesBC) take classes B and C, one owner per thread (the
+    // longer trees start first); the following blocks take class-A tiles of
+    // 2 * blockDim owners, two per thread (coalesced record loads), so both
+    // kinds of trees run side by side
+    const int64_t tilesA = (nA + 2 * kThreads - 1) / (2 * kThreads);
+    const int64_t tilesBC = (nB + nC + kThreads - 1) / kThreads;
     const int64_t n = nA + nB + nC;
-    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n;
-         m += (int64_t)gridDim.x * blockDim.x) {
-        if (m < nA) {
-            const int4 r = __ldg(recA + m);
-            const int32_t ent[3] = {r.y, r.z, r.w};
-            reduce_tree<3>(f, r.x & kNodeMask, (int)((unsigned)r.x >> kNodeBits), ent);
-        } else if (m < nA + nB) {
-            const int4 r0 = __ldg(recB + 2 * (m - nA)), r1 = __ldg(recB + 2 * (m - nA) + 1);
-            const int32_t ent[7] = {r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-            reduce_tree<7>(f, r0.x & kNodeMask, (int)((unsigned)r0.x >> kNodeBits), ent);
+    for (int64_t bb = blockIdx.x; bb < tilesA + tilesBC; bb += gridDim.x) {
+        if (bb >= tilesBC) {
+            const int64_t b = bb - tilesBC;
+            const int64_t m0 = b * 2 * kThreads + threadIdx.x, m1 = m0 + kThreads;
+            const int4 r0 = m0 < nA ? __ldg(recA + m0) : make_int4(0, 0, 0, 0);
+            const int4 r1 = m1 < nA ? __ldg(recA + m1) : make_int4(0, 0, 0, 0);
+            const int32_t home[2] = {r0.x & kNodeMask, r1.x & kNodeMask};
+            const int kk[2] = {m0 < nA ? (int)((unsigned)r0.x >> kNodeBits) : 0,
+                               m1 < nA ? (int)((unsigned)r1.x >> kNodeBits) : 0};
+            const int32_t ent[2][3] = {{r0.y, r0.z, r0.w}, {r1.y, r1.z, r1.w}};
+            reduce_trees<3, 2>(f, home, kk, ent);
+            continue;
+        }
+        const int64_t m = nA + bb * kThreads + threadIdx.x;
+        if (m >= n) continue;
+        if (m < nA + nB) {
+            const int4 r0 = __ldg(recB + 3 * (m - nA)), r1 = __ldg(recB + 3 * (m - nA) + 1);
+            const int4 r2 = KB > 7 ? __ldg(recB + 3 * (m - nA) + 2) : make_int4(0, 0, 0, 0);
+            const int32_t all[11] = {r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w, r2.x, r2.y, r2.z, r2.w};
+            int32_t ent[KB];
+#pragma unroll
+            for (int j = 0; j < KB; j++) ent[j] = all[j];
+            reduce_tree<KB>(f, r0.x & kNodeMask, (int)((unsigned)r0.x >> kNodeBits), ent);
         } else {
             const int4 r = __ldg(recC + (m - nA - nB));
-            if (WIDE && ((unsigned)r.x >> kNodeBits) <= 16) {
-                // plans with deeper trees (several pulses per dim): up to 16
-                // copies in registers
-                const int k = (int)((unsigned)r.x >> kNodeBits);
-                int32_t ent[16];
+            if constexpr (KW > 0) {
+                if (((unsigned)r.x >> kNodeBits) <= (unsigned)KW) {
+                    // plans with deeper trees (several pulses per dim): up to
+                    // KW copies in registers
+                    const int k = (int)((unsigned)r.x >> kNodeBits);
+                    int32_t ent[KW];
 #pragma unroll
-                for (int j = 0; j < 16; j++) ent[j] = j < k ? __ldg(fent + r.y + j) : 0;
-                reduce_tree<16>(f, r.x & kNodeMask, k, ent);
-                continue;
+                    for (int j = 0; j < KW; j++) ent[j] = j < k ? __ldg(fent + r.y + j) : 0;
+                    reduce_tree<KW>(f, r.x & kNodeMask, k, ent);
+                    continue;
+                }
             }
             // every slot of this tree belongs to this thread alone: plain
             // sequential read-modify-write in the same order, through L2
@@ -341,14 +404,14 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
     }
 }
 
-// Record classes of the owners (A: k <= 3, B: k <= 7, C: more).
+// Record classes of the owners (A: k <= 3, B: k <= 11, C: more).
 __global__ void owner_class_kernel(const int32_t* __restrict__ fstart, int64_t n_owners,
                                    int32_t* __restrict__ isA, int32_t* __restrict__ isB) {
     for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
          m += (int64_t)gridDim.x * blockDim.x) {
         const int k = fstart[m + 1] - fstart[m];
         isA[m] = k <= 3 ? 1 : 0;
-        isB[m] = (k > 3 && k <= 7) ? 1 : 0;
+        isB[m] = (k > 3 && k <= 11) ? 1 : 0;
     }
 }
 
@@ -361,13 +424,14 @@ __global__ void owner_record_kernel(const int32_t* __restrict__ fown, const int3
          m += (int64_t)gridDim.x * blockDim.x) {
         const int s0 = fstart[m], k = fstart[m + 1] - s0;
         const int32_t hdr = fown[m] | (k << kNodeBits);
-        int32_t e[7] = {0, 0, 0, 0, 0, 0, 0};
-        for (int j = 0; j < k && j < 7; j++) e[j] = fent[s0 + j];
+        int32_t e[11] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < k && j < 11; j++) e[j] = fent[s0 + j];
         if (k <= 3) {
             recA[posA[m]] = make_int4(hdr, e[0], e[1], e[2]);
-        } else if (k <= 7) {
-            recB[2 * (int64_t)posB[m]] = make_int4(hdr, e[0], e[1], e[2]);
-            recB[2 * (int64_t)posB[m] + 1] = make_int4(e[3], e[4], e[5], e[6]);
+        } else if (k <= 11) {
+            recB[3 * (int64_t)posB[m]] = make_int4(hdr, e[0], e[1], e[2]);
+            recB[3 * (int64_t)posB[m] + 1] = make_int4(e[3], e[4], e[5], e[6]);
+            recB[3 * (int64_t)posB[m] + 2] = make_int4(e[7], e[8], e[9], e[10]);
         } else {
             const int64_t c = m - posA[m] - posB[m];  // class-C owners before m
             recC[c] = make_int4(hdr, s0, 0, 0);
@@ -403,7 +467,13 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
     const int nd = pl->n_dom, P = pl->P;
     if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
-    // coordinate items: halo range of every domain, in chunks
+    // coordinate items: halo range of every domain, in chunks of 256 * E
+    // slots; smaller chunks when the halo is too small to give every SM a
+    // few blocks of 1024
+    int E = 4;
+    while (E > 1 && H / (kThreads * E) < 4 * (int64_t)pl->num_sms) E /= 2;
+    pl->flat_x_e = E;
+    const int kFlatChunk = kThreads * E;
     std::vector<int4> items;
     int64_t k = 0;
     for (int D = 0; D < nd; D++) {
@@ -520,7 +590,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             pl->n_rec[1] = (int64_t)tail[2] + tail[3];
             pl->n_rec[2] = n_owners - pl->n_rec[0] - pl->n_rec[1];
             if ((rc = dev_alloc(&pl->d_frec[0], (size_t)std::max<int64_t>(pl->n_rec[0], 1))) != HALO_OK) break;
-            if ((rc = dev_alloc(&pl->d_frec[1], (size_t)std::max<int64_t>(2 * pl->n_rec[1], 1))) != HALO_OK) break;
+            if ((rc = dev_alloc(&pl->d_frec[1], (size_t)std::max<int64_t>(3 * pl->n_rec[1], 1))) != HALO_OK) break;
             if ((rc = dev_alloc(&pl->d_frec[2], (size_t)std::max<int64_t>(pl->n_rec[2], 1))) != HALO_OK) break;
             owner_record_kernel<<<gbo, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB,
                                                           n_owners, pl->d_frec[0], pl->d_frec[1],
@@ -558,21 +628,35 @@ int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st) {
 
 int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     if (pl->n_xflat_items == 0) return HALO_OK;
-    flat_x_kernel<kFlatChunk / kThreads><<<pl->n_xflat_items, kThreads, 0, st>>>(
-        xyz, pl->d_xflat, pl->d_xflat_items, pl->box[0], pl->box[1], pl->box[2]);
+    if (pl->flat_x_e == 4)
+        flat_x_kernel<4><<<pl->n_xflat_items, kThreads, 0, st>>>(xyz, pl->d_xflat, pl->d_xflat_items,
+                                                                 pl->box[0], pl->box[1], pl->box[2]);
+    else if (pl->flat_x_e == 2)
+        flat_x_kernel<2><<<pl->n_xflat_items, kThreads, 0, st>>>(xyz, pl->d_xflat, pl->d_xflat_items,
+                                                                 pl->box[0], pl->box[1], pl->box[2]);
+    else
+        flat_x_kernel<1><<<pl->n_xflat_items, kThreads, 0, st>>>(xyz, pl->d_xflat, pl->d_xflat_items,
+                                                                 pl->box[0], pl->box[1], pl->box[2]);
     pl->launches_x++;
     return cuda_code(cudaGetLastError());
 }
 
 int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
     if (pl->n_owners == 0) return HALO_OK;
-    const int gb = blocks_for(pl->n_owners, pl->num_sms);
-    if (pl->max_copies > 7)
-        flat_f_kernel<true><<<gb, kThreads, 0, st>>>(f, pl->d_frec[0], pl->n_rec[0], pl->d_frec[1],
-                                                     pl->n_rec[1], pl->d_frec[2], pl->n_rec[2], pl->d_fent);
+    // class A goes two owners per thread, classes B and C one per thread
+    const int64_t tilesA = (pl->n_rec[0] + 2 * kThreads - 1) / (2 * kThreads);
+    const int64_t tilesBC = (pl->n_rec[1] + pl->n_rec[2] + kThreads - 1) / kThreads;
+    const int gb = (int)std::max<int64_t>(1, std::min<int64_t>(tilesA + tilesBC, (int64_t)pl->num_sms * 16));
+#define HALO_FLAT_F(KB, KW)                                                                      \
+    flat_f_kernel<KB, KW><<<gb, kThreads, 0, st>>>(f, pl->d_frec[0], pl->n_rec[0], pl->d_frec[1],  \
+                                                   pl->n_rec[1], pl->d_frec[2], pl->n_rec[2], pl->d_fent)
+    if (pl->max_copies <= 7)
+        HALO_FLAT_F(7, 0);
+    else if (pl->max_copies <= 11)
+        HALO_FLAT_F(11, 0);
     else
-        flat_f_kernel<false><<<gb, kThreads, 0, st>>>(f, pl->d_frec[0], pl->n_rec[0], pl->d_frec[1],
-                                                      pl->n_rec[1], pl->d_frec[2], pl->n_rec[2], pl->d_fent);
+        HALO_FLAT_F(11, 16);
+#undef HALO_FLAT_F
     pl->launches_f++;
     return cuda_code(cudaGetLastError());
 }
