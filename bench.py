@@ -177,16 +177,20 @@ def setup_workload(name, device):
     return w, xyz, dom, x, plan, loc, f0
 
 
-def time_steps(plan, loc, f, steps, warmup, flush, stream, sampler=None, barrier=None):
-    """Per-step CUDA-event timing of x and f; returns lists of (x_ms, f_ms)."""
+def time_steps(plan, loc, f, steps, warmup, flush, stream, sampler=None, barrier=None,
+               split_steps=None):
+    """CUDA-event timing of K steps.  Pass 1 (the timed region): one event pair
+    around each step's x + f.  Pass 2 (split_steps, after it): an extra event
+    between x and f, for the per-kernel split used by the roofline.  Returns
+    (step_ms list, x_ms list, f_ms list, wall, clocks, launches in pass 1)."""
     import torch
     for _ in range(warmup):
         flush()
         plan.exchange_x(loc, stream)
         plan.exchange_f(f, stream)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
     if barrier:
         barrier()
     torch.cuda.synchronize()
@@ -194,11 +198,10 @@ def time_steps(plan, loc, f, steps, warmup, flush, stream, sampler=None, barrier
         sampler.start()
     lx0, lf0 = plan.launch_counts()
     t0 = time.perf_counter()
-    for a, b, c in ev:
+    for a, c in ev:
         flush()
         a.record(stream)
         plan.exchange_x(loc, stream)
-        b.record(stream)
         plan.exchange_f(f, stream)
         c.record(stream)
     torch.cuda.synchronize()
@@ -207,9 +210,52 @@ def time_steps(plan, loc, f, steps, warmup, flush, stream, sampler=None, barrier
         barrier()
     clocks = sampler.stop() if sampler else None
     lx1, lf1 = plan.launch_counts()
-    xs = [a.elapsed_time(b) for a, b, c in ev]
-    fs = [b.elapsed_time(c) for a, b, c in ev]
-    return xs, fs, wall, clocks, (lx1 - lx0) + (lf1 - lf0)
+    steps_ms = [a.elapsed_time(c) for a, c in ev]
+    n2 = steps if split_steps is None else split_steps
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(n2)]
+    for a, b, c in ev2:
+        flush()
+        a.record(stream)
+        plan.exchange_x(loc, stream)
+        b.record(stream)
+        plan.exchange_f(f, stream)
+        c.record(stream)
+    torch.cuda.synchronize()
+    xs = [a.elapsed_time(b) for a, b, c in ev2]
+    fs = [b.elapsed_time(c) for a, b, c in ev2]
+    return steps_ms, xs, fs, wall, clocks, (lx1 - lx0) + (lf1 - lf0)
+
+
+def time_graph_steps(plan, loc, f, steps, warmup, flush, stream):
+    """x + f captured once as a CUDA graph; per-step CUDA-event time of one
+    replay, L2 flushed between steps."""
+    import torch
+    side = torch.cuda.Stream(device=loc.device)
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        plan.exchange_x(loc, side)
+        plan.exchange_f(f, side)
+        with torch.cuda.graph(g, stream=side):
+            plan.exchange_x(loc, side)
+            plan.exchange_f(f, side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        flush()
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    cur = torch.cuda.current_stream()
+    for a, b in ev:
+        flush()
+        a.record(cur)
+        g.replay()
+        b.record(cur)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def make_flush(device):
@@ -277,9 +323,9 @@ def rebuild_case(device, stream, flush, steps, warmup, reps=5):
     for mode in ("fused", "flat"):
         plan.set_mode(mode)
         f = f0.clone()
-        xs, fs, _, _, _ = time_steps(plan, loc, f, steps, warmup, flush, stream)
+        sts, xs, fs, _, _, _ = time_steps(plan, loc, f, steps, warmup, flush, stream, split_steps=50)
         assert plan.status() == 0
-        ex_us = 1e3 * statistics.fmean(a + b for a, b in zip(xs, fs))
+        ex_us = 1e3 * statistics.fmean(sts)
         times = []
         for k in range(1, reps + 1):
             xk, dk = synth.displaced(xyz, w.box, w.grid, k)
@@ -409,16 +455,17 @@ def main():
         f = f0.clone()
         sampler = ClockSampler(gpu_index(local)) if mode == args.mode else None
         steps = args.steps if mode == args.mode else min(args.steps, 500)
-        xs, fs, wall, clocks, launches = time_steps(plan, loc, f, steps, args.warmup, flush,
-                                                    stream, sampler, barrier)
+        sts, xs, fs, wall, clocks, launches = time_steps(plan, loc, f, steps, args.warmup, flush,
+                                                         stream, sampler, barrier,
+                                                         split_steps=min(steps, 500))
         code = plan.status()
         if code != 0:
             raise SystemExit("device error %d during the timed region" % code)
         if mode != args.mode:
-            others[mode] = {"us_per_exchange": 1e3 * statistics.fmean(a + b for a, b in zip(xs, fs)),
+            others[mode] = {"us_per_exchange": 1e3 * statistics.fmean(sts),
                             "us_x": 1e3 * statistics.fmean(xs), "us_f": 1e3 * statistics.fmean(fs),
                             "launches_per_step": launches / steps}
-    step_ms = statistics.fmean(a + b for a, b in zip(xs, fs))
+    step_ms = statistics.fmean(sts)
     x_ms, f_ms = statistics.fmean(xs), statistics.fmean(fs)
     step_ms, x_ms, f_ms = max_over_ranks([step_ms, x_ms, f_ms], device, dist)
     halo_slots = plan.n_halo_total
@@ -443,12 +490,21 @@ def main():
     for mode in modes:
         lplan.set_mode(mode)
         lf = lf0.clone()
-        lxs, lfs, _, _, llaunch = time_steps(lplan, lloc, lf, lsteps, args.warmup, flush, stream)
+        lsts, lxs, lfs, _, _, llaunch = time_steps(lplan, lloc, lf, lsteps, args.warmup, flush, stream)
         assert lplan.status() == 0
-        lat[mode] = {"us_per_exchange": 1e3 * statistics.fmean(a + b for a, b in zip(lxs, lfs)),
+        lat[mode] = {"us_per_exchange": 1e3 * statistics.fmean(lsts),
                      "us_x": 1e3 * statistics.fmean(lxs), "us_f": 1e3 * statistics.fmean(lfs),
                      "launches_per_direction": llaunch / (2 * lsteps)}
     lplan.close()
+    plan.set_mode(args.mode)
+
+    # the same step captured as a CUDA graph (one graph launch per x + f)
+    graph = {}
+    for mode in (args.mode, "fused"):
+        plan.set_mode(mode)
+        gs = time_graph_steps(plan, loc, f0.clone(), min(args.steps, 1000), args.warmup, flush, stream)
+        assert plan.status() == 0
+        graph[mode] = {"us_per_exchange": 1e3 * statistics.fmean(gs)}
     plan.set_mode(args.mode)
 
     rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
@@ -482,6 +538,7 @@ def main():
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": per_slot * halo_slots},
             "other_modes": others,
+            "cuda_graph": graph,
             "latency_case": lat,
             "rebuild_case": rebuild,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

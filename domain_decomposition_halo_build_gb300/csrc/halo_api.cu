@@ -89,7 +89,7 @@ int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, 
     const cudaStream_t st = as_stream(stream);
     pl->trace = nullptr;  // item counts change with the plan: the caller re-arms tracing
     pl->trace_cap = 0;
-    halo::free_flat(pl);  // the flattened tables describe the previous plan
+    pl->flat_ready = false;  // the flattened tables describe the previous plan
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
     HALO_TRY(halo::prepare_exchange(pl, st));
     if (pl->mode == HALO_MODE_FLAT) return halo::prepare_flat(pl, st);

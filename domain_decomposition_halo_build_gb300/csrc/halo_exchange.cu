@@ -455,11 +455,10 @@ int grid_cells(const halo_plan* pl, int D, int c[3]) {
 }
 
 template <class T>
-int upload(T** d, const std::vector<T>& h) {
-    dev_free(*d);
-    HALO_TRY(dev_alloc(d, h.size()));
+int upload(T** d, int64_t* cap, const std::vector<T>& h, cudaStream_t st) {
+    HALO_TRY(dev_reserve(d, cap, (int64_t)h.size()));
     if (!h.empty())
-        HALO_CUDA(cudaMemcpy(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice));
+        HALO_CUDA(cudaMemcpyAsync(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice, st));
     return HALO_OK;
 }
 
@@ -485,6 +484,8 @@ void free_exchange(halo_plan* pl) {
     dev_free(pl->d_err);
     pl->fpairs_cap = 0;
     pl->wmax_cap = 0;
+    pl->cap_sp = pl->cap_items_x = pl->cap_items_f = pl->cap_target = pl->cap_flags = 0;
+    pl->cap_nindep = 0;
 }
 
 int reset_flags(halo_plan* pl, cudaStream_t st) {
@@ -534,24 +535,15 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
             pl->max_chunks[p] = std::max(pl->max_chunks[p], (x.send + kThreads - 1) / kThreads);
         }
     }
-    HALO_TRY(upload(&pl->d_sp, pl->sp));
+    HALO_TRY(upload(&pl->d_sp, &pl->cap_sp, pl->sp, st));
 
     // force-entry classification on the device: last pulse adding into each
     // slot, then a stable independent/dependent partition per (s, p)
     std::vector<int32_t> nindep(nsp, 0);
     if (P > 0) {
-        if (pl->n_local_total > pl->wmax_cap) {
-            dev_free(pl->d_wmax);
-            HALO_TRY(dev_alloc(&pl->d_wmax, (size_t)pl->n_local_total));
-            pl->wmax_cap = pl->n_local_total;
-        }
-        if (pl->n_halo_total > pl->fpairs_cap || !pl->d_fpairs) {
-            dev_free(pl->d_fpairs);
-            HALO_TRY(dev_alloc(&pl->d_fpairs, (size_t)std::max<int64_t>(pl->n_halo_total, 1)));
-            pl->fpairs_cap = pl->n_halo_total;
-        }
-        dev_free(pl->d_nindep);
-        HALO_TRY(dev_alloc(&pl->d_nindep, nsp));
+        HALO_TRY(dev_reserve(&pl->d_wmax, &pl->wmax_cap, pl->n_local_total));
+        HALO_TRY(dev_reserve(&pl->d_fpairs, &pl->fpairs_cap, pl->n_halo_total));
+        HALO_TRY(dev_reserve(&pl->d_nindep, &pl->cap_nindep, (int64_t)nsp));
         HALO_CUDA(cudaMemsetAsync(pl->d_wmax, 0xff, (size_t)pl->n_local_total, st));
         for (int p = 0; p < P; p++) {
             const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
@@ -639,11 +631,10 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
     }
     pl->n_items_x = (int)ix.size();
     pl->n_items_f = (int)iff.size();
-    HALO_TRY(upload(&pl->d_items_x, ix));
-    HALO_TRY(upload(&pl->d_items_f, iff));
-    HALO_TRY(upload(&pl->d_target, target));
-    dev_free(pl->d_flags);
-    HALO_TRY(dev_alloc(&pl->d_flags, 2 * nsp));
+    HALO_TRY(upload(&pl->d_items_x, &pl->cap_items_x, ix, st));
+    HALO_TRY(upload(&pl->d_items_f, &pl->cap_items_f, iff, st));
+    HALO_TRY(upload(&pl->d_target, &pl->cap_target, target, st));
+    HALO_TRY(dev_reserve(&pl->d_flags, &pl->cap_flags, (int64_t)(2 * nsp)));
     if (!pl->d_tickets) HALO_TRY(dev_alloc(&pl->d_tickets, 2));
     if (!pl->d_err) HALO_TRY(dev_alloc(&pl->d_err, 8));
     int bx = 1, bf = 1;

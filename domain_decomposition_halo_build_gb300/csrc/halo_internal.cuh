@@ -97,6 +97,8 @@ struct halo_plan {
     halo::SPDesc* d_sp = nullptr;
     halo::XItem* d_items_x = nullptr;
     halo::FItem* d_items_f = nullptr;
+    int64_t cap_sp = 0, cap_items_x = 0, cap_items_f = 0, cap_target = 0, cap_flags = 0,
+            cap_nindep = 0;
     int n_items_x = 0, n_items_f = 0;
     std::vector<int32_t> max_chunks;  // per pulse: most chunks of one sender (utility grids)
     int chunk = 256;                // entries per work item
@@ -128,6 +130,11 @@ struct halo_plan {
     int32_t* d_fent = nullptr;       // per copy, in reduction order: node slot | parent << 26
     int64_t n_owners = 0;
     int max_copies = 0;
+    int64_t cap_xflat = 0, cap_xflat_items = 0, cap_fent = 0, cap_fown = 0, cap_fstart = 0;
+    int64_t cap_frec[3] = {0, 0, 0};
+    int32_t* d_flat_pool32 = nullptr;  // scratch of the flat-table build (kept across rebuilds)
+    int8_t* d_flat_pool8 = nullptr;
+    int64_t cap_pool32 = 0, cap_pool8 = 0;
     int4* d_frec[3] = {nullptr, nullptr, nullptr};  // owner records: A (<=3), B (<=7), C (more)
     int64_t n_rec[3] = {0, 0, 0};
     int flat_x_e = 4;                // entries per thread of the flat coordinate kernel
@@ -184,6 +191,21 @@ template <class T>
 inline void dev_free(T*& p) {
     if (p) cudaFree((void*)p);
     p = nullptr;
+}
+
+// Grow-only device buffer: reallocates (with 25 % headroom) only when `count`
+// exceeds the capacity, so rebuilds of a plan do not free and re-allocate
+// (cudaFree synchronises the device).
+template <class T>
+inline int dev_reserve(T** p, int64_t* cap, int64_t count) {
+    if (*p && *cap >= count) return HALO_OK;
+    dev_free(*p);
+    *cap = 0;
+    int64_t want = count < 1 ? 1 : count;
+    want += want / 4;
+    const int rc = dev_alloc(p, (size_t)want);
+    if (rc == HALO_OK) *cap = want;
+    return rc;
 }
 
 }  // namespace halo

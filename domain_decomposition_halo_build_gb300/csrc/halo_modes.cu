@@ -452,10 +452,15 @@ void free_flat(halo_plan* pl) {
     dev_free(pl->d_fown);
     dev_free(pl->d_fstart);
     dev_free(pl->d_fent);
+    dev_free(pl->d_flat_pool32);
+    dev_free(pl->d_flat_pool8);
     for (int c = 0; c < 3; c++) {
         dev_free(pl->d_frec[c]);
         pl->n_rec[c] = 0;
+        pl->cap_frec[c] = 0;
     }
+    pl->cap_xflat = pl->cap_xflat_items = pl->cap_fent = pl->cap_fown = pl->cap_fstart = 0;
+    pl->cap_pool32 = pl->cap_pool8 = 0;
     pl->flat_ready = false;
     pl->n_xflat_items = 0;
     pl->n_owners = 0;
@@ -463,7 +468,7 @@ void free_flat(halo_plan* pl) {
 }
 
 int prepare_flat(halo_plan* pl, cudaStream_t st) {
-    free_flat(pl);
+    pl->flat_ready = false;  // buffers are kept (grow-only) across rebuilds
     const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
     const int nd = pl->n_dom, P = pl->P;
     if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
@@ -485,43 +490,30 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         k += nh;
     }
     pl->n_xflat_items = (int)items.size();
-    HALO_TRY(dev_alloc(&pl->d_xflat_items, items.size()));
+    HALO_TRY(dev_reserve(&pl->d_xflat_items, &pl->cap_xflat_items, (int64_t)items.size()));
     if (!items.empty())
-        HALO_CUDA(cudaMemcpy(pl->d_xflat_items, items.data(), items.size() * sizeof(int4),
-                             cudaMemcpyHostToDevice));
-    HALO_TRY(dev_alloc(&pl->d_xflat, (size_t)std::max<int64_t>(H, 1)));
-    HALO_TRY(dev_alloc(&pl->d_fent, (size_t)std::max<int64_t>(H, 1)));
+        HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, items.data(), items.size() * sizeof(int4),
+                                  cudaMemcpyHostToDevice, st));
+    HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat, H));
+    HALO_TRY(dev_reserve(&pl->d_fent, &pl->cap_fent, H));
 
-    // scratch for the build of the tables
-    int32_t *owner = nullptr, *parent = nullptr, *ncopies = nullptr, *entry_pos = nullptr,
-            *flag = nullptr, *owner_idx = nullptr, *tmp = nullptr, *scan_tmp = nullptr, *misc = nullptr;
-    int8_t *hop = nullptr, *code = nullptr;
+    // scratch of the table build, carved from two pools kept in the plan
+    const int64_t nsc = nl / kScanTile + 2;
+    HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, 6 * nl + std::max<int64_t>(H, 1) + nsc + 8));
+    HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
+    int32_t* owner = pl->d_flat_pool32;
+    int32_t* parent = owner + nl;
+    int32_t* ncopies = parent + nl;
+    int32_t* entry_pos = ncopies + nl;
+    int32_t* flag = entry_pos + nl;
+    int32_t* owner_idx = flag + nl;
+    int32_t* tmp = owner_idx + nl;
+    int32_t* scan_tmp = tmp + std::max<int64_t>(H, 1);
+    int32_t* misc = scan_tmp + nsc;
+    int8_t* hop = pl->d_flat_pool8;
+    int8_t* code = hop + nl;
     int rc = HALO_OK;
-    auto cleanup = [&]() {
-        dev_free(owner);
-        dev_free(parent);
-        dev_free(ncopies);
-        dev_free(entry_pos);
-        dev_free(flag);
-        dev_free(owner_idx);
-        dev_free(tmp);
-        dev_free(scan_tmp);
-        dev_free(misc);
-        dev_free(hop);
-        dev_free(code);
-    };
     do {
-        if ((rc = dev_alloc(&owner, (size_t)nl)) != HALO_OK) break;
-        if ((rc = dev_alloc(&parent, (size_t)nl)) != HALO_OK) break;
-        if ((rc = dev_alloc(&ncopies, (size_t)nl)) != HALO_OK) break;
-        if ((rc = dev_alloc(&entry_pos, (size_t)nl)) != HALO_OK) break;
-        if ((rc = dev_alloc(&flag, (size_t)nl)) != HALO_OK) break;
-        if ((rc = dev_alloc(&owner_idx, (size_t)nl)) != HALO_OK) break;
-        if ((rc = dev_alloc(&tmp, (size_t)std::max<int64_t>(H, 1))) != HALO_OK) break;
-        if ((rc = dev_alloc(&scan_tmp, (size_t)(nl / kScanTile + 2))) != HALO_OK) break;
-        if ((rc = dev_alloc(&misc, 4)) != HALO_OK) break;
-        if ((rc = dev_alloc(&hop, (size_t)nl)) != HALO_OK) break;
-        if ((rc = dev_alloc(&code, (size_t)nl)) != HALO_OK) break;
         const int gb = blocks_for(nl, pl->num_sms);
         chain_init_kernel<<<gb, kThreads, 0, st>>>(owner, parent, hop, code, nl);
         for (int p = 0; p < P; p++) {
@@ -544,8 +536,8 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
         const int64_t n_owners = (int64_t)last[0] + last[1];
         pl->n_owners = n_owners;
-        if ((rc = dev_alloc(&pl->d_fown, (size_t)std::max<int64_t>(n_owners, 1))) != HALO_OK) break;
-        if ((rc = dev_alloc(&pl->d_fstart, (size_t)n_owners + 1)) != HALO_OK) break;
+        if ((rc = dev_reserve(&pl->d_fown, &pl->cap_fown, n_owners)) != HALO_OK) break;
+        if ((rc = dev_reserve(&pl->d_fstart, &pl->cap_fstart, n_owners + 1)) != HALO_OK) break;
         owner_list_kernel<<<gb, kThreads, 0, st>>>(ncopies, entry_pos, owner_idx, nl, pl->d_fown,
                                                    pl->d_fstart);
         const int32_t Hi = (int32_t)H;
@@ -589,9 +581,9 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             pl->n_rec[0] = (int64_t)tail[0] + tail[1];
             pl->n_rec[1] = (int64_t)tail[2] + tail[3];
             pl->n_rec[2] = n_owners - pl->n_rec[0] - pl->n_rec[1];
-            if ((rc = dev_alloc(&pl->d_frec[0], (size_t)std::max<int64_t>(pl->n_rec[0], 1))) != HALO_OK) break;
-            if ((rc = dev_alloc(&pl->d_frec[1], (size_t)std::max<int64_t>(3 * pl->n_rec[1], 1))) != HALO_OK) break;
-            if ((rc = dev_alloc(&pl->d_frec[2], (size_t)std::max<int64_t>(pl->n_rec[2], 1))) != HALO_OK) break;
+            if ((rc = dev_reserve(&pl->d_frec[0], &pl->cap_frec[0], pl->n_rec[0])) != HALO_OK) break;
+            if ((rc = dev_reserve(&pl->d_frec[1], &pl->cap_frec[1], 3 * pl->n_rec[1])) != HALO_OK) break;
+            if ((rc = dev_reserve(&pl->d_frec[2], &pl->cap_frec[2], pl->n_rec[2])) != HALO_OK) break;
             owner_record_kernel<<<gbo, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB,
                                                           n_owners, pl->d_frec[0], pl->d_frec[1],
                                                           pl->d_frec[2]);
@@ -599,11 +591,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             if ((rc = cuda_code(cudaGetLastError())) != HALO_OK) break;
         }
     } while (false);
-    cleanup();
-    if (rc != HALO_OK) {
-        free_flat(pl);
-        return rc;
-    }
+    if (rc != HALO_OK) return rc;
     pl->flat_ready = true;
     return HALO_OK;
 }

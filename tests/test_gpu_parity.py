@@ -244,3 +244,46 @@ def test_determinism_repeated(cases):
             np.testing.assert_array_equal(out[0], ref[0])
             np.testing.assert_array_equal(out[1], ref[1])
     assert g.plan.status() == 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_cuda_graph_replay(cases, mode):
+    """x + f captured once in a CUDA graph and replayed three times: the fused
+    kernels' epochs come from their ever-increasing tickets, so replays (and
+    direct calls mixed with them) stay exact."""
+    import torch
+    w, xyz, dom, o, g = cases("water24k_2x4x8")
+    g.plan.set_mode(mode)
+    try:
+        loc = g.plan.load_home(g.xyz_d)
+        f0 = synth.forces(o.n_local_total, seed=4)
+        f = torch.from_numpy(f0).cuda()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            g.plan.exchange_x(loc)          # warm-up outside capture, on the capture stream
+            g.plan.exchange_f(torch.zeros_like(f))
+            with torch.cuda.graph(graph, stream=s):
+                g.plan.exchange_x(loc)
+                g.plan.exchange_f(f)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        want_x = o.load_home(xyz)
+        o.exchange_x(want_x)
+        want_f = f0.copy()
+        for rep in range(3):
+            loc.copy_(g.plan.load_home(g.xyz_d))
+            graph.replay()
+            o.exchange_f(want_f)
+            torch.cuda.synchronize()
+            assert g.plan.status() == 0
+            np.testing.assert_array_equal(bits(loc.cpu().numpy()), bits(want_x))
+            np.testing.assert_array_equal(bits(f.cpu().numpy()), bits(want_f), err_msg="replay %d" % rep)
+        # a direct call after the replays still agrees
+        g.plan.exchange_f(f)
+        o.exchange_f(want_f)
+        assert g.plan.status() == 0
+        np.testing.assert_array_equal(bits(f.cpu().numpy()), bits(want_f))
+    finally:
+        g.plan.set_mode("fused")
