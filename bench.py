@@ -307,6 +307,64 @@ def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
     return ms, h2d, d2h
 
 
+def overlap_case(plan, loc, f, steps, warmup, flush, mode, device, priority=0):
+    """The GPU-resident step schedule of Algorithm 2 (page "Redesigning GROMACS
+    Halo Exchange ...", section 3): a stand-in for the local non-bonded kernel
+    (a bf16 matmul, tensor cores) runs on a local stream while the coordinate
+    exchange and the force reduction run on a non-local stream.  Metrics as the
+    page defines them (section 6): local work (start to end of the local
+    kernel), non-local work (first pack start to last unpack end) and
+    non-overlap (local end to last unpack end, clamped at 0)."""
+    import torch
+    plan.set_mode(mode)
+    a = torch.randn(2048, 4096, device=device, dtype=torch.bfloat16)
+    b = torch.randn(4096, 4096, device=device, dtype=torch.bfloat16)
+    c = torch.empty(2048, 4096, device=device, dtype=torch.bfloat16)
+    s_loc = torch.cuda.Stream(device=device)
+    s_nl = torch.cuda.Stream(device=device, priority=priority)
+    main = torch.cuda.current_stream(device)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def step(rec):
+        flush()
+        e0 = ev()
+        e0.record(main)
+        s_loc.wait_event(e0)
+        s_nl.wait_event(e0)
+        l0, l1, n0, n1 = ev(), ev(), ev(), ev()
+        l0.record(s_loc)
+        with torch.cuda.stream(s_loc):
+            torch.mm(a, b, out=c)
+        l1.record(s_loc)
+        n0.record(s_nl)
+        plan.exchange_x(loc, s_nl)
+        plan.exchange_f(f, s_nl)
+        n1.record(s_nl)
+        main.wait_stream(s_loc)
+        main.wait_stream(s_nl)
+        rec.append((e0, l0, l1, n0, n1))
+
+    tmp = []
+    for _ in range(warmup):
+        step(tmp)
+    torch.cuda.synchronize()
+    rec = []
+    for _ in range(steps):
+        step(rec)
+    torch.cuda.synchronize()
+    loc_us = [1e3 * l0.elapsed_time(l1) for e0, l0, l1, n0, n1 in rec]
+    nl_us = [1e3 * n0.elapsed_time(n1) for e0, l0, l1, n0, n1 in rec]
+    nov = [max(0.0, 1e3 * l1.elapsed_time(n1)) for e0, l0, l1, n0, n1 in rec]
+    step_us = [1e3 * max(e0.elapsed_time(l1), e0.elapsed_time(n1)) for e0, l0, l1, n0, n1 in rec]
+    assert plan.status() == 0
+    return {"mode": mode, "local_us": statistics.fmean(loc_us), "nonlocal_us": statistics.fmean(nl_us),
+            "non_overlap_us": statistics.fmean(nov), "step_us": statistics.fmean(step_us),
+            "nonlocal_stream_priority": priority,
+            "local_stand_in": "bf16 matmul 2048x4096x4096 on a second stream"}
+
+
 REBUILD_WORKLOAD = "water3M_8x8x8"
 
 
@@ -508,6 +566,9 @@ def main():
     plan.set_mode(args.mode)
 
     rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
+    overlap = [overlap_case(plan, loc, f0.clone(), min(args.steps, 300), args.warmup, flush, m, device,
+                            prio) for m in (args.mode, "fused") for prio in (0, -1)]
+    plan.set_mode(args.mode)
 
     # end to end through the public API with host buffers
     e2e_ms, h2d, d2h = e2e_steps(w, xyz, plan, max(20, min(args.steps, 200)), 5, device, stream)
@@ -541,6 +602,7 @@ def main():
             "cuda_graph": graph,
             "latency_case": lat,
             "rebuild_case": rebuild,
+            "overlap_case": overlap,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms},
             "gpu_launches": launches,
