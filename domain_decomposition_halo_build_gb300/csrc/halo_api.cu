@@ -81,6 +81,8 @@ void destroy_plan(halo_plan* pl) {
         halo::free_exchange(pl);
         halo::free_flat(pl);
         halo::free_build(pl);
+        if (pl->h_stage) cudaFreeHost(pl->h_stage);
+        pl->h_stage = nullptr;
     }
     delete pl;
 }

@@ -543,8 +543,10 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
     want = std::max(want, pl->cap_slots);
 
     const Meta m = meta_ptrs(pl->d_meta, nd, P);
-    std::vector<int64_t> hm(meta_count(nd, P));
-    const Meta h = meta_ptrs(hm.data(), nd, P);
+    void* hstage = nullptr;
+    HALO_TRY(host_stage(pl, mbytes, &hstage));
+    int64_t* hm = static_cast<int64_t*>(hstage);
+    const Meta h = meta_ptrs(hm, nd, P);
 
     int wpb = (int)std::min<int64_t>(8, std::max<int64_t>(1, (48 * 1024) / ((int64_t)nd * 4)));
     const size_t hist_smem = (size_t)wpb * nd * sizeof(int32_t);
@@ -602,7 +604,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         finalize_kernel<<<1, 1024, 0, st>>>(m, nd, P);
         home_dst_kernel<<<nd, 256, 0, st>>>(m, pl->d_home_dst);
         HALO_CUDA(cudaGetLastError());
-        HALO_CUDA(cudaMemcpyAsync(hm.data(), pl->d_meta, mbytes, cudaMemcpyDeviceToHost, st));
+        HALO_CUDA(cudaMemcpyAsync(hm, pl->d_meta, mbytes, cudaMemcpyDeviceToHost, st));
         HALO_CUDA(cudaStreamSynchronize(st));
         if (h.flags[1]) return HALO_EDOMAIN;
         if (!h.flags[0]) break;

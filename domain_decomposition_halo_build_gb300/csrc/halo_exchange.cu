@@ -447,6 +447,116 @@ __global__ void halo_gid_kernel(const SPDesc* __restrict__ sp, const int32_t* __
         out[d.dst + i] = out[d.src_base + maps[d.map_off + i]];
 }
 
+// ---- work lists, generated on the device ------------------------------------
+// Groups of chunks, in ticket order.  Coordinates: for p ascending, the
+// dependent chunks of every sender, then the independent ones.  Forces: for p
+// descending, the dependent chunks of every sender, then the independent ones.
+struct ItemGen {
+    const SPDesc* sp;
+    const int32_t* nindep;          // independent force entries per (s, p)
+    const uint64_t* recv_mask;      // per domain: pulses that delivered a nonempty slice
+    int nd, P, CH, CHF;
+    uint64_t fms[HALO_MAX_PULSES];  // force waits on s per pulse
+    uint64_t fmr[HALO_MAX_PULSES];  // force waits on r per pulse
+};
+
+__global__ void recv_mask_kernel(const SPDesc* __restrict__ sp, int nsp, uint64_t* mask) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nsp; i += gridDim.x * blockDim.x) {
+        const SPDesc d = sp[i];
+        if (d.send > 0) atomicOr((unsigned long long*)(mask + d.r), 1ull << d.p);
+    }
+}
+
+// Group g of the coordinate list: p = g / (2 nd), dependent first, sender s.
+__device__ __forceinline__ void x_group(const ItemGen& a, int g, int* sp, int* lo, int* hi, bool* dep) {
+    const int p = g / (2 * a.nd), s = g % a.nd;
+    *dep = ((g / a.nd) % 2) == 0;
+    *sp = s * a.P + p;
+    const SPDesc& d = a.sp[*sp];
+    *lo = *dep ? d.split : 0;
+    *hi = *dep ? d.send : d.split;
+}
+
+// Group g of the force list: p = P - 1 - g / (2 nd), dependent first, sender s.
+__device__ __forceinline__ void f_group(const ItemGen& a, int g, int* sp, int* lo, int* hi, bool* dep) {
+    const int p = a.P - 1 - g / (2 * a.nd), s = g % a.nd;
+    *dep = ((g / a.nd) % 2) == 0;
+    *sp = s * a.P + p;
+    const int ni = a.nindep[*sp];
+    *lo = *dep ? ni : 0;
+    *hi = *dep ? a.sp[*sp].send : ni;
+}
+
+__global__ void item_count_kernel(ItemGen a, int32_t* cx, int32_t* cf, uint32_t* target) {
+    const int ng = 2 * a.P * a.nd;
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < ng; g += gridDim.x * blockDim.x) {
+        int sp, lo, hi;
+        bool dep;
+        x_group(a, g, &sp, &lo, &hi, &dep);
+        cx[g] = (hi - lo + a.CH - 1) / a.CH;
+        f_group(a, g, &sp, &lo, &hi, &dep);
+        cf[g] = (hi - lo + a.CHF - 1) / a.CHF;
+    }
+    const int nsp = a.P * a.nd;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nsp; i += gridDim.x * blockDim.x) {
+        const SPDesc d = a.sp[i];
+        const int ni = a.nindep[i];
+        target[d.r * a.P + d.p] = (uint32_t)((d.split + a.CH - 1) / a.CH +
+                                             (d.send - d.split + a.CH - 1) / a.CH);
+        target[nsp + i] = (uint32_t)((ni + a.CHF - 1) / a.CHF + (d.send - ni + a.CHF - 1) / a.CHF);
+    }
+}
+
+__global__ void item_fill_kernel(ItemGen a, const int32_t* __restrict__ bx,
+                                 const int32_t* __restrict__ bf, XItem* __restrict__ ix,
+                                 FItem* __restrict__ iff) {
+    const int g = blockIdx.x;
+    int sp, lo, hi;
+    bool dep;
+    x_group(a, g, &sp, &lo, &hi, &dep);
+    {
+        const SPDesc d = a.sp[sp];
+        const uint64_t below = d.p > 0 ? (~0ull >> (64 - d.p)) : 0ull;
+        const uint64_t mask = dep ? (a.recv_mask[d.s] & below) : 0ull;
+        const int n = (hi - lo + a.CH - 1) / a.CH;
+        for (int c = threadIdx.x; c < n; c += blockDim.x) {
+            const int st0 = lo + c * a.CH;
+            XItem w;
+            w.map_off = d.map_off + st0;
+            w.src_base = d.src_base;
+            w.dst = d.dst + st0;
+            w.len = min(a.CH, hi - st0);
+            w.flag = d.r * a.P + d.p;
+            w.wait_base = d.s * a.P;
+            w.pad = dep ? 1 : 0;
+            w.wait_mask = mask;
+            w.shift[0] = d.shift[0];
+            w.shift[1] = d.shift[1];
+            w.shift[2] = d.shift[2];
+            w.pad2 = 0;
+            ix[bx[g] + c] = w;
+        }
+    }
+    f_group(a, g, &sp, &lo, &hi, &dep);
+    {
+        const SPDesc d = a.sp[sp];
+        const bool waits = dep && (a.fms[d.p] | a.fmr[d.p]) != 0;
+        const int n = (hi - lo + a.CHF - 1) / a.CHF;
+        for (int c = threadIdx.x; c < n; c += blockDim.x) {
+            const int st0 = lo + c * a.CHF;
+            FItem w;
+            w.off = d.map_off + st0;
+            w.len = min(a.CHF, hi - st0);
+            w.flag = d.s * a.P + d.p;
+            w.s_base = d.s * a.P;
+            w.r_base = d.r * a.P;
+            w.ms = waits ? a.fms[d.p] : 0ull;
+            w.mr = waits ? a.fmr[d.p] : 0ull;
+            iff[bf[g] + c] = w;
+        }
+    }
+}
+
 int grid_cells(const halo_plan* pl, int D, int c[3]) {
     c[0] = D % pl->grid[0];
     c[1] = (D / pl->grid[0]) % pl->grid[1];
@@ -454,11 +564,23 @@ int grid_cells(const halo_plan* pl, int D, int c[3]) {
     return 0;
 }
 
+// Bytes of pinned staging a vector needs (16-byte granules).
 template <class T>
-int upload(T** d, int64_t* cap, const std::vector<T>& h, cudaStream_t st) {
+size_t stage_bytes(const std::vector<T>& h) {
+    return (h.size() * sizeof(T) + 15) & ~(size_t)15;
+}
+
+// Copy `h` to the device buffer through the pinned staging at *off (the
+// staging must stay untouched until the stream has passed the copy).
+template <class T>
+int upload(T** d, int64_t* cap, const std::vector<T>& h, char* stage, size_t* off,
+           cudaStream_t st) {
     HALO_TRY(dev_reserve(d, cap, (int64_t)h.size()));
-    if (!h.empty())
-        HALO_CUDA(cudaMemcpyAsync(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice, st));
+    if (h.empty()) return HALO_OK;
+    char* src = stage + *off;
+    memcpy(src, h.data(), h.size() * sizeof(T));
+    *off += stage_bytes(h);
+    HALO_CUDA(cudaMemcpyAsync(*d, src, h.size() * sizeof(T), cudaMemcpyHostToDevice, st));
     return HALO_OK;
 }
 
@@ -482,6 +604,9 @@ void free_exchange(halo_plan* pl) {
     dev_free(pl->d_flags);
     dev_free(pl->d_tickets);
     dev_free(pl->d_err);
+    dev_free(pl->d_recv_mask);
+    dev_free(pl->d_itemgen);
+    pl->cap_recv_mask = pl->cap_itemgen = 0;
     pl->fpairs_cap = 0;
     pl->wmax_cap = 0;
     pl->cap_sp = pl->cap_items_x = pl->cap_items_f = pl->cap_target = pl->cap_flags = 0;
@@ -535,15 +660,22 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
             pl->max_chunks[p] = std::max(pl->max_chunks[p], (x.send + kThreads - 1) / kThreads);
         }
     }
-    HALO_TRY(upload(&pl->d_sp, &pl->cap_sp, pl->sp, st));
+    char* stage = nullptr;
+    size_t off = 0;
+    {
+        void* hs = nullptr;
+        HALO_TRY(host_stage(pl, stage_bytes(pl->sp) + 64, &hs));
+        stage = static_cast<char*>(hs);
+    }
+    HALO_TRY(upload(&pl->d_sp, &pl->cap_sp, pl->sp, stage, &off, st));
+    int32_t* h_tot = reinterpret_cast<int32_t*>(stage + off);  // 4 words read back below
 
     // force-entry classification on the device: last pulse adding into each
     // slot, then a stable independent/dependent partition per (s, p)
-    std::vector<int32_t> nindep(nsp, 0);
+    HALO_TRY(dev_reserve(&pl->d_nindep, &pl->cap_nindep, (int64_t)nsp));
     if (P > 0) {
         HALO_TRY(dev_reserve(&pl->d_wmax, &pl->wmax_cap, pl->n_local_total));
         HALO_TRY(dev_reserve(&pl->d_fpairs, &pl->fpairs_cap, pl->n_halo_total));
-        HALO_TRY(dev_reserve(&pl->d_nindep, &pl->cap_nindep, (int64_t)nsp));
         HALO_CUDA(cudaMemsetAsync(pl->d_wmax, 0xff, (size_t)pl->n_local_total, st));
         for (int p = 0; p < P; p++) {
             const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
@@ -552,97 +684,71 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
         classify_kernel<<<(unsigned)(nd * P), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, pl->d_wmax,
                                                                   pl->d_fpairs, pl->d_nindep);
         HALO_CUDA(cudaGetLastError());
-        HALO_CUDA(cudaMemcpyAsync(nindep.data(), pl->d_nindep, sizeof(int32_t) * nsp,
-                                  cudaMemcpyDeviceToHost, st));
-        HALO_CUDA(cudaStreamSynchronize(st));
     }
 
-    // coordinate items, pulse by pulse; within a pulse the dependent chunks
-    // (the forwarding chain) come before the independent ones, so the chain
-    // is served first and the rest streams behind it.  Dependent chunks wait
-    // only on earlier pulses, i.e. on earlier tickets.
-    std::vector<uint32_t> target((size_t)2 * nsp, 0);
-    std::vector<XItem> ix;
-    for (int p = 0; p < P; p++)
-        for (int pass = 1; pass >= 0; pass--)
-            for (int s = 0; s < nd; s++) {
-                const size_t sp = (size_t)s * P + p;
-                const SPDesc& d = pl->sp[sp];
-                const int lo = pass == 0 ? 0 : d.split, hi = pass == 0 ? d.split : d.send;
-                uint64_t mask = 0;
-                if (pass == 1)
-                    for (int q = 0; q < p; q++)
-                        if (pl->own_off[(size_t)s * (P + 1) + q + 1] > pl->own_off[(size_t)s * (P + 1) + q])
-                            mask |= 1ull << q;
-                for (int st0 = lo; st0 < hi; st0 += CH) {
-                    XItem w{};
-                    w.map_off = d.map_off + st0;
-                    w.src_base = d.src_base;
-                    w.dst = d.dst + st0;
-                    w.len = std::min(CH, hi - st0);
-                    w.flag = d.r * P + p;
-                    w.wait_base = s * P;
-                    w.wait_mask = mask;
-                    w.pad = pass;
-                    for (int e = 0; e < 3; e++) w.shift[e] = d.shift[e];
-                    ix.push_back(w);
-                    target[(size_t)d.r * P + p]++;
-                }
-            }
-    // force items: independent chunks first, then dependent ones, pulses from
-    // the last to the first.  Dependent (s, p) waits for (s, q) and (r, q), q > p,
+    // work lists on the device: chunk counts per group, scans, fill
+    const int ng = 2 * P * nd;
+    ItemGen a;
+    a.sp = pl->d_sp;
+    a.nindep = pl->d_nindep;
+    a.nd = nd;
+    a.P = P;
+    a.CH = CH;
+    a.CHF = CHF;
+    for (int p = 0; p < HALO_MAX_PULSES; p++) a.fms[p] = a.fmr[p] = 0;
+    // dependent force entries of (s, p) wait for (s, q) and (r, q), q > p,
     // whose index maps can touch the same slots: pulse 0 of a later dim (its
     // candidates include every earlier slot) and, on r, the next pulse of the
-    // same dim (its candidates are exactly this pulse's slice).
-    std::vector<FItem> iff;
-    std::vector<uint64_t> fms((size_t)std::max(P, 1), 0), fmr((size_t)std::max(P, 1), 0);
+    // same dim (its candidates are exactly this pulse's slice)
     for (int p = 0; p < P; p++)
         for (int q = p + 1; q < P; q++) {
             if (pl->pulse_k[q] == 0) {
-                fms[p] |= 1ull << q;
-                fmr[p] |= 1ull << q;
+                a.fms[p] |= 1ull << q;
+                a.fmr[p] |= 1ull << q;
             } else if (q == p + 1) {
-                fmr[p] |= 1ull << q;
+                a.fmr[p] |= 1ull << q;
             }
         }
-    // pulses from the last to the first; within a pulse the dependent chunks
-    // (the reverse chain) come first
-    for (int p = P - 1; p >= 0; p--) {
-        const bool no_wait = (fms[p] | fmr[p]) == 0;
-        for (int level = 1; level >= 0; level--)
-            for (int s = 0; s < nd; s++) {
-                const size_t sp = (size_t)s * P + p;
-                const SPDesc& d = pl->sp[sp];
-                const int lo = level == 0 ? 0 : nindep[sp];
-                const int hi = level == 0 ? nindep[sp] : d.send;
-                for (int st0 = lo; st0 < hi; st0 += CHF) {
-                    FItem w{};
-                    w.off = d.map_off + st0;
-                    w.len = std::min(CHF, hi - st0);
-                    w.flag = s * P + p;
-                    w.s_base = s * P;
-                    w.r_base = d.r * P;
-                    w.ms = (level == 0 || no_wait) ? 0 : fms[p];
-                    w.mr = (level == 0 || no_wait) ? 0 : fmr[p];
-                    iff.push_back(w);
-                    target[nsp + (size_t)s * P + p]++;
-                }
-            }
+    HALO_TRY(dev_reserve(&pl->d_target, &pl->cap_target, (int64_t)(2 * nsp)));
+    HALO_TRY(dev_reserve(&pl->d_recv_mask, &pl->cap_recv_mask, (int64_t)nd));
+    const int64_t nsc = (int64_t)ng / kScanTile + 2;
+    HALO_TRY(dev_reserve(&pl->d_itemgen, &pl->cap_itemgen, 4 * (int64_t)std::max(ng, 1) + nsc));
+    int32_t* cx = pl->d_itemgen;
+    int32_t* cf = cx + std::max(ng, 1);
+    int32_t* bx = cf + std::max(ng, 1);
+    int32_t* bf = bx + std::max(ng, 1);
+    int32_t* sct = bf + std::max(ng, 1);
+    const int64_t ub_x = pl->n_halo_total / CH + ng + 1, ub_f = pl->n_halo_total / CHF + ng + 1;
+    HALO_TRY(dev_reserve(&pl->d_items_x, &pl->cap_items_x, ub_x));
+    HALO_TRY(dev_reserve(&pl->d_items_f, &pl->cap_items_f, ub_f));
+    a.recv_mask = pl->d_recv_mask;
+    h_tot[0] = h_tot[1] = h_tot[2] = h_tot[3] = 0;
+    if (ng > 0) {
+        HALO_CUDA(cudaMemsetAsync(pl->d_recv_mask, 0, sizeof(uint64_t) * nd, st));
+        recv_mask_kernel<<<(unsigned)((nsp + 255) / 256), 256, 0, st>>>(pl->d_sp, (int)nsp,
+                                                                         pl->d_recv_mask);
+        item_count_kernel<<<(unsigned)((ng + 255) / 256), 256, 0, st>>>(a, cx, cf, pl->d_target);
+        HALO_TRY(device_exclusive_scan(cx, bx, ng, sct, st));
+        HALO_TRY(device_exclusive_scan(cf, bf, ng, sct, st));
+        item_fill_kernel<<<(unsigned)ng, 128, 0, st>>>(a, bx, bf, pl->d_items_x, pl->d_items_f);
+        HALO_CUDA(cudaGetLastError());
+        HALO_CUDA(cudaMemcpyAsync(h_tot, bx + ng - 1, 4, cudaMemcpyDeviceToHost, st));
+        HALO_CUDA(cudaMemcpyAsync(h_tot + 1, cx + ng - 1, 4, cudaMemcpyDeviceToHost, st));
+        HALO_CUDA(cudaMemcpyAsync(h_tot + 2, bf + ng - 1, 4, cudaMemcpyDeviceToHost, st));
+        HALO_CUDA(cudaMemcpyAsync(h_tot + 3, cf + ng - 1, 4, cudaMemcpyDeviceToHost, st));
     }
-    pl->n_items_x = (int)ix.size();
-    pl->n_items_f = (int)iff.size();
-    HALO_TRY(upload(&pl->d_items_x, &pl->cap_items_x, ix, st));
-    HALO_TRY(upload(&pl->d_items_f, &pl->cap_items_f, iff, st));
-    HALO_TRY(upload(&pl->d_target, &pl->cap_target, target, st));
+    HALO_CUDA(cudaStreamSynchronize(st));
+    pl->n_items_x = h_tot[0] + h_tot[1];
+    pl->n_items_f = h_tot[2] + h_tot[3];
     HALO_TRY(dev_reserve(&pl->d_flags, &pl->cap_flags, (int64_t)(2 * nsp)));
     if (!pl->d_tickets) HALO_TRY(dev_alloc(&pl->d_tickets, 2));
     if (!pl->d_err) HALO_TRY(dev_alloc(&pl->d_err, 8));
-    int bx = 1, bf = 1;
-    HALO_TRY(occupancy<4>(&bx, &bf));
-    pl->grid_x = (int)std::max<int64_t>(1, std::min<int64_t>(pl->n_items_x,
-                                                              (int64_t)pl->num_sms * std::max(bx, 1)));
-    pl->grid_f = (int)std::max<int64_t>(1, std::min<int64_t>((pl->n_items_f + kWarps - 1) / kWarps,
-                                                              (int64_t)pl->num_sms * std::max(bf, 1)));
+    if (pl->occ_x <= 0 || pl->occ_f <= 0) HALO_TRY(occupancy<4>(&pl->occ_x, &pl->occ_f));
+    pl->grid_x = (int)std::max<int64_t>(
+        1, std::min<int64_t>(pl->n_items_x, (int64_t)pl->num_sms * std::max(pl->occ_x, 1)));
+    pl->grid_f = (int)std::max<int64_t>(
+        1, std::min<int64_t>((pl->n_items_f + kWarps - 1) / kWarps,
+                             (int64_t)pl->num_sms * std::max(pl->occ_f, 1)));
     HALO_TRY(reset_flags(pl, st));
     return cuda_code(cudaStreamSynchronize(st));
 }

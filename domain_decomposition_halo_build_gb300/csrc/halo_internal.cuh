@@ -99,6 +99,9 @@ struct halo_plan {
     halo::FItem* d_items_f = nullptr;
     int64_t cap_sp = 0, cap_items_x = 0, cap_items_f = 0, cap_target = 0, cap_flags = 0,
             cap_nindep = 0;
+    uint64_t* d_recv_mask = nullptr;  // per domain: pulses that delivered a nonempty slice
+    int32_t* d_itemgen = nullptr;     // scratch of the device-side work-list generation
+    int64_t cap_recv_mask = 0, cap_itemgen = 0;
     int n_items_x = 0, n_items_f = 0;
     std::vector<int32_t> max_chunks;  // per pulse: most chunks of one sender (utility grids)
     int chunk = 256;                // entries per work item
@@ -118,6 +121,11 @@ struct halo_plan {
     unsigned long long* trace = nullptr;  // caller's trace buffer (device), or null
     int64_t trace_cap = 0;                // its size in items
     int64_t launches_x = 0, launches_f = 0;
+
+    // pinned host staging for the build's host<->device copies (grow-only)
+    void* h_stage = nullptr;
+    size_t h_stage_cap = 0;
+    int occ_x = 0, occ_f = 0;        // resident blocks per SM of the fused kernels (cached)
 
     // exchange mode (HALO_MODE_*) and the flattened exchange's tables
     int mode = 0;
@@ -206,6 +214,25 @@ inline int dev_reserve(T** p, int64_t* cap, int64_t count) {
     const int rc = dev_alloc(p, (size_t)want);
     if (rc == HALO_OK) *cap = want;
     return rc;
+}
+
+// Pinned host staging of at least `bytes` (grow-only; the stream must be idle
+// when it grows, which holds at the points the build calls it).
+inline int host_stage(halo_plan* pl, size_t bytes, void** out) {
+    if (pl->h_stage_cap < bytes) {
+        if (pl->h_stage) cudaFreeHost(pl->h_stage);
+        pl->h_stage = nullptr;
+        pl->h_stage_cap = 0;
+        const size_t want = bytes + bytes / 4 + 4096;
+        if (cudaMallocHost(&pl->h_stage, want) != cudaSuccess) {
+            (void)cudaGetLastError();
+            pl->h_stage = nullptr;
+            return HALO_ENOMEM;
+        }
+        pl->h_stage_cap = want;
+    }
+    *out = pl->h_stage;
+    return HALO_OK;
 }
 
 }  // namespace halo

@@ -25,6 +25,8 @@
 //     same fp32 additions in the same order, so the results (owners and
 //     intermediate halo slots) are bit-identical.
 // Both passes then have no waits and no cross-block dependencies.
+#include <string.h>
+
 #include <algorithm>
 #include <vector>
 
@@ -491,9 +493,20 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     }
     pl->n_xflat_items = (int)items.size();
     HALO_TRY(dev_reserve(&pl->d_xflat_items, &pl->cap_xflat_items, (int64_t)items.size()));
-    if (!items.empty())
-        HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, items.data(), items.size() * sizeof(int4),
+    // pinned staging: the item list, then a few words read back below
+    HALO_CUDA(cudaStreamSynchronize(st));  // the staging may grow: nothing in flight uses it
+    char* stage = nullptr;
+    {
+        void* hs = nullptr;
+        HALO_TRY(host_stage(pl, items.size() * sizeof(int4) + 256, &hs));
+        stage = static_cast<char*>(hs);
+    }
+    int32_t* hw = reinterpret_cast<int32_t*>(stage + items.size() * sizeof(int4));  // 16 words
+    if (!items.empty()) {
+        memcpy(stage, items.data(), items.size() * sizeof(int4));
+        HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, stage, items.size() * sizeof(int4),
                                   cudaMemcpyHostToDevice, st));
+    }
     HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat, H));
     HALO_TRY(dev_reserve(&pl->d_fent, &pl->cap_fent, H));
 
@@ -528,7 +541,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if ((rc = device_exclusive_scan(ncopies, entry_pos, nl, scan_tmp, st)) != HALO_OK) break;
         owner_flag_kernel<<<gb, kThreads, 0, st>>>(ncopies, flag, nl);
         if ((rc = device_exclusive_scan(flag, owner_idx, nl, scan_tmp, st)) != HALO_OK) break;
-        int32_t last[4] = {0, 0, 0, 0};
+        int32_t* last = hw;
         if ((rc = cuda_code(cudaMemcpyAsync(last, owner_idx + nl - 1, sizeof(int32_t),
                                             cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaMemcpyAsync(last + 1, flag + nl - 1, sizeof(int32_t),
@@ -540,8 +553,8 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if ((rc = dev_reserve(&pl->d_fstart, &pl->cap_fstart, n_owners + 1)) != HALO_OK) break;
         owner_list_kernel<<<gb, kThreads, 0, st>>>(ncopies, entry_pos, owner_idx, nl, pl->d_fown,
                                                    pl->d_fstart);
-        const int32_t Hi = (int32_t)H;
-        if ((rc = cuda_code(cudaMemcpyAsync(pl->d_fstart + n_owners, &Hi, sizeof(int32_t),
+        hw[2] = (int32_t)H;
+        if ((rc = cuda_code(cudaMemcpyAsync(pl->d_fstart + n_owners, hw + 2, sizeof(int32_t),
                                             cudaMemcpyHostToDevice, st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaMemsetAsync(flag, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
         if (!items.empty())
@@ -551,9 +564,9 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if (n_owners > 0)
             owner_sort_kernel<<<blocks_for(n_owners, pl->num_sms), kThreads, 0, st>>>(
                 pl->d_fown, pl->d_fstart, tmp, parent, hop, n_owners, pl->d_fent, misc, misc + 1);
-        int32_t info[2] = {0, 0};
-        if ((rc = cuda_code(cudaMemcpyAsync(info, misc, sizeof(info), cudaMemcpyDeviceToHost, st))) !=
-            HALO_OK)
+        int32_t* info = hw + 4;
+        if ((rc = cuda_code(cudaMemcpyAsync(info, misc, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                            st))) != HALO_OK)
             break;
         if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaGetLastError())) != HALO_OK) break;
@@ -572,7 +585,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             owner_class_kernel<<<gbo, kThreads, 0, st>>>(pl->d_fstart, n_owners, isA, isB);
             if ((rc = device_exclusive_scan(isA, posA, n_owners, scan_tmp, st)) != HALO_OK) break;
             if ((rc = device_exclusive_scan(isB, posB, n_owners, scan_tmp, st)) != HALO_OK) break;
-            int32_t tail[4] = {0, 0, 0, 0};
+            int32_t* tail = hw + 8;
             if ((rc = cuda_code(cudaMemcpyAsync(tail, posA + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
             if ((rc = cuda_code(cudaMemcpyAsync(tail + 1, isA + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
             if ((rc = cuda_code(cudaMemcpyAsync(tail + 2, posB + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
