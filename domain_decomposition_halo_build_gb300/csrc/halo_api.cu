@@ -89,12 +89,14 @@ void destroy_plan(halo_plan* pl) {
 
 int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, void* stream) {
     const cudaStream_t st = as_stream(stream);
+    pl->valid = false;  // until every table of the new plan is in place
     pl->trace = nullptr;  // item counts change with the plan: the caller re-arms tracing
     pl->trace_cap = 0;
     pl->flat_ready = false;  // the flattened tables describe the previous plan
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
     HALO_TRY(halo::prepare_exchange(pl, st));
-    if (pl->mode == HALO_MODE_FLAT) return halo::prepare_flat(pl, st);
+    if (pl->mode == HALO_MODE_FLAT) HALO_TRY(halo::prepare_flat(pl, st));
+    pl->valid = true;
     return HALO_OK;
 }
 
@@ -207,19 +209,20 @@ int halo_get_index_maps(const halo_plan* pl, int32_t* maps, int64_t* offsets) {
 }
 
 int halo_local_to_global(const halo_plan* pl, int32_t* out, void* stream) {
-    if (!pl || !out) return HALO_EINVAL;
+    if (!pl || !out || !pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
     return halo::launch_local_to_global(pl, out, as_stream(stream));
 }
 
 int halo_load_home(const halo_plan* pl, const float* global_xyz, float* local_xyz, void* stream) {
-    if (!pl || !global_xyz || !local_xyz) return HALO_EINVAL;
+    if (!pl || !global_xyz || !local_xyz || !pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
     return halo::launch_load_home(pl, global_xyz, local_xyz, as_stream(stream));
 }
 
 int halo_exchange_x(halo_plan* pl, float* local_coords, void* stream) {
     if (!pl || !local_coords || ((uintptr_t)local_coords & 3u)) return HALO_EINVAL;
+    if (!pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
     switch (pl->mode) {
         case HALO_MODE_STEPWISE: return halo::launch_stepwise_x(pl, local_coords, as_stream(stream));
@@ -229,7 +232,8 @@ int halo_exchange_x(halo_plan* pl, float* local_coords, void* stream) {
 }
 
 int halo_exchange_f(halo_plan* pl, float* local_forces, void* stream) {
-    if (!pl || !local_forces) return HALO_EINVAL;
+    if (!pl || !local_forces || ((uintptr_t)local_forces & 3u)) return HALO_EINVAL;
+    if (!pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
     switch (pl->mode) {
         case HALO_MODE_STEPWISE: return halo::launch_stepwise_f(pl, local_forces, as_stream(stream));

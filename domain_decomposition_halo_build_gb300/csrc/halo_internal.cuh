@@ -59,6 +59,7 @@ struct FItem {
 struct halo_plan {
     int dev = 0;
     int num_sms = 0;
+    bool valid = false;              // false while (or after a failed) rebuild: exchanges refuse
     int grid[3] = {1, 1, 1};
     float box[3] = {0, 0, 0};
     float rc = 0;

@@ -58,3 +58,33 @@ def test_bad_arguments_return_codes():
     grid = (ctypes.c_int32 * 3)(1, 1, 1)
     assert lib.halo_setup(box, grid, ctypes.c_float(0.1), None, None, 10, None,
                           ctypes.byref(h)) == halo.EINVAL
+
+
+def test_failed_rebuild_refuses_exchanges_until_rebuilt():
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    w = synth.WORKLOADS["water48k_2x2x2"]
+    xyz, dom = synth.system(w)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d)
+    try:
+        loc = plan.load_home(x)
+        bad = d.clone()
+        bad[123] = 99                                   # domain id out of range
+        with pytest.raises(halo.HaloError) as e:
+            plan.rebuild(x, bad)
+        assert e.value.code == halo.EDOMAIN
+        with pytest.raises(halo.HaloError) as e:
+            plan.exchange_x(loc)
+        assert e.value.code == halo.EINVAL
+        plan.rebuild(x, d)                              # a good rebuild restores it
+        loc = plan.load_home(x)
+        plan.exchange_x(loc)
+        assert plan.status() == halo.OK
+        o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+        want = o.load_home(xyz)
+        o.exchange_x(want)
+        np.testing.assert_array_equal(loc.cpu().numpy(), want)
+    finally:
+        plan.close()
