@@ -58,4 +58,22 @@ __device__ __forceinline__ void bulk_store_floats(float* gdst, const float* stag
     }
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; it reads only the plan's own tables (written by a rebuild, which
+// ends with a synchronisation) before grid_dependency_wait(), which returns
+// once the preceding grids have completed and their writes are visible.
+// Every read of coordinates or forces, and every write, comes after it.
+// Without the launch attribute both are no-ops.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next programmatically serialised kernel in the stream be scheduled
+// as soon as every block of this one has started (its blocks still wait for
+// this grid's completion before touching its data).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace halo

@@ -183,6 +183,26 @@ void free_build(halo_plan* pl);
 
 inline int cuda_code(cudaError_t e) { return e == cudaSuccess ? HALO_OK : HALO_ECUDA; }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor in the stream drains, and holds back every access to
+// exchanged data until grid_dependency_wait() (kernels of the flat and
+// stepwise modes).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                                    Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <class T>
 inline int dev_alloc(T** p, size_t count) {
     *p = nullptr;

@@ -44,9 +44,14 @@ constexpr int kMaxCopies = 63;            // parent positions fit in 6 bits
 // ---- stepwise ----------------------------------------------------------------
 __global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
                               float* xyz, int P, int p) {
+    grid_launch_dependents();
     const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
-        const float* s = xyz + 3 * (d.src_base + maps[d.map_off + i]);
+    const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
+    int m = i0 < d.send ? maps[d.map_off + i0] : 0;  // plan table: read before the wait
+    grid_dependency_wait();  // pulse p - 1 (or whatever came before) has landed
+    for (int i = i0; i < d.send; i += gridDim.x * blockDim.x) {
+        if (i != i0) m = maps[d.map_off + i];
+        const float* s = xyz + 3 * (d.src_base + m);
         float* q = xyz + 3 * (d.dst + i);
         const float v0 = s[0], v1 = s[1], v2 = s[2];
         q[0] = v0 + d.shift[0];
@@ -57,10 +62,15 @@ __global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __re
 
 __global__ void step_f_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
                               float* f, int P, int p) {
+    grid_launch_dependents();
     const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
+    const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
+    int m = i0 < d.send ? maps[d.map_off + i0] : 0;  // plan table: read before the wait
+    grid_dependency_wait();
+    for (int i = i0; i < d.send; i += gridDim.x * blockDim.x) {
+        if (i != i0) m = maps[d.map_off + i];
         const float* h = f + 3 * (d.dst + i);
-        float* o = f + 3 * (d.src_base + maps[d.map_off + i]);
+        float* o = f + 3 * (d.src_base + m);
         const float h0 = h[0], h1 = h[1], h2 = h[2];
         o[0] = o[0] + h0;
         o[1] = o[1] + h1;
@@ -197,6 +207,7 @@ template <int E>
 __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int32_t* __restrict__ xflat,
                                                           const int4* __restrict__ items, float L0,
                                                           float L1, float L2) {
+    grid_launch_dependents();
     const int4 it = items[blockIdx.x];
     int32_t v[E];
 #pragma unroll
@@ -204,6 +215,8 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
         const int i = threadIdx.x + e * kThreads;
         v[e] = i < it.z ? __ldg(xflat + it.x + i) : 0;
     }
+    // the chunk and its codes are plan tables; coordinates only after the wait
+    grid_dependency_wait();
     float a[E][3];
 #pragma unroll
     for (int e = 0; e < E; e++) {
@@ -351,6 +364,8 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
     const int64_t tilesA = (nA + 2 * kThreads - 1) / (2 * kThreads);
     const int64_t tilesBC = (nB + nC + kThreads - 1) / kThreads;
     const int64_t n = nA + nB + nC;
+    grid_launch_dependents();
+    // records are plan tables, read before grid_dependency_wait(); forces after it
     for (int64_t bb = blockIdx.x; bb < tilesA + tilesBC; bb += gridDim.x) {
         if (bb >= tilesBC) {
             const int64_t b = bb - tilesBC;
@@ -361,11 +376,12 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
             const int kk[2] = {m0 < nA ? (int)((unsigned)r0.x >> kNodeBits) : 0,
                                m1 < nA ? (int)((unsigned)r1.x >> kNodeBits) : 0};
             const int32_t ent[2][3] = {{r0.y, r0.z, r0.w}, {r1.y, r1.z, r1.w}};
+            grid_dependency_wait();
             reduce_trees<3, 2>(f, home, kk, ent);
             continue;
         }
         const int64_t m = nA + bb * kThreads + threadIdx.x;
-        if (m >= n) continue;
+        if (m >= n) continue;  // touches nothing
         if (m < nA + nB) {
             const int4 r0 = __ldg(recB + 3 * (m - nA)), r1 = __ldg(recB + 3 * (m - nA) + 1);
             const int4 r2 = KB > 7 ? __ldg(recB + 3 * (m - nA) + 2) : make_int4(0, 0, 0, 0);
@@ -373,9 +389,11 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
             int32_t ent[KB];
 #pragma unroll
             for (int j = 0; j < KB; j++) ent[j] = all[j];
+            grid_dependency_wait();
             reduce_tree<KB>(f, r0.x & kNodeMask, (int)((unsigned)r0.x >> kNodeBits), ent);
         } else {
             const int4 r = __ldg(recC + (m - nA - nB));
+            grid_dependency_wait();
             if constexpr (KW > 0) {
                 if (((unsigned)r.x >> kNodeBits) <= (unsigned)KW) {
                     // plans with deeper trees (several pulses per dim): up to
@@ -612,7 +630,10 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
 int launch_stepwise_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     for (int p = 0; p < pl->P; p++) {
         const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
-        step_x_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, xyz, pl->P, p);
+        const cudaError_t e = launch_dependent(step_x_kernel, dim3(gx, pl->n_dom), dim3(kThreads), st,
+                                               (const SPDesc*)pl->d_sp, (const int32_t*)pl->d_maps, xyz,
+                                               pl->P, p);
+        if (e != cudaSuccess) return cuda_code(e);
         pl->launches_x++;
     }
     return cuda_code(cudaGetLastError());
@@ -621,7 +642,10 @@ int launch_stepwise_x(halo_plan* pl, float* xyz, cudaStream_t st) {
 int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st) {
     for (int p = pl->P - 1; p >= 0; p--) {
         const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
-        step_f_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, f, pl->P, p);
+        const cudaError_t e = launch_dependent(step_f_kernel, dim3(gx, pl->n_dom), dim3(kThreads), st,
+                                               (const SPDesc*)pl->d_sp, (const int32_t*)pl->d_maps, f,
+                                               pl->P, p);
+        if (e != cudaSuccess) return cuda_code(e);
         pl->launches_f++;
     }
     return cuda_code(cudaGetLastError());
@@ -629,17 +653,13 @@ int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st) {
 
 int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     if (pl->n_xflat_items == 0) return HALO_OK;
-    if (pl->flat_x_e == 4)
-        flat_x_kernel<4><<<pl->n_xflat_items, kThreads, 0, st>>>(xyz, pl->d_xflat, pl->d_xflat_items,
-                                                                 pl->box[0], pl->box[1], pl->box[2]);
-    else if (pl->flat_x_e == 2)
-        flat_x_kernel<2><<<pl->n_xflat_items, kThreads, 0, st>>>(xyz, pl->d_xflat, pl->d_xflat_items,
-                                                                 pl->box[0], pl->box[1], pl->box[2]);
-    else
-        flat_x_kernel<1><<<pl->n_xflat_items, kThreads, 0, st>>>(xyz, pl->d_xflat, pl->d_xflat_items,
-                                                                 pl->box[0], pl->box[1], pl->box[2]);
+    auto* k = pl->flat_x_e == 4 ? flat_x_kernel<4> : pl->flat_x_e == 2 ? flat_x_kernel<2> : flat_x_kernel<1>;
+    const cudaError_t e = launch_dependent(k, dim3(pl->n_xflat_items), dim3(kThreads), st, xyz,
+                                           (const int32_t*)pl->d_xflat, (const int4*)pl->d_xflat_items,
+                                           pl->box[0], pl->box[1], pl->box[2]);
+    if (e != cudaSuccess) return cuda_code(e);
     pl->launches_x++;
-    return cuda_code(cudaGetLastError());
+    return HALO_OK;
 }
 
 int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
@@ -648,18 +668,15 @@ int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
     const int64_t tilesA = (pl->n_rec[0] + 2 * kThreads - 1) / (2 * kThreads);
     const int64_t tilesBC = (pl->n_rec[1] + pl->n_rec[2] + kThreads - 1) / kThreads;
     const int gb = (int)std::max<int64_t>(1, std::min<int64_t>(tilesA + tilesBC, (int64_t)pl->num_sms * 16));
-#define HALO_FLAT_F(KB, KW)                                                                      \
-    flat_f_kernel<KB, KW><<<gb, kThreads, 0, st>>>(f, pl->d_frec[0], pl->n_rec[0], pl->d_frec[1],  \
-                                                   pl->n_rec[1], pl->d_frec[2], pl->n_rec[2], pl->d_fent)
-    if (pl->max_copies <= 7)
-        HALO_FLAT_F(7, 0);
-    else if (pl->max_copies <= 11)
-        HALO_FLAT_F(11, 0);
-    else
-        HALO_FLAT_F(11, 16);
-#undef HALO_FLAT_F
+    auto* k = pl->max_copies <= 7 ? flat_f_kernel<7, 0> : pl->max_copies <= 11 ? flat_f_kernel<11, 0>
+                                                                               : flat_f_kernel<11, 16>;
+    const cudaError_t e = launch_dependent(k, dim3(gb), dim3(kThreads), st, f, (const int4*)pl->d_frec[0],
+                                           pl->n_rec[0], (const int4*)pl->d_frec[1], pl->n_rec[1],
+                                           (const int4*)pl->d_frec[2], pl->n_rec[2],
+                                           (const int32_t*)pl->d_fent);
+    if (e != cudaSuccess) return cuda_code(e);
     pl->launches_f++;
-    return cuda_code(cudaGetLastError());
+    return HALO_OK;
 }
 
 }  // namespace halo
