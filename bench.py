@@ -405,16 +405,15 @@ def rebuild_case(device, stream, flush, steps, warmup, reps=5):
     return out
 
 
-def cpu_baseline(name, budget_s=10.0):
-    """The CPU oracle as it stands, single-threaded, on a bounded sample."""
-    import oracle
-    from domain_decomposition_halo_build_gb300 import synth
-    w = synth.WORKLOADS[name]
-    xyz, dom = synth.system(w)
-    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
-    loc = o.load_home(xyz)
-    f = synth.forces(o.n_local_total, seed=1)
-    halo_slots = o.n_local_total - o.n_atoms
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(o, loc, f, budget_s):
+    """Whole coordinate + force exchanges of the oracle for about budget_s."""
     n = 0
     t0 = time.perf_counter()
     while True:
@@ -423,11 +422,36 @@ def cpu_baseline(name, budget_s=10.0):
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
-            break
-    return {"value": halo_slots * n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d full coord+force exchanges of %s (%d halo slots each), %.1f s, "
-                      "single-threaded C oracle" % (n, name, halo_slots, el),
-            "us_per_exchange": 1e6 * el / n}
+            return n, el
+
+
+def cpu_baseline(name, budget_s=10.0):
+    """The CPU oracle as it stands on a bounded sample: its exchanges on all
+    host cores (OpenMP over the senders of each pulse) and on one core, and
+    one oracle setup (the halo build) of the same system."""
+    import oracle
+    from domain_decomposition_halo_build_gb300 import synth
+    w = synth.WORKLOADS[name]
+    xyz, dom = synth.system(w)
+    t0 = time.perf_counter()
+    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+    setup_s = time.perf_counter() - t0
+    loc = o.load_home(xyz)
+    f = synth.forces(o.n_local_total, seed=1)
+    halo_slots = o.n_local_total - o.n_atoms
+    cores = host_cores() if o.openmp else 1
+    o.set_threads(cores)
+    n, el = time_oracle(o, loc, f, budget_s / 2)
+    o.set_threads(1)
+    n1, el1 = time_oracle(o, loc, f, budget_s / 2)
+    return {"value": halo_slots * n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d full coord+force exchanges of %s (%d halo slots each) in %.1f s on %d "
+                      "threads (C oracle, OpenMP over the senders of each pulse)"
+                      % (n, name, halo_slots, el, cores),
+            "us_per_exchange": 1e6 * el / n,
+            "single_core": {"value": halo_slots * n1 / el1, "us_per_exchange": 1e6 * el1 / n1,
+                            "sample": "%d exchanges in %.1f s, 1 thread" % (n1, el1)},
+            "setup_ms": 1e3 * setup_s}
 
 
 def run_reference(args):
@@ -440,6 +464,8 @@ def run_reference(args):
     w = synth.WORKLOADS[args.workload]
     xyz, dom = synth.system(w)
     o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+    cores = host_cores() if o.openmp else 1
+    o.set_threads(cores)
     loc = o.load_home(xyz)
     f = synth.forces(o.n_local_total, seed=1)
     halo_slots = o.n_local_total - o.n_atoms
@@ -459,9 +485,9 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "n_atoms": w.n_atoms, "grid": list(w.grid),
                    "rc_nm": w.rc, "halo_slots": halo_slots},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "%d full coord+force exchanges (single-threaded C oracle)"
-                                   % args.steps},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d full coord+force exchanges (C oracle, %d threads)"
+                                   % (args.steps, cores)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }))

@@ -34,11 +34,16 @@ CFLAGS = ["-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-shared", "
 
 
 def build_oracle(src: str = SOURCE, out: str = LIBRARY, force: bool = False) -> str:
-    """Compile ``src`` into the shared library ``out`` with gcc (plain C11)."""
+    """Compile ``src`` into the shared library ``out`` with gcc (plain C11).
+
+    With OpenMP where the compiler has it (only the optional host threads of
+    the two exchanges use it); without, the same source builds sequential."""
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
         return out
     tmp = out + ".tmp%d" % os.getpid()
-    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    r = subprocess.run(["gcc", *CFLAGS, "-fopenmp", "-o", tmp, src, "-lm"], capture_output=True)
+    if r.returncode != 0:
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
     os.replace(tmp, out)
     return out
 
@@ -90,6 +95,10 @@ def _bind(lib):
         fn = getattr(lib, name)
         fn.argtypes = [vp, ctypes.POINTER(ctypes.c_float)]
         fn.restype = None
+    lib.oracle_set_threads.argtypes = [vp, ctypes.c_int]
+    lib.oracle_set_threads.restype = None
+    lib.oracle_openmp.argtypes = []
+    lib.oracle_openmp.restype = ctypes.c_int
     lib.oracle_local_to_global.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.oracle_local_to_global.restype = None
     lib.oracle_load_home.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
@@ -194,6 +203,15 @@ class Oracle:
         return out
 
     # -- exchanges (in place on a dense local array) ----------------------------
+    def set_threads(self, threads: int) -> None:
+        """Run the senders of each pulse on ``threads`` OpenMP threads (1: none)."""
+        self.lib.oracle_set_threads(self._h, int(threads))
+
+    @property
+    def openmp(self) -> bool:
+        """Whether this oracle build has OpenMP (else set_threads has no effect)."""
+        return bool(self.lib.oracle_openmp())
+
     def exchange_x(self, local: np.ndarray) -> np.ndarray:
         assert local.dtype == np.float32 and local.flags.c_contiguous
         assert local.shape == (self.n_local_total, 3)

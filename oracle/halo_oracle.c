@@ -90,6 +90,7 @@ typedef struct {
     int32_t *atom_offset; /* first slot of this pulse's halo in the receiver */
     float *shift;         /* 3 per (s, p) */
     ivec *map;
+    int threads; /* exchanges: OpenMP threads over the domains of one pulse (<= 1: none) */
 } oracle_t;
 
 static int ivec_push(ivec *a, int32_t x)
@@ -412,13 +413,38 @@ void oracle_load_home(const oracle_t *o, const float *global_xyz, float *local)
         }
 }
 
+/* Host threads for the two exchanges (default: none).  The senders of one
+ * pulse are independent.  Coordinates: a sender writes only its receiver's
+ * slots of this pulse (each receiver has one sender per pulse) and reads only
+ * slots filled before this pulse.  Forces: a sender adds into its own mapped
+ * slots, which are home or earlier-pulse slots that no other sender of the
+ * pulse touches, from its receiver's slots of this pulse, which no sender of
+ * the pulse writes.  So running the senders of a pulse on several threads
+ * changes neither a value nor the order of the adds into any slot; pulses stay
+ * in sequence. */
+void oracle_set_threads(oracle_t *o, int threads)
+{
+    o->threads = threads;
+}
+
+int oracle_openmp(void)
+{
+#ifdef _OPENMP
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 /* Coordinate halo exchange on the dense local layout: for every pulse in
  * order and every sender, gather the index-mapped slots, add coordShift and
  * write them to the receiver's halo slots (Algorithms 3 and 4). */
 void oracle_exchange_x(const oracle_t *o, float *local)
 {
     const int P = o->n_pulses;
+    const int nt = o->threads > 1 ? o->threads : 1;
     for (int p = 0; p < P; p++)
+#pragma omp parallel for schedule(static) if (nt > 1) num_threads(nt)
         for (int s = 0; s < o->n_dom; s++) {
             const int sp = s * P + p;
             const ivec *m = &o->map[sp];
@@ -438,7 +464,9 @@ void oracle_exchange_x(const oracle_t *o, float *local)
 void oracle_exchange_f(const oracle_t *o, float *local)
 {
     const int P = o->n_pulses;
+    const int nt = o->threads > 1 ? o->threads : 1;
     for (int p = P - 1; p >= 0; p--)
+#pragma omp parallel for schedule(static) if (nt > 1) num_threads(nt)
         for (int s = 0; s < o->n_dom; s++) {
             const int sp = s * P + p;
             const ivec *m = &o->map[sp];

@@ -154,3 +154,26 @@ def test_degenerate_cases():
     pins.check_maps(o)
     pins.check_geometric(o, xyz, dom)
     pins.check_forces_integer(o)
+
+
+@pytest.mark.parametrize("name", ["water24k_2x4x8", "water48k_2x2x2"])
+def test_threaded_exchanges_match_sequential(plans, name):
+    """The senders of one pulse are independent, so the host-threaded exchanges
+    (used only to time the oracle on all cores) give the same bits."""
+    w, xyz, dom, o = plans(name)
+    if not o.openmp:
+        pytest.skip("oracle built without OpenMP")
+    loc = o.load_home(xyz)
+    f = synth.forces(o.n_local_total, seed=5)
+    seq_x, seq_f = loc.copy(), f.copy()
+    o.exchange_x(seq_x)
+    o.exchange_f(seq_f)
+    try:
+        o.set_threads(4)
+        par_x, par_f = loc.copy(), f.copy()
+        o.exchange_x(par_x)
+        o.exchange_f(par_f)
+    finally:
+        o.set_threads(1)
+    np.testing.assert_array_equal(par_x.view(np.uint32), seq_x.view(np.uint32))
+    np.testing.assert_array_equal(par_f.view(np.uint32), seq_f.view(np.uint32))
