@@ -73,6 +73,11 @@ def _bind(lib):
                                  ctypes.POINTER(ctypes.c_int32), ctypes.c_int64,
                                  ctypes.POINTER(vp)]
     lib.oracle_setup.restype = ctypes.c_int
+    lib.oracle_setup_ex.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int),
+                                    ctypes.c_float, ctypes.POINTER(ctypes.c_float),
+                                    ctypes.POINTER(ctypes.c_int32), ctypes.c_int64, ctypes.c_int,
+                                    ctypes.POINTER(vp)]
+    lib.oracle_setup_ex.restype = ctypes.c_int
     lib.oracle_free.argtypes = [vp]
     lib.oracle_free.restype = None
     lib.oracle_num_domains.argtypes = [vp]
@@ -138,8 +143,12 @@ class Oracle:
     ... | halo of pulse P-1]``.
     """
 
-    def __init__(self, box, grid, rc, xyz, dom, lib=None):
+    def __init__(self, box, grid, rc, xyz, dom, lib=None, prune=False):
+        """``prune``: keep a forwarded candidate only if it lies within rc of
+        the receiver's home box over all dims where it is beyond it (corner
+        pruning; off by default, the page's one-dimensional slabs)."""
         self.lib = lib if lib is not None else load()
+        self.prune = bool(prune)
         self.box = np.ascontiguousarray(box, dtype=np.float32)
         self.grid = np.ascontiguousarray(grid, dtype=np.int32)
         self.rc = float(np.float32(rc))
@@ -147,9 +156,10 @@ class Oracle:
         dom = np.ascontiguousarray(dom, dtype=np.int32)
         self.n_atoms = xyz.shape[0]
         h = ctypes.c_void_p()
-        code = self.lib.oracle_setup(_f32p(self.box), self.grid.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
-                                     ctypes.c_float(self.rc), _f32p(xyz), _i32p(dom),
-                                     ctypes.c_int64(self.n_atoms), ctypes.byref(h))
+        code = self.lib.oracle_setup_ex(_f32p(self.box), self.grid.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                        ctypes.c_float(self.rc), _f32p(xyz), _i32p(dom),
+                                        ctypes.c_int64(self.n_atoms), 1 if self.prune else 0,
+                                        ctypes.byref(h))
         if code != OK:
             raise OracleError(code)
         self._h = h

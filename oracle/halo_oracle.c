@@ -40,6 +40,19 @@
  *       coordinate is one fp32 add per component.
  *   R7  force reduction: pulses P-1 ... 0; plain add (entries are unique
  *       within a pulse); halo force slots keep whatever they hold.
+ *   R8  optional corner pruning (off unless asked for; the page describes
+ *       one-dimensional face slabs only): a candidate that passes R3 is kept
+ *       only if its distance to the receiver's home box, over the dims in
+ *       which it is beyond that box, is below rc.  The dims are d itself (the
+ *       distance past the receiver's upper face, which is the sender's lower
+ *       face) and every dim across whose upper face the slot was received on
+ *       its way to the sender (its forwarding path).  In double: each term
+ *       max(0, x - face) squared, d's term first and then the other dims in
+ *       ascending order, compared strictly with rc * rc; faces c * L / n in
+ *       double as in R3.  No pair within rc that the receiver computes (both
+ *       atoms inside its home slab in every dim where either is beyond it, the
+ *       eighth-shell assignment) loses an atom: the partner lies inside the
+ *       box in those dims, so their distance is at least this one.
  *
  * Build: gcc -std=c11 -O2 -fno-fast-math -ffp-contract=off -shared -fPIC
  */
@@ -90,6 +103,9 @@ typedef struct {
     int32_t *atom_offset; /* first slot of this pulse's halo in the receiver */
     float *shift;         /* 3 per (s, p) */
     ivec *map;
+    int prune;   /* reading R8 */
+    ivec *disp;  /* per domain and local slot: bit e set iff the slot was received
+                    across an upper face in dim e (on its whole forwarding path) */
     int threads; /* exchanges: OpenMP threads over the domains of one pulse (<= 1: none) */
 } oracle_t;
 
@@ -129,10 +145,13 @@ void oracle_free(oracle_t *o)
         for (int d = 0; d < o->n_dom; d++) free(o->xyz[d].v);
     if (o->gid)
         for (int d = 0; d < o->n_dom; d++) free(o->gid[d].v);
+    if (o->disp)
+        for (int d = 0; d < o->n_dom; d++) free(o->disp[d].v);
     if (o->map)
         for (int i = 0; i < o->n_dom * o->n_pulses; i++) free(o->map[i].v);
     free(o->xyz);
     free(o->gid);
+    free(o->disp);
     free(o->map);
     free(o->n_home);
     free(o->n_local);
@@ -158,9 +177,42 @@ static int domain_id(const oracle_t *o, const int c[3])
     return c[0] + o->grid[0] * (c[1] + o->grid[1] * c[2]);
 }
 
+/* Reading R8: is local slot i of sender s (cell c), a candidate of a pulse in
+ * dim d, within rc of the receiver's home box over the dims where it lies
+ * beyond it? */
+static int within_corner(const oracle_t *o, int s, const int c[3], int d, int32_t i)
+{
+    const float *x = &o->xyz[s].v[3 * (int64_t)i];
+    const int32_t m = o->disp[s].v[i];
+    const double lo_d = (double)c[d] * (double)o->box[d] / (double)o->grid[d];
+    double t = (double)x[d] - lo_d;
+    if (t < 0.0) t = 0.0;
+    double r2 = t * t;
+    for (int e = 0; e < 3; e++) {
+        if (e == d || !((m >> e) & 1)) continue;
+        const double hi_e = (double)(c[e] + 1) * (double)o->box[e] / (double)o->grid[e];
+        double u = (double)x[e] - hi_e;
+        if (u < 0.0) u = 0.0;
+        r2 = r2 + u * u;
+    }
+    return r2 < (double)o->rc * (double)o->rc;
+}
+
+int oracle_setup_ex(const float box[3], const int grid[3], float rc,
+                    const float *xyz, const int32_t *dom, int64_t n_atoms,
+                    int flags, oracle_t **out);
+
 int oracle_setup(const float box[3], const int grid[3], float rc,
                  const float *xyz, const int32_t *dom, int64_t n_atoms,
                  oracle_t **out)
+{
+    return oracle_setup_ex(box, grid, rc, xyz, dom, n_atoms, 0, out);
+}
+
+/* flags: 1 = corner pruning (reading R8). */
+int oracle_setup_ex(const float box[3], const int grid[3], float rc,
+                    const float *xyz, const int32_t *dom, int64_t n_atoms,
+                    int flags, oracle_t **out)
 {
     *out = NULL;
     if (!box || !grid || !xyz || !dom || n_atoms <= 0) return ORC_EINVAL;
@@ -175,6 +227,7 @@ int oracle_setup(const float box[3], const int grid[3], float rc,
         o->box[d] = box[d];
     }
     o->rc = rc;
+    o->prune = (flags & 1) != 0;
     o->n_atoms = n_atoms;
     o->n_dom = grid[0] * grid[1] * grid[2];
 
@@ -218,6 +271,7 @@ int oracle_setup(const float box[3], const int grid[3], float rc,
     o->base = (int64_t *)calloc((size_t)ND, sizeof(int64_t));
     o->xyz = (fvec3 *)calloc((size_t)ND, sizeof(fvec3));
     o->gid = (ivec *)calloc((size_t)ND, sizeof(ivec));
+    o->disp = (ivec *)calloc((size_t)ND, sizeof(ivec));
     size_t nsp = (size_t)ND * (size_t)(P > 0 ? P : 1);
     o->recv_dom = (int32_t *)calloc(nsp, sizeof(int32_t));
     o->send_size = (int32_t *)calloc(nsp, sizeof(int32_t));
@@ -225,7 +279,7 @@ int oracle_setup(const float box[3], const int grid[3], float rc,
     o->atom_offset = (int32_t *)calloc(nsp, sizeof(int32_t));
     o->shift = (float *)calloc(3 * nsp, sizeof(float));
     o->map = (ivec *)calloc(nsp, sizeof(ivec));
-    if (!o->n_home || !o->n_local || !o->base || !o->xyz || !o->gid ||
+    if (!o->n_home || !o->n_local || !o->base || !o->xyz || !o->gid || !o->disp ||
         !o->recv_dom || !o->send_size || !o->split || !o->atom_offset ||
         !o->shift || !o->map) {
         oracle_free(o);
@@ -237,7 +291,7 @@ int oracle_setup(const float box[3], const int grid[3], float rc,
     for (int64_t a = 0; a < n_atoms; a++) {
         int D = dom[a];
         if (fvec3_push(&o->xyz[D], xyz[3 * a], xyz[3 * a + 1], xyz[3 * a + 2]) ||
-            ivec_push(&o->gid[D], (int32_t)a)) {
+            ivec_push(&o->gid[D], (int32_t)a) || ivec_push(&o->disp[D], 0)) {
             oracle_free(o);
             return ORC_ENOMEM;
         }
@@ -278,7 +332,8 @@ int oracle_setup(const float box[3], const int grid[3], float rc,
                                       (double)rc);
             ivec *m = &o->map[sp];
             for (int32_t i = cand_lo[s]; i < cand_hi[s]; i++) {
-                if (o->xyz[s].v[3 * (int64_t)i + d] < thr) {
+                if (o->xyz[s].v[3 * (int64_t)i + d] < thr &&
+                    (!o->prune || within_corner(o, s, c, d, i))) {
                     if (ivec_push(m, i)) {
                         free(cand_lo);
                         free(cand_hi);
@@ -309,7 +364,8 @@ int oracle_setup(const float box[3], const int grid[3], float rc,
                 const float *src = &o->xyz[s].v[3 * (int64_t)m->v[j]];
                 if (fvec3_push(&o->xyz[r], src[0] + sh[0], src[1] + sh[1],
                                src[2] + sh[2]) ||
-                    ivec_push(&o->gid[r], o->gid[s].v[m->v[j]])) {
+                    ivec_push(&o->gid[r], o->gid[s].v[m->v[j]]) ||
+                    ivec_push(&o->disp[r], o->disp[s].v[m->v[j]] | (1 << d))) {
                     free(cand_lo);
                     free(cand_hi);
                     free(prev_start);

@@ -76,16 +76,19 @@ def load_example(name):
     return ex
 
 
-EXAMPLES = ["tiny_2x1x1.txt", "tiny_4x1x1_two_pulse.txt", "tiny_2x2x1_corner.txt"]
+EXAMPLES = ["tiny_2x1x1.txt", "tiny_4x1x1_two_pulse.txt", "tiny_2x2x1_corner.txt",
+            "tiny_2x2x1_corner_pruned.txt"]
 
 
 def check_example(make_plan, ex):
     """Compare a plan (oracle or library adaptor) with a hand-worked example.
 
-    ``make_plan(box, grid, rc, xyz, dom)`` returns an object with the
-    attributes/methods of ``oracle.Oracle``.
+    ``make_plan(box, grid, rc, xyz, dom, prune=...)`` returns an object with
+    the attributes/methods of ``oracle.Oracle``.
     """
-    o = make_plan(ex["box"], ex["grid"], ex["rc"], ex["atoms"], ex["domains"].astype(np.int32))
+    prune = bool(ex["prune"][0]) if "prune" in ex else False
+    o = make_plan(ex["box"], ex["grid"], ex["rc"], ex["atoms"], ex["domains"].astype(np.int32),
+                  prune=prune)
     assert list(o.pulse_dim) == list(ex["pulse_dims"]), ("pulse dims", o.pulse_dim)
     np.testing.assert_array_equal(o.n_home, ex["n_home"], err_msg="n_home")
     np.testing.assert_array_equal(o.n_local, ex["n_local"], err_msg="n_local")
@@ -148,7 +151,7 @@ def halo_images(o, xyz):
     return out
 
 
-def geometric_halo(xyz, dom, box, grid, rc, per_dim, domains=None):
+def geometric_halo(xyz, dom, box, grid, rc, per_dim, domains=None, prune=False):
     """Direct construction of every domain's eighth-shell halo, atom by atom.
 
     An atom whose home cell is H appears in domain D's halo iff, in every
@@ -159,19 +162,31 @@ def geometric_halo(xyz, dom, box, grid, rc, per_dim, domains=None):
     coordinate held at offset j carries +L_d iff the chain crossed the
     periodic boundary between offset o_d and offset j.  Image shift = +L_d iff
     D_d + o_d >= n_d.
+
+    prune (corner pruning): at every forwarding step the atom must also lie
+    within rc of the receiving domain's box over the dims in which it is beyond
+    that box.  Steps go z, then y, then x; at step j of dim d the receiving
+    domain is at offset j - 1 in d and already at D in the dims forwarded
+    before d, so the distance is
+        max(0, held_d - lower face of the domain at offset j)^2
+      + sum over earlier-forwarded dims e with o_e > 0, ascending e, of
+        max(0, x_e as held in D - upper face of D in e)^2
+    in double, compared with rc^2 (rc as fp32, squared in double).
     """
     L = np.asarray(box, np.float32)
     n = np.asarray(grid, np.int64)
     cells = cells_of(dom, grid)
     N = xyz.shape[0]
     nd = int(np.prod(n))
+    rc2 = float(np.float32(rc)) * float(np.float32(rc))
     out = {}
     for D in (range(nd) if domains is None else domains):
         cD = cells_of(np.asarray([D]), grid)[0]
         ok = np.ones(N, bool)
         moved = np.zeros(N, bool)
         shift = np.zeros((N, 3), np.int64)
-        for d in range(3):
+        final = {}   # dim -> (offset, coordinate as held in D)
+        for d in (2, 1, 0):
             if n[d] == 1:
                 continue
             o = (cells[:, d] - cD[d]) % n[d]
@@ -184,9 +199,23 @@ def geometric_halo(xyz, dom, box, grid, rc, per_dim, domains=None):
                 S = U % n[d]
                 held = np.where(wrap_o & (U < n[d]), xs, x)
                 thr = np.float32(float(S) * float(L[d]) / float(n[d]) + float(np.float32(rc)))
-                ok &= (o < j) | (held < thr)
+                step_ok = held < thr
+                if prune:
+                    lo = float(S) * float(L[d]) / float(n[d])
+                    t = np.maximum(held.astype(np.float64) - lo, 0.0)
+                    r2 = t * t
+                    for e in (0, 1, 2):
+                        if e == d or e not in final:
+                            continue
+                        oe, xe = final[e]
+                        hi = float(cD[e] + 1) * float(L[e]) / float(n[e])
+                        u = np.maximum(xe.astype(np.float64) - hi, 0.0)
+                        r2 = r2 + np.where(oe > 0, u * u, 0.0)
+                    step_ok &= r2 < rc2
+                ok &= (o < j) | step_ok
             shift[:, d] = wrap_o.astype(np.int64)
             moved |= o > 0
+            final[d] = (o, np.where(wrap_o, xs, x))
         ok &= moved
         idx = np.nonzero(ok)[0]
         out[D] = sorted(zip(idx.tolist(), *[shift[idx, e].tolist() for e in range(3)]))
@@ -195,7 +224,8 @@ def geometric_halo(xyz, dom, box, grid, rc, per_dim, domains=None):
 
 def check_geometric(o, xyz, dom, domains=None):
     per_dim = [int(v) for v in o.pulses_per_dim]
-    want = geometric_halo(xyz, dom, o.box, o.grid, o.rc, per_dim, domains)
+    want = geometric_halo(xyz, dom, o.box, o.grid, o.rc, per_dim, domains,
+                          prune=getattr(o, "prune", False))
     got = halo_images(o, xyz)
     for D, w in want.items():
         g = got[D]

@@ -34,8 +34,8 @@ MUTANTS = {
         "cand_hi[s] = (int32_t)o->xyz[s].n;",
         "cand_hi[s] = (k == 0) ? o->n_home[s] : (int32_t)o->xyz[s].n;"),
     "predicate_not_strict": (
-        "if (o->xyz[s].v[3 * (int64_t)i + d] < thr) {",
-        "if (o->xyz[s].v[3 * (int64_t)i + d] <= thr) {"),
+        "if (o->xyz[s].v[3 * (int64_t)i + d] < thr &&",
+        "if (o->xyz[s].v[3 * (int64_t)i + d] <= thr &&"),
     "split_off_by_one": (
         "if (m->v[j] < o->n_home[s]) nsplit++;",
         "if (m->v[j] <= o->n_home[s]) nsplit++;"),
@@ -57,6 +57,18 @@ MUTANTS = {
     "forces_wrong_halo_slice": (
         "const float *halo = local + 3 * (o->base[r] + o->atom_offset[sp]);",
         "const float *halo = local + 3 * (o->base[r] + o->n_home[r]);"),
+    "corner_distance_from_upper_face": (
+        "const double lo_d = (double)c[d] * (double)o->box[d] / (double)o->grid[d];",
+        "const double lo_d = (double)(c[d] + 1) * (double)o->box[d] / (double)o->grid[d];"),
+    "corner_ignores_path_dims": (
+        "r2 = r2 + u * u;",
+        "r2 = r2 + 0.0 * u * u;"),
+    "corner_path_dims_lower_face": (
+        "const double hi_e = (double)(c[e] + 1) * (double)o->box[e] / (double)o->grid[e];",
+        "const double hi_e = (double)c[e] * (double)o->box[e] / (double)o->grid[e];"),
+    "corner_path_not_inherited": (
+        "ivec_push(&o->disp[r], o->disp[s].v[m->v[j]] | (1 << d))",
+        "ivec_push(&o->disp[r], (1 << d))"),
     "control_comment_only": (
         "/* dense layout: base[D] = sum of local sizes of lower domain ids */",
         "/* dense layout (unchanged code; only this comment differs) */"),
@@ -76,8 +88,8 @@ def _build_mutant(tmp, name):
 
 
 def _run_pins(lib):
-    def make(box, grid, rc, xyz, dom):
-        return oracle.Oracle(box, grid, rc, xyz, dom, lib=lib)
+    def make(box, grid, rc, xyz, dom, prune=False):
+        return oracle.Oracle(box, grid, rc, xyz, dom, lib=lib, prune=prune)
 
     for ex in pins.EXAMPLES:
         pins.check_example(make, pins.load_example(ex))
@@ -96,6 +108,17 @@ def _run_pins(lib):
         o = make(box, grid, rc, xyz, dom)
         pins.check_pair_coverage(o, xyz, dom)
         pins.check_forces_integer(o)
+    # corner pruning: the direct construction, pair coverage and the forces
+    w = synth.WORKLOADS["water24k_2x4x8"]
+    xyz, dom = synth.system(w)
+    o = make(w.box, w.grid, w.rc, xyz, dom, prune=True)
+    pins.check_maps(o)
+    pins.check_geometric(o, xyz, dom)
+    pins.check_forces_integer(o)
+    box, grid, rc = (3.0, 2.6, 2.2), (3, 2, 2), 0.6
+    xyz, dom = synth.custom_system(300, box, grid, seed=11)
+    o = make(box, grid, rc, xyz, dom, prune=True)
+    pins.check_pair_coverage(o, xyz, dom)
 
 
 @pytest.fixture(scope="module")

@@ -12,8 +12,8 @@ from domain_decomposition_halo_build_gb300 import synth
 STRUCT = pins.load_pulse_structure()
 
 
-def make_oracle(box, grid, rc, xyz, dom):
-    return oracle.Oracle(box, grid, rc, xyz, dom)
+def make_oracle(box, grid, rc, xyz, dom, prune=False):
+    return oracle.Oracle(box, grid, rc, xyz, dom, prune=prune)
 
 
 # -- hand-worked golden examples ------------------------------------------------
@@ -152,6 +152,68 @@ def test_degenerate_cases():
     o = oracle.Oracle((4, 4, 4), (4, 1, 1), 0.05, xyz, dom)
     assert o.n_home[3] == 0
     pins.check_maps(o)
+    pins.check_geometric(o, xyz, dom)
+    pins.check_forces_integer(o)
+
+
+# -- corner pruning (optional plan flag) ------------------------------------------
+@pytest.fixture(scope="module")
+def pruned():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            w = synth.WORKLOADS[name]
+            xyz, dom = synth.system(w)
+            cache[name] = (w, xyz, dom, oracle.Oracle(w.box, w.grid, w.rc, xyz, dom, prune=True))
+        return cache[name]
+
+    return get
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_pruned_geometric_maps_forces(pruned, name):
+    w, xyz, dom, o = pruned(name)
+    pins.check_geometric(o, xyz, dom)
+    pins.check_maps(o)
+    pins.check_load_and_exchange_x(o, xyz)
+    pins.check_forces_integer(o)
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_pruned_geometric_sampled_domains(pruned, name):
+    w, xyz, dom, o = pruned(name)
+    nd = o.n_domains
+    pins.check_geometric(o, xyz, dom, domains=[0, nd // 3, nd - 1])
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_pruned_halo_is_a_subset(plans, pruned, name):
+    """Pruning only removes halo images: every domain's pruned set is contained
+    in its unpruned set, and on these 3D workloads it removes some."""
+    w, xyz, dom, o = plans(name)
+    _, _, _, q = pruned(name)
+    full, part = pins.halo_images(o, xyz), pins.halo_images(q, xyz)
+    removed = 0
+    for D in range(o.n_domains):
+        assert set(part[D]) <= set(full[D]), D
+        removed += len(full[D]) - len(part[D])
+    assert (removed > 0) == (int(np.sum(np.asarray(w.grid) > 1)) > 1), removed
+
+
+def test_pruned_example_prunes_one_atom_that_the_slabs_keep():
+    """The hand-worked pruning example built without pruning: the x pulse of
+    sender 3 also sends the atom whose corner distance is 1.27 > rc."""
+    ex = pins.load_example("tiny_2x2x1_corner_pruned.txt")
+    o = oracle.Oracle(ex["box"], ex["grid"], ex["rc"], ex["atoms"], ex["domains"].astype(np.int32))
+    np.testing.assert_array_equal(o.index_map(3, 1), [0, 1, 2])
+
+
+@pytest.mark.parametrize("box,grid,rc,n", TINY)
+def test_pruned_pair_coverage_bruteforce(box, grid, rc, n):
+    xyz, dom = synth.custom_system(n, box, grid, seed=11)
+    o = oracle.Oracle(box, grid, rc, xyz, dom, prune=True)
+    assert pins.check_pair_coverage(o, xyz, dom) > 50
     pins.check_geometric(o, xyz, dom)
     pins.check_forces_integer(o)
 
