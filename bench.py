@@ -164,14 +164,14 @@ def gpu_index(local_rank):
     return local_rank
 
 
-def setup_workload(name, device):
+def setup_workload(name, device, prune=False):
     import torch
     from domain_decomposition_halo_build_gb300 import halo, synth
     w = synth.WORKLOADS[name]
     xyz, dom = synth.system(w)
     x = torch.from_numpy(xyz).to(device)
     d = torch.from_numpy(dom).to(device)
-    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d)
+    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d, prune=prune)
     loc = plan.load_home(x)
     f0 = torch.from_numpy(synth.forces(plan.n_local_total, seed=1)).to(device)
     return w, xyz, dom, x, plan, loc, f0
@@ -363,6 +363,26 @@ def overlap_case(plan, loc, f, steps, warmup, flush, mode, device, priority=0):
             "non_overlap_us": statistics.fmean(nov), "step_us": statistics.fmean(step_us),
             "nonlocal_stream_priority": priority,
             "local_stand_in": "bf16 matmul 2048x4096x4096 on a second stream"}
+
+
+def pruned_case(name, mode, device, stream, flush, steps, warmup, unpruned_slots):
+    """The same system built with corner pruning (HALO_SETUP_PRUNE_CORNERS):
+    fewer halo slots, the same exchanges."""
+    import torch
+    w, xyz, dom, x, plan, loc, f0 = setup_workload(name, device, prune=True)
+    plan.set_mode(mode)
+    sts, xs, fs, _, _, _ = time_steps(plan, loc, f0.clone(), steps, warmup, flush, stream,
+                                      split_steps=min(steps, 200))
+    assert plan.status() == 0
+    us = 1e3 * statistics.fmean(sts)
+    slots = plan.n_halo_total
+    plan.close()
+    torch.cuda.synchronize()
+    return {"workload": name, "mode": mode, "halo_slots": slots,
+            "halo_slots_unpruned": unpruned_slots, "slots_kept": slots / unpruned_slots,
+            "us_per_exchange": us, "us_x": 1e3 * statistics.fmean(xs),
+            "us_f": 1e3 * statistics.fmean(fs), "value": slots / (us * 1e-6),
+            "hbm_frac": (BYTES_X + BYTES_F) * slots / (us * 1e-6) / 1e9 / measured_peak()[0]}
 
 
 REBUILD_WORKLOAD = "water3M_8x8x8"
@@ -579,8 +599,16 @@ def main():
         lat[mode] = {"us_per_exchange": 1e3 * statistics.fmean(lsts),
                      "us_x": 1e3 * statistics.fmean(lxs), "us_f": 1e3 * statistics.fmean(lfs),
                      "launches_per_direction": llaunch / (2 * lsteps)}
+    lat_slots = lplan.n_halo_total
     lplan.close()
     plan.set_mode(args.mode)
+
+    # corner pruning: the headline and the latency systems, headline mode
+    pruned = [pruned_case(args.workload, args.mode, device, stream, flush, min(args.steps, 500),
+                          args.warmup, halo_slots),
+              pruned_case(LATENCY_WORKLOAD, args.mode, device, stream, flush, min(args.steps, 500),
+                          args.warmup, lat_slots)]
+
 
     # the same step captured as a CUDA graph (one graph launch per x + f)
     graph = {}
@@ -592,6 +620,8 @@ def main():
     plan.set_mode(args.mode)
 
     rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
+    pruned.append(pruned_case(REBUILD_WORKLOAD, args.mode, device, stream, flush,
+                              min(args.steps, 300), args.warmup, rebuild["halo_slots"]))
     overlap = [overlap_case(plan, loc, f0.clone(), min(args.steps, 300), args.warmup, flush, m, device,
                             prio) for m in (args.mode, "fused") for prio in (0, -1)]
     plan.set_mode(args.mode)
@@ -627,6 +657,7 @@ def main():
             "other_modes": others,
             "cuda_graph": graph,
             "latency_case": lat,
+            "pruned_case": pruned,
             "rebuild_case": rebuild,
             "overlap_case": overlap,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -107,14 +107,22 @@ extern "C" {
 int halo_setup(const float box[3], const int32_t grid[3], float rc, const float* coords,
                const int32_t* domain_of_atom, int64_t n_atoms, void* stream,
                halo_plan** out_plan) {
+    return halo_setup_ex(box, grid, rc, coords, domain_of_atom, n_atoms, 0u, stream, out_plan);
+}
+
+int halo_setup_ex(const float box[3], const int32_t grid[3], float rc, const float* coords,
+                  const int32_t* domain_of_atom, int64_t n_atoms, uint32_t flags, void* stream,
+                  halo_plan** out_plan) {
     if (!out_plan) return HALO_EINVAL;
     *out_plan = nullptr;
     if (!coords || !domain_of_atom || n_atoms <= 0 || n_atoms > INT32_MAX / 2)
         return HALO_EINVAL;
+    if (flags & ~HALO_SETUP_PRUNE_CORNERS) return HALO_EINVAL;
     HALO_TRY(check_problem(box, grid, rc, nullptr));
     halo_plan* pl = new (std::nothrow) halo_plan();
     if (!pl) return HALO_ENOMEM;
     int rc_ = HALO_OK;
+    pl->flags = flags;
     try {
         rc_ = check_problem(box, grid, rc, pl);
         if (rc_ == HALO_OK && cudaGetDevice(&pl->dev) != cudaSuccess) rc_ = HALO_ECUDA;
@@ -158,6 +166,7 @@ int halo_query(const halo_plan* pl, halo_info* out) {
     out->n_pulses = pl->P;
     for (int d = 0; d < 3; d++) out->pulses_per_dim[d] = pl->pulses_per_dim[d];
     for (int p = 0; p < pl->P; p++) out->pulse_dim[p] = pl->pulse_dim[p];
+    out->flags = pl->flags;
     out->n_atoms = pl->n_atoms;
     out->n_local_total = pl->n_local_total;
     out->n_halo_total = pl->n_halo_total;

@@ -263,7 +263,35 @@ struct PulseArgs {
     int nd, P, p, d, k, B;
     int nx, ny, nz;
     float Ld;
+    // corner pruning (prune != 0)
+    int prune;
+    int nmax;
+    double rc2;           // rc * rc in double, rc as fp32
+    const double* faces;  // lower faces [3][nmax], then upper faces [3][nmax]
+    uint8_t* bmask;       // per build slot >= N: dims the slot was received across
 };
+
+// Corner pruning: distance of a candidate (coordinates v, build slot pos) of
+// sender cell c to the receiver's home box, over the pulse's dim d and the
+// dims the slot was received across, below rc?  Double precision with
+// explicit round-to-nearest operations (no contraction), d's term first, then
+// ascending dims.  *mask receives the slot's dims (0 for a home slot).
+__device__ __forceinline__ bool corner_within(const PulseArgs& a, const int c[3], int64_t pos,
+                                              const float v[3], unsigned* mask) {
+    const unsigned m = pos < a.N ? 0u : (unsigned)a.bmask[pos];
+    *mask = m;
+    double t = __dsub_rn((double)v[a.d], a.faces[a.d * a.nmax + c[a.d]]);
+    t = t > 0.0 ? t : 0.0;
+    double r2 = __dmul_rn(t, t);
+#pragma unroll
+    for (int e = 0; e < 3; e++) {
+        if (e == a.d || !((m >> e) & 1u)) continue;
+        double u = __dsub_rn((double)v[e], a.faces[(3 + e) * a.nmax + c[e]]);
+        u = u > 0.0 ? u : 0.0;
+        r2 = __dadd_rn(r2, __dmul_rn(u, u));
+    }
+    return r2 < a.rc2;
+}
 
 struct Locator {
     int64_t oo[HALO_MAX_PULSES + 1];
@@ -303,6 +331,7 @@ __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
     load_locator(L, a, s);
     const int cs = cell_of(s, a.d, a.nx, a.ny);
     const float thr = a.thr[cs];
+    const int cell[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
     int64_t lo, hi;
     sub_range(L, a, b, &lo, &hi);
     const int64_t nh = L.oo[0];
@@ -310,6 +339,11 @@ __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
     for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
         const int64_t pos = locate(L, a.p, i);
         if (pos >= 0 && pos < a.cap && a.bxyz[3 * pos + a.d] < thr) {
+            if (a.prune) {
+                const float v[3] = {a.bxyz[3 * pos], a.bxyz[3 * pos + 1], a.bxyz[3 * pos + 2]};
+                unsigned m;
+                if (!corner_within(a, cell, pos, v, &m)) continue;
+            }
             c++;
             if (i < nh) ch++;
         }
@@ -369,6 +403,7 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cs = cell_of(s, a.d, a.nx, a.ny);
     const float thr = a.thr[cs];
+    const int cell[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
     float sh[3] = {0.0f, 0.0f, 0.0f};
     if (cs == 0) sh[a.d] = a.Ld;
     int64_t lo, hi;
@@ -379,6 +414,7 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
         const int64_t i = t0 + threadIdx.x;
         bool sel = false;
         float v0 = 0, v1 = 0, v2 = 0;
+        unsigned m = 0;
         if (i < hi) {
             const int64_t pos = locate(L, a.p, i);
             if (pos >= 0 && pos < a.cap) {
@@ -387,6 +423,10 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
                 v2 = a.bxyz[3 * pos + 2];
                 const float vd = a.d == 0 ? v0 : (a.d == 1 ? v1 : v2);
                 sel = vd < thr;
+                if (sel && a.prune) {
+                    const float v[3] = {v0, v1, v2};
+                    sel = corner_within(a, cell, pos, v, &m);
+                }
             }
         }
         const unsigned bal = __ballot_sync(kFull, sel);
@@ -403,6 +443,7 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
             const int64_t o = out + before + __popc(bal & lt);
             if (o >= a.N && o < a.cap) {
                 a.maps[o - a.N] = (int32_t)i;
+                if (a.prune) a.bmask[o] = (uint8_t)(m | (1u << a.d));
                 a.bxyz[3 * o + 0] = v0 + sh[0];
                 a.bxyz[3 * o + 1] = v1 + sh[1];
                 a.bxyz[3 * o + 2] = v2 + sh[2];
@@ -463,6 +504,9 @@ void free_build(halo_plan* pl) {
     dev_free(pl->d_meta);
     dev_free(pl->d_pulse_scratch);
     dev_free(pl->d_thr);
+    dev_free(pl->d_faces);
+    dev_free(pl->d_bmask);
+    pl->cap_bmask = 0;
     pl->cap_slots = 0;
     pl->n_alloc_atoms = 0;
     pl->counts_cap = 0;
@@ -534,6 +578,20 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
                              cudaMemcpyHostToDevice));
     }
     const int nmax = std::max(pl->grid[0], std::max(pl->grid[1], pl->grid[2]));
+    const bool prune = (pl->flags & HALO_SETUP_PRUNE_CORNERS) != 0;
+    // corner pruning: faces c * L_d / n_d (lower) and (c + 1) * L_d / n_d (upper), in double
+    if (prune && !pl->d_faces) {
+        std::vector<double> faces((size_t)6 * nmax, 0.0);
+        for (int d = 0; d < 3; d++)
+            for (int c = 0; c < pl->grid[d]; c++) {
+                faces[(size_t)d * nmax + c] = (double)c * (double)pl->box[d] / (double)pl->grid[d];
+                faces[(size_t)(3 + d) * nmax + c] =
+                    (double)(c + 1) * (double)pl->box[d] / (double)pl->grid[d];
+            }
+        HALO_TRY(dev_alloc(&pl->d_faces, faces.size()));
+        HALO_CUDA(cudaMemcpy(pl->d_faces, faces.data(), faces.size() * sizeof(double),
+                             cudaMemcpyHostToDevice));
+    }
 
     // capacity estimate: each decomposed dim widens a domain by rc
     double grow_f = 1.0;
@@ -563,6 +621,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         } else if (!pl->d_maps) {
             HALO_TRY(dev_alloc(&pl->d_maps, (size_t)pl->cap_slots));
         }
+        if (prune) HALO_TRY(dev_reserve(&pl->d_bmask, &pl->cap_bmask, pl->cap_slots));
         HALO_CUDA(cudaMemsetAsync(pl->d_meta, 0, mbytes, st));
         // 1. home partition
         home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(dom, n, nd, ntiles,
@@ -595,6 +654,11 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
             a.ny = pl->grid[1];
             a.nz = pl->grid[2];
             a.Ld = pl->box[a.d];
+            a.prune = prune ? 1 : 0;
+            a.nmax = nmax;
+            a.rc2 = (double)pl->rc * (double)pl->rc;
+            a.faces = pl->d_faces;
+            a.bmask = pl->d_bmask;
             dim3 g((unsigned)B, (unsigned)nd);
             pulse_count_kernel<<<g, kThreads, 0, st>>>(a);
             pulse_scan_kernel<<<1, 1024, 0, st>>>(a);

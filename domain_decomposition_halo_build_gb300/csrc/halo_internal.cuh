@@ -93,6 +93,10 @@ struct halo_plan {
     int32_t* d_pulse_scratch = nullptr;  // per-pulse block counts (3 * n_dom * B)
     int build_blocks_per_domain = 1;
     float* d_thr = nullptr;         // thresholds per pulse and sender cell
+    uint32_t flags = 0;             // HALO_SETUP_* options
+    double* d_faces = nullptr;      // corner pruning: lower faces [3][nmax], upper faces [3][nmax]
+    uint8_t* d_bmask = nullptr;     // corner pruning: per build slot, dims it was received across
+    int64_t cap_bmask = 0;
 
     // device memory owned by the plan: exchange
     halo::SPDesc* d_sp = nullptr;

@@ -22,6 +22,7 @@ OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM, ESCRA
     0, -1, -2, -3, -4, -5, -6, -7, -8, -9)
 NOALLOC_MAX_COUNTERS = 16384
 MAX_PULSES = 64
+SETUP_PRUNE_CORNERS = 1
 MODE_FUSED, MODE_STEPWISE, MODE_FLAT = 0, 1, 2
 MODES = {"fused": MODE_FUSED, "stepwise": MODE_STEPWISE, "flat": MODE_FLAT}
 
@@ -37,7 +38,7 @@ class halo_info(ctypes.Structure):
                 ("pulses_per_dim", ctypes.c_int32 * 3),
                 ("pulse_dim", ctypes.c_int32 * MAX_PULSES),
                 ("n_atoms", ctypes.c_int64), ("n_local_total", ctypes.c_int64),
-                ("n_halo_total", ctypes.c_int64)]
+                ("n_halo_total", ctypes.c_int64), ("flags", ctypes.c_uint32)]
 
 
 class halo_pulse_info(ctypes.Structure):
@@ -55,6 +56,8 @@ _P = ctypes.POINTER
 SIGNATURES = {
     "halo_setup": (ctypes.c_int, [_P(ctypes.c_float), _P(_i32), ctypes.c_float, _vp, _vp, _i64,
                                   _vp, _P(_vp)]),
+    "halo_setup_ex": (ctypes.c_int, [_P(ctypes.c_float), _P(_i32), ctypes.c_float, _vp, _vp, _i64,
+                                     ctypes.c_uint32, _vp, _P(_vp)]),
     "halo_rebuild": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
     "halo_query": (ctypes.c_int, [_vp, _P(halo_info)]),
     "halo_domain_layout": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
@@ -130,17 +133,23 @@ def _dev_ptr(t, dtype=None, shape=None):
 # --------------------------------------------------------------------------- #
 def halo_setup(box, grid, rc, coords, domain_of_atom, stream=None):
     """Build a plan on the device; returns the raw handle (c_void_p)."""
+    return halo_setup_ex(box, grid, rc, coords, domain_of_atom, 0, stream)
+
+
+def halo_setup_ex(box, grid, rc, coords, domain_of_atom, flags, stream=None):
+    """halo_setup with HALO_SETUP_* option flags; returns the raw handle."""
     import torch
     lib = load_library()
     n = int(coords.shape[0])
     boxa = (ctypes.c_float * 3)(*[float(v) for v in box])
     grida = (_i32 * 3)(*[int(v) for v in grid])
     h = ctypes.c_void_p()
-    code = lib.halo_setup(boxa, grida, ctypes.c_float(float(rc)),
-                          _dev_ptr(coords, torch.float32, (n, 3)),
-                          _dev_ptr(domain_of_atom, torch.int32, (n,)),
-                          _i64(n), _stream_handle(stream), ctypes.byref(h))
-    _check(code, "halo_setup")
+    code = lib.halo_setup_ex(boxa, grida, ctypes.c_float(float(rc)),
+                             _dev_ptr(coords, torch.float32, (n, 3)),
+                             _dev_ptr(domain_of_atom, torch.int32, (n,)),
+                             _i64(n), ctypes.c_uint32(int(flags)), _stream_handle(stream),
+                             ctypes.byref(h))
+    _check(code, "halo_setup_ex")
     return h
 
 
@@ -182,12 +191,14 @@ def halo_destroy(plan):
 class HaloPlan:
     """One plan.  Tensors are torch CUDA tensors; host results are numpy."""
 
-    def __init__(self, box, grid, rc, coords, domain_of_atom, stream=None):
+    def __init__(self, box, grid, rc, coords, domain_of_atom, stream=None, prune=False):
+        """prune: corner pruning of forwarded candidates (HALO_SETUP_PRUNE_CORNERS)."""
         self.box = np.asarray(box, np.float32)
         self.grid = np.asarray(grid, np.int32)
         self.rc = float(np.float32(rc))
         self._lib = load_library()
-        self._h = halo_setup(box, grid, rc, coords, domain_of_atom, stream)
+        flags = SETUP_PRUNE_CORNERS if prune else 0
+        self._h = halo_setup_ex(box, grid, rc, coords, domain_of_atom, flags, stream)
         self._refresh()
 
     def _refresh(self):
@@ -199,6 +210,8 @@ class HaloPlan:
         self.n_atoms = info.n_atoms
         self.n_local_total = info.n_local_total
         self.n_halo_total = info.n_halo_total
+        self.flags = int(info.flags)
+        self.prune = bool(self.flags & SETUP_PRUNE_CORNERS)
         nd = self.n_domains
         self.base = np.zeros(nd, np.int64)
         self.n_home = np.zeros(nd, np.int32)

@@ -82,6 +82,7 @@ typedef struct {
     int64_t n_atoms;
     int64_t n_local_total;                  /* home + halo slots of all domains */
     int64_t n_halo_total;
+    uint32_t flags;                         /* HALO_SETUP_* flags the plan was built with */
 } halo_info;
 
 typedef struct {
@@ -105,6 +106,31 @@ typedef struct {
 int halo_setup(const float box[3], const int32_t grid[3], float rc, const float* coords,
                const int32_t* domain_of_atom, int64_t n_atoms, void* stream,
                halo_plan** out_plan);
+
+/* Plan options of halo_setup_ex.
+ *   HALO_SETUP_PRUNE_CORNERS: corner pruning of forwarded candidates.  The
+ *     page "Redesigning GROMACS Halo Exchange ..." (section 3) selects, per
+ *     pulse, the atoms within the cut-off of the neighbour's face (a
+ *     one-dimensional slab) and has no counterpart for this option.  With it,
+ *     a candidate of a pulse in dim d that passes the face threshold is sent
+ *     only if its distance to the receiver's home box, over d and every dim
+ *     across whose upper face the slot was received on its forwarding path, is
+ *     below rc: in double, max(0, x_d - the sender's lower face)^2 first, then
+ *     max(0, x_e - the sender's upper face in e)^2 for those dims e in
+ *     ascending order, compared strictly with rc * rc (faces c * L / n in
+ *     double).  Every pair within rc that the receiver computes under the
+ *     eighth-shell assignment keeps both atoms; only corner and edge atoms
+ *     that no such pair needs are dropped, so halos shrink (more in thin
+ *     domains and several-pulse dims).  Everything else, including the
+ *     exchanges and their modes, is unchanged. */
+#define HALO_SETUP_PRUNE_CORNERS 1u
+
+/* halo_setup with options (a bitwise or of HALO_SETUP_* flags; 0 gives
+ * halo_setup).  Unknown bits: HALO_EINVAL.  The flags are kept across
+ * halo_rebuild and reported by halo_query. */
+int halo_setup_ex(const float box[3], const int32_t grid[3], float rc, const float* coords,
+                  const int32_t* domain_of_atom, int64_t n_atoms, uint32_t flags, void* stream,
+                  halo_plan** out_plan);
 
 /* Rebuild the plan's maps for new positions / domain ids (same box, grid and
  * cut-off; n_atoms may change).  Synchronises `stream`.  Sizes and layout

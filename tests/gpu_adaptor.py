@@ -7,14 +7,15 @@ import numpy as np
 
 
 class GpuPlan:
-    def __init__(self, box, grid, rc, xyz, dom, device="cuda:0"):
+    def __init__(self, box, grid, rc, xyz, dom, device="cuda:0", prune=False):
         import torch
         from domain_decomposition_halo_build_gb300 import halo
         self.torch = torch
         self.device = device
         self.xyz_d = torch.from_numpy(np.ascontiguousarray(xyz, np.float32).reshape(-1, 3)).to(device)
         self.dom_d = torch.from_numpy(np.ascontiguousarray(dom, np.int32)).to(device)
-        self.plan = halo.HaloPlan(box, grid, rc, self.xyz_d, self.dom_d)
+        self.plan = halo.HaloPlan(box, grid, rc, self.xyz_d, self.dom_d, prune=prune)
+        self.prune = bool(prune)
         p = self.plan
         self.box, self.grid, self.rc = p.box, p.grid, p.rc
         self._sync()

@@ -23,9 +23,9 @@ def built():
     __graft_entry__.build()
 
 
-def gpu_plan(box, grid, rc, xyz, dom):
+def gpu_plan(box, grid, rc, xyz, dom, prune=False):
     from gpu_adaptor import GpuPlan
-    return GpuPlan(box, grid, rc, xyz, dom)
+    return GpuPlan(box, grid, rc, xyz, dom, prune=prune)
 
 
 def bits(a):
@@ -287,3 +287,54 @@ def test_cuda_graph_replay(cases, mode):
         np.testing.assert_array_equal(bits(f.cpu().numpy()), bits(want_f))
     finally:
         g.plan.set_mode("fused")
+
+
+# -- corner pruning -------------------------------------------------------------------
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_pruned_plan_and_exchange_parity(name):
+    """HALO_SETUP_PRUNE_CORNERS: maps, sizes, shifts and both exchanges in every
+    mode bit-identical to the pruning oracle; a rebuild keeps the option."""
+    w = synth.WORKLOADS[name]
+    xyz, dom = synth.system(w)
+    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom, prune=True)
+    g = gpu_plan(w.box, w.grid, w.rc, xyz, dom, prune=True)
+    try:
+        assert g.plan.prune
+        compare_plans(g, o)
+        for mode in MODES:
+            g.plan.set_mode(mode)
+            compare_exchanges(g, o, xyz, reps=1)
+        if name == "water3M_8x8x8":
+            xk, dk = synth.displaced(xyz, w.box, w.grid, k=1)
+            g.rebuild(xk, dk)
+            assert g.plan.prune
+            ok = oracle.Oracle(w.box, w.grid, w.rc, xk, dk, prune=True)
+            compare_plans(g, ok)
+            compare_exchanges(g, ok, xk, reps=1)
+    finally:
+        g.close()
+
+
+@pytest.mark.parametrize("box,grid,rc,n,seed", EDGE)
+def test_pruned_edge_cases(box, grid, rc, n, seed):
+    xyz, dom = synth.custom_system(n, box, grid, seed=seed)
+    o = oracle.Oracle(box, grid, rc, xyz, dom, prune=True)
+    g = gpu_plan(box, grid, rc, xyz, dom, prune=True)
+    try:
+        compare_plans(g, o)
+        for mode in MODES:
+            g.plan.set_mode(mode)
+            compare_exchanges(g, o, xyz, reps=1)
+    finally:
+        g.close()
+
+
+def test_setup_ex_rejects_unknown_flags():
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    xyz, dom = synth.custom_system(100, (3, 3, 3), (3, 1, 1), seed=1)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    with pytest.raises(halo.HaloError) as e:
+        halo.halo_setup_ex((3, 3, 3), (3, 1, 1), 0.5, x, d, 2)
+    assert e.value.code == halo.EINVAL
