@@ -427,6 +427,58 @@ def pruned_case(name, mode, device, stream, flush, steps, warmup, unpruned_slots
             "hbm_frac": (BYTES_X + BYTES_F) * slots / (us * 1e-6) / 1e9 / measured_peak()[0]}
 
 
+STENCIL_GRID = (2, 4)               # blocks along columns, rows: the page's 8-node 2-D layout
+STENCIL_SIZES = (512, 2048, 8192)   # cells per block edge (the page sweeps 512^2 .. 32K^2 per GPU)
+
+
+def stencil_case(device, stream, flush, iters, warmup):
+    """The second workload: a 2-D stencil on px x py blocks, each iteration a
+    Jacobi sweep of every block and the exchange of block edges.  Unfused: a
+    sweep launch and an exchange launch (the MPI version's separate kernels);
+    fused: one launch that sweeps and stores the new edges into the
+    neighbours' ghost cells (the page's single kernel).  L2 flushed between
+    iterations; algorithmic bytes 8 per cell (one read, one write)."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import stencil
+    px, py = STENCIL_GRID
+    peak = measured_peak()[0]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(0)
+    res = []
+    for n in STENCIL_SIZES:
+        p = stencil.StencilPlan(px, py, n)
+        a = torch.rand(p.total_floats, device=device, generator=gen)
+        b = a.clone()
+        ops = {"exchange": lambda: p.exchange(a, stream),
+               "sweep": lambda: p.sweep(a, b, stream),
+               "sweep_then_exchange": lambda: (p.sweep(a, b, stream), p.exchange(b, stream)),
+               "fused": lambda: p.sweep_fused(a, b, stream)}
+        row = {"blocks": [px, py], "n": n, "cells": px * py * n * n}
+        for name, fn in ops.items():
+            for _ in range(warmup):
+                flush()
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(iters)]
+            for e0, e1 in ev:
+                flush()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            row[name + "_us"] = 1e3 * statistics.fmean(e0.elapsed_time(e1) for e0, e1 in ev)
+        sweep_gbs = 8.0 * row["cells"] / (row["sweep_us"] * 1e-6) / 1e9
+        row["sweep_gbs"] = sweep_gbs
+        row["sweep_hbm_frac"] = sweep_gbs / peak
+        row["fused_hbm_frac"] = 8.0 * row["cells"] / (row["fused_us"] * 1e-6) / 1e9 / peak
+        row["fused_speedup"] = row["sweep_then_exchange_us"] / row["fused_us"]
+        row["exchange_bytes"] = 8 * 4 * n * px * py   # edge cells read + written (at most)
+        res.append(row)
+        p.close()
+        del a, b
+    return res
+
+
 REBUILD_WORKLOAD = "water3M_8x8x8"
 
 
@@ -664,6 +716,7 @@ def main():
     rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
     pruned.append(pruned_case(REBUILD_WORKLOAD, args.mode, device, stream, flush,
                               min(args.steps, 300), args.warmup, rebuild["halo_slots"]))
+    stencil_res = stencil_case(device, stream, flush, min(args.steps, 50), max(3, min(args.warmup, 5)))
     overlap = [overlap_case(plan, loc, f0.clone(), min(args.steps, 300), args.warmup, flush, m, device,
                             prio) for m in (args.mode, "fused") for prio in (0, -1)]
     plan.set_mode(args.mode)
@@ -703,6 +756,7 @@ def main():
             "pruned_case": pruned,
             "rebuild_case": rebuild,
             "overlap_case": overlap,
+            "stencil_case": stencil_res,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms,
                     "schedule": "steps pipelined: H2D of step i+1 overlaps D2H of step i",

@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libhalo.so")
-SOURCES = ["halo_api.cu", "halo_build.cu", "halo_exchange.cu", "halo_modes.cu", "halo_noalloc.cu"]
+SOURCES = ["halo_api.cu", "halo_build.cu", "halo_exchange.cu", "halo_modes.cu", "halo_noalloc.cu",
+           "stencil.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-I" + INCLUDE, "-I" + CSRC]

@@ -12,10 +12,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "halo.h")
 
 
-def declared_functions():
-    text = open(HEADER).read()
+STENCIL_HEADER = os.path.join(ROOT, "include", "stencil.h")
+
+
+def declared_functions(header=HEADER, prefix="halo_"):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(halo_\w+)\s*\(", text, flags=re.M)))
+    pat = r"^[A-Za-z_][\w\s\*]*?\b(%s\w+)\s*\(" % prefix
+    return sorted(set(re.findall(pat, text, flags=re.M)))
 
 
 @pytest.fixture(scope="module")
@@ -40,6 +44,35 @@ def test_every_declared_symbol_is_exported(lib):
 def test_binding_covers_the_header():
     from domain_decomposition_halo_build_gb300 import halo
     assert set(declared_functions()) == set(halo.SIGNATURES)
+
+
+def test_stencil_header_symbols_exported_and_bound(lib):
+    from domain_decomposition_halo_build_gb300 import stencil
+    names = declared_functions(STENCIL_HEADER, "stencil_")
+    assert {"stencil_setup", "stencil_exchange", "stencil_sweep", "stencil_sweep_fused"} <= set(names)
+    assert not [n for n in names if not hasattr(lib, n)]
+    assert set(names) == set(stencil.SIGNATURES)
+
+
+def test_stencil_host_only_checks(lib):
+    from domain_decomposition_halo_build_gb300 import halo, stencil
+    stencil.load_library()
+    h = ctypes.c_void_p()
+    assert lib.stencil_setup(2, 2, 6, ctypes.byref(h)) == halo.EINVAL    # n % 4 != 0
+    assert lib.stencil_setup(0, 2, 8, ctypes.byref(h)) == halo.EINVAL
+    assert lib.stencil_setup(300, 300, 8, ctypes.byref(h)) == halo.EINVAL  # > 65535 tiles
+    assert lib.stencil_setup(2, 3, 8, ctypes.byref(h)) == halo.OK
+    pitch, rows, col0 = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    tile, total = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.stencil_layout(h, ctypes.byref(pitch), ctypes.byref(rows), ctypes.byref(col0),
+                              ctypes.byref(tile), ctypes.byref(total)) == halo.OK
+    from oracle import stencil as S
+    assert (pitch.value, rows.value, col0.value) == (S.pitch(8), 10, S.COL0)
+    assert (tile.value, total.value) == (S.tile_floats(8), 6 * S.tile_floats(8))
+    # misaligned or aliased fields are refused before any launch
+    assert lib.stencil_exchange(h, ctypes.c_void_p(8), None) == halo.EINVAL
+    assert lib.stencil_sweep(h, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == halo.EINVAL
+    lib.stencil_destroy(h)
 
 
 def test_host_only_argument_checks(lib):
