@@ -366,7 +366,12 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
     const int64_t n = nA + nB + nC;
     grid_launch_dependents();
     // records are plan tables, read before grid_dependency_wait(); forces after it
-    for (int64_t bb = blockIdx.x; bb < tilesA + tilesBC; bb += gridDim.x) {
+    // one tile per block, the grid covering every tile: without a grid-stride
+    // loop the paths are straight-line and the kernel needs 60 registers
+    // instead of 79 (four resident blocks per SM instead of three)
+    const int64_t bb = blockIdx.x;
+    if (bb >= tilesA + tilesBC) return;
+    {
         if (bb >= tilesBC) {
             const int64_t b = bb - tilesBC;
             const int64_t m0 = b * 2 * kThreads + threadIdx.x, m1 = m0 + kThreads;
@@ -378,10 +383,10 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
             const int32_t ent[2][3] = {{r0.y, r0.z, r0.w}, {r1.y, r1.z, r1.w}};
             grid_dependency_wait();
             reduce_trees<3, 2>(f, home, kk, ent);
-            continue;
+            return;
         }
         const int64_t m = nA + bb * kThreads + threadIdx.x;
-        if (m >= n) continue;  // touches nothing
+        if (m >= n) return;  // touches nothing
         if (m < nA + nB) {
             const int4 r0 = __ldg(recB + 3 * (m - nA)), r1 = __ldg(recB + 3 * (m - nA) + 1);
             const int4 r2 = KB > 7 ? __ldg(recB + 3 * (m - nA) + 2) : make_int4(0, 0, 0, 0);
@@ -403,7 +408,7 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
 #pragma unroll
                     for (int j = 0; j < KW; j++) ent[j] = j < k ? __ldg(fent + r.y + j) : 0;
                     reduce_tree<KW>(f, r.x & kNodeMask, k, ent);
-                    continue;
+                    return;
                 }
             }
             // every slot of this tree belongs to this thread alone: plain
@@ -667,7 +672,7 @@ int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
     // class A goes two owners per thread, classes B and C one per thread
     const int64_t tilesA = (pl->n_rec[0] + 2 * kThreads - 1) / (2 * kThreads);
     const int64_t tilesBC = (pl->n_rec[1] + pl->n_rec[2] + kThreads - 1) / kThreads;
-    const int gb = (int)std::max<int64_t>(1, std::min<int64_t>(tilesA + tilesBC, (int64_t)pl->num_sms * 16));
+    const int gb = (int)std::max<int64_t>(1, tilesA + tilesBC);
     auto* k = pl->max_copies <= 7 ? flat_f_kernel<7, 0> : pl->max_copies <= 11 ? flat_f_kernel<11, 0>
                                                                                : flat_f_kernel<11, 16>;
     const cudaError_t e = launch_dependent(k, dim3(gb), dim3(kThreads), st, f, (const int4*)pl->d_frec[0],
