@@ -274,7 +274,8 @@ def make_flush(device):
 
 def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
     """Public API with host buffers, every step: H2D of the step's positions
-    and forces (pinned), load_home, exchange_x, exchange_f, D2H of the forces.
+    (input order) and local forces (pinned), load_home, exchange_x, exchange_f,
+    store_home of the reduced forces and their D2H in input atom order.
     Steps are pipelined the way a caller would run them: copies in on one
     stream, the exchanges on the plan's stream, copies out on a third, with two
     device buffer sets, so step i+1's inputs go in while step i's forces come
@@ -284,9 +285,10 @@ def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
     from domain_decomposition_halo_build_gb300 import synth
     h_xyz = torch.from_numpy(xyz).pin_memory()
     h_f = torch.from_numpy(synth.forces(plan.n_local_total, seed=2)).pin_memory()
-    h_out = [torch.empty_like(h_f).pin_memory() for _ in range(2)]
+    h_out = [torch.empty_like(h_xyz).pin_memory() for _ in range(2)]   # per-atom forces
     d_xyz = [torch.empty_like(h_xyz, device=device) for _ in range(2)]
     d_f = [torch.empty_like(h_f, device=device) for _ in range(2)]
+    d_out = [torch.empty_like(h_xyz, device=device) for _ in range(2)]
     loc = torch.empty((plan.n_local_total, 3), dtype=torch.float32, device=device)
     s_in = torch.cuda.Stream(device=device)
     s_out = torch.cuda.Stream(device=device)
@@ -297,7 +299,7 @@ def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
     def step(i):
         k = i % 2
         if ev_out[k] is not None:
-            s_in.wait_event(ev_out[k])       # step i-2's forces have left d_f[k]
+            s_in.wait_event(ev_out[k])       # step i-2 has finished with d_f[k] and d_out[k]
         with torch.cuda.stream(s_in):
             d_xyz[k].copy_(h_xyz, non_blocking=True)
             d_f[k].copy_(h_f, non_blocking=True)
@@ -306,10 +308,11 @@ def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
         plan.load_home(d_xyz[k], loc, stream)
         plan.exchange_x(loc, stream)
         plan.exchange_f(d_f[k], stream)
+        plan.store_home(d_f[k], d_out[k], stream)
         ev_comp[k].record(stream)
         s_out.wait_event(ev_comp[k])
         with torch.cuda.stream(s_out):
-            h_out[k].copy_(d_f[k], non_blocking=True)
+            h_out[k].copy_(d_out[k], non_blocking=True)
         e = torch.cuda.Event()
         e.record(s_out)
         ev_out[k] = e
@@ -321,7 +324,8 @@ def e2e_steps(w, xyz, plan, steps, warmup, device, stream):
             plan.exchange_x(loc, stream)
             d_f[0].copy_(h_f, non_blocking=True)
             plan.exchange_f(d_f[0], stream)
-            h_out[0].copy_(d_f[0], non_blocking=True)
+            plan.store_home(d_f[0], d_out[0], stream)
+            h_out[0].copy_(d_out[0], non_blocking=True)
 
     for i in range(warmup):
         step(i)

@@ -229,6 +229,12 @@ int halo_load_home(const halo_plan* pl, const float* global_xyz, float* local_xy
     return halo::launch_load_home(pl, global_xyz, local_xyz, as_stream(stream));
 }
 
+int halo_store_home(const halo_plan* pl, const float* local_xyz, float* global_xyz, void* stream) {
+    if (!pl || !global_xyz || !local_xyz || !pl->valid) return HALO_EINVAL;
+    DeviceGuard g(pl->dev);
+    return halo::launch_store_home(pl, local_xyz, global_xyz, as_stream(stream));
+}
+
 int halo_exchange_x(halo_plan* pl, float* local_coords, void* stream) {
     if (!pl || !local_coords || ((uintptr_t)local_coords & 3u)) return HALO_EINVAL;
     if (!pl->valid) return HALO_EINVAL;

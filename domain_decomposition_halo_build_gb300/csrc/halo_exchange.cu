@@ -431,6 +431,20 @@ __global__ void load_home_kernel(const int64_t* __restrict__ home_dst,
     }
 }
 
+// global[atom] = local[its home slot]: every atom has exactly one home slot,
+// so the writes are disjoint
+__global__ void store_home_kernel(const int64_t* __restrict__ home_dst,
+                                  const int32_t* __restrict__ home_gid, int64_t n,
+                                  const float* __restrict__ local, float* __restrict__ g) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t dd = home_dst[i], a = home_gid[i];
+        g[3 * a + 0] = local[3 * dd + 0];
+        g[3 * a + 1] = local[3 * dd + 1];
+        g[3 * a + 2] = local[3 * dd + 2];
+    }
+}
+
 __global__ void home_gid_kernel(const int64_t* __restrict__ home_dst,
                                 const int32_t* __restrict__ home_gid, int64_t n,
                                 int32_t* __restrict__ out) {
@@ -810,6 +824,13 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
     a.trace = pl->trace ? pl->trace + 4 * (size_t)pl->n_items_x : nullptr;
     unpack_f_kernel<4><<<pl->grid_f, kThreads, 0, st>>>(a);
     pl->launches_f++;
+    return cuda_code(cudaGetLastError());
+}
+
+int launch_store_home(const halo_plan* pl, const float* local, float* g, cudaStream_t st) {
+    const int64_t n = pl->n_atoms;
+    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
+    store_home_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, local, g);
     return cuda_code(cudaGetLastError());
 }
 

@@ -179,6 +179,7 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st);
 int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
                               unsigned long long* ticket, cudaStream_t st);
 int launch_load_home(const halo_plan* pl, const float* g, float* local, cudaStream_t st);
+int launch_store_home(const halo_plan* pl, const float* local, float* g, cudaStream_t st);
 int launch_local_to_global(const halo_plan* pl, int32_t* out, cudaStream_t st);
 void free_exchange(halo_plan* pl);
 int reset_flags(halo_plan* pl, cudaStream_t st);

@@ -65,6 +65,7 @@ SIGNATURES = {
     "halo_get_index_maps": (ctypes.c_int, [_vp, _vp, _vp]),
     "halo_local_to_global": (ctypes.c_int, [_vp, _vp, _vp]),
     "halo_load_home": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "halo_store_home": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "halo_exchange_x": (ctypes.c_int, [_vp, _vp, _vp]),
     "halo_exchange_f": (ctypes.c_int, [_vp, _vp, _vp]),
     "halo_exchange_x_noalloc": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -263,6 +264,17 @@ class HaloPlan:
             _dev_ptr(local_xyz, torch.float32, (self.n_local_total, 3)), _stream_handle(stream)),
             "halo_load_home")
         return local_xyz
+
+    def store_home(self, local_xyz, global_xyz=None, stream=None):
+        """halo_store_home: home slots of a local array back to input atom order."""
+        import torch
+        if global_xyz is None:
+            global_xyz = torch.empty((self.n_atoms, 3), dtype=torch.float32, device="cuda")
+        _check(self._lib.halo_store_home(
+            self._h, _dev_ptr(local_xyz, torch.float32, (self.n_local_total, 3)),
+            _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)), _stream_handle(stream)),
+            "halo_store_home")
+        return global_xyz
 
     def exchange_x(self, local_xyz, stream=None):
         import torch

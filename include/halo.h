@@ -164,6 +164,14 @@ int halo_local_to_global(const halo_plan* plan, int32_t* out, void* stream);
 int halo_load_home(const halo_plan* plan, const float* global_xyz, float* local_xyz,
                    void* stream);
 
+/* The inverse of halo_load_home: copy the home slots of the dense local
+ * layout (n_local_total x 3, e.g. the forces after halo_exchange_f) back to a
+ * global array (n_atoms x 3) in input atom order; halo slots are not read.
+ * The pages have no counterpart (their ranks keep their atoms); a caller
+ * integrating in input order needs it.  Asynchronous. */
+int halo_store_home(const halo_plan* plan, const float* local_xyz, float* global_xyz,
+                    void* stream);
+
 /* Coordinate halo exchange (FusedPackCommX, Algorithms 3/4), one kernel
  * launch for all pulses: for every pulse p and sender s,
  *   local_coords[base[r] + atom_offset + i] = local_coords[base[s] + map[i]] + coord_shift,

@@ -338,3 +338,25 @@ def test_setup_ex_rejects_unknown_flags():
     with pytest.raises(halo.HaloError) as e:
         halo.halo_setup_ex((3, 3, 3), (3, 1, 1), 0.5, x, d, 2)
     assert e.value.code == halo.EINVAL
+
+
+@pytest.mark.parametrize("name", ["water24k_2x4x8", "water1M_4x4x4"])
+def test_store_home_round_trip_and_forces(cases, name):
+    """halo_store_home is the inverse of halo_load_home, and after the force
+    reduction it returns every atom's total force in input order: the oracle's
+    home slots, placed by their global ids."""
+    import torch
+    w, xyz, dom, o, g = cases(name)
+    loc = g.plan.load_home(g.xyz_d)
+    back = g.plan.store_home(loc)
+    np.testing.assert_array_equal(bits(back.cpu().numpy()), bits(xyz))
+    f0 = synth.forces(o.n_local_total, seed=8)
+    want_local = f0.copy()
+    o.exchange_f(want_local)
+    gid, home, _ = pins.home_slot_of(o)
+    want = want_local[home]
+    f = torch.from_numpy(f0).cuda()
+    g.plan.exchange_f(f)
+    got = g.plan.store_home(f)
+    assert g.plan.status() == 0
+    np.testing.assert_array_equal(bits(got.cpu().numpy()), bits(want))
