@@ -27,12 +27,12 @@
 
 #include <algorithm>
 
+#include "halo_device.cuh"
 #include "halo_internal.cuh"
 
 namespace halo {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
 
 // ---- packed metadata (int64 entries) -----------------------------------------
 struct Meta {
@@ -77,44 +77,11 @@ Meta meta_ptrs(void* m, int nd, int P) {
     return r;
 }
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-    unsigned m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
 
 __device__ __forceinline__ int cell_of(int D, int d, int nx, int ny) {
     return d == 0 ? D % nx : (d == 1 ? (D / nx) % ny : D / (nx * ny));
 }
 
-// Exclusive scan across a block of NT threads (NT a multiple of 32, <= 1024).
-template <int NT>
-__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
-    __shared__ int64_t ws[NT / 32];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int64_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int64_t y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) ws[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        int64_t t = lane < NT / 32 ? ws[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int64_t y = __shfl_up_sync(kFull, t, o);
-            if (lane >= o) t += y;
-        }
-        if (lane < NT / 32) ws[lane] = t;
-    }
-    __syncthreads();
-    int64_t pre = (w > 0 ? ws[w - 1] : 0) + x - v;
-    *total = ws[NT / 32 - 1];
-    __syncthreads();
-    return pre;
-}
 
 // ---- 1. home partition ------------------------------------------------------------
 // Warp tile t covers atoms [t*kHistTile, (t+1)*kHistTile).  counts is domain-major:

@@ -5,6 +5,44 @@
 
 namespace halo {
 
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exclusive scan across a block of NT threads (NT a multiple of 32, <= 1024).
+template <int NT>
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* total) {
+    __shared__ int64_t ws[NT / 32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int64_t t = lane < NT / 32 ? ws[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(kFull, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < NT / 32) ws[lane] = t;
+    }
+    __syncthreads();
+    int64_t pre = (w > 0 ? ws[w - 1] : 0) + x - v;
+    *total = ws[NT / 32 - 1];
+    __syncthreads();
+    return pre;
+}
+
+
 // A block's chunk of halo coordinates is one contiguous range of 12-byte
 // slots in the destination domain.  The block stages it in shared memory and
 // one thread writes it back with a bulk asynchronous copy (cp.async.bulk,

@@ -48,7 +48,6 @@
 namespace halo {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
@@ -93,11 +92,6 @@ __device__ __forceinline__ void trace_item(unsigned long long* trace, int item, 
     r[3] = smid();
 }
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-    unsigned m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
 
 // Bounded wait until *c has reached target (modulo 2^32).  On timeout the
 // first waiter records where it gave up; every waiter gives up as soon as the

@@ -120,11 +120,84 @@ __global__ void xflat_kernel(const int4* __restrict__ items, const int32_t* __re
     }
 }
 
-__global__ void owner_flag_kernel(const int32_t* __restrict__ ncopies, int32_t* __restrict__ flag,
-                                  int64_t n) {
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
-         j += (int64_t)gridDim.x * blockDim.x)
-        flag[j] = ncopies[j] > 0 ? 1 : 0;
+// Two exclusive scans in one pass over an int32 array: channel a in the low
+// 32 bits of an int64, channel b in the high 32 bits (no carry: every prefix
+// of a stays below 2^32).  SRC 0, over local slots: a = copies of the slot,
+// b = 1 if it has any (an owner).  SRC 1, over owners: a = 1 for a class-A
+// tree (<= 3 copies), b = 1 for class B (4..11 copies), from the entry
+// offsets (element i reads in[i] and in[i + 1]).
+template <int SRC>
+__device__ __forceinline__ int64_t pair_value(const int32_t* __restrict__ in, int64_t i) {
+    if (SRC == 0) {
+        const int32_t v = in[i];
+        return (int64_t)v | ((int64_t)(v > 0 ? 1 : 0) << 32);
+    }
+    const int32_t k = in[i + 1] - in[i];
+    return (int64_t)(k <= 3 ? 1 : 0) | ((int64_t)(k > 3 && k <= 11 ? 1 : 0) << 32);
+}
+
+template <int SRC>
+__global__ void __launch_bounds__(kThreads) pair_reduce_kernel(const int32_t* __restrict__ in,
+                                                               int64_t n, int64_t* __restrict__ sums) {
+    const int64_t b0 = (int64_t)blockIdx.x * kScanTile;
+    int64_t s = 0;
+    for (int j = threadIdx.x; j < kScanTile; j += kThreads)
+        if (b0 + j < n) s += pair_value<SRC>(in, b0 + j);
+    int64_t tot;
+    block_exclusive_scan<kThreads>(s, &tot);
+    if (threadIdx.x == 0) sums[blockIdx.x] = tot;
+}
+
+// Scans the nb tile sums in place and stores the grand total in sums[nb].
+__global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ sums, int64_t nb) {
+    int64_t carry = 0;
+    for (int64_t b = 0; b < nb; b += 1024) {
+        const int64_t i = b + threadIdx.x;
+        const int64_t v = i < nb ? sums[i] : 0;
+        int64_t tot;
+        const int64_t pre = block_exclusive_scan<1024>(v, &tot);
+        if (i < nb) sums[i] = carry + pre;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) sums[nb] = carry;
+}
+
+template <int SRC>
+__global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __restrict__ in, int64_t n,
+                                                             const int64_t* __restrict__ sums,
+                                                             int32_t* __restrict__ out_a,
+                                                             int32_t* __restrict__ out_b) {
+    constexpr int E = kScanTile / kThreads;
+    const int64_t b0 = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * E;
+    int64_t v[E];
+    int64_t s = 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        v[e] = (b0 + e < n) ? pair_value<SRC>(in, b0 + e) : 0;
+        s += v[e];
+    }
+    int64_t tot;
+    int64_t pre = block_exclusive_scan<kThreads>(s, &tot) + sums[blockIdx.x];
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        if (b0 + e < n) {
+            out_a[b0 + e] = (int32_t)(pre & 0xffffffffll);
+            out_b[b0 + e] = (int32_t)(pre >> 32);
+        }
+        pre += v[e];
+    }
+}
+
+// Launches the three passes; sums holds ceil(n / kScanTile) + 1 int64 (the
+// grand total lands in its last entry).
+template <int SRC>
+int pair_scan(const int32_t* in, int64_t n, int64_t* sums, int32_t* out_a, int32_t* out_b,
+              cudaStream_t st) {
+    const int64_t nb = (n + kScanTile - 1) / kScanTile;
+    if (nb > 0) pair_reduce_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, sums);
+    pair_top_kernel<<<1, 1024, 0, st>>>(sums, nb);
+    if (nb > 0) pair_down_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, sums, out_a, out_b);
+    return cuda_code(cudaGetLastError());
 }
 
 __global__ void owner_list_kernel(const int32_t* __restrict__ ncopies,
@@ -429,16 +502,6 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
     }
 }
 
-// Record classes of the owners (A: k <= 3, B: k <= 11, C: more).
-__global__ void owner_class_kernel(const int32_t* __restrict__ fstart, int64_t n_owners,
-                                   int32_t* __restrict__ isA, int32_t* __restrict__ isB) {
-    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
-         m += (int64_t)gridDim.x * blockDim.x) {
-        const int k = fstart[m + 1] - fstart[m];
-        isA[m] = k <= 3 ? 1 : 0;
-        isB[m] = (k > 3 && k <= 11) ? 1 : 0;
-    }
-}
 
 __global__ void owner_record_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
                                     const int32_t* __restrict__ fent, const int32_t* __restrict__ posA,
@@ -534,8 +597,9 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     HALO_TRY(dev_reserve(&pl->d_fent, &pl->cap_fent, H));
 
     // scratch of the table build, carved from two pools kept in the plan
-    const int64_t nsc = nl / kScanTile + 2;
-    HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, 6 * nl + std::max<int64_t>(H, 1) + nsc + 8));
+    const int64_t nsums = nl / kScanTile + 2;            // int64 tile sums + grand total
+    const int64_t off_sums = (6 * nl + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
+    HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 8));
     HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
     int32_t* owner = pl->d_flat_pool32;
     int32_t* parent = owner + nl;
@@ -544,10 +608,11 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int32_t* flag = entry_pos + nl;
     int32_t* owner_idx = flag + nl;
     int32_t* tmp = owner_idx + nl;
-    int32_t* scan_tmp = tmp + std::max<int64_t>(H, 1);
-    int32_t* misc = scan_tmp + nsc;
+    int64_t* sums = reinterpret_cast<int64_t*>(pl->d_flat_pool32 + off_sums);
+    int32_t* misc = pl->d_flat_pool32 + off_sums + 2 * nsums;
     int8_t* hop = pl->d_flat_pool8;
     int8_t* code = hop + nl;
+    int64_t* h64 = reinterpret_cast<int64_t*>(hw + 8);     // 8-byte aligned words read back
     int rc = HALO_OK;
     do {
         const int gb = blocks_for(nl, pl->num_sms);
@@ -561,16 +626,18 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if (!items.empty())
             xflat_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
                                                                        pl->d_xflat, ncopies);
-        if ((rc = device_exclusive_scan(ncopies, entry_pos, nl, scan_tmp, st)) != HALO_OK) break;
-        owner_flag_kernel<<<gb, kThreads, 0, st>>>(ncopies, flag, nl);
-        if ((rc = device_exclusive_scan(flag, owner_idx, nl, scan_tmp, st)) != HALO_OK) break;
-        int32_t* last = hw;
-        if ((rc = cuda_code(cudaMemcpyAsync(last, owner_idx + nl - 1, sizeof(int32_t),
-                                            cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
-        if ((rc = cuda_code(cudaMemcpyAsync(last + 1, flag + nl - 1, sizeof(int32_t),
+        // entry offsets of every slot's copy list and the owner index of every
+        // slot with copies, in one pass; the grand total gives the owner count
+        if ((rc = pair_scan<0>(ncopies, nl, sums, entry_pos, owner_idx, st)) != HALO_OK) break;
+        const int64_t nb_l = (nl + kScanTile - 1) / kScanTile;
+        if ((rc = cuda_code(cudaMemcpyAsync(h64, sums + nb_l, sizeof(int64_t),
                                             cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
-        const int64_t n_owners = (int64_t)last[0] + last[1];
+        const int64_t n_owners = h64[0] >> 32;
+        if ((h64[0] & 0xffffffffll) != H) {  // every halo slot is one copy of one owner
+            rc = HALO_ECAPACITY;
+            break;
+        }
         pl->n_owners = n_owners;
         if ((rc = dev_reserve(&pl->d_fown, &pl->cap_fown, n_owners)) != HALO_OK) break;
         if ((rc = dev_reserve(&pl->d_fstart, &pl->cap_fstart, n_owners + 1)) != HALO_OK) break;
@@ -584,9 +651,20 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             owner_fill_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner,
                                                                             entry_pos, flag, tmp);
         if ((rc = cuda_code(cudaMemsetAsync(misc, 0, sizeof(int32_t) * 4, st))) != HALO_OK) break;
-        if (n_owners > 0)
+        // record classes (A: <= 3 copies, B: 4..11, C: more): slots in each
+        // class from one paired scan of the owners' copy counts
+        int32_t* posA = entry_pos;  // scratch reuse: owner_fill has read entry_pos
+        int32_t* posB = ncopies;    // and owner_list ncopies
+        if (n_owners > 0) {
             owner_sort_kernel<<<blocks_for(n_owners, pl->num_sms), kThreads, 0, st>>>(
                 pl->d_fown, pl->d_fstart, tmp, parent, hop, n_owners, pl->d_fent, misc, misc + 1);
+            if ((rc = pair_scan<1>(pl->d_fstart, n_owners, sums, posA, posB, st)) != HALO_OK) break;
+            const int64_t nb_o = (n_owners + kScanTile - 1) / kScanTile;
+            if ((rc = cuda_code(cudaMemcpyAsync(h64 + 1, sums + nb_o, sizeof(int64_t),
+                                                cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
+        } else {
+            h64[1] = 0;
+        }
         int32_t* info = hw + 4;
         if ((rc = cuda_code(cudaMemcpyAsync(info, misc, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost,
                                             st))) != HALO_OK)
@@ -598,31 +676,16 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             break;
         }
         pl->max_copies = info[0];
-        // record classes: indicator scans give every owner's slot in its class
+        pl->n_rec[0] = h64[1] & 0xffffffffll;
+        pl->n_rec[1] = h64[1] >> 32;
+        pl->n_rec[2] = n_owners - pl->n_rec[0] - pl->n_rec[1];
         if (n_owners > 0) {
-            int32_t* isA = owner_idx;  // scratch reuse: n_owners <= nl
-            int32_t* isB = flag;
-            int32_t* posA = entry_pos;
-            int32_t* posB = ncopies;
-            const int gbo = blocks_for(n_owners, pl->num_sms);
-            owner_class_kernel<<<gbo, kThreads, 0, st>>>(pl->d_fstart, n_owners, isA, isB);
-            if ((rc = device_exclusive_scan(isA, posA, n_owners, scan_tmp, st)) != HALO_OK) break;
-            if ((rc = device_exclusive_scan(isB, posB, n_owners, scan_tmp, st)) != HALO_OK) break;
-            int32_t* tail = hw + 8;
-            if ((rc = cuda_code(cudaMemcpyAsync(tail, posA + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
-            if ((rc = cuda_code(cudaMemcpyAsync(tail + 1, isA + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
-            if ((rc = cuda_code(cudaMemcpyAsync(tail + 2, posB + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
-            if ((rc = cuda_code(cudaMemcpyAsync(tail + 3, isB + n_owners - 1, 4, cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
-            if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
-            pl->n_rec[0] = (int64_t)tail[0] + tail[1];
-            pl->n_rec[1] = (int64_t)tail[2] + tail[3];
-            pl->n_rec[2] = n_owners - pl->n_rec[0] - pl->n_rec[1];
             if ((rc = dev_reserve(&pl->d_frec[0], &pl->cap_frec[0], pl->n_rec[0])) != HALO_OK) break;
             if ((rc = dev_reserve(&pl->d_frec[1], &pl->cap_frec[1], 3 * pl->n_rec[1])) != HALO_OK) break;
             if ((rc = dev_reserve(&pl->d_frec[2], &pl->cap_frec[2], pl->n_rec[2])) != HALO_OK) break;
-            owner_record_kernel<<<gbo, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB,
-                                                          n_owners, pl->d_frec[0], pl->d_frec[1],
-                                                          pl->d_frec[2]);
+            owner_record_kernel<<<blocks_for(n_owners, pl->num_sms), kThreads, 0, st>>>(
+                pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB, n_owners, pl->d_frec[0],
+                pl->d_frec[1], pl->d_frec[2]);
             if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
             if ((rc = cuda_code(cudaGetLastError())) != HALO_OK) break;
         }
