@@ -84,54 +84,67 @@ __device__ __forceinline__ int cell_of(int D, int d, int nx, int ny) {
 
 
 // ---- 1. home partition ------------------------------------------------------------
-// Warp tile t covers atoms [t*kHistTile, (t+1)*kHistTile).  counts is domain-major:
-// counts[D*ntiles + t], so one exclusive scan gives every (domain, tile) start.
-__global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int nd,
-                                 int64_t ntiles, int32_t* __restrict__ counts,
+// A block of W warps covers the block tile b of W * kHistTile atoms; warp w
+// its sub-tile [(b*W + w)*kHistTile, ... + kHistTile).  Each warp counts its
+// sub-tile into its own shared histogram (shared-memory atomics); the block
+// writes one count per domain, counts[D*nbt + b] (domain-major, so one
+// exclusive scan gives every (domain, block tile) start), and every warp's
+// counts, wcounts[(b*W + w)*nd + D] (contiguous per block, for the scatter).
+__global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int nd, int64_t nbt,
+                                 int32_t* __restrict__ counts, int32_t* __restrict__ wcounts,
                                  int64_t* __restrict__ flags) {
     extern __shared__ int32_t sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int wpb = blockDim.x >> 5;
+    const int W = blockDim.x >> 5;
     int32_t* h = sh + (size_t)warp * nd;
     for (int i = lane; i < nd; i += 32) h[i] = 0;
     __syncwarp();
-    const int64_t tile = (int64_t)blockIdx.x * wpb + warp;
-    if (tile >= ntiles) return;
-    const int64_t a0 = tile * kHistTile;
+    const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * kHistTile;
     bool bad = false;
     for (int it = 0; it < kHistTile / 32; it++) {
         const int64_t a = a0 + it * 32 + lane;
-        int d = -1;
         if (a < n) {
-            d = __ldg(dom + a);
-            if (d < 0 || d >= nd) {
+            const int d = __ldg(dom + a);
+            if (d < 0 || d >= nd)
                 bad = true;
-                d = -1;
-            }
+            else
+                atomicAdd(&h[d], 1);
         }
-        const unsigned peers = __match_any_sync(kFull, d);
-        if (d >= 0 && lane == __ffs(peers) - 1) h[d] += __popc(peers);
-        __syncwarp();
     }
     if (bad) flags[1] = 1;
-    for (int i = lane; i < nd; i += 32) counts[(int64_t)i * ntiles + tile] = h[i];
+    __syncthreads();
+    int32_t* wc = wcounts + (int64_t)blockIdx.x * W * nd;
+    for (int i = threadIdx.x; i < W * nd; i += blockDim.x) wc[i] = sh[i];
+    for (int d = threadIdx.x; d < nd; d += blockDim.x) {
+        int32_t t = 0;
+        for (int w = 0; w < W; w++) t += sh[(size_t)w * nd + d];
+        counts[(int64_t)d * nbt + blockIdx.x] = t;
+    }
 }
 
-// Stable scatter: atoms of each tile are visited in input order; within 32
-// atoms the rank among equal domain ids comes from the warp match mask.
+// Stable scatter: every warp's start per domain is its block tile's start
+// plus the counts of the warps before it; then each warp visits its atoms in
+// input order, and within 32 atoms the rank among equal domain ids comes from
+// the warp match mask.
 __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t* __restrict__ dom,
-                                    int64_t n, int nd, int64_t ntiles,
+                                    int64_t n, int nd, int64_t nbt,
                                     const int32_t* __restrict__ offs,
+                                    const int32_t* __restrict__ wcounts,
                                     int32_t* __restrict__ home_gid, float* __restrict__ bxyz) {
     extern __shared__ int32_t sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int wpb = blockDim.x >> 5;
+    const int W = blockDim.x >> 5;
     int32_t* run = sh + (size_t)warp * nd;
-    const int64_t tile = (int64_t)blockIdx.x * wpb + warp;
-    if (tile >= ntiles) return;
-    for (int i = lane; i < nd; i += 32) run[i] = offs[(int64_t)i * ntiles + tile];
-    __syncwarp();
-    const int64_t a0 = tile * kHistTile;
+    const int32_t* wc = wcounts + (int64_t)blockIdx.x * W * nd;
+    for (int d = threadIdx.x; d < nd; d += blockDim.x) {
+        int32_t acc = offs[(int64_t)d * nbt + blockIdx.x];
+        for (int w = 0; w < W; w++) {
+            sh[(size_t)w * nd + d] = acc;
+            acc += wc[(size_t)w * nd + d];
+        }
+    }
+    __syncthreads();
+    const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * kHistTile;
     const unsigned lt = lanemask_lt();
     for (int it = 0; it < kHistTile / 32; it++) {
         const int64_t a = a0 + it * 32 + lane;
@@ -180,23 +193,41 @@ __global__ void scan_top_kernel(int32_t* __restrict__ sums, int64_t nb) {
     }
 }
 
-__global__ void scan_down_kernel(const int32_t* __restrict__ in, int32_t* __restrict__ out,
-                                 int64_t n, const int32_t* __restrict__ sums) {
-    constexpr int E = kScanTile / kThreads;
-    const int64_t b0 = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * E;
-    int32_t v[E];
+__global__ void __launch_bounds__(kThreads) scan_down_kernel(const int32_t* __restrict__ in,
+                                                             int32_t* __restrict__ out, int64_t n,
+                                                             const int32_t* __restrict__ sums) {
+    // each warp walks a contiguous run of the tile 32 elements at a time
+    // (coalesced), a shuffle scan per 32, warp totals scanned across the block
+    constexpr int kWarps = kThreads / 32;
+    constexpr int R = kScanTile / kThreads;
+    __shared__ int64_t wsum[kWarps];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t r0 = (int64_t)blockIdx.x * kScanTile + (int64_t)w * 32 * R;
+    int32_t v[R];
     int64_t s = 0;
 #pragma unroll
-    for (int e = 0; e < E; e++) {
-        v[e] = (b0 + e < n) ? in[b0 + e] : 0;
-        s += v[e];
+    for (int r = 0; r < R; r++) {
+        const int64_t i = r0 + r * 32 + lane;
+        v[r] = i < n ? in[i] : 0;
+        s += v[r];
     }
-    int64_t tot;
-    int64_t pre = block_exclusive_scan<kThreads>(s, &tot) + sums[blockIdx.x];
 #pragma unroll
-    for (int e = 0; e < E; e++) {
-        if (b0 + e < n) out[b0 + e] = (int32_t)pre;
-        pre += v[e];
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if (lane == 0) wsum[w] = s;
+    __syncthreads();
+    int64_t carry = sums[blockIdx.x];
+    for (int q = 0; q < w; q++) carry += wsum[q];
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        int64_t x = v[r];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        const int64_t i = r0 + r * 32 + lane;
+        if (i < n) out[i] = (int32_t)(carry + x - v[r]);
+        carry += __shfl_sync(kFull, x, 31);
     }
 }
 
@@ -485,6 +516,12 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
                cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
     const int64_t ntiles = (n + kHistTile - 1) / kHistTile;
+    // home partition: W warps per block (their histograms share 48 KB of
+    // shared memory), one block tile of W * kHistTile atoms per block
+    const int wpb = (int)std::min<int64_t>(8, std::max<int64_t>(1, (48 * 1024) / ((int64_t)nd * 4)));
+    const size_t hist_smem = (size_t)wpb * nd * sizeof(int32_t);
+    const int64_t nbt = (ntiles + wpb - 1) / wpb;
+    const unsigned hist_blocks = (unsigned)std::max<int64_t>(nbt, 1);
 
     // --- buffers that depend on N
     if (n > pl->n_alloc_atoms) {
@@ -495,12 +532,15 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         HALO_TRY(dev_alloc(&pl->d_home_dst, (size_t)n));
         pl->n_alloc_atoms = n;
     }
-    const int64_t ncount = (int64_t)nd * ntiles;
-    if (ncount > pl->counts_cap) {
+    const int64_t ncount = (int64_t)nd * nbt;
+    // block-tile counts, their scanned offsets, then every warp's counts
+    // (block-major: [block tile][warp][domain]) for the scatter
+    const int64_t nwc = (int64_t)nd * nbt * wpb;
+    if (2 * ncount + nwc > pl->counts_cap) {
         dev_free(pl->d_counts);
         pl->counts_cap = 0;
-        HALO_TRY(dev_alloc(&pl->d_counts, (size_t)ncount * 2));  // counts + scanned offsets
-        pl->counts_cap = ncount;
+        HALO_TRY(dev_alloc(&pl->d_counts, (size_t)(2 * ncount + nwc)));
+        pl->counts_cap = 2 * ncount + nwc;
     }
     const int64_t nsum = std::max<int64_t>((ncount + kScanTile - 1) / kScanTile, 1);
     if (nsum > pl->scan_tmp_cap) {
@@ -573,9 +613,6 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
     int64_t* hm = static_cast<int64_t*>(hstage);
     const Meta h = meta_ptrs(hm, nd, P);
 
-    int wpb = (int)std::min<int64_t>(8, std::max<int64_t>(1, (48 * 1024) / ((int64_t)nd * 4)));
-    const size_t hist_smem = (size_t)wpb * nd * sizeof(int32_t);
-    const unsigned hist_blocks = (unsigned)((ntiles + wpb - 1) / wpb);
 
     for (int attempt = 0; attempt < 6; attempt++) {
         if (want > pl->cap_slots) {
@@ -591,13 +628,14 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         if (prune) HALO_TRY(dev_reserve(&pl->d_bmask, &pl->cap_bmask, pl->cap_slots));
         HALO_CUDA(cudaMemsetAsync(pl->d_meta, 0, mbytes, st));
         // 1. home partition
-        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(dom, n, nd, ntiles,
-                                                                  pl->d_counts, m.flags);
+        int32_t* wcounts = pl->d_counts + 2 * ncount;
+        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(dom, n, nd, nbt,
+                                                                  pl->d_counts, wcounts, m.flags);
         int32_t* offs = pl->d_counts + ncount;
         HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
         home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
-            coords, dom, n, nd, ntiles, offs, pl->d_home_gid, pl->d_bxyz);
-        home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, ntiles, n, nd, P, m);
+            coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid, pl->d_bxyz);
+        home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, nbt, n, nd, P, m);
         HALO_CUDA(cudaGetLastError());
         // 2. pulses in global order
         for (int p = 0; p < P; p++) {

@@ -162,29 +162,49 @@ __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ su
     if (threadIdx.x == 0) sums[nb] = carry;
 }
 
+// Down pass: each warp takes a contiguous run of kScanTile / warps elements
+// and walks it 32 at a time (coalesced loads and stores): a first walk sums
+// the run, the warp totals are scanned across the block, a second walk writes
+// the exclusive prefixes with a shuffle scan per 32 elements.
 template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __restrict__ in, int64_t n,
                                                              const int64_t* __restrict__ sums,
                                                              int32_t* __restrict__ out_a,
                                                              int32_t* __restrict__ out_b) {
-    constexpr int E = kScanTile / kThreads;
-    const int64_t b0 = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * E;
-    int64_t v[E];
+    constexpr int kWarps = kThreads / 32;
+    constexpr int R = kScanTile / kThreads;  // rounds of 32 per warp
+    __shared__ int64_t wsum[kWarps];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t r0 = (int64_t)blockIdx.x * kScanTile + (int64_t)w * 32 * R;
+    int64_t v[R];
     int64_t s = 0;
 #pragma unroll
-    for (int e = 0; e < E; e++) {
-        v[e] = (b0 + e < n) ? pair_value<SRC>(in, b0 + e) : 0;
-        s += v[e];
+    for (int r = 0; r < R; r++) {
+        const int64_t i = r0 + r * 32 + lane;
+        v[r] = i < n ? pair_value<SRC>(in, i) : 0;
+        s += v[r];
     }
-    int64_t tot;
-    int64_t pre = block_exclusive_scan<kThreads>(s, &tot) + sums[blockIdx.x];
 #pragma unroll
-    for (int e = 0; e < E; e++) {
-        if (b0 + e < n) {
-            out_a[b0 + e] = (int32_t)(pre & 0xffffffffll);
-            out_b[b0 + e] = (int32_t)(pre >> 32);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if (lane == 0) wsum[w] = s;
+    __syncthreads();
+    int64_t carry = sums[blockIdx.x];
+    for (int q = 0; q < w; q++) carry += wsum[q];
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        int64_t x = v[r];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
         }
-        pre += v[e];
+        const int64_t i = r0 + r * 32 + lane;
+        const int64_t pre = carry + x - v[r];
+        if (i < n) {
+            out_a[i] = (int32_t)(pre & 0xffffffffll);
+            out_b[i] = (int32_t)(pre >> 32);
+        }
+        carry += __shfl_sync(kFull, x, 31);
     }
 }
 
@@ -239,6 +259,12 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
         my_max = max(my_max, k);
         if (k > kMaxCopies) {
             atomicCAS(err, 0, HALO_ECAPACITY);
+            continue;
+        }
+        if (k == 1) {  // most owners: a single copy, received from the owner itself
+            const int32_t v = tmp[s0];
+            if (parent[v] != fown[m]) atomicCAS(err, 0, HALO_ECAPACITY);
+            fent[s0] = v;
             continue;
         }
         int32_t node[kMaxCopies];
