@@ -40,6 +40,7 @@ constexpr int kFlatChunkMax = 4 * kThreads;  // halo slots per coordinate item (
 constexpr int kNodeBits = 26;             // entry = node slot | parent position << 26
 constexpr int32_t kNodeMask = (1 << kNodeBits) - 1;
 constexpr int kMaxCopies = 63;            // parent positions fit in 6 bits
+constexpr int kSortRegs = 8;              // copy lists sorted in registers up to this length
 
 // ---- stepwise ----------------------------------------------------------------
 __global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
@@ -265,6 +266,47 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
             const int32_t v = tmp[s0];
             if (parent[v] != fown[m]) atomicCAS(err, 0, HALO_ECAPACITY);
             fent[s0] = v;
+            continue;
+        }
+        if (k <= kSortRegs) {
+            // the same order in registers: a fully unrolled exchange sort on
+            // (pulse descending, slot ascending); unused places sort last
+            int32_t nd8[kSortRegs];
+            int hp8[kSortRegs];
+#pragma unroll
+            for (int j = 0; j < kSortRegs; j++) {
+                nd8[j] = j < k ? tmp[s0 + j] : INT32_MAX;
+                hp8[j] = j < k ? (int)hop[nd8[j]] : -1000;
+            }
+#pragma unroll
+            for (int a = 0; a < kSortRegs - 1; a++)
+#pragma unroll
+                for (int b = 0; b < kSortRegs - 1 - a; b++) {
+                    const bool swap = hp8[b] < hp8[b + 1] || (hp8[b] == hp8[b + 1] && nd8[b] > nd8[b + 1]);
+                    if (swap) {
+                        const int32_t tn = nd8[b];
+                        nd8[b] = nd8[b + 1];
+                        nd8[b + 1] = tn;
+                        const int th = hp8[b];
+                        hp8[b] = hp8[b + 1];
+                        hp8[b + 1] = th;
+                    }
+                }
+            const int32_t home = fown[m];
+#pragma unroll
+            for (int j = 0; j < kSortRegs; j++) {
+                if (j < k) {
+                    const int32_t ps = parent[nd8[j]];
+                    int pos = 0;
+                    if (ps != home) {
+#pragma unroll
+                        for (int q = kSortRegs - 1; q > j; q--)
+                            if (q < k && nd8[q] == ps) pos = q + 1;
+                        if (pos == 0) atomicCAS(err, 0, HALO_ECAPACITY);  // parent not among the copies
+                    }
+                    fent[s0 + j] = nd8[j] | (pos << kNodeBits);
+                }
+            }
             continue;
         }
         int32_t node[kMaxCopies];
