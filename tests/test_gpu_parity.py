@@ -360,3 +360,40 @@ def test_store_home_round_trip_and_forces(cases, name):
     got = g.plan.store_home(f)
     assert g.plan.status() == 0
     np.testing.assert_array_equal(bits(got.cpu().numpy()), bits(want))
+
+
+def random_problem(seed):
+    """A seeded random decomposition: grid 1..5 per dim, box 2..8 nm, a cut-off
+    that gives 1..(n_d - 1) pulses in decomposed dims, 50..20000 atoms."""
+    rng = np.random.default_rng(1000 + seed)
+    grid = tuple(int(v) for v in rng.integers(1, 6, size=3))
+    box = tuple(float(np.float32(v)) for v in rng.uniform(2.0, 8.0, size=3))
+    widths = [box[d] / grid[d] for d in range(3) if grid[d] > 1]
+    if widths:
+        # the largest rc with p_d = ceil(rc / w_d) <= n_d - 1 in every decomposed dim
+        cap = min((grid[d] - 1) * box[d] / grid[d] for d in range(3) if grid[d] > 1)
+        rc = float(rng.uniform(0.05, 1.0) * cap * 0.999)
+    else:
+        rc = float(rng.uniform(0.1, 1.0))
+    n = int(rng.integers(50, 20000))
+    return box, grid, rc, n, bool(rng.integers(0, 2))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_problems(seed):
+    """Random boxes, grids, cut-offs and sizes, with and without pruning: plans
+    and every mode's exchanges bit-identical to the oracle."""
+    box, grid, rc, n, prune = random_problem(seed)
+    xyz, dom = synth.custom_system(n, box, grid, seed=seed)
+    try:
+        o = oracle.Oracle(box, grid, rc, xyz, dom, prune=prune)
+    except oracle.OracleError as e:
+        pytest.skip("oracle rejects the problem (%d)" % e.code)
+    g = gpu_plan(box, grid, rc, xyz, dom, prune=prune)
+    try:
+        compare_plans(g, o)
+        for mode in MODES:
+            g.plan.set_mode(mode)
+            compare_exchanges(g, o, xyz, reps=1, seed=seed)
+    finally:
+        g.close()
