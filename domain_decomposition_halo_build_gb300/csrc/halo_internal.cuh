@@ -148,7 +148,7 @@ struct halo_plan {
     int32_t* d_flat_pool32 = nullptr;  // scratch of the flat-table build (kept across rebuilds)
     int8_t* d_flat_pool8 = nullptr;
     int64_t cap_pool32 = 0, cap_pool8 = 0;
-    int4* d_frec[3] = {nullptr, nullptr, nullptr};  // owner records: A (<=3), B (<=7), C (more)
+    int4* d_frec[3] = {nullptr, nullptr, nullptr};  // owner records: A (<=3), B (<=11), C (more)
     int64_t n_rec[3] = {0, 0, 0};
     int flat_x_e = 4;                // entries per thread of the flat coordinate kernel
 };
