@@ -169,6 +169,10 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
     __shared__ __align__(128) float stage[3 * kThreads * E + 4];
     __shared__ unsigned long long s_ticket;
     __shared__ int s_go;
+    // programmatic dependent launch: the launch overlaps the kernel before this
+    // one in the stream; nothing (tickets included) is touched before it ends
+    grid_launch_dependents();
+    grid_dependency_wait();
     const unsigned long long T = (unsigned long long)a.n_items + gridDim.x;
     unsigned long long next = 0;
     if (threadIdx.x == 0) next = atomicAdd(a.ticket, 1ull);
@@ -256,6 +260,8 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
 template <int E>
 __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
     const int lane = threadIdx.x & 31;
+    grid_launch_dependents();  // as in pack_x_kernel
+    grid_dependency_wait();
     const unsigned long long T = (unsigned long long)a.n_items + (unsigned long long)gridDim.x * kWarps;
     unsigned long long next = 0;
     if (lane == 0) next = atomicAdd(a.ticket, 1ull);
@@ -776,9 +782,10 @@ int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
-    pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a);
+    const cudaError_t e = launch_dependent(pack_x_kernel<4>, dim3(pl->grid_x), dim3(kThreads), st, a);
+    if (e != cudaSuccess) return cuda_code(e);
     pl->launches_x++;
-    return cuda_code(cudaGetLastError());
+    return HALO_OK;
 }
 
 int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
@@ -797,9 +804,10 @@ int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
-    pack_x_kernel<4><<<pl->grid_x, kThreads, 0, st>>>(a);
+    const cudaError_t e = launch_dependent(pack_x_kernel<4>, dim3(pl->grid_x), dim3(kThreads), st, a);
+    if (e != cudaSuccess) return cuda_code(e);
     pl->launches_x++;
-    return cuda_code(cudaGetLastError());
+    return HALO_OK;
 }
 
 int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
@@ -816,9 +824,10 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
     a.n_items = pl->n_items_f;
     a.timeout_ns = pl->wait_timeout_ns;
     a.trace = pl->trace ? pl->trace + 4 * (size_t)pl->n_items_x : nullptr;
-    unpack_f_kernel<4><<<pl->grid_f, kThreads, 0, st>>>(a);
+    const cudaError_t e = launch_dependent(unpack_f_kernel<4>, dim3(pl->grid_f), dim3(kThreads), st, a);
+    if (e != cudaSuccess) return cuda_code(e);
     pl->launches_f++;
-    return cuda_code(cudaGetLastError());
+    return HALO_OK;
 }
 
 int launch_store_home(const halo_plan* pl, const float* local, float* g, cudaStream_t st) {
