@@ -174,7 +174,7 @@ int halo_query(const halo_plan* pl, halo_info* out) {
 }
 
 int halo_domain_layout(const halo_plan* pl, int64_t* base, int32_t* n_home, int32_t* n_local) {
-    if (!pl) return HALO_EINVAL;
+    if (!pl || !pl->valid) return HALO_EINVAL;
     for (int D = 0; D < pl->n_dom; D++) {
         if (base) base[D] = pl->base[D];
         if (n_home) n_home[D] = pl->n_home[D];
@@ -185,7 +185,8 @@ int halo_domain_layout(const halo_plan* pl, int64_t* base, int32_t* n_home, int3
 
 int halo_get_pulse(const halo_plan* pl, int32_t domain, int32_t pulse, halo_pulse_info* out,
                    int32_t* index_map) {
-    if (!pl || !out || domain < 0 || domain >= pl->n_dom || pulse < 0 || pulse >= pl->P)
+    if (!pl || !out || !pl->valid || domain < 0 || domain >= pl->n_dom || pulse < 0 ||
+        pulse >= pl->P)
         return HALO_EINVAL;
     const halo::SPDesc& d = pl->sp[(size_t)domain * pl->P + pulse];
     out->send_domain = domain;
@@ -204,7 +205,7 @@ int halo_get_pulse(const halo_plan* pl, int32_t domain, int32_t pulse, halo_puls
 }
 
 int halo_get_index_maps(const halo_plan* pl, int32_t* maps, int64_t* offsets) {
-    if (!pl || !offsets || (!maps && pl->n_halo_total > 0)) return HALO_EINVAL;
+    if (!pl || !offsets || !pl->valid || (!maps && pl->n_halo_total > 0)) return HALO_EINVAL;
     const int nd = pl->n_dom, P = pl->P;
     for (int p = 0; p < P; p++)
         for (int s = 0; s < nd; s++) offsets[(size_t)p * nd + s] = pl->map_off[(size_t)s * P + p];

@@ -135,7 +135,8 @@ int halo_setup_ex(const float box[3], const int32_t grid[3], float rc, const flo
 /* Rebuild the plan's maps for new positions / domain ids (same box, grid and
  * cut-off; n_atoms may change).  Synchronises `stream`.  Sizes and layout
  * change: query them again and re-size the caller's buffers.  If the rebuild
- * fails, the plan refuses exchanges (HALO_EINVAL) until a rebuild succeeds. */
+ * fails, the plan refuses exchanges and the layout, pulse and index-map
+ * queries (HALO_EINVAL) until a rebuild succeeds. */
 int halo_rebuild(halo_plan* plan, const float* coords, const int32_t* domain_of_atom,
                  int64_t n_atoms, void* stream);
 

@@ -78,6 +78,9 @@ def test_failed_rebuild_refuses_exchanges_until_rebuilt():
         with pytest.raises(halo.HaloError) as e:
             plan.exchange_x(loc)
         assert e.value.code == halo.EINVAL
+        with pytest.raises(halo.HaloError) as e:        # so do the plan queries
+            plan.pulse(0, 0)
+        assert e.value.code == halo.EINVAL
         plan.rebuild(x, d)                              # a good rebuild restores it
         loc = plan.load_home(x)
         plan.exchange_x(loc)
