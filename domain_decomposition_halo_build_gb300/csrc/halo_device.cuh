@@ -3,7 +3,23 @@
 
 #include <stdint.h>
 
+#include "halo.h"
+
 namespace halo {
+
+// Debug builds (-DHALO_DEBUG): every slot index that a kernel gathers from or
+// scatters to is checked against its buffer before the access; a bad one
+// records HALO_EBOUNDS in the plan's error word (halo_status reports it) and
+// the access is skipped.  Release builds compile the check away.
+#ifdef HALO_DEBUG
+__device__ __forceinline__ bool in_range(int64_t i, int64_t n, int* err) {
+    if ((uint64_t)i < (uint64_t)n) return true;
+    atomicCAS(err, 0, HALO_EBOUNDS);
+    return false;
+}
+#else
+__device__ __forceinline__ bool in_range(int64_t, int64_t, int*) { return true; }
+#endif
 
 constexpr unsigned kFull = 0xffffffffu;
 

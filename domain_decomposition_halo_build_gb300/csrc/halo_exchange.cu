@@ -127,6 +127,7 @@ struct XArgs {
     int n_items;
     long long timeout_ns;
     int drop_flag;
+    int64_t n_slots;  // local slots (checked in debug builds)
     unsigned long long* trace;  // optional: 4 words per item (see halo_set_trace)
 };
 
@@ -141,6 +142,7 @@ struct FArgs {
     int n_items;
     long long timeout_ns;
     unsigned long long* trace;
+    int64_t n_slots;  // local slots (checked in debug builds)
 };
 
 constexpr int kWarps = kThreads / 32;
@@ -194,10 +196,13 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
         float* dst = a.xyz + 3 * w.dst;
         // index loads first: only the forwarded coordinates remain after a wait
         int idx[E];
+        const bool dst_ok = w.len <= 0 || in_range(w.dst + w.len - 1, a.n_slots, a.err);
 #pragma unroll
         for (int e = 0; e < E; e++) {
             const int i = threadIdx.x + e * kThreads;
             idx[e] = i < w.len ? __ldg(map + i) : -1;
+            if (idx[e] >= 0 && !(dst_ok && in_range(w.src_base + idx[e], a.n_slots, a.err)))
+                idx[e] = -1;
         }
         if (dependent) {
             // packWithDeps: one thread waits for the pulses that delivered the
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
         fence_smem_to_async();
         __syncthreads();
         if (threadIdx.x == 0) {
-            bulk_store_floats(dst, stage, 3 * w.len, true);
+            if (dst_ok) bulk_store_floats(dst, stage, 3 * w.len, true);
             if (w.flag != a.drop_flag) red_release_gpu_add(a.arrived + w.flag, 1u);
             if (a.trace) trace_item(a.trace, tk.item, t_take, t_wait);
         }
@@ -283,6 +288,9 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
         for (int e = 0; e < E; e++) {
             const int i = lane + 32 * e;
             sd[e] = i < w.len ? __ldg(pr + i) : make_int2(-1, -1);
+            if (sd[e].x >= 0 && !(in_range(sd[e].x, a.n_slots, a.err) &&
+                                  in_range(sd[e].y, a.n_slots, a.err)))
+                sd[e] = make_int2(-1, -1);
         }
         if (w.ms | w.mr) {
             // warm L2 with the lines read after the wait (L2 is coherent, so
@@ -421,10 +429,12 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(const SPDesc* __rest
 
 __global__ void load_home_kernel(const int64_t* __restrict__ home_dst,
                                  const int32_t* __restrict__ home_gid, int64_t n,
-                                 const float* __restrict__ g, float* __restrict__ local) {
+                                 const float* __restrict__ g, float* __restrict__ local,
+                                 int64_t n_slots, int* err) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t dd = home_dst[i], a = home_gid[i];
+        if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
         local[3 * dd + 0] = g[3 * a + 0];
         local[3 * dd + 1] = g[3 * a + 1];
         local[3 * dd + 2] = g[3 * a + 2];
@@ -435,10 +445,12 @@ __global__ void load_home_kernel(const int64_t* __restrict__ home_dst,
 // so the writes are disjoint
 __global__ void store_home_kernel(const int64_t* __restrict__ home_dst,
                                   const int32_t* __restrict__ home_gid, int64_t n,
-                                  const float* __restrict__ local, float* __restrict__ g) {
+                                  const float* __restrict__ local, float* __restrict__ g,
+                                  int64_t n_slots, int* err) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t dd = home_dst[i], a = home_gid[i];
+        if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
         g[3 * a + 0] = local[3 * dd + 0];
         g[3 * a + 1] = local[3 * dd + 1];
         g[3 * a + 2] = local[3 * dd + 2];
@@ -779,6 +791,7 @@ int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     a.err = pl->d_err;
     a.n_items = pl->n_items_x;
     a.timeout_ns = pl->wait_timeout_ns;
+    a.n_slots = pl->n_local_total;
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
@@ -801,6 +814,7 @@ int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
     a.err = pl->d_err;
     a.n_items = pl->n_items_x;
     a.timeout_ns = pl->wait_timeout_ns;
+    a.n_slots = pl->n_local_total;
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
@@ -823,6 +837,7 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
     a.err = pl->d_err;
     a.n_items = pl->n_items_f;
     a.timeout_ns = pl->wait_timeout_ns;
+    a.n_slots = pl->n_local_total;
     a.trace = pl->trace ? pl->trace + 4 * (size_t)pl->n_items_x : nullptr;
     const cudaError_t e = launch_dependent(unpack_f_kernel<4>, dim3(pl->grid_f), dim3(kThreads), st, a);
     if (e != cudaSuccess) return cuda_code(e);
@@ -833,14 +848,16 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
 int launch_store_home(const halo_plan* pl, const float* local, float* g, cudaStream_t st) {
     const int64_t n = pl->n_atoms;
     const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
-    store_home_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, local, g);
+    store_home_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, local, g,
+                                              pl->n_local_total, pl->d_err);
     return cuda_code(cudaGetLastError());
 }
 
 int launch_load_home(const halo_plan* pl, const float* g, float* local, cudaStream_t st) {
     const int64_t n = pl->n_atoms;
     const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
-    load_home_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, g, local);
+    load_home_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, g, local,
+                                             pl->n_local_total, pl->d_err);
     return cuda_code(cudaGetLastError());
 }
 

@@ -36,7 +36,6 @@
 namespace halo {
 namespace {
 
-constexpr int kFlatChunkMax = 4 * kThreads;  // halo slots per coordinate item (at most)
 constexpr int kNodeBits = 26;             // entry = node slot | parent position << 26
 constexpr int32_t kNodeMask = (1 << kNodeBits) - 1;
 constexpr int kMaxCopies = 63;            // parent positions fit in 6 bits
@@ -44,7 +43,7 @@ constexpr int kSortRegs = 8;              // copy lists sorted in registers up t
 
 // ---- stepwise ----------------------------------------------------------------
 __global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
-                              float* xyz, int P, int p) {
+                              float* xyz, int P, int p, int64_t n_slots, int* err) {
     grid_launch_dependents();
     const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
     const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
@@ -52,6 +51,7 @@ __global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __re
     grid_dependency_wait();  // pulse p - 1 (or whatever came before) has landed
     for (int i = i0; i < d.send; i += gridDim.x * blockDim.x) {
         if (i != i0) m = maps[d.map_off + i];
+        if (!in_range(d.src_base + m, n_slots, err) || !in_range(d.dst + i, n_slots, err)) continue;
         const float* s = xyz + 3 * (d.src_base + m);
         float* q = xyz + 3 * (d.dst + i);
         const float v0 = s[0], v1 = s[1], v2 = s[2];
@@ -62,7 +62,7 @@ __global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __re
 }
 
 __global__ void step_f_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
-                              float* f, int P, int p) {
+                              float* f, int P, int p, int64_t n_slots, int* err) {
     grid_launch_dependents();
     const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
     const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
@@ -70,6 +70,7 @@ __global__ void step_f_kernel(const SPDesc* __restrict__ sp, const int32_t* __re
     grid_dependency_wait();
     for (int i = i0; i < d.send; i += gridDim.x * blockDim.x) {
         if (i != i0) m = maps[d.map_off + i];
+        if (!in_range(d.src_base + m, n_slots, err) || !in_range(d.dst + i, n_slots, err)) continue;
         const float* h = f + 3 * (d.dst + i);
         float* o = f + 3 * (d.src_base + m);
         const float h0 = h[0], h1 = h[1], h2 = h[2];
@@ -347,9 +348,11 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
 template <int E>
 __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int32_t* __restrict__ xflat,
                                                           const int4* __restrict__ items, float L0,
-                                                          float L1, float L2) {
+                                                          float L1, float L2, int64_t n_slots,
+                                                          int* err) {
     grid_launch_dependents();
-    const int4 it = items[blockIdx.x];
+    int4 it = items[blockIdx.x];
+    if (!in_range((int64_t)it.y + it.z - 1, n_slots, err)) it.z = 0;
     int32_t v[E];
 #pragma unroll
     for (int e = 0; e < E; e++) {
@@ -363,7 +366,8 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
     for (int e = 0; e < E; e++) {
         if (threadIdx.x + e * kThreads < it.z) {
             // owners are home slots, never written by this kernel
-            const float* s = xyz + 3 * (int64_t)(v[e] & ((1 << 29) - 1));
+            const int64_t o = v[e] & ((1 << 29) - 1);
+            const float* s = xyz + 3 * (in_range(o, n_slots, err) ? o : 0);
             a[e][0] = __ldg(s);
             a[e][1] = __ldg(s + 1);
             a[e][2] = __ldg(s + 2);
@@ -493,11 +497,30 @@ __device__ __forceinline__ void reduce_tree(float* f, int32_t home, int k, const
 // trip.  KB: copies held in registers for class B (7 or 11, the plan's
 // largest tree); KW: class C trees of up to KW copies in registers (0: none),
 // larger ones reduced sequentially through memory in the same order.
+// Debug builds: a tree whose home slot, node slots or parent positions fall
+// outside their ranges is skipped (0 copies) and HALO_EBOUNDS recorded.
+template <int K>
+__device__ __forceinline__ int checked_copies(int32_t home, int k, const int32_t (&ent)[K],
+                                              int64_t n_slots, int* err) {
+#ifdef HALO_DEBUG
+    bool ok = k <= K && in_range(home, n_slots, err);
+#pragma unroll
+    for (int j = 0; j < K; j++)
+        if (j < k)
+            ok = ok && in_range(ent[j] & kNodeMask, n_slots, err) &&
+                 in_range((unsigned)ent[j] >> kNodeBits, k + 1, err);
+    return ok ? k : 0;
+#else
+    return k;
+#endif
+}
+
 template <int KB, int KW>
 __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* __restrict__ recA,
                                                           int64_t nA, const int4* __restrict__ recB,
                                                           int64_t nB, const int4* __restrict__ recC,
-                                                          int64_t nC, const int32_t* __restrict__ fent) {
+                                                          int64_t nC, const int32_t* __restrict__ fent,
+                                                          int64_t n_slots, int64_t n_fent, int* err) {
     // blocks [0, tilesBC) take classes B and C, one owner per thread (the
     // longer trees start first); the following blocks take class-A tiles of
     // 2 * blockDim owners, two per thread (coalesced record loads), so both
@@ -519,9 +542,10 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
             const int4 r0 = m0 < nA ? __ldg(recA + m0) : make_int4(0, 0, 0, 0);
             const int4 r1 = m1 < nA ? __ldg(recA + m1) : make_int4(0, 0, 0, 0);
             const int32_t home[2] = {r0.x & kNodeMask, r1.x & kNodeMask};
-            const int kk[2] = {m0 < nA ? (int)((unsigned)r0.x >> kNodeBits) : 0,
-                               m1 < nA ? (int)((unsigned)r1.x >> kNodeBits) : 0};
             const int32_t ent[2][3] = {{r0.y, r0.z, r0.w}, {r1.y, r1.z, r1.w}};
+            const int kk[2] = {
+                m0 < nA ? checked_copies<3>(home[0], (int)((unsigned)r0.x >> kNodeBits), ent[0], n_slots, err) : 0,
+                m1 < nA ? checked_copies<3>(home[1], (int)((unsigned)r1.x >> kNodeBits), ent[1], n_slots, err) : 0};
             grid_dependency_wait();
             reduce_trees<3, 2>(f, home, kk, ent);
             return;
@@ -535,8 +559,10 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
             int32_t ent[KB];
 #pragma unroll
             for (int j = 0; j < KB; j++) ent[j] = all[j];
+            const int kb = checked_copies<KB>(r0.x & kNodeMask, (int)((unsigned)r0.x >> kNodeBits), ent,
+                                              n_slots, err);
             grid_dependency_wait();
-            reduce_tree<KB>(f, r0.x & kNodeMask, (int)((unsigned)r0.x >> kNodeBits), ent);
+            reduce_tree<KB>(f, r0.x & kNodeMask, kb, ent);
         } else {
             const int4 r = __ldg(recC + (m - nA - nB));
             grid_dependency_wait();
@@ -544,21 +570,27 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
                 if (((unsigned)r.x >> kNodeBits) <= (unsigned)KW) {
                     // plans with deeper trees (several pulses per dim): up to
                     // KW copies in registers
-                    const int k = (int)((unsigned)r.x >> kNodeBits);
+                    int k = (int)((unsigned)r.x >> kNodeBits);
+                    if (k > 0 && !in_range((int64_t)r.y + k - 1, n_fent, err)) k = 0;
                     int32_t ent[KW];
 #pragma unroll
                     for (int j = 0; j < KW; j++) ent[j] = j < k ? __ldg(fent + r.y + j) : 0;
-                    reduce_tree<KW>(f, r.x & kNodeMask, k, ent);
+                    reduce_tree<KW>(f, r.x & kNodeMask, checked_copies<KW>(r.x & kNodeMask, k, ent, n_slots, err), ent);
                     return;
                 }
             }
             // every slot of this tree belongs to this thread alone: plain
             // sequential read-modify-write in the same order, through L2
             float* fh = f + 3 * (int64_t)(r.x & kNodeMask);
-            const int k = (int)((unsigned)r.x >> kNodeBits), s0 = r.y;
+            int k = (int)((unsigned)r.x >> kNodeBits);
+            const int s0 = r.y;
+            if (k > 0 && !(in_range(r.x & kNodeMask, n_slots, err) &&
+                           in_range((int64_t)s0 + k - 1, n_fent, err)))
+                k = 0;
             for (int j = 0; j < k; j++) {
                 const int32_t e = __ldg(fent + s0 + j);
                 const int par = (int)((unsigned)e >> kNodeBits);
+                if (!in_range(e & kNodeMask, n_slots, err) || !in_range(par, k + 1, err)) continue;
                 const float* fn = f + 3 * (int64_t)(e & kNodeMask);
                 float* fp = par == 0 ? fh : f + 3 * (int64_t)(__ldg(fent + s0 + par - 1) & kNodeMask);
                 const float n0 = __ldcg(fn), n1 = __ldcg(fn + 1), n2 = __ldcg(fn + 2);
@@ -768,7 +800,7 @@ int launch_stepwise_x(halo_plan* pl, float* xyz, cudaStream_t st) {
         const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
         const cudaError_t e = launch_dependent(step_x_kernel, dim3(gx, pl->n_dom), dim3(kThreads), st,
                                                (const SPDesc*)pl->d_sp, (const int32_t*)pl->d_maps, xyz,
-                                               pl->P, p);
+                                               pl->P, p, pl->n_local_total, pl->d_err);
         if (e != cudaSuccess) return cuda_code(e);
         pl->launches_x++;
     }
@@ -780,7 +812,7 @@ int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st) {
         const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
         const cudaError_t e = launch_dependent(step_f_kernel, dim3(gx, pl->n_dom), dim3(kThreads), st,
                                                (const SPDesc*)pl->d_sp, (const int32_t*)pl->d_maps, f,
-                                               pl->P, p);
+                                               pl->P, p, pl->n_local_total, pl->d_err);
         if (e != cudaSuccess) return cuda_code(e);
         pl->launches_f++;
     }
@@ -792,7 +824,8 @@ int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     auto* k = pl->flat_x_e == 4 ? flat_x_kernel<4> : pl->flat_x_e == 2 ? flat_x_kernel<2> : flat_x_kernel<1>;
     const cudaError_t e = launch_dependent(k, dim3(pl->n_xflat_items), dim3(kThreads), st, xyz,
                                            (const int32_t*)pl->d_xflat, (const int4*)pl->d_xflat_items,
-                                           pl->box[0], pl->box[1], pl->box[2]);
+                                           pl->box[0], pl->box[1], pl->box[2], pl->n_local_total,
+                                           pl->d_err);
     if (e != cudaSuccess) return cuda_code(e);
     pl->launches_x++;
     return HALO_OK;
@@ -809,7 +842,8 @@ int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
     const cudaError_t e = launch_dependent(k, dim3(gb), dim3(kThreads), st, f, (const int4*)pl->d_frec[0],
                                            pl->n_rec[0], (const int4*)pl->d_frec[1], pl->n_rec[1],
                                            (const int4*)pl->d_frec[2], pl->n_rec[2],
-                                           (const int32_t*)pl->d_fent);
+                                           (const int32_t*)pl->d_fent, pl->n_local_total,
+                                           pl->n_halo_total, pl->d_err);
     if (e != cudaSuccess) return cuda_code(e);
     pl->launches_f++;
     return HALO_OK;

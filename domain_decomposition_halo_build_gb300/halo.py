@@ -16,7 +16,9 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIBRARY = os.path.join(_PKG, "libhalo.so")
+# HALO_LIBRARY selects another build of the same library (the bounds-checking
+# libhalo_debug.so); there is no fallback either way
+LIBRARY = os.environ.get("HALO_LIBRARY") or os.path.join(_PKG, "libhalo.so")
 
 OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM, ESCRATCH = (
     0, -1, -2, -3, -4, -5, -6, -7, -8, -9)

@@ -60,7 +60,8 @@ extern "C" {
 #define HALO_ECAPACITY (-4) /* build buffers could not be sized (internal retries exhausted) */
 #define HALO_ECUDA (-5)     /* a CUDA runtime call failed */
 #define HALO_ETIMEOUT (-6)  /* a device-side wait gave up after the plan's time limit */
-#define HALO_EBOUNDS (-7)   /* an index outside its buffer was met and skipped */
+#define HALO_EBOUNDS (-7)   /* an index outside its buffer was met and skipped (bounds-checking
+                               build libhalo_debug.so only) */
 #define HALO_ENOMEM (-8)    /* device or host allocation failed */
 #define HALO_ESCRATCH (-9)  /* the plan needs more counters than halo_exchange_x_noalloc's fixed array */
 
