@@ -167,6 +167,7 @@ int halo_query(const halo_plan* pl, halo_info* out) {
     for (int d = 0; d < 3; d++) out->pulses_per_dim[d] = pl->pulses_per_dim[d];
     for (int p = 0; p < pl->P; p++) out->pulse_dim[p] = pl->pulse_dim[p];
     out->flags = pl->flags;
+    out->build_attempts = pl->build_attempts;
     out->n_atoms = pl->n_atoms;
     out->n_local_total = pl->n_local_total;
     out->n_halo_total = pl->n_halo_total;
@@ -271,6 +272,12 @@ int halo_status(halo_plan* pl, void* stream) {
         HALO_CUDA(cudaStreamSynchronize(st));
     }
     return e[0];
+}
+
+int halo_debug_set_build_capacity(halo_plan* pl, int64_t slots) {
+    if (!pl || slots <= 0) return HALO_EINVAL;
+    pl->debug_capacity = slots;
+    return HALO_OK;
 }
 
 int halo_set_wait_timeout(halo_plan* pl, double seconds) {

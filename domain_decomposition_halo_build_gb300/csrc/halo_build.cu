@@ -606,6 +606,15 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         if (pl->grid[d] > 1) grow_f *= 1.0 + (double)pl->rc / ((double)pl->box[d] / pl->grid[d]);
     int64_t want = n + (int64_t)ceil((double)n * (grow_f - 1.0) * 1.15) + (int64_t)256 * nd * P + 1024;
     want = std::max(want, pl->cap_slots);
+    if (pl->debug_capacity > 0) {
+        // test hook: start from the given capacity (the retry below grows it)
+        dev_free(pl->d_bxyz);
+        dev_free(pl->d_maps);
+        pl->cap_slots = 0;
+        want = std::max<int64_t>(pl->debug_capacity, n + 1);  // the home region always fits
+        pl->debug_capacity = 0;
+    }
+    pl->build_attempts = 0;
 
     const Meta m = meta_ptrs(pl->d_meta, nd, P);
     void* hstage = nullptr;
@@ -615,6 +624,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
 
 
     for (int attempt = 0; attempt < 6; attempt++) {
+        pl->build_attempts = attempt + 1;
         if (want > pl->cap_slots) {
             int64_t have = pl->cap_slots;
             HALO_TRY(grow(&pl->d_bxyz, &have, want));

@@ -93,6 +93,8 @@ struct halo_plan {
     int32_t* d_pulse_scratch = nullptr;  // per-pulse block counts (3 * n_dom * B)
     int build_blocks_per_domain = 1;
     float* d_thr = nullptr;         // thresholds per pulse and sender cell
+    int64_t debug_capacity = 0;     // test hook: build-buffer slots of the next build's first attempt
+    int build_attempts = 0;         // attempts the last build needed (capacity retries + 1)
     uint32_t flags = 0;             // HALO_SETUP_* options
     double* d_faces = nullptr;      // corner pruning: lower faces [3][nmax], upper faces [3][nmax]
     uint8_t* d_bmask = nullptr;     // corner pruning: per build slot, dims it was received across

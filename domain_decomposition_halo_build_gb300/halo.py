@@ -40,7 +40,8 @@ class halo_info(ctypes.Structure):
                 ("pulses_per_dim", ctypes.c_int32 * 3),
                 ("pulse_dim", ctypes.c_int32 * MAX_PULSES),
                 ("n_atoms", ctypes.c_int64), ("n_local_total", ctypes.c_int64),
-                ("n_halo_total", ctypes.c_int64), ("flags", ctypes.c_uint32)]
+                ("n_halo_total", ctypes.c_int64), ("flags", ctypes.c_uint32),
+                ("build_attempts", ctypes.c_int32)]
 
 
 class halo_pulse_info(ctypes.Structure):
@@ -61,6 +62,7 @@ SIGNATURES = {
     "halo_setup_ex": (ctypes.c_int, [_P(ctypes.c_float), _P(_i32), ctypes.c_float, _vp, _vp, _i64,
                                      ctypes.c_uint32, _vp, _P(_vp)]),
     "halo_rebuild": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp]),
+    "halo_debug_set_build_capacity": (ctypes.c_int, [_vp, _i64]),
     "halo_query": (ctypes.c_int, [_vp, _P(halo_info)]),
     "halo_domain_layout": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "halo_get_pulse": (ctypes.c_int, [_vp, _i32, _i32, _P(halo_pulse_info), _vp]),
@@ -214,6 +216,7 @@ class HaloPlan:
         self.n_local_total = info.n_local_total
         self.n_halo_total = info.n_halo_total
         self.flags = int(info.flags)
+        self.build_attempts = int(info.build_attempts)
         self.prune = bool(self.flags & SETUP_PRUNE_CORNERS)
         nd = self.n_domains
         self.base = np.zeros(nd, np.int64)
@@ -306,6 +309,10 @@ class HaloPlan:
 
     def set_wait_timeout(self, seconds: float):
         _check(self._lib.halo_set_wait_timeout(self._h, float(seconds)), "halo_set_wait_timeout")
+
+    def debug_set_build_capacity(self, slots: int):
+        _check(self._lib.halo_debug_set_build_capacity(self._h, int(slots)),
+               "halo_debug_set_build_capacity")
 
     def debug_drop_signal(self, domain: int, pulse: int):
         _check(self._lib.halo_debug_drop_signal(self._h, domain, pulse), "halo_debug_drop_signal")

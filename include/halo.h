@@ -84,6 +84,8 @@ typedef struct {
     int64_t n_local_total;                  /* home + halo slots of all domains */
     int64_t n_halo_total;
     uint32_t flags;                         /* HALO_SETUP_* flags the plan was built with */
+    int32_t build_attempts;                 /* passes the last build needed: 1, or more when the
+                                               build buffer overflowed and was grown (retry) */
 } halo_info;
 
 typedef struct {
@@ -229,6 +231,13 @@ int halo_get_mode(const halo_plan* plan, int32_t* mode);
 /* Synchronise `stream`, return the plan's sticky device error (HALO_OK if
  * none) and clear it, resetting the plan's flags. */
 int halo_status(halo_plan* plan, void* stream);
+
+/* Test hook: the next halo_rebuild starts with a build buffer of `slots`
+ * slots (> 0; never fewer than the home atoms + 1) instead of its geometric
+ * estimate.  If that is too small, the build overflows, detects it and
+ * retries with a larger buffer (see halo_info.build_attempts).  The device
+ * kernels never write past the buffer they were given. */
+int halo_debug_set_build_capacity(halo_plan* plan, int64_t slots);
 
 /* Time limit of every device-side wait (default 1 s).  seconds > 0. */
 int halo_set_wait_timeout(halo_plan* plan, double seconds);

@@ -91,3 +91,39 @@ def test_failed_rebuild_refuses_exchanges_until_rebuilt():
         np.testing.assert_array_equal(loc.cpu().numpy(), want)
     finally:
         plan.close()
+
+
+def test_build_buffer_overflow_is_detected_and_retried():
+    """A build buffer far too small for the halo (test hook): the pulse kernels
+    stop writing at its end, the build detects the overflow, grows the buffer
+    and runs again; the result is the oracle's."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    w = synth.WORKLOADS["water24k_2x4x8"]
+    xyz, dom = synth.system(w)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d)
+    try:
+        assert plan.build_attempts == 1
+        plan.debug_set_build_capacity(w.n_atoms + 100)     # room for 100 halo slots
+        plan.rebuild(x, d)
+        assert plan.build_attempts > 1
+        o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+        assert plan.n_local_total == o.n_local_total
+        maps, offs = plan.index_maps()
+        for p in range(o.n_pulses):
+            for s in range(o.n_domains):
+                want = o.index_map(s, p)
+                got = maps[offs[p * o.n_domains + s]:offs[p * o.n_domains + s + 1]]
+                np.testing.assert_array_equal(got, want)
+        loc = plan.load_home(x)
+        plan.exchange_x(loc)
+        assert plan.status() == halo.OK
+        want = o.load_home(xyz)
+        o.exchange_x(want)
+        np.testing.assert_array_equal(loc.cpu().numpy(), want)
+        with pytest.raises(halo.HaloError):
+            plan.debug_set_build_capacity(0)
+    finally:
+        plan.close()
