@@ -471,6 +471,23 @@ def stencil_case(device, stream, flush, iters, warmup):
                 e1.record(stream)
             torch.cuda.synchronize()
             row[name + "_us"] = 1e3 * statistics.fmean(e0.elapsed_time(e1) for e0, e1 in ev)
+        # the whole run in one launch: K fused iterations with grid-wide
+        # barriers between them (stencil_iterate), flushed before each launch
+        K = 50
+        for _ in range(2):
+            flush()
+            p.iterate(a, b, K, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(max(3, min(iters, 10)))]
+        for e0, e1 in ev:
+            flush()
+            e0.record(stream)
+            p.iterate(a, b, K, stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        assert p.status(stream) == 0
+        row["iterate_us_per_iteration"] = 1e3 * statistics.fmean(e0.elapsed_time(e1) for e0, e1 in ev) / K
+        row["iterate_speedup_vs_fused_launches"] = row["fused_us"] / row["iterate_us_per_iteration"]
         sweep_gbs = 8.0 * row["cells"] / (row["sweep_us"] * 1e-6) / 1e9
         row["sweep_gbs"] = sweep_gbs
         row["sweep_hbm_frac"] = sweep_gbs / peak

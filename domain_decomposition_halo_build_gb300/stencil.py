@@ -19,6 +19,8 @@ SIGNATURES = {
     "stencil_exchange": (ctypes.c_int, [_vp, _vp, _vp]),
     "stencil_sweep": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "stencil_sweep_fused": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "stencil_iterate": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp]),
+    "stencil_status": (ctypes.c_int, [_vp, _vp]),
     "stencil_destroy": (None, [_vp]),
 }
 
@@ -75,6 +77,17 @@ class StencilPlan:
         halo._check(self._lib.stencil_sweep_fused(self._h, self._field(src), self._field(dst),
                                                   halo._stream_handle(stream)),
                     "stencil_sweep_fused")
+
+    def iterate(self, a, b, iterations, stream=None):
+        """stencil_iterate: `iterations` fused iterations in one launch; the
+        result is in a (even count) or b (odd)."""
+        halo._check(self._lib.stencil_iterate(self._h, self._field(a), self._field(b),
+                                              int(iterations), halo._stream_handle(stream)),
+                    "stencil_iterate")
+        return a if iterations % 2 == 0 else b
+
+    def status(self, stream=None) -> int:
+        return self._lib.stencil_status(self._h, halo._stream_handle(stream))
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

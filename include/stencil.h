@@ -47,7 +47,8 @@ extern "C" {
 typedef struct stencil_plan stencil_plan; /* opaque; host-side sizes only */
 
 /* A plan for px x py blocks of n x n cells (px, py >= 1; n >= 4, n % 4 == 0).
- * Allocates no device memory. */
+ * Allocates no device memory (stencil_iterate allocates one small word on
+ * first use). */
 int stencil_setup(int32_t px, int32_t py, int32_t n, stencil_plan** out_plan);
 
 /* The field layout (host outputs, any may be NULL): floats per row, rows per
@@ -73,6 +74,24 @@ int stencil_sweep(const stencil_plan* plan, const float* in, float* out, void* s
  * next sweep without a separate exchange.  Same result as stencil_sweep
  * followed by stencil_exchange on `out`.  One kernel launch. */
 int stencil_sweep_fused(const stencil_plan* plan, const float* in, float* out, void* stream);
+
+/* `iterations` fused iterations in ONE kernel launch, with no host in the
+ * loop (the page's GPU-initiated scheme taken to the whole run): iteration i
+ * sweeps a into b when i is even, b into a when i is odd, and stores the new
+ * edges into the neighbours' ghost cells; the blocks of the launch meet at a
+ * grid-wide barrier between iterations.  The result is in a when iterations
+ * is even, in b when it is odd; a and b must hold the same matrix border and
+ * a must hold valid ghost cells (after stencil_exchange or a fused step).
+ * Same result as that many stencil_sweep_fused calls.  The launch is
+ * cooperative (all its blocks resident at once); every barrier wait is
+ * bounded (1 s): a wait that runs out records HALO_ETIMEOUT for
+ * stencil_status and the kernel returns.  The first call allocates the
+ * barrier's 64-byte device word for the plan.  iterations >= 0. */
+int stencil_iterate(stencil_plan* plan, float* a, float* b, int32_t iterations, void* stream);
+
+/* Synchronise `stream` and return (and clear) the error recorded by the last
+ * stencil_iterate: HALO_OK or HALO_ETIMEOUT. */
+int stencil_status(stencil_plan* plan, void* stream);
 
 void stencil_destroy(stencil_plan* plan);
 

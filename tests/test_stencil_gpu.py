@@ -140,3 +140,39 @@ def test_bad_arguments():
         p.sweep(d, d)                       # in == out
     with pytest.raises(ValueError):
         p.exchange(torch.zeros(p.total_floats + 4, device="cuda"))
+
+
+@pytest.mark.parametrize("px,py,n", [(1, 1, 4), (2, 4, 8), (3, 2, 36), (2, 2, 520), (4, 2, 1000)])
+@pytest.mark.parametrize("iterations", [0, 1, 2, 5])
+def test_iterate_in_one_launch(px, py, n, iterations):
+    """stencil_iterate: that many fused iterations in one cooperative launch
+    (grid-wide barriers between them) give the tile field of that many sweeps
+    of the whole matrix, in a for an even count and in b for an odd one."""
+    import torch
+    a, f = make_field(px, py, n, seed=iterations + 7)
+    want = S.to_tiles(S.jacobi_global(a, iterations), px, py, n)
+    want[unused(px, py, n)] = SENTINEL
+    p = plan_for(px, py, n)
+    da = torch.from_numpy(f).cuda()
+    db = da.clone()
+    res = p.iterate(da, db, iterations)
+    assert p.status() == 0
+    assert (res is da) == (iterations % 2 == 0)
+    np.testing.assert_array_equal(bits(res.cpu().numpy()), bits(want))
+
+
+def test_iterate_matches_separate_fused_launches():
+    """Twelve iterations in one launch and twelve fused launches agree bit for
+    bit on the bench's 2 x 4 grid of blocks."""
+    import torch
+    px, py, n = 2, 4, 512
+    a, f = make_field(px, py, n, seed=21)
+    p = plan_for(px, py, n)
+    da, db = torch.from_numpy(f).cuda(), torch.from_numpy(f).cuda()
+    one = p.iterate(da, db, 12)
+    cur, nxt = torch.from_numpy(f).cuda(), torch.from_numpy(f).cuda()
+    for _ in range(12):
+        p.sweep_fused(cur, nxt)
+        cur, nxt = nxt, cur
+    assert p.status() == 0
+    assert torch.equal(one, cur)
