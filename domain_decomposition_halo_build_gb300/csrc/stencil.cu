@@ -33,19 +33,22 @@ struct stencil_plan {
     unsigned* d_sync = nullptr;
     int dev = -1;
     int iterate_grid = 0;  // co-resident blocks of the persistent kernel
+    int band = 16;         // rows per sweep unit
 };
 
 namespace {
 
 constexpr int kCol0 = 4;     // first block column of a tile row
 constexpr int kQuads = 128;  // threads per sweep block, 4 cells each
-constexpr int kBand = 16;    // rows per sweep block
+constexpr int kBand = 16;    // rows per sweep unit (at most; fewer for small blocks)
+constexpr int kMinUnits = 1024;  // sweep units wanted per launch before bands shrink
 constexpr int kExchThreads = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct Geo {
     int px, py, n, pitch;
     int64_t tile;  // floats per tile
+    int band;      // rows per sweep unit
 };
 
 __device__ __forceinline__ float4 ld4(const float* p) {
@@ -116,7 +119,7 @@ __device__ __forceinline__ float jacobi(float n, float s, float w, float e) {
 }
 
 // One unit of a sweep: 512 columns (128 threads x 4) of block t over the
-// band of rows starting at 1 + by * kBand.  COHERENT: `in` was written earlier
+// band of rows starting at 1 + by * g.band.  COHERENT: `in` was written earlier
 // in the same launch (the persistent kernel), so it is read through L2 (.cg)
 // rather than the non-coherent path.
 template <bool FUSED, bool COHERENT>
@@ -124,8 +127,8 @@ __device__ __forceinline__ void sweep_unit(const float* __restrict__ in, float* 
                                            int cx, int by, int t) {
     const int nq = g.n / 4;
     const int q = cx * kQuads + threadIdx.x;  // group of 4 columns
-    const int r0 = 1 + by * kBand;             // first row of the band (<= n)
-    const int r1 = min(r0 + kBand, g.n + 1);   // one past its last row
+    const int r0 = 1 + by * g.band;            // first row of the band (<= n)
+    const int r1 = min(r0 + g.band, g.n + 1);  // one past its last row
     const int tx = t % g.px, ty = t / g.px;
     const float* src = in + (int64_t)t * g.tile;
     float* dst = out + (int64_t)t * g.tile;
@@ -241,14 +244,14 @@ __global__ void __launch_bounds__(kQuads) stencil_iterate_kernel(float* a, float
     }
 }
 
-Geo geo(const stencil_plan* p) { return Geo{p->px, p->py, p->n, p->pitch, p->tile_floats}; }
+Geo geo(const stencil_plan* p) { return Geo{p->px, p->py, p->n, p->pitch, p->tile_floats, p->band}; }
 
 bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 
 int launch_sweep(const stencil_plan* p, const float* in, float* out, void* stream, bool fused) {
     if (!p || !aligned16(in) || !aligned16(out) || in == out) return HALO_EINVAL;
     const int nq = p->n / 4;
-    const dim3 grid((unsigned)((nq + kQuads - 1) / kQuads), (unsigned)((p->n + kBand - 1) / kBand),
+    const dim3 grid((unsigned)((nq + kQuads - 1) / kQuads), (unsigned)((p->n + p->band - 1) / p->band),
                     (unsigned)(p->px * p->py));
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (fused)
@@ -277,6 +280,13 @@ int stencil_setup(int32_t px, int32_t py, int32_t n, stencil_plan** out_plan) {
     p->rows = n + 2;
     p->tile_floats = (int64_t)p->rows * p->pitch;
     p->total_floats = p->tile_floats * px * py;
+    // rows per sweep unit: 16 (each input row read once per 16 output rows,
+    // plus the two around them) unless that leaves too few units to keep the
+    // GPU's warps busy, when the per-thread chain of row loads is the limit;
+    // then 8 or 4
+    const int64_t cols = ((int64_t)n / 4 + kQuads - 1) / kQuads;
+    p->band = kBand;
+    while (p->band > 4 && cols * ((n + p->band - 1) / p->band) * px * py < kMinUnits) p->band /= 2;
     *out_plan = p;
     return HALO_OK;
 }
@@ -329,7 +339,7 @@ int stencil_iterate(stencil_plan* p, float* a, float* b, int32_t iterations, voi
         p->iterate_grid = sms * occ;
     }
     const int units_x = (p->n / 4 + kQuads - 1) / kQuads;
-    const int units_y = (p->n + kBand - 1) / kBand;
+    const int units_y = (p->n + p->band - 1) / p->band;
     const int64_t units = (int64_t)units_x * units_y * p->px * p->py;
     const int grid = (int)std::min<int64_t>(units, p->iterate_grid);
     // the barrier counter reaches iterations * grid
