@@ -12,12 +12,14 @@
 // (independent) and entries that arrived in earlier pulses (dependent).
 //
 // Device pipeline (one stream, one host synchronisation at the end):
-//   1. home partition: per-warp-tile histogram of domain ids, exclusive scan,
-//      stable scatter (warp match + running per-domain counters) -> every
-//      domain's home atoms in input order, in a home-compact region;
-//   2. per pulse: count kernel (predicate per candidate), scan kernel (block
-//      offsets, sizes, receiver offsets), write kernel (stable block-wide
-//      ballot compaction -> ascending index map + the new halo coordinates);
+//   1. home partition: a histogram of domain ids per block tile (per-warp
+//      shared histograms), exclusive scan, stable scatter (warp match +
+//      running per-domain counters) -> every domain's home atoms in input
+//      order, in a home-compact region;
+//   2. per pulse: count kernel (predicate per candidate, with the optional
+//      corner test), scan kernel (block offsets, sizes, receiver offsets),
+//      write kernel (stable block-wide ballot compaction -> ascending index
+//      map + the new halo coordinates);
 //   3. finalize: dense bases, home slot -> dense slot map; one D2H copy of the
 //      metadata.
 // Index maps hold domain-relative local indices, so the dense relayout touches
@@ -32,7 +34,6 @@
 
 namespace halo {
 namespace {
-
 
 // ---- packed metadata (int64 entries) -----------------------------------------
 struct Meta {

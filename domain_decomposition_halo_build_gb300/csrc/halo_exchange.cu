@@ -31,12 +31,13 @@
 // slice.  Each destination slot still receives its adds in reverse pulse
 // order, so the result is bit-identical to the sequential reduction.
 //
-// Forward progress: warps take work items from one atomic ticket counter in
-// that order, and an item only waits on items with earlier tickets.  The
-// earliest unfinished item was taken by a warp that is running (a warp holds
-// at most the item it works on and one prefetched ticket), and everything it
-// waits on has an earlier ticket, so by induction every wait ends -- whatever
-// the grid size and however blocks are scheduled.  Every wait is still bounded
+// Forward progress: blocks (coordinate items) and warps (force items) take
+// work items from one atomic ticket counter in that order, and an item only
+// waits on items with earlier tickets.  The earliest unfinished item is the
+// current item of a running block or warp (each holds at most the item it
+// works on and one prefetched, later ticket), and everything it waits on has
+// an earlier ticket, so by induction every wait ends -- whatever the grid size
+// and however blocks are scheduled.  Every wait is still bounded
 // in time and reports HALO_ETIMEOUT through the plan's error word.
 #include <string.h>
 
@@ -47,7 +48,6 @@
 
 namespace halo {
 namespace {
-
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
