@@ -131,7 +131,7 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
                                     int64_t n, int nd, int64_t nbt,
                                     const int32_t* __restrict__ offs,
                                     const int32_t* __restrict__ wcounts,
-                                    int32_t* __restrict__ home_gid, float* __restrict__ bxyz) {
+                                    int32_t* __restrict__ home_gid, float4* __restrict__ bxyz) {
     extern __shared__ int32_t sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int W = blockDim.x >> 5;
@@ -158,9 +158,9 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
         if (d >= 0) {
             const int64_t pos = (int64_t)run[d] + __popc(peers & lt);
             home_gid[pos] = (int32_t)a;
-            bxyz[3 * pos + 0] = __ldg(xyz + 3 * a + 0);
-            bxyz[3 * pos + 1] = __ldg(xyz + 3 * a + 1);
-            bxyz[3 * pos + 2] = __ldg(xyz + 3 * a + 2);
+            // one 16-byte store: the coordinates, and no forwarding dims
+            bxyz[pos] = make_float4(__ldg(xyz + 3 * a + 0), __ldg(xyz + 3 * a + 1),
+                                    __ldg(xyz + 3 * a + 2), __int_as_float(0));
         }
         __syncwarp();
         if (d >= 0 && lane == __ffs(peers) - 1) run[d] += __popc(peers);
@@ -250,7 +250,7 @@ __global__ void home_meta_kernel(const int32_t* __restrict__ offs, int64_t ntile
 
 // ---- 2. one pulse ---------------------------------------------------------------
 struct PulseArgs {
-    float* bxyz;
+    float4* bxyz;       // per build slot: x, y, z and (as int bits) the dims it was received across
     int32_t* maps;  // maps[slot - N]
     int64_t N;
     int64_t cap;    // slots of bxyz
@@ -267,18 +267,15 @@ struct PulseArgs {
     int nmax;
     double rc2;           // rc * rc in double, rc as fp32
     const double* faces;  // lower faces [3][nmax], then upper faces [3][nmax]
-    uint8_t* bmask;       // per build slot >= N: dims the slot was received across
 };
 
-// Corner pruning: distance of a candidate (coordinates v, build slot pos) of
-// sender cell c to the receiver's home box, over the pulse's dim d and the
+// Corner pruning: distance of a candidate (coordinates v, forwarding dims m)
+// of sender cell c to the receiver's home box, over the pulse's dim d and the
 // dims the slot was received across, below rc?  Double precision with
 // explicit round-to-nearest operations (no contraction), d's term first, then
-// ascending dims.  *mask receives the slot's dims (0 for a home slot).
-__device__ __forceinline__ bool corner_within(const PulseArgs& a, const int c[3], int64_t pos,
-                                              const float v[3], unsigned* mask) {
-    const unsigned m = pos < a.N ? 0u : (unsigned)a.bmask[pos];
-    *mask = m;
+// ascending dims.
+__device__ __forceinline__ bool corner_within(const PulseArgs& a, const int c[3], const float v[3],
+                                              unsigned m) {
     double t = __dsub_rn((double)v[a.d], a.faces[a.d * a.nmax + c[a.d]]);
     t = t > 0.0 ? t : 0.0;
     double r2 = __dmul_rn(t, t);
@@ -337,11 +334,13 @@ __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
     int64_t c = 0, ch = 0;
     for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
         const int64_t pos = locate(L, a.p, i);
-        if (pos >= 0 && pos < a.cap && a.bxyz[3 * pos + a.d] < thr) {
+        if (pos < 0 || pos >= a.cap) continue;
+        const float4 slot = a.bxyz[pos];
+        const float vd = a.d == 0 ? slot.x : (a.d == 1 ? slot.y : slot.z);
+        if (vd < thr) {
             if (a.prune) {
-                const float v[3] = {a.bxyz[3 * pos], a.bxyz[3 * pos + 1], a.bxyz[3 * pos + 2]};
-                unsigned m;
-                if (!corner_within(a, cell, pos, v, &m)) continue;
+                const float v[3] = {slot.x, slot.y, slot.z};
+                if (!corner_within(a, cell, v, (unsigned)__float_as_int(slot.w))) continue;
             }
             c++;
             if (i < nh) ch++;
@@ -417,14 +416,16 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
         if (i < hi) {
             const int64_t pos = locate(L, a.p, i);
             if (pos >= 0 && pos < a.cap) {
-                v0 = a.bxyz[3 * pos + 0];
-                v1 = a.bxyz[3 * pos + 1];
-                v2 = a.bxyz[3 * pos + 2];
+                const float4 slot = a.bxyz[pos];
+                v0 = slot.x;
+                v1 = slot.y;
+                v2 = slot.z;
+                m = (unsigned)__float_as_int(slot.w);
                 const float vd = a.d == 0 ? v0 : (a.d == 1 ? v1 : v2);
                 sel = vd < thr;
                 if (sel && a.prune) {
                     const float v[3] = {v0, v1, v2};
-                    sel = corner_within(a, cell, pos, v, &m);
+                    sel = corner_within(a, cell, v, m);
                 }
             }
         }
@@ -442,10 +443,8 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
             const int64_t o = out + before + __popc(bal & lt);
             if (o >= a.N && o < a.cap) {
                 a.maps[o - a.N] = (int32_t)i;
-                if (a.prune) a.bmask[o] = (uint8_t)(m | (1u << a.d));
-                a.bxyz[3 * o + 0] = v0 + sh[0];
-                a.bxyz[3 * o + 1] = v1 + sh[1];
-                a.bxyz[3 * o + 2] = v2 + sh[2];
+                a.bxyz[o] = make_float4(v0 + sh[0], v1 + sh[1], v2 + sh[2],
+                                        __int_as_float((int)(m | (1u << a.d))));
             }
         }
         out += total;
@@ -476,7 +475,7 @@ int grow(float** p, int64_t* cap_have, int64_t need_slots) {
     if (*p && *cap_have >= need_slots) return HALO_OK;
     dev_free(*p);
     *cap_have = 0;
-    HALO_TRY(dev_alloc(p, (size_t)need_slots * 3));
+    HALO_TRY(dev_alloc(p, (size_t)need_slots * 4));  // one float4 per slot
     *cap_have = need_slots;
     return HALO_OK;
 }
@@ -504,8 +503,6 @@ void free_build(halo_plan* pl) {
     dev_free(pl->d_pulse_scratch);
     dev_free(pl->d_thr);
     dev_free(pl->d_faces);
-    dev_free(pl->d_bmask);
-    pl->cap_bmask = 0;
     pl->cap_slots = 0;
     pl->n_alloc_atoms = 0;
     pl->counts_cap = 0;
@@ -636,7 +633,6 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         } else if (!pl->d_maps) {
             HALO_TRY(dev_alloc(&pl->d_maps, (size_t)pl->cap_slots));
         }
-        if (prune) HALO_TRY(dev_reserve(&pl->d_bmask, &pl->cap_bmask, pl->cap_slots));
         HALO_CUDA(cudaMemsetAsync(pl->d_meta, 0, mbytes, st));
         // 1. home partition
         int32_t* wcounts = pl->d_counts + 2 * ncount;
@@ -645,13 +641,13 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         int32_t* offs = pl->d_counts + ncount;
         HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
         home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
-            coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid, pl->d_bxyz);
+            coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid, reinterpret_cast<float4*>(pl->d_bxyz));
         home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, nbt, n, nd, P, m);
         HALO_CUDA(cudaGetLastError());
         // 2. pulses in global order
         for (int p = 0; p < P; p++) {
             PulseArgs a;
-            a.bxyz = pl->d_bxyz;
+            a.bxyz = reinterpret_cast<float4*>(pl->d_bxyz);
             a.maps = pl->d_maps;
             a.N = n;
             a.cap = pl->cap_slots;
@@ -674,7 +670,6 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
             a.nmax = nmax;
             a.rc2 = (double)pl->rc * (double)pl->rc;
             a.faces = pl->d_faces;
-            a.bmask = pl->d_bmask;
             dim3 g((unsigned)B, (unsigned)nd);
             pulse_count_kernel<<<g, kThreads, 0, st>>>(a);
             pulse_scan_kernel<<<1, 1024, 0, st>>>(a);

@@ -78,7 +78,8 @@ struct halo_plan {
     std::vector<halo::SPDesc> sp;
 
     // device memory owned by the plan: build
-    float* d_bxyz = nullptr;        // build buffer: home-compact region + halo regions
+    float* d_bxyz = nullptr;        // build buffer (float4 per slot: x, y, z, forwarding dims):
+                                    // home-compact region + halo regions
     int64_t cap_slots = 0;          // capacity of d_bxyz in slots (and of d_maps)
     int32_t* d_maps = nullptr;      // index maps, (pulse, sender) order
     int32_t* d_home_gid = nullptr;  // global id of each home-compact slot
@@ -97,8 +98,6 @@ struct halo_plan {
     int build_attempts = 0;         // attempts the last build needed (capacity retries + 1)
     uint32_t flags = 0;             // HALO_SETUP_* options
     double* d_faces = nullptr;      // corner pruning: lower faces [3][nmax], upper faces [3][nmax]
-    uint8_t* d_bmask = nullptr;     // corner pruning: per build slot, dims it was received across
-    int64_t cap_bmask = 0;
 
     // device memory owned by the plan: exchange
     halo::SPDesc* d_sp = nullptr;

@@ -81,16 +81,6 @@ __global__ void step_f_kernel(const SPDesc* __restrict__ sp, const int32_t* __re
 }
 
 // ---- flat: build-time composition of the chains -------------------------------
-__global__ void chain_init_kernel(int32_t* owner, int32_t* parent, int8_t* hop, int8_t* code,
-                                  int64_t n) {
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
-         j += (int64_t)gridDim.x * blockDim.x) {
-        owner[j] = (int32_t)j;
-        parent[j] = -1;
-        hop[j] = -1;
-        code[j] = 0;
-    }
-}
 
 // Pulse p, in ascending order: every received slot inherits its source's owner
 // and boundary crossings, and remembers its source (parent) and pulse.
@@ -102,10 +92,15 @@ __global__ void chain_pulse_kernel(const SPDesc* __restrict__ sp, const int32_t*
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
         const int64_t h = d.dst + i;
         const int64_t src = d.src_base + maps[d.map_off + i];
-        owner[h] = owner[src];
+        // entries below the split are home slots: their own owner, no
+        // crossings; the rest were received (and filled) in earlier pulses.
+        // Home slots' entries of these arrays are never read, so nothing
+        // initialises them.
+        const bool home = i < d.split;
+        owner[h] = home ? (int32_t)src : owner[src];
         parent[h] = (int32_t)src;
         hop[h] = (int8_t)p;
-        code[h] = (int8_t)(code[src] | bit);
+        code[h] = (int8_t)((home ? 0 : code[src]) | bit);
     }
 }
 
@@ -716,7 +711,6 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int rc = HALO_OK;
     do {
         const int gb = blocks_for(nl, pl->num_sms);
-        chain_init_kernel<<<gb, kThreads, 0, st>>>(owner, parent, hop, code, nl);
         for (int p = 0; p < P; p++) {
             const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
             chain_pulse_kernel<<<dim3(gx, nd), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, owner, parent,

@@ -397,3 +397,44 @@ def test_random_problems(seed):
             compare_exchanges(g, o, xyz, reps=1, seed=seed)
     finally:
         g.close()
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_two_plans_on_two_streams(mode):
+    """Two independent systems exchanged concurrently on two streams (20
+    rounds each, interleaved launches): plans share no device state, so both
+    stay bit-identical to the oracle."""
+    import torch
+    sysA = synth.WORKLOADS["water24k_2x4x8"]
+    sysB = synth.WORKLOADS["water48k_2x2x2"]
+    runs = []
+    for w in (sysA, sysB):
+        xyz, dom = synth.system(w)
+        o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+        g = gpu_plan(w.box, w.grid, w.rc, xyz, dom)
+        g.plan.set_mode(mode)
+        want_x = o.load_home(xyz)
+        o.exchange_x(want_x)
+        f0 = synth.forces(o.n_local_total, seed=12)
+        want_f = f0.copy()
+        o.exchange_f(want_f)
+        runs.append(dict(g=g, want_x=want_x, want_f=want_f, f0=torch.from_numpy(f0).cuda(),
+                         stream=torch.cuda.Stream()))
+    try:
+        for r in runs:
+            r["loc"] = r["g"].plan.load_home(r["g"].xyz_d)
+        torch.cuda.synchronize()
+        for _ in range(20):
+            for r in runs:
+                with torch.cuda.stream(r["stream"]):
+                    r["g"].plan.exchange_x(r["loc"], r["stream"])
+                    r["f"] = r["f0"].clone()
+                    r["g"].plan.exchange_f(r["f"], r["stream"])
+        torch.cuda.synchronize()
+        for r in runs:
+            assert r["g"].plan.status(r["stream"]) == 0
+            np.testing.assert_array_equal(bits(r["loc"].cpu().numpy()), bits(r["want_x"]))
+            np.testing.assert_array_equal(bits(r["f"].cpu().numpy()), bits(r["want_f"]))
+    finally:
+        for r in runs:
+            r["g"].close()
