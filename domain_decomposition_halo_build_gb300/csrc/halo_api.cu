@@ -6,6 +6,7 @@
 // y, then np(x) in x) and section 4 (Total Pulses = np(x)+np(y)+np(z)); the
 // device work lives in halo_build.cu and halo_exchange.cu.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <new>
@@ -123,6 +124,10 @@ int halo_setup_ex(const float box[3], const int32_t grid[3], float rc, const flo
     if (!pl) return HALO_ENOMEM;
     int rc_ = HALO_OK;
     pl->flags = flags;
+    if (const char* env = getenv("HALO_WAIT_TIMEOUT_MS")) {
+        const double ms = atof(env);
+        if (ms > 0.0 && isfinite(ms)) pl->wait_timeout_ns = (long long)(ms * 1e6);
+    }
     try {
         rc_ = check_problem(box, grid, rc, pl);
         if (rc_ == HALO_OK && cudaGetDevice(&pl->dev) != cudaSuccess) rc_ = HALO_ECUDA;

@@ -239,7 +239,9 @@ int halo_status(halo_plan* plan, void* stream);
  * kernels never write past the buffer they were given. */
 int halo_debug_set_build_capacity(halo_plan* plan, int64_t slots);
 
-/* Time limit of every device-side wait (default 1 s).  seconds > 0. */
+/* Time limit of every device-side wait.  seconds > 0.  The default of a new
+ * plan is 1 s, or HALO_WAIT_TIMEOUT_MS milliseconds when that environment
+ * variable holds a positive number at halo_setup. */
 int halo_set_wait_timeout(halo_plan* plan, double seconds);
 
 /* Test hook: in the next halo_exchange_x, the producer of (domain, pulse)

@@ -127,3 +127,31 @@ def test_build_buffer_overflow_is_detected_and_retried():
             plan.debug_set_build_capacity(0)
     finally:
         plan.close()
+
+
+def test_wait_timeout_from_the_environment(monkeypatch):
+    """HALO_WAIT_TIMEOUT_MS sets a new plan's wait limit: with 30 ms a dropped
+    signal ends the exchange well before the 1 s default could."""
+    import time
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    monkeypatch.setenv("HALO_WAIT_TIMEOUT_MS", "30")
+    w = synth.WORKLOADS["water24k_2x4x8"]
+    xyz, dom = synth.system(w)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d)
+    try:
+        loc = plan.load_home(x)
+        torch.cuda.synchronize()
+        plan.debug_drop_signal(0, 0)
+        t0 = time.perf_counter()
+        plan.exchange_x(loc)
+        code = plan.status()
+        elapsed = time.perf_counter() - t0
+        assert code == halo.ETIMEOUT
+        assert elapsed < 0.6, elapsed
+        plan.exchange_x(loc)
+        assert plan.status() == halo.OK
+    finally:
+        plan.close()
