@@ -10,12 +10,18 @@ fraction of the dominant kernel.
   python bench.py [--gpus N --steps K --warmup W --workload NAME]
   python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
 
-Timing: CUDA events on the launching stream around every step; the L2 is
-flushed between steps (a write of 2x L2 bytes, then a read of another 2x L2
-buffer so the flush's dirty lines are written back before the next step);
-warm-up steps are untimed.  N > 1: one process per GPU (torchrun), each an
-independent replica of the workload (the path has no cross-GPU exchange on one
-box), barrier + synchronize around the timed loop, max time over ranks.
+Timing (the headline): K back-to-back steps bracketed by one pair of CUDA
+events on the launching stream, with inputs larger than L2: R copies of the
+system (each its own plan, coordinates and forces) are stepped in turn, R
+chosen so that they hold at least 4x the L2 size, so every step reads its
+tables and data from HBM.  The per-kernel split times K back-to-back launches
+of one direction the same way.  Also reported: the same steps one at a time
+with the L2 flushed between them (a write of 2x L2 bytes, then a read of
+another 2x L2 buffer so the flush's dirty lines are written back) and an event
+pair around each.  Warm-up steps are untimed.  N > 1: one process per GPU
+(torchrun), each an independent replica of the workload (the path has no
+cross-GPU exchange on one box), barrier + synchronize around the timed loop,
+max time over ranks.
 """
 from __future__ import annotations
 
@@ -175,6 +181,65 @@ def setup_workload(name, device, prune=False):
     loc = plan.load_home(x)
     f0 = torch.from_numpy(synth.forces(plan.n_local_total, seed=1)).to(device)
     return w, xyz, dom, x, plan, loc, f0
+
+
+def setup_replicas(name, device, l2_multiple=4, prune=False):
+    """R copies of one system (each its own plan, local coordinates and
+    forces), R >= 2 chosen so that their coordinates, forces and exchange
+    bytes add up to at least l2_multiple x the L2 size."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo, synth
+    w, xyz, dom, x, plan, loc, f0 = setup_workload(name, device, prune=prune)
+    per = 24 * plan.n_local_total + (BYTES_X + BYTES_F) * plan.n_halo_total
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    n = max(2, -(-l2_multiple * l2 // per))
+    d = torch.from_numpy(dom).to(device)
+    reps = [(plan, loc, f0.clone())]
+    for _ in range(n - 1):
+        p = halo.HaloPlan(w.box, w.grid, w.rc, x, d, prune=prune)
+        reps.append((p, p.load_home(x), f0.clone()))
+    return w, xyz, dom, x, reps, f0, n * per
+
+
+def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=None):
+    """K back-to-back steps, step i on replica i mod R; one CUDA event pair
+    around all K.  which: "xf" (the step), "x" or "f" (one direction alone).
+    Returns (ms per step, wall seconds, clocks, launches in the timed region)."""
+    import torch
+    R = len(reps)
+
+    def run(i):
+        plan, loc, f = reps[i % R]
+        if "x" in which:
+            plan.exchange_x(loc, stream)
+        if "f" in which:
+            plan.exchange_f(f, stream)
+    for i in range(max(warmup, 1) * R):
+        run(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    l0 = sum(sum(p.launch_counts()) for p, _, _ in reps)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(steps):
+        run(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if barrier:
+        barrier()
+    clocks = sampler.stop() if sampler else None
+    l1 = sum(sum(p.launch_counts()) for p, _, _ in reps)
+    for p, _, _ in reps:
+        code = p.status()
+        if code != 0:
+            raise SystemExit("device error %d during the timed region" % code)
+    return e0.elapsed_time(e1) / steps, wall, clocks, l1 - l0
 
 
 def time_steps(plan, loc, f, steps, warmup, flush, stream, sampler=None, barrier=None,
@@ -696,7 +761,8 @@ def main():
     stream = torch.cuda.current_stream(device)
     barrier = (lambda: dist.barrier()) if dist else None
 
-    w, xyz, dom, x, plan, loc, f0 = setup_workload(args.workload, device)
+    w, xyz, dom, x, reps, f0, rep_bytes = setup_replicas(args.workload, device)
+    plan, loc, _ = reps[0]
     # halo_rebuild of the same system (the build without first-time allocations)
     rb = []
     for _ in range(5):
@@ -707,33 +773,42 @@ def main():
         rb.append(1e3 * (time.perf_counter() - t0))
     build_ms = statistics.median(rb[1:])
     flush, flush_bytes = make_flush(device)
+    peak, peak_kind = measured_peak()
+    halo_slots = plan.n_halo_total
     modes = ["fused", "stepwise", "flat"]
     others = {}
     for mode in [m for m in modes if m != args.mode] + [args.mode]:
-        plan.set_mode(mode)
-        f = f0.clone()
-        sampler = ClockSampler(gpu_index(local)) if mode == args.mode else None
-        steps = args.steps if mode == args.mode else min(args.steps, 500)
-        sts, xs, fs, wall, clocks, launches = time_steps(plan, loc, f, steps, args.warmup, flush,
-                                                         stream, sampler, barrier,
-                                                         split_steps=min(steps, 500))
-        code = plan.status()
-        if code != 0:
-            raise SystemExit("device error %d during the timed region" % code)
-        if mode != args.mode:
-            others[mode] = {"us_per_exchange": 1e3 * statistics.fmean(sts),
-                            "us_x": 1e3 * statistics.fmean(xs), "us_f": 1e3 * statistics.fmean(fs),
-                            "launches_per_step": launches / steps}
-    step_ms = statistics.fmean(sts)
-    x_ms, f_ms = statistics.fmean(xs), statistics.fmean(fs)
+        for p, _, _ in reps:
+            p.set_mode(mode)
+        head = mode == args.mode
+        sampler = ClockSampler(gpu_index(local)) if head else None
+        steps = args.steps if head else min(args.steps, 500)
+        # the timed region: K back-to-back steps over the replicas in turn
+        m_step, m_wall, m_clocks, m_launches = time_rotated(reps, steps, args.warmup, stream, "xf",
+                                                            sampler, barrier)
+        # per-direction split: K back-to-back launches of one direction
+        ksplit = min(steps, 1000)
+        m_x = time_rotated(reps, ksplit, args.warmup, stream, "x")[0]
+        m_f = time_rotated(reps, ksplit, args.warmup, stream, "f")[0]
+        # context: one step at a time with the L2 flushed before each
+        sts, xs, fs, _, _, _ = time_steps(plan, loc, f0.clone(), min(steps, 500), args.warmup, flush,
+                                          stream, split_steps=min(steps, 500))
+        assert plan.status() == 0
+        flushed = {"us_per_exchange": 1e3 * statistics.fmean(sts), "us_x": 1e3 * statistics.fmean(xs),
+                   "us_f": 1e3 * statistics.fmean(fs),
+                   "hbm_frac": (BYTES_X + BYTES_F) * halo_slots / (1e-3 * statistics.fmean(sts)) / 1e9
+                   / peak}
+        if not head:
+            others[mode] = {"us_per_exchange": 1e3 * m_step, "us_x": 1e3 * m_x, "us_f": 1e3 * m_f,
+                            "launches_per_step": m_launches / steps, "per_step_flushed": flushed}
+        else:
+            step_ms, x_ms, f_ms = m_step, m_x, m_f
+            wall, clocks, launches, head_flushed = m_wall, m_clocks, m_launches, flushed
     step_ms, x_ms, f_ms = max_over_ranks([step_ms, x_ms, f_ms], device, dist)
-    halo_slots = plan.n_halo_total
     value = whole_job_rate(halo_slots, world, step_ms * 1e-3)
     for m in others.values():
         m["value"] = world * halo_slots / (m["us_per_exchange"] * 1e-6)
-        m["hbm_frac"] = (BYTES_X + BYTES_F) * halo_slots / (m["us_per_exchange"] * 1e-6) / 1e9 \
-            / measured_peak()[0]
-    peak, peak_kind = measured_peak()
+        m["hbm_frac"] = (BYTES_X + BYTES_F) * halo_slots / (m["us_per_exchange"] * 1e-6) / 1e9 / peak
     kname = {"fused": ("unpack_f_kernel", "pack_x_kernel"), "stepwise": ("step_f_kernel", "step_x_kernel"),
              "flat": ("flat_f_kernel", "flat_x_kernel")}[args.mode]
     dom_kernel, dom_ms, per_slot = ((kname[0], f_ms, BYTES_F) if f_ms >= x_ms
@@ -823,15 +898,23 @@ def main():
                        "grid": list(w.grid),
                        "box_nm": list(w.box), "rc_nm": w.rc, "pulses": plan.n_pulses,
                        "halo_slots": halo_slots, "parallelism": "replicas" if world > 1 else "1 GPU",
-                       "l2": "flushed between steps (%d MB written+read)" % (flush_bytes >> 20)},
+                       "l2": "inputs larger than L2: %d copies of the system (%d MB, %.1fx L2) stepped "
+                             "in turn, back to back" % (len(reps), rep_bytes >> 20,
+                                                        rep_bytes / torch.cuda.get_device_properties(
+                                                            device).L2_cache_size)},
             "us_per_exchange": 1e3 * step_ms, "us_x": 1e3 * x_ms, "us_f": 1e3 * f_ms,
+            "per_step_flushed": dict(head_flushed, note="one step at a time, L2 flushed before each "
+                                     "(%d MB written+read), an event pair around each" % (flush_bytes >> 20)),
             "halo_build_ms": build_ms,
             "algorithmic_gbs": alg_gbs, "hbm_frac": alg_gbs / peak,
             "hbm_frac_nominal_8tbs": alg_gbs / 8000.0,
             "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": per_slot * halo_slots},
+                         "algorithmic_bytes_per_launch": per_slot * halo_slots,
+                         "us_per_launch": 1e3 * dom_ms,
+                         "timing": "CUDA events around %d back-to-back launches of this kernel alone, "
+                                   "over the copies of the system in turn" % min(args.steps, 1000)},
             "other_modes": others,
             "cuda_graph": graph,
             "l2_warm_case": warm,
@@ -850,7 +933,8 @@ def main():
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line))
-    plan.close()
+    for p, _, _ in reps:
+        p.close()
     if dist:
         dist.barrier()
         dist.destroy_process_group()

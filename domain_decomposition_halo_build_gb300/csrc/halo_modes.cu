@@ -346,14 +346,15 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
                                                           float L1, float L2, int64_t n_slots,
                                                           int* err) {
     grid_launch_dependents();
-    int4 it = items[blockIdx.x];
-    if (!in_range((int64_t)it.y + it.z - 1, n_slots, err)) it.z = 0;
+    // block b's table entries start at b * 256 * E (the table is padded per
+    // chunk), so they load alongside the item instead of after it; entries
+    // at or past the item's count are padding and never used
     int32_t v[E];
 #pragma unroll
-    for (int e = 0; e < E; e++) {
-        const int i = threadIdx.x + e * kThreads;
-        v[e] = i < it.z ? __ldg(xflat + it.x + i) : 0;
-    }
+    for (int e = 0; e < E; e++)
+        v[e] = __ldg(xflat + (int64_t)blockIdx.x * (kThreads * E) + threadIdx.x + e * kThreads);
+    int4 it = items[blockIdx.x];
+    if (!in_range((int64_t)it.y + it.z - 1, n_slots, err)) it.z = 0;
     // the chunk and its codes are plan tables; coordinates only after the wait
     grid_dependency_wait();
     float a[E][3];
@@ -510,6 +511,10 @@ __device__ __forceinline__ int checked_copies(int32_t home, int k, const int32_t
 #endif
 }
 
+// class-A owners per thread: a tile is kFlatA * kThreads owners (at 2 the
+// kernel needs 56 registers; 3 and 4 need 80 and 114 and fit fewer blocks)
+constexpr int kFlatA = 2;
+
 template <int KB, int KW>
 __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* __restrict__ recA,
                                                           int64_t nA, const int4* __restrict__ recB,
@@ -518,9 +523,9 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
                                                           int64_t n_slots, int64_t n_fent, int* err) {
     // blocks [0, tilesBC) take classes B and C, one owner per thread (the
     // longer trees start first); the following blocks take class-A tiles of
-    // 2 * blockDim owners, two per thread (coalesced record loads), so both
-    // kinds of trees run side by side
-    const int64_t tilesA = (nA + 2 * kThreads - 1) / (2 * kThreads);
+    // kFlatA * blockDim owners, kFlatA per thread (coalesced record loads), so
+    // both kinds of trees run side by side
+    const int64_t tilesA = (nA + kFlatA * kThreads - 1) / (kFlatA * kThreads);
     const int64_t tilesBC = (nB + nC + kThreads - 1) / kThreads;
     const int64_t n = nA + nB + nC;
     grid_launch_dependents();
@@ -532,17 +537,23 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
     if (bb >= tilesA + tilesBC) return;
     {
         if (bb >= tilesBC) {
-            const int64_t b = bb - tilesBC;
-            const int64_t m0 = b * 2 * kThreads + threadIdx.x, m1 = m0 + kThreads;
-            const int4 r0 = m0 < nA ? __ldg(recA + m0) : make_int4(0, 0, 0, 0);
-            const int4 r1 = m1 < nA ? __ldg(recA + m1) : make_int4(0, 0, 0, 0);
-            const int32_t home[2] = {r0.x & kNodeMask, r1.x & kNodeMask};
-            const int32_t ent[2][3] = {{r0.y, r0.z, r0.w}, {r1.y, r1.z, r1.w}};
-            const int kk[2] = {
-                m0 < nA ? checked_copies<3>(home[0], (int)((unsigned)r0.x >> kNodeBits), ent[0], n_slots, err) : 0,
-                m1 < nA ? checked_copies<3>(home[1], (int)((unsigned)r1.x >> kNodeBits), ent[1], n_slots, err) : 0};
+            const int64_t m0 = (bb - tilesBC) * kFlatA * kThreads + threadIdx.x;
+            int32_t home[kFlatA], ent[kFlatA][3];
+            int kk[kFlatA];
+#pragma unroll
+            for (int e = 0; e < kFlatA; e++) {
+                const int64_t m = m0 + e * kThreads;
+                const int4 r = m < nA ? __ldg(recA + m) : make_int4(0, 0, 0, 0);
+                home[e] = r.x & kNodeMask;
+                ent[e][0] = r.y;
+                ent[e][1] = r.z;
+                ent[e][2] = r.w;
+                kk[e] = m < nA ? checked_copies<3>(home[e], (int)((unsigned)r.x >> kNodeBits), ent[e],
+                                                   n_slots, err)
+                               : 0;
+            }
             grid_dependency_wait();
-            reduce_trees<3, 2>(f, home, kk, ent);
+            reduce_trees<3, kFlatA>(f, home, kk, ent);
             return;
         }
         const int64_t m = nA + bb * kThreads + threadIdx.x;
@@ -662,15 +673,16 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     while (E > 1 && H / (kThreads * E) < 4 * (int64_t)pl->num_sms) E /= 2;
     pl->flat_x_e = E;
     const int kFlatChunk = kThreads * E;
+    // item b = {table offset b * kFlatChunk, first halo slot, count}: the
+    // table is padded to whole chunks so a block can address its entries
+    // from its index alone
     std::vector<int4> items;
-    int64_t k = 0;
     for (int D = 0; D < nd; D++) {
         const int64_t d0 = pl->base[D] + pl->n_home[D];
         const int64_t nh = (int64_t)pl->n_local[D] - pl->n_home[D];
         for (int64_t i = 0; i < nh; i += kFlatChunk)
-            items.push_back(make_int4((int)(k + i), (int)(d0 + i),
+            items.push_back(make_int4((int)(items.size() * kFlatChunk), (int)(d0 + i),
                                       (int)std::min<int64_t>(kFlatChunk, nh - i), 0));
-        k += nh;
     }
     pl->n_xflat_items = (int)items.size();
     HALO_TRY(dev_reserve(&pl->d_xflat_items, &pl->cap_xflat_items, (int64_t)items.size()));
@@ -688,7 +700,8 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, stage, items.size() * sizeof(int4),
                                   cudaMemcpyHostToDevice, st));
     }
-    HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat, H));
+    HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat,
+                         std::max<int64_t>((int64_t)items.size() * kFlatChunk, 1)));
     HALO_TRY(dev_reserve(&pl->d_fent, &pl->cap_fent, H));
 
     // scratch of the table build, carved from two pools kept in the plan
@@ -827,8 +840,8 @@ int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
 
 int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st) {
     if (pl->n_owners == 0) return HALO_OK;
-    // class A goes two owners per thread, classes B and C one per thread
-    const int64_t tilesA = (pl->n_rec[0] + 2 * kThreads - 1) / (2 * kThreads);
+    // class A goes kFlatA owners per thread, classes B and C one per thread
+    const int64_t tilesA = (pl->n_rec[0] + kFlatA * kThreads - 1) / (kFlatA * kThreads);
     const int64_t tilesBC = (pl->n_rec[1] + pl->n_rec[2] + kThreads - 1) / kThreads;
     const int gb = (int)std::max<int64_t>(1, tilesA + tilesBC);
     auto* k = pl->max_copies <= 7 ? flat_f_kernel<7, 0> : pl->max_copies <= 11 ? flat_f_kernel<11, 0>
