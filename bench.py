@@ -483,6 +483,37 @@ def overlap_case(plan, loc, f, steps, warmup, flush, mode, device, priority=0):
             "local_stand_in": "bf16 matmul 2048x4096x4096 on a second stream"}
 
 
+def configs_case(mode, device, stream, flush, steps, warmup):
+    """Every configuration of the workload table in one mode: one step at a
+    time after an L2 flush (event pair around each step and, in a second
+    pass, around each direction), and back to back on one copy (the small
+    systems stay in L2, as they would in an MD step)."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import synth
+    out = []
+    for name in synth.WORKLOADS:
+        w, xyz, dom, x, plan, loc, f0 = setup_workload(name, device)
+        plan.set_mode(mode)
+        f = f0.clone()
+        n = steps if plan.n_halo_total < 10_000_000 else max(steps // 4, 20)
+        sts, xs, fs, _, _, launches = time_steps(plan, loc, f, n, warmup, flush, stream,
+                                                 split_steps=min(n, 200))
+        b2b = time_rotated([(plan, loc, f)], n, warmup, stream, "xf")[0]
+        assert plan.status() == 0
+        us = 1e3 * statistics.fmean(sts)
+        out.append({"workload": name, "n_atoms": w.n_atoms, "grid": list(w.grid), "pulses": plan.n_pulses,
+                    "halo_slots": plan.n_halo_total, "us_per_exchange": us,
+                    "us_x": 1e3 * statistics.fmean(xs), "us_f": 1e3 * statistics.fmean(fs),
+                    "launches_per_direction": launches / (2 * n),
+                    "halo_atoms_per_s": plan.n_halo_total / (us * 1e-6),
+                    "us_per_exchange_back_to_back_one_copy": 1e3 * b2b})
+        plan.close()
+        del loc, f, f0, x
+        torch.cuda.synchronize()
+    return {"mode": mode, "timing": "one step at a time after an L2 flush; back to back on one copy "
+                                    "beside it", "configs": out}
+
+
 def pruned_case(name, mode, device, stream, flush, steps, warmup, unpruned_slots):
     """The same system built with corner pruning (HALO_SETUP_PRUNE_CORNERS):
     fewer halo slots, the same exchanges."""
@@ -876,6 +907,7 @@ def main():
         graph[mode] = {"us_per_exchange": 1e3 * statistics.fmean(gs)}
     plan.set_mode(args.mode)
 
+    all_configs = configs_case(args.mode, device, stream, flush, min(args.steps, 300), args.warmup)
     rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
     pruned.append(pruned_case(REBUILD_WORKLOAD, args.mode, device, stream, flush,
                               min(args.steps, 300), args.warmup, rebuild["halo_slots"]))
@@ -926,6 +958,7 @@ def main():
             "cuda_graph": graph,
             "l2_warm_case": warm,
             "latency_case": lat,
+            "all_configs": all_configs,
             "pruned_case": pruned,
             "rebuild_case": rebuild,
             "overlap_case": overlap,
