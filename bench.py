@@ -58,7 +58,8 @@ def measured_peak():
 
 KERNEL_SOURCE = {"pack_x_kernel": "halo_exchange.cu", "unpack_f_kernel": "halo_exchange.cu",
                  "step_x_kernel": "halo_modes.cu", "step_f_kernel": "halo_modes.cu",
-                 "flat_x_kernel": "halo_modes.cu", "flat_f_kernel": "halo_modes.cu"}
+                 "flat_x_kernel": "halo_modes.cu", "flat_f_kernel": "halo_modes.cu",
+                 "staged_pack_x_kernel": "halo_modes.cu", "staged_unpack_f_kernel": "halo_modes.cu"}
 
 
 def source_digest(kernel):
@@ -770,7 +771,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--mode", default="flat", choices=["fused", "stepwise", "flat"],
+    ap.add_argument("--mode", default="flat", choices=["fused", "stepwise", "flat", "staged"],
                     help="exchange mode of the headline value; every mode is also reported")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -813,7 +814,7 @@ def main():
     flush, flush_bytes = make_flush(device)
     peak, peak_kind = measured_peak()
     halo_slots = plan.n_halo_total
-    modes = ["fused", "stepwise", "flat"]
+    modes = ["staged", "fused", "stepwise", "flat"]
     others = {}
     for mode in [m for m in modes if m != args.mode] + [args.mode]:
         for p, _, _ in reps:
@@ -848,6 +849,7 @@ def main():
         m["value"] = world * halo_slots / (m["us_per_exchange"] * 1e-6)
         m["hbm_frac"] = (BYTES_X + BYTES_F) * halo_slots / (m["us_per_exchange"] * 1e-6) / 1e9 / peak
     kname = {"fused": ("unpack_f_kernel", "pack_x_kernel"), "stepwise": ("step_f_kernel", "step_x_kernel"),
+             "staged": ("staged_unpack_f_kernel", "staged_pack_x_kernel"),
              "flat": ("flat_f_kernel", "flat_x_kernel")}[args.mode]
     dom_kernel, dom_ms, per_slot = ((kname[0], f_ms, BYTES_F) if f_ms >= x_ms
                                     else (kname[1], x_ms, BYTES_X))
@@ -900,7 +902,7 @@ def main():
 
     # the same step captured as a CUDA graph (one graph launch per x + f)
     graph = {}
-    for mode in (args.mode, "fused"):
+    for mode in [m for m in (args.mode, "fused") if m != "staged"]:  # staged cannot be captured
         plan.set_mode(mode)
         gs = time_graph_steps(plan, loc, f0.clone(), min(args.steps, 1000), args.warmup, flush, stream)
         assert plan.status() == 0

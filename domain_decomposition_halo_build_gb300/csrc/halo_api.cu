@@ -97,6 +97,7 @@ int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, 
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
     HALO_TRY(halo::prepare_exchange(pl, st));
     if (pl->mode == HALO_MODE_FLAT) HALO_TRY(halo::prepare_flat(pl, st));
+    if (pl->mode == HALO_MODE_STAGED) HALO_TRY(halo::prepare_staged(pl));
     pl->valid = true;
     return HALO_OK;
 }
@@ -249,6 +250,7 @@ int halo_exchange_x(halo_plan* pl, float* local_coords, void* stream) {
     switch (pl->mode) {
         case HALO_MODE_STEPWISE: return halo::launch_stepwise_x(pl, local_coords, as_stream(stream));
         case HALO_MODE_FLAT: return halo::launch_flat_x(pl, local_coords, as_stream(stream));
+        case HALO_MODE_STAGED: return halo::launch_staged_x(pl, local_coords, as_stream(stream));
         default: return halo::launch_exchange_x(pl, local_coords, as_stream(stream));
     }
 }
@@ -260,6 +262,7 @@ int halo_exchange_f(halo_plan* pl, float* local_forces, void* stream) {
     switch (pl->mode) {
         case HALO_MODE_STEPWISE: return halo::launch_stepwise_f(pl, local_forces, as_stream(stream));
         case HALO_MODE_FLAT: return halo::launch_flat_f(pl, local_forces, as_stream(stream));
+        case HALO_MODE_STAGED: return halo::launch_staged_f(pl, local_forces, as_stream(stream));
         default: return halo::launch_exchange_f(pl, local_forces, as_stream(stream));
     }
 }
@@ -305,15 +308,15 @@ int halo_debug_drop_signal(halo_plan* pl, int32_t domain, int32_t pulse) {
 
 int halo_set_mode(halo_plan* pl, int32_t mode, void* stream) {
     if (!pl) return HALO_EINVAL;
-    if (mode != HALO_MODE_FUSED && mode != HALO_MODE_STEPWISE && mode != HALO_MODE_FLAT)
+    if (mode != HALO_MODE_FUSED && mode != HALO_MODE_STEPWISE && mode != HALO_MODE_FLAT &&
+        mode != HALO_MODE_STAGED)
         return HALO_EINVAL;
     DeviceGuard g(pl->dev);
-    if (mode == HALO_MODE_FLAT && !pl->flat_ready) {
-        try {
-            HALO_TRY(halo::prepare_flat(pl, as_stream(stream)));
-        } catch (const std::bad_alloc&) {
-            return HALO_ENOMEM;
-        }
+    try {
+        if (mode == HALO_MODE_FLAT && !pl->flat_ready) HALO_TRY(halo::prepare_flat(pl, as_stream(stream)));
+        if (mode == HALO_MODE_STAGED) HALO_TRY(halo::prepare_staged(pl));
+    } catch (const std::bad_alloc&) {
+        return HALO_ENOMEM;
     }
     pl->mode = mode;
     return HALO_OK;

@@ -152,6 +152,9 @@ struct halo_plan {
     int4* d_frec[3] = {nullptr, nullptr, nullptr};  // owner records: A (<=3), B (<=11), C (more)
     int64_t n_rec[3] = {0, 0, 0};
     int flat_x_e = 4;                // entries per thread of the flat coordinate kernel
+    // staged (MPI-era) mode: one send/receive buffer element per halo slot
+    float* d_stage_buf = nullptr;
+    int64_t cap_stage_buf = 0, n_stage_buf = 0;
 };
 
 namespace halo {
@@ -168,6 +171,9 @@ int prepare_flat(halo_plan* pl, cudaStream_t st);
 void free_flat(halo_plan* pl);
 int launch_stepwise_x(halo_plan* pl, float* xyz, cudaStream_t st);
 int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st);
+int prepare_staged(halo_plan* pl);
+int launch_staged_x(halo_plan* pl, float* xyz, cudaStream_t st);
+int launch_staged_f(halo_plan* pl, float* f, cudaStream_t st);
 int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st);
 int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st);
 

@@ -1,13 +1,15 @@
-// halo_modes.cu -- two more ways to run the same exchange on one GPU.
+// halo_modes.cu -- three more ways to run the same exchange on one GPU.
 //
 // STEPWISE: one kernel launch per pulse and direction, in pulse order for
-// coordinates and reverse pulse order for forces, ordered by the stream alone.
-// This is the shape of the GPU-aware-MPI schedule the page "GPU-Initiated Halo
-// Exchange Cuts CPU Bottlenecks in GROMACS" describes (section "The CPU
-// bottleneck in halo exchange": a pack kernel per pulse, pulses chained Z -> Y
-// -> X) and of the first fused design ("Fusing pack, put, and wait into one
-// kernel": one kernel per pulse, stream-ordered), without the MPI transfers that
-// one GPU does not need.
+// coordinates and reverse pulse order for forces, ordered by the stream alone:
+// the first fused design of the page "GPU-Initiated Halo Exchange Cuts CPU
+// Bottlenecks in GROMACS" (section "Fusing pack, put, and wait into one
+// kernel": one kernel per pulse, stream-ordered).
+//
+// STAGED: the GPU-aware-MPI schedule that page starts from (section "The CPU
+// bottleneck in halo exchange"): per pulse, pulses chained Z -> Y -> X, a pack
+// kernel into a send buffer, a host wait, the transfer (one kernel standing in
+// for every domain's message), a host wait; forces the other way round.
 //
 // FLAT: because every domain lives in the same HBM, each halo slot's forwarding
 // chain (page "Redesigning GROMACS Halo Exchange ...", section 3: eighth-shell
@@ -73,6 +75,64 @@ __global__ void step_f_kernel(const SPDesc* __restrict__ sp, const int32_t* __re
         if (!in_range(d.src_base + m, n_slots, err) || !in_range(d.dst + i, n_slots, err)) continue;
         const float* h = f + 3 * (d.dst + i);
         float* o = f + 3 * (d.src_base + m);
+        const float h0 = h[0], h1 = h[1], h2 = h[2];
+        o[0] = o[0] + h0;
+        o[1] = o[1] + h1;
+        o[2] = o[2] + h2;
+    }
+}
+
+// ---- staged (MPI-era) -----------------------------------------------------------
+// Per pulse, as the GPU-aware-MPI schedule runs it: a pack kernel gathers the
+// sender's entries (shifted) into a send buffer; the host waits for it; a
+// transfer moves every sender's buffer slice into its receiver's halo slice
+// (the MPI message; all ranks' messages of the pulse in one launch); the host
+// waits for the transfer before the next pulse.  Forces run the other way,
+// last pulse first: the transfer copies each receiver's halo slice into the
+// buffer, the host waits, the unpack kernel adds it into the sender's mapped
+// slots, the host waits.  The buffer slice of (s, p) sits at the map's own
+// offset (the maps tile the halo slots pulse by pulse), so the buffer has one
+// 12-byte element per halo slot.
+__global__ void staged_pack_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
+                                     const float* __restrict__ xyz, float* __restrict__ buf, int P,
+                                     int p, int64_t n_slots, int64_t n_buf, int* err) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
+        const int64_t m = d.src_base + maps[d.map_off + i];
+        if (!in_range(m, n_slots, err) || !in_range(d.map_off + i, n_buf, err)) continue;
+        const float* s = xyz + 3 * m;
+        float* b = buf + 3 * (d.map_off + i);
+        b[0] = s[0] + d.shift[0];
+        b[1] = s[1] + d.shift[1];
+        b[2] = s[2] + d.shift[2];
+    }
+}
+
+// TO_HALO: buffer slice -> receiver's halo slice (coordinates); else the
+// halo slice -> buffer slice (forces).
+template <bool TO_HALO>
+__global__ void staged_move_kernel(const SPDesc* __restrict__ sp, float* local, float* buf, int P, int p,
+                                   int64_t n_slots, int64_t n_buf, int* err) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    const int n = 3 * d.send;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n; j += gridDim.x * blockDim.x) {
+        if (!in_range(d.dst + j / 3, n_slots, err) || !in_range(d.map_off + j / 3, n_buf, err)) continue;
+        if (TO_HALO)
+            local[3 * d.dst + j] = buf[3 * d.map_off + j];
+        else
+            buf[3 * d.map_off + j] = local[3 * d.dst + j];
+    }
+}
+
+__global__ void staged_unpack_f_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
+                                       float* f, const float* __restrict__ buf, int P, int p,
+                                       int64_t n_slots, int64_t n_buf, int* err) {
+    const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
+        const int64_t m = d.src_base + maps[d.map_off + i];
+        if (!in_range(m, n_slots, err) || !in_range(d.map_off + i, n_buf, err)) continue;
+        const float* h = buf + 3 * (d.map_off + i);
+        float* o = f + 3 * m;
         const float h0 = h[0], h1 = h[1], h2 = h[2];
         o[0] = o[0] + h0;
         o[1] = o[1] + h1;
@@ -641,6 +701,8 @@ int blocks_for(int64_t n, int num_sms) {
 }  // namespace
 
 void free_flat(halo_plan* pl) {
+    dev_free(pl->d_stage_buf);
+    pl->cap_stage_buf = pl->n_stage_buf = 0;
     dev_free(pl->d_xflat);
     dev_free(pl->d_xflat_items);
     dev_free(pl->d_fown);
@@ -822,6 +884,47 @@ int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st) {
                                                pl->P, p, pl->n_local_total, pl->d_err);
         if (e != cudaSuccess) return cuda_code(e);
         pl->launches_f++;
+    }
+    return cuda_code(cudaGetLastError());
+}
+
+int prepare_staged(halo_plan* pl) {
+    int64_t n = 0;
+    for (const SPDesc& d : pl->sp) n = std::max<int64_t>(n, d.map_off + d.send);
+    pl->n_stage_buf = n;
+    return dev_reserve(&pl->d_stage_buf, &pl->cap_stage_buf, std::max<int64_t>(3 * n, 1));
+}
+
+int launch_staged_x(halo_plan* pl, float* xyz, cudaStream_t st) {
+    if (!pl->d_stage_buf) return HALO_EINVAL;
+    for (int p = 0; p < pl->P; p++) {
+        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+        staged_pack_x_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(
+            pl->d_sp, pl->d_maps, xyz, pl->d_stage_buf, pl->P, p, pl->n_local_total, pl->n_stage_buf,
+            pl->d_err);
+        pl->launches_x++;
+        HALO_CUDA(cudaStreamSynchronize(st));  // the host waits for the send buffer
+        staged_move_kernel<true><<<dim3(std::min(3 * gx, 1024u), pl->n_dom), kThreads, 0, st>>>(
+            pl->d_sp, xyz, pl->d_stage_buf, pl->P, p, pl->n_local_total, pl->n_stage_buf, pl->d_err);
+        pl->launches_x++;
+        HALO_CUDA(cudaStreamSynchronize(st));  // and for the message before the next pulse
+    }
+    return cuda_code(cudaGetLastError());
+}
+
+int launch_staged_f(halo_plan* pl, float* f, cudaStream_t st) {
+    if (!pl->d_stage_buf) return HALO_EINVAL;
+    for (int p = pl->P - 1; p >= 0; p--) {
+        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+        staged_move_kernel<false><<<dim3(std::min(3 * gx, 1024u), pl->n_dom), kThreads, 0, st>>>(
+            pl->d_sp, f, pl->d_stage_buf, pl->P, p, pl->n_local_total, pl->n_stage_buf, pl->d_err);
+        pl->launches_f++;
+        HALO_CUDA(cudaStreamSynchronize(st));  // the message has arrived
+        staged_unpack_f_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(
+            pl->d_sp, pl->d_maps, f, pl->d_stage_buf, pl->P, p, pl->n_local_total, pl->n_stage_buf,
+            pl->d_err);
+        pl->launches_f++;
+        HALO_CUDA(cudaStreamSynchronize(st));  // unpacked before the next pulse's send
     }
     return cuda_code(cudaGetLastError());
 }

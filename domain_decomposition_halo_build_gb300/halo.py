@@ -25,8 +25,8 @@ OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM, ESCRA
 NOALLOC_MAX_COUNTERS = 16384
 MAX_PULSES = 64
 SETUP_PRUNE_CORNERS = 1
-MODE_FUSED, MODE_STEPWISE, MODE_FLAT = 0, 1, 2
-MODES = {"fused": MODE_FUSED, "stepwise": MODE_STEPWISE, "flat": MODE_FLAT}
+MODE_FUSED, MODE_STEPWISE, MODE_FLAT, MODE_STAGED = 0, 1, 2, 3
+MODES = {"fused": MODE_FUSED, "stepwise": MODE_STEPWISE, "flat": MODE_FLAT, "staged": MODE_STAGED}
 
 
 class HaloError(RuntimeError):
@@ -324,7 +324,7 @@ class HaloPlan:
         return x.value, f.value
 
     def set_mode(self, mode, stream=None):
-        """'fused' (default), 'stepwise' or 'flat' (or a MODE_* value)."""
+        """'fused' (default), 'stepwise', 'flat' or 'staged' (or a MODE_* value)."""
         m = MODES[mode] if isinstance(mode, str) else int(mode)
         _check(self._lib.halo_set_mode(self._h, m, _stream_handle(stream)), "halo_set_mode")
 

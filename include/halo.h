@@ -65,10 +65,11 @@ extern "C" {
 #define HALO_ENOMEM (-8)    /* device or host allocation failed */
 #define HALO_ESCRATCH (-9)  /* the plan needs more counters than halo_exchange_x_noalloc's fixed array */
 
-/* Exchange modes (halo_set_mode).  All three compute bit-identical results. */
+/* Exchange modes (halo_set_mode).  All four compute bit-identical results. */
 #define HALO_MODE_FUSED 0    /* one launch per direction, per-(domain, pulse) signals (default) */
 #define HALO_MODE_STEPWISE 1 /* one launch per pulse and direction, ordered by the stream */
 #define HALO_MODE_FLAT 2     /* forwarding chains composed at build time, one wait-free pass */
+#define HALO_MODE_STAGED 3   /* MPI-era baseline: pack, host wait, transfer, host wait per pulse */
 
 #define HALO_MAX_PULSES 64
 #define HALO_MAX_DOMAINS 4096
@@ -216,8 +217,17 @@ int halo_exchange_f(halo_plan* plan, float* local_forces, void* stream);
  *   FUSED: the pages' design (Algorithms 3-6): one launch per direction; the
  *     entries below depOffset stream at once, forwarded entries wait on
  *     per-(domain, pulse) release/acquire counters.
- *   STEPWISE: one launch per pulse and direction (the MPI-era schedule without
- *     the transfers); P launches per call.
+ *   STEPWISE: one launch per pulse and direction (the pages' first design,
+ *     one kernel per pulse ordered by the stream); P launches per call.
+ *   STAGED: the GPU-aware-MPI schedule the page "GPU-Initiated Halo Exchange
+ *     Cuts CPU Bottlenecks in GROMACS" starts from (section "The CPU
+ *     bottleneck in halo exchange"): per pulse a pack kernel into a send
+ *     buffer, a host wait, a transfer kernel standing in for the MPI
+ *     messages of all domains, a host wait (forces: transfer, wait, unpack
+ *     kernel, wait; last pulse first).  2P launches and 2P stream
+ *     synchronisations per call, so the calls block the host and cannot be
+ *     captured in a CUDA graph.  Needs a buffer of 12 bytes per halo slot
+ *     (allocated here and by halo_rebuild).
  *   FLAT: every halo slot's forwarding chain composed at build time (owner,
  *     periodic shift; per owner the tree of its copies in reverse creation
  *     order); one launch per direction with no waits.  Needs extra tables

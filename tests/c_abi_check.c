@@ -87,10 +87,11 @@ static int run_modes(void) {
     CU(cudaMalloc((void**)&d_gid, sizeof(int32_t) * nl));
     float* f0 = (float*)malloc(sizeof(float) * 3 * nl);
     for (int64_t i = 0; i < 3 * nl; i++) f0[i] = (float)((int)(lcg01() * 17.0) - 8);
-    float* loc[3];
-    float* fr[3];
-    const int32_t modes[3] = {HALO_MODE_FUSED, HALO_MODE_STEPWISE, HALO_MODE_FLAT};
-    for (int m = 0; m < 3; m++) {
+    enum { NM = 4 };
+    float* loc[NM];
+    float* fr[NM];
+    const int32_t modes[NM] = {HALO_MODE_FUSED, HALO_MODE_STEPWISE, HALO_MODE_FLAT, HALO_MODE_STAGED};
+    for (int m = 0; m < NM; m++) {
         HL(halo_set_mode(plan, modes[m], NULL));
         HL(halo_load_home(plan, d_xyz, d_loc, NULL));
         HL(halo_exchange_x(plan, d_loc, NULL));
@@ -102,7 +103,7 @@ static int run_modes(void) {
         CU(cudaMemcpy(loc[m], d_loc, sizeof(float) * 3 * nl, cudaMemcpyDeviceToHost));
         CU(cudaMemcpy(fr[m], d_f, sizeof(float) * 3 * nl, cudaMemcpyDeviceToHost));
     }
-    for (int m = 1; m < 3; m++) {
+    for (int m = 1; m < NM; m++) {
         CHECK(memcmp(loc[0], loc[m], sizeof(float) * 3 * nl) == 0, "coordinates differ between modes");
         CHECK(memcmp(fr[0], fr[m], sizeof(float) * 3 * nl) == 0, "forces differ between modes");
     }
@@ -129,7 +130,7 @@ static int run_modes(void) {
     for (int64_t i = 0; i < 3 * n; i++) CHECK((double)out[i] == want[i], "per-atom force");
 
     halo_destroy(plan);
-    for (int m = 0; m < 3; m++) {
+    for (int m = 0; m < NM; m++) {
         free(loc[m]);
         free(fr[m]);
     }

@@ -35,7 +35,7 @@ def main():
             f0 = synth.forces(o.n_local_total, seed=3)
             want_f = f0.copy()
             o.exchange_f(want_f)
-            for mode in ("fused", "stepwise", "flat"):
+            for mode in ("fused", "stepwise", "flat", "staged"):
                 g.plan.set_mode(mode)
                 loc = g.plan.load_home(g.xyz_d)
                 g.plan.exchange_x(loc)
