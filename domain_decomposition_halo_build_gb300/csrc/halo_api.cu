@@ -205,6 +205,7 @@ int halo_get_pulse(const halo_plan* pl, int32_t domain, int32_t pulse, halo_puls
     for (int e = 0; e < 3; e++) out->coord_shift[e] = d.shift[e];
     if (index_map && d.send > 0) {
         DeviceGuard g(pl->dev);
+        if (!g.ok) return HALO_ECUDA;
         HALO_CUDA(cudaMemcpy(index_map, pl->d_maps + d.map_off, sizeof(int32_t) * d.send,
                              cudaMemcpyDeviceToHost));
     }
@@ -219,6 +220,7 @@ int halo_get_index_maps(const halo_plan* pl, int32_t* maps, int64_t* offsets) {
     offsets[(size_t)P * nd] = pl->n_halo_total;
     if (pl->n_halo_total > 0) {
         DeviceGuard g(pl->dev);
+        if (!g.ok) return HALO_ECUDA;
         HALO_CUDA(cudaMemcpy(maps, pl->d_maps, sizeof(int32_t) * (size_t)pl->n_halo_total,
                              cudaMemcpyDeviceToHost));
     }
@@ -228,18 +230,21 @@ int halo_get_index_maps(const halo_plan* pl, int32_t* maps, int64_t* offsets) {
 int halo_local_to_global(const halo_plan* pl, int32_t* out, void* stream) {
     if (!pl || !out || !pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
     return halo::launch_local_to_global(pl, out, as_stream(stream));
 }
 
 int halo_load_home(const halo_plan* pl, const float* global_xyz, float* local_xyz, void* stream) {
     if (!pl || !global_xyz || !local_xyz || !pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
     return halo::launch_load_home(pl, global_xyz, local_xyz, as_stream(stream));
 }
 
 int halo_store_home(const halo_plan* pl, const float* local_xyz, float* global_xyz, void* stream) {
     if (!pl || !global_xyz || !local_xyz || !pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
     return halo::launch_store_home(pl, local_xyz, global_xyz, as_stream(stream));
 }
 
@@ -247,6 +252,7 @@ int halo_exchange_x(halo_plan* pl, float* local_coords, void* stream) {
     if (!pl || !local_coords || ((uintptr_t)local_coords & 3u)) return HALO_EINVAL;
     if (!pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
     switch (pl->mode) {
         case HALO_MODE_STEPWISE: return halo::launch_stepwise_x(pl, local_coords, as_stream(stream));
         case HALO_MODE_FLAT: return halo::launch_flat_x(pl, local_coords, as_stream(stream));
@@ -259,6 +265,7 @@ int halo_exchange_f(halo_plan* pl, float* local_forces, void* stream) {
     if (!pl || !local_forces || ((uintptr_t)local_forces & 3u)) return HALO_EINVAL;
     if (!pl->valid) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
     switch (pl->mode) {
         case HALO_MODE_STEPWISE: return halo::launch_stepwise_f(pl, local_forces, as_stream(stream));
         case HALO_MODE_FLAT: return halo::launch_flat_f(pl, local_forces, as_stream(stream));
@@ -270,6 +277,7 @@ int halo_exchange_f(halo_plan* pl, float* local_forces, void* stream) {
 int halo_status(halo_plan* pl, void* stream) {
     if (!pl) return HALO_EINVAL;
     DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
     const cudaStream_t st = as_stream(stream);
     HALO_CUDA(cudaStreamSynchronize(st));
     HALO_CUDA(cudaGetLastError());
@@ -312,6 +320,7 @@ int halo_set_mode(halo_plan* pl, int32_t mode, void* stream) {
         mode != HALO_MODE_STAGED)
         return HALO_EINVAL;
     DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
     try {
         if (mode == HALO_MODE_FLAT && !pl->flat_ready) HALO_TRY(halo::prepare_flat(pl, as_stream(stream)));
         if (mode == HALO_MODE_STAGED) HALO_TRY(halo::prepare_staged(pl));
