@@ -95,7 +95,9 @@ int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, 
     pl->trace_cap = 0;
     pl->flat_ready = false;  // the flattened tables describe the previous plan
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
-    HALO_TRY(halo::prepare_exchange(pl, st));
+    HALO_TRY(halo::prepare_common(pl, st));
+    // each mode's own tables; the others are built when a mode is selected
+    if (pl->mode == HALO_MODE_FUSED) HALO_TRY(halo::prepare_fused(pl, st));
     if (pl->mode == HALO_MODE_FLAT) HALO_TRY(halo::prepare_flat(pl, st));
     if (pl->mode == HALO_MODE_STAGED) HALO_TRY(halo::prepare_staged(pl));
     pl->valid = true;
@@ -321,7 +323,11 @@ int halo_set_mode(halo_plan* pl, int32_t mode, void* stream) {
         return HALO_EINVAL;
     DeviceGuard g(pl->dev);
     if (!g.ok) return HALO_ECUDA;
+    const bool build = (mode == HALO_MODE_FUSED && !pl->fused_ready) ||
+                       (mode == HALO_MODE_FLAT && !pl->flat_ready) || mode == HALO_MODE_STAGED;
+    if (build && !pl->valid) return HALO_EINVAL;  // a failed rebuild: nothing to build from
     try {
+        if (mode == HALO_MODE_FUSED && !pl->fused_ready) HALO_TRY(halo::prepare_fused(pl, as_stream(stream)));
         if (mode == HALO_MODE_FLAT && !pl->flat_ready) HALO_TRY(halo::prepare_flat(pl, as_stream(stream)));
         if (mode == HALO_MODE_STAGED) HALO_TRY(halo::prepare_staged(pl));
     } catch (const std::bad_alloc&) {
@@ -344,14 +350,14 @@ int halo_set_trace(halo_plan* pl, uint64_t* trace, int64_t capacity_items) {
         pl->trace_cap = 0;
         return HALO_OK;
     }
-    if (capacity_items < (int64_t)pl->n_items_x + pl->n_items_f) return HALO_EINVAL;
+    if (!pl->fused_ready || capacity_items < (int64_t)pl->n_items_x + pl->n_items_f) return HALO_EINVAL;
     pl->trace = reinterpret_cast<unsigned long long*>(trace);
     pl->trace_cap = capacity_items;
     return HALO_OK;
 }
 
 int halo_work_items(const halo_plan* pl, int32_t* x_items, int32_t* f_items, int32_t* chunk) {
-    if (!pl) return HALO_EINVAL;
+    if (!pl || !pl->fused_ready) return HALO_EINVAL;
     if (x_items) *x_items = pl->n_items_x;
     if (f_items) *f_items = pl->n_items_f;
     if (chunk) *chunk = pl->chunk;

@@ -648,17 +648,15 @@ int reset_flags(halo_plan* pl, cudaStream_t st) {
     return HALO_OK;
 }
 
-int prepare_exchange(halo_plan* pl, cudaStream_t st) {
+int prepare_common(halo_plan* pl, cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
-    const size_t nsp = (size_t)nd * std::max(P, 1);
+    pl->fused_ready = false;  // the FUSED work lists describe the previous plan
     if (pl->n_local_total >= ((int64_t)1 << 31)) return HALO_ECAPACITY;  // int32 dense slots
     // coordinate items: one block, kThreads * E entries; force items: one
     // warp, 32 * E entries
     const int E = 4;
     pl->entries_per_thread = E;
     pl->chunk = kThreads * E;
-    const int CHF = 32 * E;
-    const int CH = pl->chunk;
 
     // per (s, p) descriptors
     pl->sp.assign((size_t)nd * P, SPDesc{});
@@ -694,7 +692,27 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
         stage = static_cast<char*>(hs);
     }
     HALO_TRY(upload(&pl->d_sp, &pl->cap_sp, pl->sp, stage, &off, st));
-    int32_t* h_tot = reinterpret_cast<int32_t*>(stage + off);  // 4 words read back below
+    if (!pl->d_err) HALO_TRY(dev_alloc(&pl->d_err, 8));
+    HALO_CUDA(cudaMemsetAsync(pl->d_err, 0, sizeof(int) * 8, st));
+    return HALO_OK;
+}
+
+int prepare_fused(halo_plan* pl, cudaStream_t st) {
+    const int nd = pl->n_dom, P = pl->P;
+    pl->trace = nullptr;  // item counts change: the caller re-arms tracing
+    pl->trace_cap = 0;
+    const size_t nsp = (size_t)nd * std::max(P, 1);
+    const int E = pl->entries_per_thread;
+    const int CHF = 32 * E;
+    const int CH = pl->chunk;
+    // four words read back below, in the pinned staging after the descriptors
+    // (which prepare_common reserved; an upload of them may still be in flight)
+    int32_t* h_tot = nullptr;
+    {
+        void* hs = nullptr;
+        HALO_TRY(host_stage(pl, stage_bytes(pl->sp) + 64, &hs));
+        h_tot = reinterpret_cast<int32_t*>(static_cast<char*>(hs) + stage_bytes(pl->sp));
+    }
 
     // force-entry classification on the device: last pulse adding into each
     // slot, then a stable independent/dependent partition per (s, p)
@@ -768,7 +786,6 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
     pl->n_items_f = h_tot[2] + h_tot[3];
     HALO_TRY(dev_reserve(&pl->d_flags, &pl->cap_flags, (int64_t)(2 * nsp)));
     if (!pl->d_tickets) HALO_TRY(dev_alloc(&pl->d_tickets, 2));
-    if (!pl->d_err) HALO_TRY(dev_alloc(&pl->d_err, 8));
     if (pl->occ_x <= 0 || pl->occ_f <= 0) HALO_TRY(occupancy<4>(&pl->occ_x, &pl->occ_f));
     pl->grid_x = (int)std::max<int64_t>(
         1, std::min<int64_t>(pl->n_items_x, (int64_t)pl->num_sms * std::max(pl->occ_x, 1)));
@@ -776,10 +793,13 @@ int prepare_exchange(halo_plan* pl, cudaStream_t st) {
         1, std::min<int64_t>((pl->n_items_f + kWarps - 1) / kWarps,
                              (int64_t)pl->num_sms * std::max(pl->occ_f, 1)));
     HALO_TRY(reset_flags(pl, st));
-    return cuda_code(cudaStreamSynchronize(st));
+    HALO_CUDA(cudaStreamSynchronize(st));
+    pl->fused_ready = true;
+    return HALO_OK;
 }
 
 int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
+    if (!pl->fused_ready) return HALO_EINVAL;
     if (pl->n_items_x == 0) return HALO_OK;
     XArgs a;
     a.xyz = xyz;
@@ -803,6 +823,7 @@ int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
 
 int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
                               unsigned long long* ticket, cudaStream_t st) {
+    if (!pl->fused_ready) return HALO_EINVAL;
     if (pl->n_items_x == 0) return HALO_OK;
     XArgs a;
     a.xyz = xyz;
@@ -825,6 +846,7 @@ int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
 }
 
 int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
+    if (!pl->fused_ready) return HALO_EINVAL;
     if (pl->n_items_f == 0) return HALO_OK;
     const size_t nsp = (size_t)pl->n_dom * std::max(pl->P, 1);
     FArgs a;

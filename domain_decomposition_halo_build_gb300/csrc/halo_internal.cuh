@@ -135,6 +135,7 @@ struct halo_plan {
 
     // exchange mode (HALO_MODE_*) and the flattened exchange's tables
     int mode = 0;
+    bool fused_ready = false;        // FUSED work lists built for the current plan
     bool flat_ready = false;
     int32_t* d_xflat = nullptr;      // per halo slot: owner dense slot | shift bits << 29
     int4* d_xflat_items = nullptr;   // {flat halo index, dense slot, len, 0} per chunk
@@ -178,7 +179,10 @@ int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st);
 int launch_flat_f(halo_plan* pl, float* f, cudaStream_t st);
 
 // halo_exchange.cu
-int prepare_exchange(halo_plan* pl, cudaStream_t st);
+// per-(s, p) descriptors and the error word, for every mode
+int prepare_common(halo_plan* pl, cudaStream_t st);
+// the FUSED mode's work lists, counters and tickets (synchronises `st`)
+int prepare_fused(halo_plan* pl, cudaStream_t st);
 int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st);
 int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st);
 // the coordinate kernel with caller-supplied arrival counters and ticket

@@ -641,7 +641,8 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
                     int32_t ent[KW];
 #pragma unroll
                     for (int j = 0; j < KW; j++) ent[j] = j < k ? __ldg(fent + r.y + j) : 0;
-                    reduce_tree<KW>(f, r.x & kNodeMask, checked_copies<KW>(r.x & kNodeMask, k, ent, n_slots, err), ent);
+                    const int kc = checked_copies<KW>(r.x & kNodeMask, k, ent, n_slots, err);
+                    reduce_tree<KW>(f, r.x & kNodeMask, kc, ent);
                     return;
                 }
             }

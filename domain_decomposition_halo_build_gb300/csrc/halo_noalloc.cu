@@ -57,7 +57,8 @@ int scratch_address(void** out) {
 }  // namespace
 
 extern "C" int halo_exchange_x_noalloc(halo_plan* pl, float* local_coords, void* stream) {
-    if (!pl || !local_coords || ((uintptr_t)local_coords & 3u) || !pl->valid) return HALO_EINVAL;
+    if (!pl || !local_coords || ((uintptr_t)local_coords & 3u) || !pl->valid || !pl->fused_ready)
+        return HALO_EINVAL;
     const int64_t counters = (int64_t)pl->n_dom * pl->P;
     if (counters > kNoAllocMaxCounters) return HALO_ESCRATCH;
     int prev = -1;

@@ -194,6 +194,10 @@ int halo_exchange_x(halo_plan* plan, float* local_coords, void* stream);
  * fixed array compiled into the library (HALO_NOALLOC_MAX_COUNTERS counters,
  * 64 KiB, held by every GPU that loads the library until exit) instead of the
  * plan's memory.  The plan itself comes from halo_setup.
+ *   - The plan needs the FUSED mode's work lists: they exist when its last
+ *     setup or rebuild ran in HALO_MODE_FUSED (the default), or after a
+ *     halo_set_mode(HALO_MODE_FUSED) since.  Otherwise HALO_EINVAL and
+ *     nothing runs (building them would allocate).
  *   - n_domains * n_pulses must be <= HALO_NOALLOC_MAX_COUNTERS, else
  *     HALO_ESCRATCH and nothing runs.
  *   - The first call on a device looks the array's device address up
@@ -234,7 +238,10 @@ int halo_exchange_f(halo_plan* plan, float* local_forces, void* stream);
  *     (built here, synchronising `stream`; rebuilt by halo_rebuild) and
  *     n_local_total < 2^26, at most 63 copies per atom (HALO_ECAPACITY
  *     otherwise).
- * The mode is kept across halo_rebuild. */
+ * The mode is kept across halo_rebuild.  A setup or rebuild builds the
+ * tables of the plan's current mode only; selecting FUSED or FLAT later
+ * builds theirs (synchronising `stream`).  HALO_EINVAL on a plan whose last
+ * rebuild failed when the selected mode's tables would have to be built. */
 int halo_set_mode(halo_plan* plan, int32_t mode, void* stream);
 int halo_get_mode(const halo_plan* plan, int32_t* mode);
 
@@ -264,10 +271,12 @@ int halo_debug_drop_signal(halo_plan* plan, int32_t domain, int32_t pulse);
  * halo_work_items().  While armed, every work item of both exchange kernels
  * records {time it was taken, time its waits ended, time it released its
  * signal (global timer, ns), SM id}: coordinate items at [0, x_items), force
- * items after them.  NULL disarms; a rebuild disarms.  For diagnosis only. */
+ * items after them.  NULL disarms; a rebuild disarms.  HALO_EINVAL while
+ * the plan has no FUSED work lists.  For diagnosis only. */
 int halo_set_trace(halo_plan* plan, uint64_t* trace, int64_t capacity_items);
 
-/* Work decomposition of the exchanges (host): items per kernel, entries per item. */
+/* Work decomposition of the FUSED exchanges (host): items per kernel, entries
+ * per item; HALO_EINVAL while the plan has no FUSED work lists. */
 int halo_work_items(const halo_plan* plan, int32_t* x_items, int32_t* f_items, int32_t* chunk);
 
 /* Kernel launches made so far by halo_exchange_x and halo_exchange_f (host). */

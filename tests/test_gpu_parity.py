@@ -142,6 +142,29 @@ def test_rebuild_after_displacement(cases):
     g.plan.set_mode("fused")
 
 
+def test_mode_tables_after_a_rebuild_in_each_mode():
+    """A setup or rebuild builds only the current mode's tables; selecting
+    another mode afterwards builds its own (FUSED work lists, FLAT tables,
+    STAGED buffer).  After a rebuild in each mode of the multi-pulse system,
+    every mode matches the oracle of the displaced positions."""
+    w = synth.WORKLOADS["water24k_2x4x8"]
+    xyz, dom = synth.system(w)
+    g = gpu_plan(w.box, w.grid, w.rc, xyz, dom)
+    try:
+        for k, mode_a in enumerate(MODES, start=1):
+            g.plan.set_mode(mode_a)
+            xk, dk = synth.displaced(xyz, w.box, w.grid, k=k)
+            g.rebuild(xk, dk)
+            assert g.plan.mode == mode_a
+            ok = oracle.Oracle(w.box, w.grid, w.rc, xk, dk)
+            compare_plans(g, ok)
+            for mode_b in MODES:
+                g.plan.set_mode(mode_b)
+                compare_exchanges(g, ok, xk, reps=1)
+    finally:
+        g.plan.close()
+
+
 EDGE = [
     # (box, grid, rc, n_atoms, seed)
     ((2.0, 2.0, 2.0), (1, 1, 1), 0.5, 37, 0),        # one domain, no pulses

@@ -100,3 +100,33 @@ def test_noalloc_refuses_plans_beyond_the_fixed_array():
         assert torch.equal(loc, before)                       # nothing ran
     finally:
         plan.close()
+
+
+def test_noalloc_needs_the_fused_work_lists():
+    """A plan rebuilt in FLAT mode has no FUSED work lists (a rebuild builds
+    only the current mode's tables), and building them would allocate: the
+    call refuses with HALO_EINVAL and touches nothing.  After
+    halo_set_mode(FUSED) it runs and matches halo_exchange_x."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    plan, x = _plan("water24k_2x4x8")
+    try:
+        d = torch.from_numpy(synth.system(synth.WORKLOADS["water24k_2x4x8"])[1]).cuda()
+        plan.set_mode("flat")
+        plan.rebuild(x, d)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        loc = plan.load_home(x)
+        before = loc.clone()
+        code = lib.halo_exchange_x_noalloc(plan.handle, ctypes.c_void_p(loc.data_ptr()), stream)
+        assert code == halo.EINVAL
+        torch.cuda.synchronize()
+        assert torch.equal(loc, before)
+        plan.set_mode("fused")
+        want = plan.load_home(x)
+        plan.exchange_x(want)
+        assert lib.halo_exchange_x_noalloc(plan.handle, ctypes.c_void_p(loc.data_ptr()), stream) == 0
+        assert plan.status() == 0
+        assert torch.equal(loc.view(torch.int32), want.view(torch.int32))
+    finally:
+        plan.close()
