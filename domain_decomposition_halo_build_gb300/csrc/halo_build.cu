@@ -102,14 +102,22 @@ __global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int
     __syncwarp();
     const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * kHistTile;
     bool bad = false;
-    for (int it = 0; it < kHistTile / 32; it++) {
-        const int64_t a = a0 + it * 32 + lane;
-        if (a < n) {
-            const int d = __ldg(dom + a);
-            if (d < 0 || d >= nd)
+    // eight coalesced loads in flight per lane, then their counts
+    constexpr int U = 8;
+    for (int it = 0; it < kHistTile / 32; it += U) {
+        int d[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t a = a0 + (it + u) * 32 + lane;
+            d[u] = a < n ? __ldg(dom + a) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            if (a0 + (it + u) * 32 + lane >= n) continue;
+            if (d[u] < 0 || d[u] >= nd)
                 bad = true;
             else
-                atomicAdd(&h[d], 1);
+                atomicAdd(&h[d[u]], 1);
         }
     }
     if (bad) flags[1] = 1;
@@ -147,24 +155,40 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
     __syncthreads();
     const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * kHistTile;
     const unsigned lt = lanemask_lt();
-    for (int it = 0; it < kHistTile / 32; it++) {
-        const int64_t a = a0 + it * 32 + lane;
-        int d = -1;
-        if (a < n) {
-            d = __ldg(dom + a);
-            if (d < 0 || d >= nd) d = -1;
+    // four rounds of 32 atoms per step: their ids and coordinates are loaded
+    // first (independent loads in flight), then the rounds are placed in
+    // order, so the partition stays stable
+    constexpr int U = 4;
+    for (int it = 0; it < kHistTile / 32; it += U) {
+        int d[U];
+        float c[U][3];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t a = a0 + (it + u) * 32 + lane;
+            d[u] = -1;
+            c[u][0] = c[u][1] = c[u][2] = 0.0f;
+            if (a < n) {
+                d[u] = __ldg(dom + a);
+                if (d[u] < 0 || d[u] >= nd) d[u] = -1;
+                c[u][0] = __ldg(xyz + 3 * a + 0);
+                c[u][1] = __ldg(xyz + 3 * a + 1);
+                c[u][2] = __ldg(xyz + 3 * a + 2);
+            }
         }
-        const unsigned peers = __match_any_sync(kFull, d);
-        if (d >= 0) {
-            const int64_t pos = (int64_t)run[d] + __popc(peers & lt);
-            home_gid[pos] = (int32_t)a;
-            // one 16-byte store: the coordinates, and no forwarding dims
-            bxyz[pos] = make_float4(__ldg(xyz + 3 * a + 0), __ldg(xyz + 3 * a + 1),
-                                    __ldg(xyz + 3 * a + 2), __int_as_float(0));
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t a = a0 + (it + u) * 32 + lane;
+            const unsigned peers = __match_any_sync(kFull, d[u]);
+            if (d[u] >= 0) {
+                const int64_t pos = (int64_t)run[d[u]] + __popc(peers & lt);
+                home_gid[pos] = (int32_t)a;
+                // one 16-byte store: the coordinates, and no forwarding dims
+                bxyz[pos] = make_float4(c[u][0], c[u][1], c[u][2], __int_as_float(0));
+            }
+            __syncwarp();
+            if (d[u] >= 0 && lane == __ffs(peers) - 1) run[d[u]] += __popc(peers);
+            __syncwarp();
         }
-        __syncwarp();
-        if (d >= 0 && lane == __ffs(peers) - 1) run[d] += __popc(peers);
-        __syncwarp();
     }
 }
 
@@ -332,18 +356,30 @@ __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
     sub_range(L, a, b, &lo, &hi);
     const int64_t nh = L.oo[0];
     int64_t c = 0, ch = 0;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += kThreads) {
-        const int64_t pos = locate(L, a.p, i);
-        if (pos < 0 || pos >= a.cap) continue;
-        const float4 slot = a.bxyz[pos];
-        const float vd = a.d == 0 ? slot.x : (a.d == 1 ? slot.y : slot.z);
-        if (vd < thr) {
-            if (a.prune) {
-                const float v[3] = {slot.x, slot.y, slot.z};
-                if (!corner_within(a, cell, v, (unsigned)__float_as_int(slot.w))) continue;
+    // four candidates per thread and step, their loads issued together
+    constexpr int U = 4;
+    for (int64_t i0 = lo + threadIdx.x; i0 < hi; i0 += U * kThreads) {
+        float4 slot[U];
+        bool in[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t i = i0 + u * kThreads;
+            const int64_t pos = i < hi ? locate(L, a.p, i) : -1;
+            in[u] = pos >= 0 && pos < a.cap;
+            slot[u] = in[u] ? a.bxyz[pos] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            if (!in[u]) continue;
+            const float vd = a.d == 0 ? slot[u].x : (a.d == 1 ? slot[u].y : slot[u].z);
+            if (vd < thr) {
+                if (a.prune) {
+                    const float v[3] = {slot[u].x, slot[u].y, slot[u].z};
+                    if (!corner_within(a, cell, v, (unsigned)__float_as_int(slot[u].w))) continue;
+                }
+                c++;
+                if (i0 + u * kThreads < nh) ch++;
             }
-            c++;
-            if (i < nh) ch++;
         }
     }
     int64_t tc, th;
@@ -394,8 +430,9 @@ __global__ void __launch_bounds__(1024) pulse_scan_kernel(PulseArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
+    constexpr int U = 4;  // tiles of kThreads candidates per step
     __shared__ Locator L;
-    __shared__ int wcnt[kThreads / 32];
+    __shared__ int wcnt[U][kThreads / 32];
     const int s = blockIdx.y, b = blockIdx.x;
     load_locator(L, a, s);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -408,46 +445,53 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
     sub_range(L, a, b, &lo, &hi);
     int64_t out = a.m.region[a.p] + a.blk_off[(int64_t)s * a.B + b];
     const unsigned lt = lanemask_lt();
-    for (int64_t t0 = lo; t0 < hi; t0 += kThreads) {
-        const int64_t i = t0 + threadIdx.x;
-        bool sel = false;
-        float v0 = 0, v1 = 0, v2 = 0;
-        unsigned m = 0;
-        if (i < hi) {
-            const int64_t pos = locate(L, a.p, i);
-            if (pos >= 0 && pos < a.cap) {
-                const float4 slot = a.bxyz[pos];
-                v0 = slot.x;
-                v1 = slot.y;
-                v2 = slot.z;
-                m = (unsigned)__float_as_int(slot.w);
-                const float vd = a.d == 0 ? v0 : (a.d == 1 ? v1 : v2);
-                sel = vd < thr;
-                if (sel && a.prune) {
-                    const float v[3] = {v0, v1, v2};
-                    sel = corner_within(a, cell, v, m);
+    // U consecutive tiles per step: every candidate's load is issued first,
+    // then the tiles are compacted in order (one barrier pair per step)
+    for (int64_t t0 = lo; t0 < hi; t0 += U * kThreads) {
+        float4 slot[U];
+        bool sel[U];
+        unsigned bal[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t i = t0 + u * kThreads + threadIdx.x;
+            const int64_t pos = i < hi ? locate(L, a.p, i) : -1;
+            sel[u] = pos >= 0 && pos < a.cap;
+            slot[u] = sel[u] ? a.bxyz[pos] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            if (sel[u]) {
+                const float vd = a.d == 0 ? slot[u].x : (a.d == 1 ? slot[u].y : slot[u].z);
+                sel[u] = vd < thr;
+                if (sel[u] && a.prune) {
+                    const float v[3] = {slot[u].x, slot[u].y, slot[u].z};
+                    sel[u] = corner_within(a, cell, v, (unsigned)__float_as_int(slot[u].w));
                 }
             }
+            bal[u] = __ballot_sync(kFull, sel[u]);
+            if (lane == 0) wcnt[u][warp] = __popc(bal[u]);
         }
-        const unsigned bal = __ballot_sync(kFull, sel);
-        if (lane == 0) wcnt[warp] = __popc(bal);
         __syncthreads();
-        int before = 0, total = 0;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; w++) {
-            const int c = wcnt[w];
-            before += (w < warp) ? c : 0;
-            total += c;
-        }
-        if (sel) {
-            const int64_t o = out + before + __popc(bal & lt);
-            if (o >= a.N && o < a.cap) {
-                a.maps[o - a.N] = (int32_t)i;
-                a.bxyz[o] = make_float4(v0 + sh[0], v1 + sh[1], v2 + sh[2],
-                                        __int_as_float((int)(m | (1u << a.d))));
+        for (int u = 0; u < U; u++) {
+            int before = 0, total = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; w++) {
+                const int c = wcnt[u][w];
+                before += (w < warp) ? c : 0;
+                total += c;
             }
+            if (sel[u]) {
+                const int64_t o = out + before + __popc(bal[u] & lt);
+                if (o >= a.N && o < a.cap) {
+                    const unsigned m = (unsigned)__float_as_int(slot[u].w);
+                    a.maps[o - a.N] = (int32_t)(t0 + u * kThreads + threadIdx.x);
+                    a.bxyz[o] = make_float4(slot[u].x + sh[0], slot[u].y + sh[1], slot[u].z + sh[2],
+                                            __int_as_float((int)(m | (1u << a.d))));
+                }
+            }
+            out += total;
         }
-        out += total;
         __syncthreads();
     }
 }
