@@ -724,6 +724,13 @@ def cpu_baseline(name, budget_s=10.0):
             "setup_ms": 1e3 * setup_s}
 
 
+def workload_config(w, pulses, halo_slots, world):
+    """The workload keys of the JSON line's config, the same for both arms."""
+    return {"workload": w.name, "n_atoms": w.n_atoms, "grid": list(w.grid), "box_nm": list(w.box),
+            "rc_nm": w.rc, "pulses": pulses, "halo_slots": halo_slots,
+            "parallelism": "replicas" if world > 1 else "1 GPU"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -753,8 +760,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "n_atoms": w.n_atoms, "grid": list(w.grid),
-                   "rc_nm": w.rc, "halo_slots": halo_slots},
+        "config": dict(workload_config(w, o.n_pulses, halo_slots, 1), mode="oracle",
+                       l2="host: the oracle's arrays, %d threads" % cores),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d full coord+force exchanges (C oracle, %d threads)"
                                    % (args.steps, cores)},
@@ -935,14 +942,11 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": args.workload, "mode": args.mode, "n_atoms": w.n_atoms,
-                       "grid": list(w.grid),
-                       "box_nm": list(w.box), "rc_nm": w.rc, "pulses": plan.n_pulses,
-                       "halo_slots": halo_slots, "parallelism": "replicas" if world > 1 else "1 GPU",
-                       "l2": "inputs larger than L2: %d copies of the system (%d MB, %.1fx L2) stepped "
+            "config": dict(workload_config(w, plan.n_pulses, halo_slots, world), mode=args.mode,
+                           l2="inputs larger than L2: %d copies of the system (%d MB, %.1fx L2) stepped "
                              "in turn, back to back" % (len(reps), rep_bytes >> 20,
                                                         rep_bytes / torch.cuda.get_device_properties(
-                                                            device).L2_cache_size)},
+                                                            device).L2_cache_size)),
             "us_per_exchange": 1e3 * step_ms, "us_x": 1e3 * x_ms, "us_f": 1e3 * f_ms,
             "per_step_flushed": dict(head_flushed, note="one step at a time, L2 flushed before each "
                                      "(%d MB written+read), an event pair around each" % (flush_bytes >> 20)),
