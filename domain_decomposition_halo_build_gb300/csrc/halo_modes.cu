@@ -429,8 +429,9 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
             a[e][2] = __ldg(s + 2);
         }
     }
-    if (E < 4) {
-        // small chunks: direct stores (a bulk copy's round trip does not pay)
+    if (E < 3) {
+        // small chunks (256 or 512 slots): direct stores, where a bulk
+        // copy's round trip does not pay
 #pragma unroll
         for (int e = 0; e < E; e++) {
             const int i = threadIdx.x + e * kThreads;
@@ -730,10 +731,28 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
     if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
     // coordinate items: halo range of every domain, in chunks of 256 * E
-    // slots; smaller chunks when the halo is too small to give every SM a
-    // few blocks of 1024
-    int E = 4;
-    while (E > 1 && H / (kThreads * E) < 4 * (int64_t)pl->num_sms) E /= 2;
+    // slots.  E is the fewest slots per thread whose chunks all fit in one
+    // wave of resident blocks: the most blocks, so the most even spread over
+    // the SMs (on the 1M-atom system E = 3 gives 7-8 blocks per SM where E = 4
+    // gave 5-6, and the kernel 7.3 us instead of 8.3).  Systems too large for
+    // one wave take E = 3.
+    if (pl->occ_flat_x[1] <= 0) {
+        int* occ = pl->occ_flat_x;
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], flat_x_kernel<1>, kThreads, 0));
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[2], flat_x_kernel<2>, kThreads, 0));
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[3], flat_x_kernel<3>, kThreads, 0));
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[4], flat_x_kernel<4>, kThreads, 0));
+    }
+    int E = 3;
+    for (int e = 1; e <= 4; e++) {
+        int64_t n_items = 0;
+        for (int D = 0; D < nd; D++)
+            n_items += ((int64_t)pl->n_local[D] - pl->n_home[D] + kThreads * e - 1) / (kThreads * e);
+        if (n_items <= (int64_t)pl->num_sms * pl->occ_flat_x[e]) {
+            E = e;
+            break;
+        }
+    }
     pl->flat_x_e = E;
     const int kFlatChunk = kThreads * E;
     // item b = {table offset b * kFlatChunk, first halo slot, count}: the
@@ -932,7 +951,8 @@ int launch_staged_f(halo_plan* pl, float* f, cudaStream_t st) {
 
 int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     if (pl->n_xflat_items == 0) return HALO_OK;
-    auto* k = pl->flat_x_e == 4 ? flat_x_kernel<4> : pl->flat_x_e == 2 ? flat_x_kernel<2> : flat_x_kernel<1>;
+    auto* k = pl->flat_x_e == 4 ? flat_x_kernel<4> : pl->flat_x_e == 3 ? flat_x_kernel<3>
+            : pl->flat_x_e == 2 ? flat_x_kernel<2> : flat_x_kernel<1>;
     const cudaError_t e = launch_dependent(k, dim3(pl->n_xflat_items), dim3(kThreads), st, xyz,
                                            (const int32_t*)pl->d_xflat, (const int4*)pl->d_xflat_items,
                                            pl->box[0], pl->box[1], pl->box[2], pl->n_local_total,
