@@ -400,19 +400,24 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
 }
 
 // ---- flat: the exchanges ------------------------------------------------------------
+// Threads per block of the coordinate kernel.  128 rather than 256: twice the
+// blocks spread more evenly over the SMs, and as they finish they free room
+// sooner for the next kernel's blocks (programmatic dependent launch).  On
+// the 1M-atom system x + f back to back took 18.4 us instead of 19.5.
+constexpr int kXT = 128;
 template <int E>
-__global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int32_t* __restrict__ xflat,
+__global__ void __launch_bounds__(kXT) flat_x_kernel(float* xyz, const int32_t* __restrict__ xflat,
                                                           const int4* __restrict__ items, float L0,
                                                           float L1, float L2, int64_t n_slots,
                                                           int* err) {
     grid_launch_dependents();
-    // block b's table entries start at b * 256 * E (the table is padded per
+    // block b's table entries start at b * kXT * E (the table is padded per
     // chunk), so they load alongside the item instead of after it; entries
     // at or past the item's count are padding and never used
     int32_t v[E];
 #pragma unroll
     for (int e = 0; e < E; e++)
-        v[e] = __ldg(xflat + (int64_t)blockIdx.x * (kThreads * E) + threadIdx.x + e * kThreads);
+        v[e] = __ldg(xflat + (int64_t)blockIdx.x * (kXT * E) + threadIdx.x + e * kXT);
     int4 it = items[blockIdx.x];
     if (!in_range((int64_t)it.y + it.z - 1, n_slots, err)) it.z = 0;
     // the chunk and its codes are plan tables; coordinates only after the wait
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
     float a[E][3];
 #pragma unroll
     for (int e = 0; e < E; e++) {
-        if (threadIdx.x + e * kThreads < it.z) {
+        if (threadIdx.x + e * kXT < it.z) {
             // owners are home slots, never written by this kernel
             const int64_t o = v[e] & ((1 << 29) - 1);
             const float* s = xyz + 3 * (in_range(o, n_slots, err) ? o : 0);
@@ -430,11 +435,11 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
         }
     }
     if (E < 3) {
-        // small chunks (256 or 512 slots): direct stores, where a bulk
-        // copy's round trip does not pay
+        // small chunks (one or two slots per thread): direct stores, where a
+        // bulk copy's round trip does not pay
 #pragma unroll
         for (int e = 0; e < E; e++) {
-            const int i = threadIdx.x + e * kThreads;
+            const int i = threadIdx.x + e * kXT;
             if (i < it.z) {
                 const unsigned c = (unsigned)v[e] >> 29;
                 float* q = xyz + 3 * ((int64_t)it.y + i);
@@ -446,12 +451,12 @@ __global__ void __launch_bounds__(kThreads) flat_x_kernel(float* xyz, const int3
         return;
     }
     // the chunk's halo slots are contiguous: stage them, one bulk copy out
-    __shared__ __align__(128) float stage[3 * kThreads * E + 4];
+    __shared__ __align__(128) float stage[3 * kXT * E + 4];
     float* dst = xyz + 3 * (int64_t)it.y;
     const int sh = stage_shift(dst);
 #pragma unroll
     for (int e = 0; e < E; e++) {
-        const int i = threadIdx.x + e * kThreads;
+        const int i = threadIdx.x + e * kXT;
         if (i < it.z) {
             const unsigned c = (unsigned)v[e] >> 29;
             float* q = stage + sh + 3 * i;
@@ -730,18 +735,18 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
     const int nd = pl->n_dom, P = pl->P;
     if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
-    // coordinate items: halo range of every domain, in chunks of 256 * E
+    // coordinate items: halo range of every domain, in chunks of kXT * E
     // slots.  E is the fewest slots per thread whose chunks all fit in one
     // wave of resident blocks: the most blocks, so the most even spread over
-    // the SMs (on the 1M-atom system E = 3 gives 7-8 blocks per SM where E = 4
-    // gave 5-6, and the kernel 7.3 us instead of 8.3).  Systems too large for
-    // one wave take E = 3.
+    // the SMs (on the 1M-atom system, 256-thread blocks with E = 3 gave 7-8
+    // blocks per SM where E = 4 gave 5-6, and the kernel 7.3 us instead of
+    // 8.3).  Systems too large for one wave take E = 3.
     if (pl->occ_flat_x[1] <= 0) {
         int* occ = pl->occ_flat_x;
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], flat_x_kernel<1>, kThreads, 0));
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[2], flat_x_kernel<2>, kThreads, 0));
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[3], flat_x_kernel<3>, kThreads, 0));
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[4], flat_x_kernel<4>, kThreads, 0));
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], flat_x_kernel<1>, kXT, 0));
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[2], flat_x_kernel<2>, kXT, 0));
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[3], flat_x_kernel<3>, kXT, 0));
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[4], flat_x_kernel<4>, kXT, 0));
     }
     int E = 3;
     for (int e = 1; e <= 4; e++) {
@@ -754,7 +759,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         }
     }
     pl->flat_x_e = E;
-    const int kFlatChunk = kThreads * E;
+    const int kFlatChunk = kXT * E;
     // item b = {table offset b * kFlatChunk, first halo slot, count}: the
     // table is padded to whole chunks so a block can address its entries
     // from its index alone
@@ -953,7 +958,7 @@ int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     if (pl->n_xflat_items == 0) return HALO_OK;
     auto* k = pl->flat_x_e == 4 ? flat_x_kernel<4> : pl->flat_x_e == 3 ? flat_x_kernel<3>
             : pl->flat_x_e == 2 ? flat_x_kernel<2> : flat_x_kernel<1>;
-    const cudaError_t e = launch_dependent(k, dim3(pl->n_xflat_items), dim3(kThreads), st, xyz,
+    const cudaError_t e = launch_dependent(k, dim3(pl->n_xflat_items), dim3(kXT), st, xyz,
                                            (const int32_t*)pl->d_xflat, (const int4*)pl->d_xflat_items,
                                            pl->box[0], pl->box[1], pl->box[2], pl->n_local_total,
                                            pl->d_err);
