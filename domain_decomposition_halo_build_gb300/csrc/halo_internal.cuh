@@ -152,8 +152,8 @@ struct halo_plan {
     int64_t cap_pool32 = 0, cap_pool8 = 0;
     int4* d_frec[3] = {nullptr, nullptr, nullptr};  // owner records: A (<=3), B (<=11), C (more)
     int64_t n_rec[3] = {0, 0, 0};
-    int flat_x_e = 4;                // entries per thread of the flat coordinate kernel
-    int occ_flat_x[5] = {0, 0, 0, 0, 0};  // its resident blocks per SM for 1..4 entries (cached)
+    int flat_x_e = 2;                // entries per thread of the flat coordinate kernel
+    int occ_flat_x = 0;              // its resident blocks per SM at 2 entries (cached)
     // staged (MPI-era) mode: one send/receive buffer element per halo slot
     float* d_stage_buf = nullptr;
     int64_t cap_stage_buf = 0, n_stage_buf = 0;

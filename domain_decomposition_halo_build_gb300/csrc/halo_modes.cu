@@ -435,8 +435,8 @@ __global__ void __launch_bounds__(kXT) flat_x_kernel(float* xyz, const int32_t* 
         }
     }
     if (E < 3) {
-        // small chunks (one or two slots per thread): direct stores, where a
-        // bulk copy's round trip does not pay
+        // small chunks (two slots per thread): direct stores, where a bulk
+        // copy's round trip does not pay
 #pragma unroll
         for (int e = 0; e < E; e++) {
             const int i = threadIdx.x + e * kXT;
@@ -736,28 +736,17 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
     if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
     // coordinate items: halo range of every domain, in chunks of kXT * E
-    // slots.  E is the fewest slots per thread whose chunks all fit in one
-    // wave of resident blocks: the most blocks, so the most even spread over
-    // the SMs (on the 1M-atom system, 256-thread blocks with E = 3 gave 7-8
-    // blocks per SM where E = 4 gave 5-6, and the kernel 7.3 us instead of
-    // 8.3).  Systems too large for one wave take E = 3.
-    if (pl->occ_flat_x[1] <= 0) {
-        int* occ = pl->occ_flat_x;
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], flat_x_kernel<1>, kXT, 0));
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[2], flat_x_kernel<2>, kXT, 0));
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[3], flat_x_kernel<3>, kXT, 0));
-        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[4], flat_x_kernel<4>, kXT, 0));
-    }
-    int E = 3;
-    for (int e = 1; e <= 4; e++) {
-        int64_t n_items = 0;
-        for (int D = 0; D < nd; D++)
-            n_items += ((int64_t)pl->n_local[D] - pl->n_home[D] + kThreads * e - 1) / (kThreads * e);
-        if (n_items <= (int64_t)pl->num_sms * pl->occ_flat_x[e]) {
-            E = e;
-            break;
-        }
-    }
+    // slots.  E = 2 unless that needs more than two waves of resident blocks,
+    // then 3 (measured, x + f back to back, 128-thread blocks: the 1M-atom
+    // system 18.4 us at E = 2 against 18.8, 19.4 and 18.8 at E = 3, 4 and 1,
+    // where several small waves let the force kernel's blocks start early;
+    // the 3M system 53.9 at E = 3 against 54.5 at E = 2).
+    if (pl->occ_flat_x <= 0)
+        HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&pl->occ_flat_x, flat_x_kernel<2>, kXT, 0));
+    int64_t items2 = 0;
+    for (int D = 0; D < nd; D++)
+        items2 += ((int64_t)pl->n_local[D] - pl->n_home[D] + 2 * kXT - 1) / (2 * kXT);
+    const int E = items2 <= 2 * (int64_t)pl->num_sms * pl->occ_flat_x ? 2 : 3;
     pl->flat_x_e = E;
     const int kFlatChunk = kXT * E;
     // item b = {table offset b * kFlatChunk, first halo slot, count}: the
@@ -956,8 +945,7 @@ int launch_staged_f(halo_plan* pl, float* f, cudaStream_t st) {
 
 int launch_flat_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     if (pl->n_xflat_items == 0) return HALO_OK;
-    auto* k = pl->flat_x_e == 4 ? flat_x_kernel<4> : pl->flat_x_e == 3 ? flat_x_kernel<3>
-            : pl->flat_x_e == 2 ? flat_x_kernel<2> : flat_x_kernel<1>;
+    auto* k = pl->flat_x_e == 3 ? flat_x_kernel<3> : flat_x_kernel<2>;
     const cudaError_t e = launch_dependent(k, dim3(pl->n_xflat_items), dim3(kXT), st, xyz,
                                            (const int32_t*)pl->d_xflat, (const int4*)pl->d_xflat_items,
                                            pl->box[0], pl->box[1], pl->box[2], pl->n_local_total,
