@@ -407,9 +407,8 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
 constexpr int kXT = 128;
 template <int E>
 __global__ void __launch_bounds__(kXT) flat_x_kernel(float* xyz, const int32_t* __restrict__ xflat,
-                                                          const int4* __restrict__ items, float L0,
-                                                          float L1, float L2, int64_t n_slots,
-                                                          int* err) {
+                                                     const int4* __restrict__ items, float L0, float L1,
+                                                     float L2, int64_t n_slots, int* err) {
     grid_launch_dependents();
     // block b's table entries start at b * kXT * E (the table is padded per
     // chunk), so they load alongside the item instead of after it; entries
