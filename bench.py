@@ -210,18 +210,21 @@ def setup_replicas(name, device, l2_multiple=4, prune=False):
 
 
 def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=None):
-    """K back-to-back steps, step i on replica i mod R; one CUDA event pair
-    around all K.  which: "xf" (the step), "x" or "f" (one direction alone).
+    """K back-to-back steps through the C ABI, step i on replica i mod R; one
+    CUDA event pair around all K.  which: "xf" (the step), "x" or "f" (one direction alone).
     Returns (ms per step, wall seconds, clocks, launches in the timed region)."""
     import torch
     R = len(reps)
+    # each replica's arrays bound once (HaloPlan.bind): every step is then two
+    # calls into the library, without re-checking the tensors each time
+    bound = [plan.bind(loc, f, stream) for plan, loc, f in reps]
 
     def run(i):
-        plan, loc, f = reps[i % R]
+        b = bound[i % R]
         if "x" in which:
-            plan.exchange_x(loc, stream)
+            b.x()
         if "f" in which:
-            plan.exchange_f(f, stream)
+            b.f()
     for i in range(max(warmup, 1) * R):
         run(i)
     torch.cuda.synchronize()

@@ -230,6 +230,11 @@ class HaloPlan:
     def handle(self):
         return self._h
 
+    def bind(self, local_xyz=None, local_f=None, stream=None):
+        """A BoundExchange: exchange_x / exchange_f on these arrays and this
+        stream, with the argument checks done once here."""
+        return BoundExchange(self, local_xyz, local_f, stream)
+
     def rebuild(self, coords, domain_of_atom, stream=None):
         halo_rebuild(self._h, coords, domain_of_atom, stream)
         self._refresh()
@@ -357,3 +362,53 @@ class HaloPlan:
             self.close()
         except Exception:
             pass
+
+
+class BoundExchange:
+    """halo_exchange_x and halo_exchange_f on fixed arrays and a fixed stream.
+
+    HaloPlan.exchange_x checks its tensor (device, dtype, shape, layout) on
+    every call, a few microseconds of host time; a loop that steps the same
+    arrays many times can check them once here, and then each x() or f() is
+    one call into the library.  The arrays must stay alive and unchanged; a
+    rebuild that changes the plan's local slot count makes the calls raise
+    (bind again)."""
+
+    __slots__ = ("_plan", "_n", "_fx", "_ff", "_args_x", "_args_f", "_keep")
+
+    def __init__(self, plan, local_xyz=None, local_f=None, stream=None):
+        import torch
+        self._plan = plan
+        self._n = plan.n_local_total
+        shape = (plan.n_local_total, 3)
+        s = _stream_handle(stream)
+        self._keep = (local_xyz, local_f)
+        self._fx = plan._lib.halo_exchange_x
+        self._ff = plan._lib.halo_exchange_f
+        self._args_x = None if local_xyz is None else (
+            plan.handle, _dev_ptr(local_xyz, torch.float32, shape), s)
+        self._args_f = None if local_f is None else (
+            plan.handle, _dev_ptr(local_f, torch.float32, shape), s)
+
+    def _refuse(self, args):
+        p = self._plan
+        if p._h is None or not p._h.value or p.n_local_total != self._n:
+            raise HaloError(EINVAL, "bound exchange (the plan was rebuilt or closed: bind again)")
+        if args is None:
+            raise ValueError("no array bound for this direction")
+
+    def x(self):
+        p = self._plan
+        if p._h is None or p.n_local_total != self._n or self._args_x is None:
+            self._refuse(self._args_x)
+        code = self._fx(*self._args_x)
+        if code != OK:
+            raise HaloError(code, "halo_exchange_x")
+
+    def f(self):
+        p = self._plan
+        if p._h is None or p.n_local_total != self._n or self._args_f is None:
+            self._refuse(self._args_f)
+        code = self._ff(*self._args_f)
+        if code != OK:
+            raise HaloError(code, "halo_exchange_f")

@@ -139,7 +139,10 @@ def test_rebuild_after_displacement(cases):
         ok = oracle.Oracle(w.box, w.grid, w.rc, xk, dk)
         compare_plans(g, ok)
         compare_exchanges(g, ok, xk, reps=1)
+    # the cached plan serves other tests: back to the original positions
     g.plan.set_mode("fused")
+    g.rebuild(xyz, dom)
+    compare_plans(g, o)
 
 
 def test_mode_tables_after_a_rebuild_in_each_mode():
@@ -163,6 +166,47 @@ def test_mode_tables_after_a_rebuild_in_each_mode():
                 compare_exchanges(g, ok, xk, reps=1)
     finally:
         g.plan.close()
+
+
+@pytest.mark.parametrize("mode", ["fused", "flat"])
+def test_bound_exchange_matches_the_checked_calls(mode):
+    """HaloPlan.bind: the same C calls with the tensor checks done once.  Bit
+    for bit the same results; wrong shapes refused at bind time; calls after
+    a rebuild that changed the slot count, or after close, refused."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    w = synth.WORKLOADS["water24k_2x4x8"]
+    xyz, dom = synth.system(w)
+    x = torch.from_numpy(xyz).cuda()
+    d = torch.from_numpy(dom).cuda()
+    plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d)
+    try:
+        plan.set_mode(mode)
+        f0 = torch.from_numpy(synth.forces(plan.n_local_total, seed=6)).cuda()
+        want_x = plan.load_home(x)
+        plan.exchange_x(want_x)
+        want_f = f0.clone()
+        plan.exchange_f(want_f)
+        loc, f = plan.load_home(x), f0.clone()
+        b = plan.bind(loc, f)
+        b.x()
+        b.f()
+        assert plan.status() == 0
+        assert torch.equal(loc.view(torch.int32), want_x.view(torch.int32))
+        assert torch.equal(f.view(torch.int32), want_f.view(torch.int32))
+        with pytest.raises(ValueError):
+            plan.bind(loc[:-1])
+        with pytest.raises(ValueError):
+            plan.bind(None, f).x()
+        xk, dk = synth.displaced(xyz, w.box, w.grid, k=3)
+        plan.rebuild(torch.from_numpy(xk).cuda(), torch.from_numpy(dk).cuda())
+        if plan.n_local_total != loc.shape[0]:
+            with pytest.raises(halo.HaloError):
+                b.x()
+    finally:
+        plan.close()
+    with pytest.raises(halo.HaloError):
+        b.f()
 
 
 EDGE = [
