@@ -154,6 +154,8 @@ struct halo_plan {
     int64_t n_rec[3] = {0, 0, 0};
     int flat_x_e = 2;                // entries per thread of the flat coordinate kernel
     int occ_flat_x = 0;              // its resident blocks per SM at 2 entries (cached)
+    int ahead_x[4] = {0, 0, 0, 0};   // resident blocks of the flat kernels (cached), by
+    int ahead_f[3] = {0, 0, 0};      // entries per thread / largest tree
     // staged (MPI-era) mode: one send/receive buffer element per halo slot
     float* d_stage_buf = nullptr;
     int64_t cap_stage_buf = 0, n_stage_buf = 0;
