@@ -596,7 +596,8 @@ __device__ __forceinline__ int checked_copies(int32_t home, int k, const int32_t
 }
 
 // class-A owners per thread: a tile is kFlatA * kThreads owners (at 2 the
-// kernel needs 56 registers; 3 and 4 need 80 and 114 and fit fewer blocks)
+// kernel fits four blocks per SM; 3 and 4 owners needed 80 and 114 registers
+// and fit fewer blocks)
 constexpr int kFlatA = 2;
 
 template <int KB, int KW>
@@ -616,8 +617,8 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
     grid_launch_dependents();
     // records are plan tables, read before grid_dependency_wait(); forces after it
     // one tile per block, the grid covering every tile: without a grid-stride
-    // loop the paths are straight-line and the kernel needs 60 registers
-    // instead of 79 (four resident blocks per SM instead of three)
+    // loop the paths are straight-line and the kernel fits in 64 registers
+    // (four resident blocks per SM; with the loop it needed 79, three blocks)
     const int64_t bb = blockIdx.x;
     if (bb >= tilesA + tilesBC) return;
     {
