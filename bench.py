@@ -191,6 +191,13 @@ def setup_workload(name, device, prune=False):
     return w, xyz, dom, x, plan, loc, f0
 
 
+def replica_count(bytes_per_copy, l2_bytes, l2_multiple=4):
+    """Copies of a system that together hold at least l2_multiple x the L2
+    size (at least two), so that stepping them in turn reads every step's
+    data from HBM."""
+    return max(2, -(-l2_multiple * l2_bytes // max(bytes_per_copy, 1)))
+
+
 def setup_replicas(name, device, l2_multiple=4, prune=False):
     """R copies of one system (each its own plan, local coordinates and
     forces), R >= 2 chosen so that their coordinates, forces and exchange
@@ -199,8 +206,7 @@ def setup_replicas(name, device, l2_multiple=4, prune=False):
     from domain_decomposition_halo_build_gb300 import halo, synth
     w, xyz, dom, x, plan, loc, f0 = setup_workload(name, device, prune=prune)
     per = 24 * plan.n_local_total + (BYTES_X + BYTES_F) * plan.n_halo_total
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    n = max(2, -(-l2_multiple * l2 // per))
+    n = replica_count(per, torch.cuda.get_device_properties(device).L2_cache_size, l2_multiple)
     d = torch.from_numpy(dom).to(device)
     reps = [(plan, loc, f0.clone())]
     for _ in range(n - 1):

@@ -73,3 +73,18 @@ def test_reference_arm_non_zero_rank_exits_without_work(monkeypatch, capsys):
         gpus = 2
     assert bench.run_reference(A()) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_replica_count_covers_the_l2():
+    """The bench steps enough copies of a system that their data exceeds the
+    L2 by the asked multiple: the 1M-atom system (about 100 MB with its
+    tables) on a 135.5 MB L2 takes six copies; a system larger than the L2
+    still takes two; a tiny one many."""
+    sys.path.insert(0, ROOT)
+    import bench
+    l2 = 135_528_448
+    per_1m = 24 * 1_831_410 + 68 * 831_410
+    assert bench.replica_count(per_1m, l2) == 6
+    assert bench.replica_count(per_1m, l2) * per_1m >= 4 * l2
+    assert bench.replica_count(10 * l2, l2) == 2
+    assert bench.replica_count(1_000_000, l2) == 543
