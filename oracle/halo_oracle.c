@@ -2,8 +2,8 @@
  * halo_oracle.c -- plain, sequential CPU oracle for the eighth-shell
  * domain-decomposition halo exchange.
  *
- * TEST INFRASTRUCTURE ONLY.  This file is the checker that the CUDA library
- * is compared against.  Only the tests, __graft_entry__.smoke() and the
+ * TEST INFRASTRUCTURE ONLY.  This file is the reference the CUDA library's
+ * results are compared against.  Only the tests, __graft_entry__.smoke() and the
  * cpu_baseline / --impl reference legs of bench.py may load it.  It shares no
  * code, header, table or helper with the CUDA library and must never be
  * reached from the library's product path.
