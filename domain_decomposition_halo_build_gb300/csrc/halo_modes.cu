@@ -42,6 +42,7 @@ constexpr int kNodeBits = 26;             // entry = node slot | parent position
 constexpr int32_t kNodeMask = (1 << kNodeBits) - 1;
 constexpr int kMaxCopies = 63;            // parent positions fit in 6 bits
 constexpr int kSortRegs = 8;              // copy lists sorted in registers up to this length
+constexpr int32_t kXOwnerMask = (1 << 29) - 1;  // coordinate table: owner slot | crossings << 29
 
 // ---- stepwise ----------------------------------------------------------------
 __global__ void step_x_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
@@ -433,6 +434,16 @@ __global__ void __launch_bounds__(kXT) flat_x_kernel(float* xyz, const int32_t* 
         v[e] = __ldg(xflat + (int64_t)blockIdx.x * (kXT * E) + threadIdx.x + e * kXT);
     int4 it = items[blockIdx.x];
     if (!in_range((int64_t)it.y + it.z - 1, n_slots, err)) it.z = 0;
+    // Blocks of the first wave (the only ones that can start before the
+    // kernel ahead has finished) warm their gather lines in L2 meanwhile.
+    // L2 is the device's point of coherence: a prefetch hands no thread a
+    // value, so it cannot expose anything older than the preceding grid's
+    // writes.  1M-atom system, x + f back to back: 17.2 -> 15.8 us.
+    if (blockIdx.x < ahead) {
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            if (threadIdx.x + e * kXT < it.z) prefetch_table(xyz + 3 * (int64_t)(v[e] & kXOwnerMask));
+    }
     // the chunk and its codes are plan tables; coordinates only after the wait
     grid_dependency_wait();
     float a[E][3];
@@ -440,7 +451,7 @@ __global__ void __launch_bounds__(kXT) flat_x_kernel(float* xyz, const int32_t* 
     for (int e = 0; e < E; e++) {
         if (threadIdx.x + e * kXT < it.z) {
             // owners are home slots, never written by this kernel
-            const int64_t o = v[e] & ((1 << 29) - 1);
+            const int64_t o = v[e] & kXOwnerMask;
             const float* s = xyz + 3 * (in_range(o, n_slots, err) ? o : 0);
             a[e][0] = __ldg(s);
             a[e][1] = __ldg(s + 1);
@@ -640,9 +651,23 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
                 ent[e][0] = r.y;
                 ent[e][1] = r.z;
                 ent[e][2] = r.w;
-                kk[e] = m < nA ? checked_copies<3>(home[e], (int)((unsigned)r.x >> kNodeBits), ent[e],
-                                                   n_slots, err)
-                               : 0;
+                const int k = (int)((unsigned)r.x >> kNodeBits);
+                kk[e] = m < nA ? checked_copies<3>(home[e], k, ent[e], n_slots, err) : 0;
+            }
+            // first wave of a grid of more than one wave: this thread's force
+            // lines into L2 while the kernel ahead drains (as in the
+            // coordinate kernel).  The force kernel alone on the 1M-atom
+            // system 10.2 -> 9.6 us, the 3M x + f 50.6 -> 49.8 us; a one-wave
+            // grid (24k atoms) gains nothing, its prefetches only compete
+            // with the kernel ahead.
+            if (bb < ahead && tilesA + tilesBC > ahead) {
+#pragma unroll
+                for (int e = 0; e < kFlatA; e++) {
+                    if (kk[e] > 0) prefetch_table(f + 3 * (int64_t)home[e]);
+#pragma unroll
+                    for (int j = 0; j < 3; j++)
+                        if (j < kk[e]) prefetch_table(f + 3 * (int64_t)(ent[e][j] & kNodeMask));
+                }
             }
             grid_dependency_wait();
             // the replacement block's trees: its records (prefetched above,
