@@ -44,6 +44,8 @@ LATENCY_WORKLOAD = "water24k_2x4x8"
 # algorithmic bytes per halo slot: x = 4 (index) + 12 (gather) + 12 (store);
 # f = 4 (index) + 12 (halo force) + 12 (owner read) + 12 (owner write)
 BYTES_X, BYTES_F = 28, 40
+# of which reads: x = index + gather; f = index + halo force + owner read
+READ_X, READ_F = 16, 28
 HBM_FALLBACK_GBS = 6800.0
 
 
@@ -75,8 +77,8 @@ def source_digest(kernel):
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    """DRAM bytes per launch, {"read": R, "write": W}, from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -84,9 +86,9 @@ def recorded_traffic(kernel, workload):
     with open(path) as f:
         for line in f:
             v = line.split()
-            if len(v) >= 4 and not line.startswith("#") and v[0] == kernel and v[1] == workload \
+            if len(v) >= 5 and not line.startswith("#") and v[0] == kernel and v[1] == workload \
                     and v[2] == digest:
-                return int(float(v[3]))
+                return {"read": int(float(v[3])), "write": int(float(v[4]))}
     return None
 
 
@@ -215,9 +217,13 @@ def setup_replicas(name, device, l2_multiple=4, prune=False):
     return w, xyz, dom, x, reps, f0, n * per
 
 
-def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=None):
+def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=None, settle_s=0.0):
     """K back-to-back steps through the C ABI, step i on replica i mod R; one
     CUDA event pair around all K.  which: "xf" (the step), "x" or "f" (one direction alone).
+    With a clock sampler, sampling starts before the warm-up, and the warm-up
+    runs for at least settle_s seconds of the same steps, so that the samples
+    show the clocks under this load even when the timed region itself is far
+    shorter than the sampling period.
     Returns (ms per step, wall seconds, clocks, launches in the timed region)."""
     import torch
     R = len(reps)
@@ -231,15 +237,23 @@ def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=
             b.x()
         if "f" in which:
             b.f()
-    for i in range(max(warmup, 1) * R):
+    if sampler:
+        sampler.start()
+    t_settle = time.perf_counter()
+    nwarm = max(warmup, 1) * R
+    for i in range(nwarm):
         run(i)
+    while time.perf_counter() - t_settle < settle_s:
+        for _ in range(64):
+            run(nwarm)
+            nwarm += 1
+        torch.cuda.synchronize()
     torch.cuda.synchronize()
+    settle = time.perf_counter() - t_settle
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if barrier:
         barrier()
     torch.cuda.synchronize()
-    if sampler:
-        sampler.start()
     l0 = sum(sum(p.launch_counts()) for p, _, _ in reps)
     t0 = time.perf_counter()
     e0.record(stream)
@@ -251,6 +265,9 @@ def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=
     if barrier:
         barrier()
     clocks = sampler.stop() if sampler else None
+    if clocks is not None:
+        clocks["covers"] = ("the warm-up (%d steps, %.2f s) and the timed region (%d steps, %.4f s)"
+                            % (nwarm, settle, steps, wall))
     l1 = sum(sum(p.launch_counts()) for p, _, _ in reps)
     for p, _, _ in reps:
         code = p.status()
@@ -769,8 +786,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(w, o.n_pulses, halo_slots, 1), mode="oracle",
-                       l2="host: the oracle's arrays, %d threads" % cores),
+        "config": workload_config(w, o.n_pulses, halo_slots, 1),
+        "mode": "oracle", "l2": "host: the oracle's arrays, %d threads" % cores,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d full coord+force exchanges (C oracle, %d threads)"
                                    % (args.steps, cores)},
@@ -791,6 +808,11 @@ def main():
                     help="exchange mode of the headline value; every mode is also reported")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--modes", default="staged,fused,stepwise,flat",
+                    help="modes timed on the headline system (the headline mode always)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the context legs (latency, pruning, configurations, rebuild, graph, "
+                         "overlap, stencil, end-to-end): for short profiling runs")
     args = ap.parse_args()
     if args.impl == "reference":
         if args.steps == 20000 and "--steps" not in sys.argv:
@@ -831,8 +853,9 @@ def main():
     peak, peak_kind = measured_peak()
     halo_slots = plan.n_halo_total
     modes = ["staged", "fused", "stepwise", "flat"]
+    run_modes = [m for m in modes if m in args.modes.split(",") and m != args.mode] + [args.mode]
     others = {}
-    for mode in [m for m in modes if m != args.mode] + [args.mode]:
+    for mode in run_modes:
         for p, _, _ in reps:
             p.set_mode(mode)
         head = mode == args.mode
@@ -840,7 +863,8 @@ def main():
         steps = args.steps if head else min(args.steps, 500)
         # the timed region: K back-to-back steps over the replicas in turn
         m_step, m_wall, m_clocks, m_launches = time_rotated(reps, steps, args.warmup, stream, "xf",
-                                                            sampler, barrier)
+                                                            sampler, barrier,
+                                                            settle_s=1.0 if head else 0.0)
         # per-direction split: K back-to-back launches of one direction
         ksplit = min(steps, 1000)
         m_x = time_rotated(reps, ksplit, args.warmup, stream, "x")[0]
@@ -867,82 +891,85 @@ def main():
     kname = {"fused": ("unpack_f_kernel", "pack_x_kernel"), "stepwise": ("step_f_kernel", "step_x_kernel"),
              "staged": ("staged_unpack_f_kernel", "staged_pack_x_kernel"),
              "flat": ("flat_f_kernel", "flat_x_kernel")}[args.mode]
-    dom_kernel, dom_ms, per_slot = ((kname[0], f_ms, BYTES_F) if f_ms >= x_ms
-                                    else (kname[1], x_ms, BYTES_X))
+    dom_kernel, dom_ms, per_slot, read_slot = ((kname[0], f_ms, BYTES_F, READ_F) if f_ms >= x_ms
+                                               else (kname[1], x_ms, BYTES_X, READ_X))
     achieved = per_slot * halo_slots / (dom_ms * 1e-3) / 1e9
     traffic = recorded_traffic(dom_kernel, args.workload)
     alg_gbs = (BYTES_X + BYTES_F) * halo_slots / (step_ms * 1e-3) / 1e9
 
-    # latency case: the multi-pulse system, every mode
-    lw, lxyz, ldom, lx, lplan, lloc, lf0 = setup_workload(LATENCY_WORKLOAD, device)
-    lat = {"workload": LATENCY_WORKLOAD, "halo_slots": lplan.n_halo_total, "pulses": lplan.n_pulses}
-    lsteps = min(args.steps, 1000)
-    for mode in modes:
-        lplan.set_mode(mode)
-        lf = lf0.clone()
-        lsts, lxs, lfs, _, _, llaunch = time_steps(lplan, lloc, lf, lsteps, args.warmup, flush, stream)
-        assert lplan.status() == 0
-        lat[mode] = {"us_per_exchange": 1e3 * statistics.fmean(lsts),
-                     "us_x": 1e3 * statistics.fmean(lxs), "us_f": 1e3 * statistics.fmean(lfs),
-                     "launches_per_direction": llaunch / (2 * lsteps)}
-    lat_slots = lplan.n_halo_total
-    lplan.close()
-    plan.set_mode(args.mode)
+    lat = pruned = warm = graph = all_configs = rebuild = stencil_res = overlap = None
+    e2e_value = e2e_ms = h2d = d2h = e2e_serial_ms = None
+    if not args.headline_only:
+        # latency case: the multi-pulse system, every mode
+        lw, lxyz, ldom, lx, lplan, lloc, lf0 = setup_workload(LATENCY_WORKLOAD, device)
+        lat = {"workload": LATENCY_WORKLOAD, "halo_slots": lplan.n_halo_total, "pulses": lplan.n_pulses}
+        lsteps = min(args.steps, 1000)
+        for mode in modes:
+            lplan.set_mode(mode)
+            lf = lf0.clone()
+            lsts, lxs, lfs, _, _, llaunch = time_steps(lplan, lloc, lf, lsteps, args.warmup, flush, stream)
+            assert lplan.status() == 0
+            lat[mode] = {"us_per_exchange": 1e3 * statistics.fmean(lsts),
+                         "us_x": 1e3 * statistics.fmean(lxs), "us_f": 1e3 * statistics.fmean(lfs),
+                         "launches_per_direction": llaunch / (2 * lsteps)}
+        lat_slots = lplan.n_halo_total
+        lplan.close()
+        plan.set_mode(args.mode)
 
-    # corner pruning: the headline and the latency systems, headline mode
-    pruned = [pruned_case(args.workload, args.mode, device, stream, flush, min(args.steps, 500),
-                          args.warmup, halo_slots),
-              pruned_case(LATENCY_WORKLOAD, args.mode, device, stream, flush, min(args.steps, 500),
-                          args.warmup, lat_slots)]
+        # corner pruning: the headline and the latency systems, headline mode
+        pruned = [pruned_case(args.workload, args.mode, device, stream, flush, min(args.steps, 500),
+                              args.warmup, halo_slots),
+                  pruned_case(LATENCY_WORKLOAD, args.mode, device, stream, flush, min(args.steps, 500),
+                              args.warmup, lat_slots)]
 
 
-    # context only: the same steps back to back without the L2 flush (the 1M
-    # system's working set fits in L2), labelled as such
-    warm = {}
-    plan.set_mode(args.mode)
-    for _ in range(args.warmup):
-        plan.exchange_x(loc, stream)
-        plan.exchange_f(f0, stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    nwarm = min(args.steps, 1000)
-    e0.record(stream)
-    for _ in range(nwarm):
-        plan.exchange_x(loc, stream)
-        plan.exchange_f(f0, stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    assert plan.status() == 0
-    warm = {"mode": args.mode, "us_per_exchange": 1e3 * e0.elapsed_time(e1) / nwarm,
-            "note": "back to back, no L2 flush: inputs stay in L2; context, not the headline"}
-
-    # the same step captured as a CUDA graph (one graph launch per x + f)
-    graph = {}
-    for mode in [m for m in (args.mode, "fused") if m != "staged"]:  # staged cannot be captured
-        plan.set_mode(mode)
-        gs = time_graph_steps(plan, loc, f0.clone(), min(args.steps, 1000), args.warmup, flush, stream)
+        # context only: the same steps back to back without the L2 flush (the 1M
+        # system's working set fits in L2), labelled as such
+        warm = {}
+        plan.set_mode(args.mode)
+        for _ in range(args.warmup):
+            plan.exchange_x(loc, stream)
+            plan.exchange_f(f0, stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nwarm = min(args.steps, 1000)
+        e0.record(stream)
+        for _ in range(nwarm):
+            plan.exchange_x(loc, stream)
+            plan.exchange_f(f0, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
         assert plan.status() == 0
-        graph[mode] = {"us_per_exchange": 1e3 * statistics.fmean(gs)}
-    plan.set_mode(args.mode)
+        warm = {"mode": args.mode, "us_per_exchange": 1e3 * e0.elapsed_time(e1) / nwarm,
+                "note": "back to back, no L2 flush: inputs stay in L2; context, not the headline"}
 
-    all_configs = configs_case(args.mode, device, stream, flush, min(args.steps, 300), args.warmup)
-    rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
-    pruned.append(pruned_case(REBUILD_WORKLOAD, args.mode, device, stream, flush,
-                              min(args.steps, 300), args.warmup, rebuild["halo_slots"]))
-    stencil_res = stencil_case(device, stream, flush, min(args.steps, 50), max(3, min(args.warmup, 5)))
-    overlap = [overlap_case(plan, loc, f0.clone(), min(args.steps, 300), args.warmup, flush, m, device,
-                            prio) for m in (args.mode, "fused") for prio in (0, -1)]
-    plan.set_mode(args.mode)
+        # the same step captured as a CUDA graph (one graph launch per x + f)
+        graph = {}
+        for mode in [m for m in (args.mode, "fused") if m != "staged"]:  # staged cannot be captured
+            plan.set_mode(mode)
+            gs = time_graph_steps(plan, loc, f0.clone(), min(args.steps, 1000), args.warmup, flush, stream)
+            assert plan.status() == 0
+            graph[mode] = {"us_per_exchange": 1e3 * statistics.fmean(gs)}
+        plan.set_mode(args.mode)
 
-    # end to end through the public API with host buffers
-    e2e_ms, h2d, d2h, e2e_serial_ms = e2e_steps(w, xyz, plan, max(20, min(args.steps, 200)), 5,
-                                                 device, stream)
-    assert plan.status() == 0
-    (e2e_ms,) = max_over_ranks([e2e_ms], device, dist)
-    e2e_value = whole_job_rate(halo_slots, world, e2e_ms * 1e-3)
+        all_configs = configs_case(args.mode, device, stream, flush, min(args.steps, 300), args.warmup)
+        rebuild = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
+        pruned.append(pruned_case(REBUILD_WORKLOAD, args.mode, device, stream, flush,
+                                  min(args.steps, 300), args.warmup, rebuild["halo_slots"]))
+        stencil_res = stencil_case(device, stream, flush, min(args.steps, 50), max(3, min(args.warmup, 5)))
+        overlap = [overlap_case(plan, loc, f0.clone(), min(args.steps, 300), args.warmup, flush, m, device,
+                                prio) for m in (args.mode, "fused") for prio in (0, -1)]
+        plan.set_mode(args.mode)
+
+        # end to end through the public API with host buffers
+        e2e_ms, h2d, d2h, e2e_serial_ms = e2e_steps(w, xyz, plan, max(20, min(args.steps, 200)), 5,
+                                                     device, stream)
+        assert plan.status() == 0
+        (e2e_ms,) = max_over_ranks([e2e_ms], device, dist)
+        e2e_value = whole_job_rate(halo_slots, world, e2e_ms * 1e-3)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.headline_only:
         cpu = cpu_baseline(args.workload, args.cpu_seconds)
 
     if rank == 0:
@@ -951,11 +978,12 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": dict(workload_config(w, plan.n_pulses, halo_slots, world), mode=args.mode,
-                           l2="inputs larger than L2: %d copies of the system (%d MB, %.1fx L2) stepped "
-                             "in turn, back to back" % (len(reps), rep_bytes >> 20,
-                                                        rep_bytes / torch.cuda.get_device_properties(
-                                                            device).L2_cache_size)),
+            "config": workload_config(w, plan.n_pulses, halo_slots, world),
+            "mode": args.mode,
+            "l2": "inputs larger than L2: %d copies of the system (%d MB, %.1fx L2) stepped "
+                  "in turn, back to back" % (len(reps), rep_bytes >> 20,
+                                             rep_bytes / torch.cuda.get_device_properties(
+                                                 device).L2_cache_size),
             "us_per_exchange": 1e3 * step_ms, "us_x": 1e3 * x_ms, "us_f": 1e3 * f_ms,
             "per_step_flushed": dict(head_flushed, note="one step at a time, L2 flushed before each "
                                      "(%d MB written+read), an event pair around each" % (flush_bytes >> 20)),
@@ -964,8 +992,18 @@ def main():
             "hbm_frac_nominal_8tbs": alg_gbs / 8000.0,
             "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
+                         "frac": achieved / peak,
+                         "traffic": None if traffic is None else traffic["read"] + traffic["write"],
+                         "traffic_read": None if traffic is None else traffic["read"],
+                         "traffic_write": None if traffic is None else traffic["write"],
                          "algorithmic_bytes_per_launch": per_slot * halo_slots,
+                         "algorithmic_read_bytes_per_launch": read_slot * halo_slots,
+                         "read_amplification": None if traffic is None
+                         else traffic["read"] / (read_slot * halo_slots),
+                         "traffic_note": "one ncu launch (cold L2) of this kernel on this system; "
+                                         "its writes stay in the 126 MB L2 when that launch ends, so "
+                                         "traffic_write reads near 0 here (written back later); compare "
+                                         "reads with the algorithmic reads",
                          "us_per_launch": 1e3 * dom_ms,
                          "timing": "CUDA events around %d back-to-back launches of this kernel alone, "
                                    "over the copies of the system in turn" % min(args.steps, 1000)},
@@ -978,10 +1016,11 @@ def main():
             "rebuild_case": rebuild,
             "overlap_case": overlap,
             "stencil_case": stencil_res,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms,
-                    "schedule": "steps pipelined: H2D of step i+1 overlaps D2H of step i",
-                    "unpipelined_us_per_step": 1e3 * e2e_serial_ms},
+            "e2e": None if e2e_ms is None else {
+                "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms,
+                "schedule": "steps pipelined: H2D of step i+1 overlaps D2H of step i",
+                "unpipelined_us_per_step": 1e3 * e2e_serial_ms},
             "gpu_launches": launches,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -138,6 +138,9 @@ int halo_setup_ex(const float box[3], const int32_t grid[3], float rc, const flo
             cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->dev) !=
                 cudaSuccess)
             rc_ = HALO_ECUDA;
+        // the fixed array of halo_exchange_x_noalloc gets its device address
+        // here, so that call never loads or places anything itself
+        if (rc_ == HALO_OK) rc_ = halo::noalloc_prepare();
         if (rc_ == HALO_OK) rc_ = do_build(pl, coords, domain_of_atom, n_atoms, stream);
     } catch (const std::bad_alloc&) {
         rc_ = HALO_ENOMEM;

@@ -200,6 +200,10 @@ int reset_flags(halo_plan* pl, cudaStream_t st);
 
 void free_build(halo_plan* pl);
 
+// halo_noalloc.cu: stores the device address of halo_exchange_x_noalloc's
+// fixed array for the current device (once per device; called by setup)
+int noalloc_prepare();
+
 inline int cuda_code(cudaError_t e) { return e == cudaSuccess ? HALO_OK : HALO_ECUDA; }
 
 // Launch with programmatic stream serialization: the kernel may be scheduled

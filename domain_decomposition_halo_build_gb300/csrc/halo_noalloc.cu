@@ -18,6 +18,12 @@
 // counters: plans with n_domains * n_pulses above that are rejected with
 // HALO_ESCRATCH.  Every GPU that loads the library holds the array (64 KiB)
 // until the process exits.
+//
+// Where the array lives: halo_setup (which allocates anyway) looks up the
+// array's device address once per device, with that device current.  Under
+// lazy module loading that lookup is what places the array in device
+// memory, so the no-allocation call itself only reads the stored address.
+#include <atomic>
 #include <mutex>
 
 #include "halo_internal.cuh"
@@ -33,25 +39,38 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_lock;
-void* g_scratch_addr[kMaxDevices] = {};
+std::atomic<void*> g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+
+namespace halo {
 
 // Device address of the array on the current device.  In host code the
 // array's name only stands in for the symbol, so the address is looked up
-// once per device, with that device current.
-int scratch_address(void** out) {
+// (once per device, with that device current) and stored.
+int noalloc_prepare() {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HALO_ECUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return HALO_ECUDA;
+    if (dev >= kMaxDevices) return HALO_OK;  // no fixed array there: the call reports HALO_ECUDA
     std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev].load()) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             (void)cudaGetLastError();
             return HALO_ECUDA;
         }
-        g_scratch_addr[dev] = p;
+        g_scratch_addr[dev].store(p);
     }
-    *out = g_scratch_addr[dev];
     return HALO_OK;
+}
+
+}  // namespace halo
+
+namespace {
+
+// The stored address for the plan's device (set by halo_setup), or null.
+void* scratch_address(int dev) {
+    return dev >= 0 && dev < kMaxDevices ? g_scratch_addr[dev].load() : nullptr;
 }
 
 }  // namespace
@@ -67,7 +86,8 @@ extern "C" int halo_exchange_x_noalloc(halo_plan* pl, float* local_coords, void*
     int rc = HALO_OK;
     void* base = nullptr;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = scratch_address(&base);
+    base = scratch_address(pl->dev);
+    if (!base) rc = HALO_ECUDA;
     if (rc == HALO_OK && pl->n_items_x > 0) {
         // clear the ticket block and the counters this plan uses
         const size_t bytes = kTicketBytes + sizeof(uint32_t) * (size_t)counters;

@@ -200,9 +200,12 @@ int halo_exchange_x(halo_plan* plan, float* local_coords, void* stream);
  *     nothing runs (building them would allocate).
  *   - n_domains * n_pulses must be <= HALO_NOALLOC_MAX_COUNTERS, else
  *     HALO_ESCRATCH and nothing runs.
- *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *   - halo_setup looks the array's device address up (cudaGetSymbolAddress,
+ *     once per device, with that device current); under lazy module loading
+ *     that is when the array is placed in device memory.  This call only
+ *     reads the stored address, so even the first call on a device loads and
+ *     allocates nothing.  HALO_ECUDA if no address is stored for the plan's
+ *     device.
  *   - Each call clears the part of the array it uses (an asynchronous memset
  *     on `stream`) before its launch.  All calls share the array: calls whose
  *     kernels overlap on the GPU race and give wrong results.

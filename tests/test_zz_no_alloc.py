@@ -2,18 +2,28 @@
 allocate device memory when they call in (a host framework whose pool
 allocator owns all device memory, or a latency-critical loop where cudaMalloc
 / cudaFree and the device-wide synchronisation they can cause are not
-acceptable).  Its scratch is a fixed array inside the library.
+acceptable).  Its scratch is a fixed array inside the library, whose device
+address halo_setup looks up.
 
-Checked through the C ABI: two calls in a row give the same coordinates as
-halo_exchange_x (bit-exact, the tolerance of every coordinate test here), a
-plan too large for the fixed array is refused with HALO_ESCRATCH, and the
-calls leave the device's free memory unchanged.  This file is collected last
-and builds everything it needs, so it runs alone or after the other tests."""
+Checked through the C ABI:
+- two calls in a row give the oracle's coordinates and halo_exchange_x's,
+  bit-exact (the tolerance of every coordinate test here);
+- calls interleaved with halo_exchange_x on one plan (two epoch schemes: the
+  plan's growing ticket, and the fixed array cleared on every call) leave
+  each other's results intact;
+- a call whose wait times out (a dropped signal, 50 ms limit) is reported by
+  halo_status, and the next call is exact again;
+- a plan too large for the fixed array is refused with HALO_ESCRATCH;
+- the calls, the first one included, leave the device's free memory
+  unchanged (a coarse guard: free memory is counted in whole driver pages).
+This file is collected last and builds everything it needs, so it runs alone
+or after the other tests."""
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 from domain_decomposition_halo_build_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -58,7 +68,88 @@ def test_noalloc_matches_exchange_x_twice(name):
         plan.close()
 
 
+def _oracle_x(name):
+    w = synth.WORKLOADS[name]
+    xyz, dom = synth.system(w)
+    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+    want = o.load_home(xyz)
+    o.exchange_x(want)
+    return want
+
+
+def test_noalloc_matches_the_oracle_twice():
+    """Directly against the CPU oracle, on the multi-pulse system whose
+    forwarded entries wait on earlier pulses: two calls in a row."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    want = _oracle_x("water24k_2x4x8")
+    plan, x = _plan("water24k_2x4x8")
+    try:
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for call in range(2):
+            got = plan.load_home(x)
+            assert lib.halo_exchange_x_noalloc(plan.handle, ctypes.c_void_p(got.data_ptr()),
+                                               stream) == halo.OK
+            assert plan.status() == halo.OK
+            np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32), want.view(np.uint32),
+                                          err_msg="call %d" % call)
+    finally:
+        plan.close()
+
+
+def test_noalloc_interleaved_with_exchange_x():
+    """x, noalloc, x, noalloc on one plan, each result against the oracle."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    want = _oracle_x("water24k_2x4x8")
+    plan, x = _plan("water24k_2x4x8")
+    try:
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for call, fn in enumerate([lib.halo_exchange_x, lib.halo_exchange_x_noalloc] * 2):
+            got = plan.load_home(x)
+            assert fn(plan.handle, ctypes.c_void_p(got.data_ptr()), stream) == halo.OK
+            assert plan.status() == halo.OK
+            np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32), want.view(np.uint32),
+                                          err_msg="call %d" % call)
+    finally:
+        plan.close()
+
+
+def test_noalloc_after_a_timed_out_wait():
+    """A producer's signal dropped on the host side (test hook) makes the
+    call's consumers give up after 50 ms; halo_status reports HALO_ETIMEOUT
+    and clears it, and the next call is exact again.  No GPU fault: every
+    wait is bounded."""
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    lib = halo.load_library()
+    want = _oracle_x("water24k_2x4x8")
+    plan, x = _plan("water24k_2x4x8")
+    try:
+        plan.set_wait_timeout(0.05)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        plan.debug_drop_signal(0, 0)   # z0 of domain 0 feeds the z1 pulse of its receiver
+        loc = plan.load_home(x)
+        assert lib.halo_exchange_x_noalloc(plan.handle, ctypes.c_void_p(loc.data_ptr()),
+                                           stream) == halo.OK
+        assert plan.status() == halo.ETIMEOUT
+        assert plan.status() == halo.OK
+        for call in range(2):
+            got = plan.load_home(x)
+            assert lib.halo_exchange_x_noalloc(plan.handle, ctypes.c_void_p(got.data_ptr()),
+                                               stream) == halo.OK
+            assert plan.status() == halo.OK
+            np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32), want.view(np.uint32),
+                                          err_msg="call %d after the timeout" % call)
+    finally:
+        plan.close()
+
+
 def test_noalloc_leaves_free_memory_unchanged():
+    """From before the first call on the plan: halo_setup placed the fixed
+    array, so no call here allocates."""
     import torch
     from domain_decomposition_halo_build_gb300 import halo
     lib = halo.load_library()
@@ -67,10 +158,9 @@ def test_noalloc_leaves_free_memory_unchanged():
         loc = plan.load_home(x)
         stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         ptr = ctypes.c_void_p(loc.data_ptr())
-        assert lib.halo_exchange_x_noalloc(plan.handle, ptr, stream) == 0   # first call: set-up
         torch.cuda.synchronize()
         free0 = torch.cuda.mem_get_info()[0]
-        for _ in range(5):
+        for _ in range(6):
             assert lib.halo_exchange_x_noalloc(plan.handle, ptr, stream) == 0
         torch.cuda.synchronize()
         assert torch.cuda.mem_get_info()[0] == free0
