@@ -194,10 +194,20 @@ __device__ __forceinline__ int64_t pair_value(const int32_t* __restrict__ in, in
     return (int64_t)(k <= 3 ? 1 : 0) | ((int64_t)(k > 3 && k <= 11 ? 1 : 0) << 32);
 }
 
+// The element count n comes from the host, or (n_dev != nullptr) from the
+// device: the high half of *n_dev (the owner count of the SRC 0 scan's grand
+// total), with the grid sized for the host bound n.
+__device__ __forceinline__ int64_t scan_count(int64_t n, const int64_t* n_dev) {
+    return n_dev ? (*n_dev >> 32) : n;
+}
+
 template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_reduce_kernel(const int32_t* __restrict__ in,
-                                                               int64_t n, int64_t* __restrict__ sums) {
+                                                               int64_t n, const int64_t* n_dev,
+                                                               int64_t* __restrict__ sums) {
+    n = scan_count(n, n_dev);
     const int64_t b0 = (int64_t)blockIdx.x * kScanTile;
+    if (b0 >= n) return;
     int64_t s = 0;
     for (int j = threadIdx.x; j < kScanTile; j += kThreads)
         if (b0 + j < n) s += pair_value<SRC>(in, b0 + j);
@@ -206,8 +216,12 @@ __global__ void __launch_bounds__(kThreads) pair_reduce_kernel(const int32_t* __
     if (threadIdx.x == 0) sums[blockIdx.x] = tot;
 }
 
-// Scans the nb tile sums in place and stores the grand total in sums[nb].
-__global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ sums, int64_t nb) {
+// Scans the nb tile sums in place and stores the grand total in sums[nb]
+// and, if given, in *total.
+__global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ sums, int64_t n,
+                                                        const int64_t* n_dev, int64_t* total) {
+    n = scan_count(n, n_dev);
+    const int64_t nb = (n + kScanTile - 1) / kScanTile;
     int64_t carry = 0;
     for (int64_t b = 0; b < nb; b += 1024) {
         const int64_t i = b + threadIdx.x;
@@ -217,7 +231,10 @@ __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ su
         if (i < nb) sums[i] = carry + pre;
         carry += tot;
     }
-    if (threadIdx.x == 0) sums[nb] = carry;
+    if (threadIdx.x == 0) {
+        sums[nb] = carry;
+        if (total) *total = carry;
+    }
 }
 
 // Down pass: each warp takes a contiguous run of kScanTile / warps elements
@@ -226,12 +243,15 @@ __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ su
 // the exclusive prefixes with a shuffle scan per 32 elements.
 template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __restrict__ in, int64_t n,
+                                                             const int64_t* n_dev,
                                                              const int64_t* __restrict__ sums,
                                                              int32_t* __restrict__ out_a,
                                                              int32_t* __restrict__ out_b) {
     constexpr int kWarps = kThreads / 32;
     constexpr int R = kScanTile / kThreads;  // rounds of 32 per warp
     __shared__ int64_t wsum[kWarps];
+    n = scan_count(n, n_dev);
+    if ((int64_t)blockIdx.x * kScanTile >= n) return;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t r0 = (int64_t)blockIdx.x * kScanTile + (int64_t)w * 32 * R;
     int64_t v[R];
@@ -267,21 +287,25 @@ __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __re
 }
 
 // Launches the three passes; sums holds ceil(n / kScanTile) + 1 int64 (the
-// grand total lands in its last entry).
+// grand total lands in its last entry, and in *total if given).  n_dev: see
+// scan_count (n is then the bound the grids are sized for).
 template <int SRC>
-int pair_scan(const int32_t* in, int64_t n, int64_t* sums, int32_t* out_a, int32_t* out_b,
-              cudaStream_t st) {
+int pair_scan(const int32_t* in, int64_t n, const int64_t* n_dev, int64_t* sums, int32_t* out_a,
+              int32_t* out_b, int64_t* total, cudaStream_t st) {
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
-    if (nb > 0) pair_reduce_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, sums);
-    pair_top_kernel<<<1, 1024, 0, st>>>(sums, nb);
-    if (nb > 0) pair_down_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, sums, out_a, out_b);
+    if (nb > 0) pair_reduce_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, n_dev, sums);
+    pair_top_kernel<<<1, 1024, 0, st>>>(sums, n, n_dev, total);
+    if (nb > 0)
+        pair_down_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, n_dev, sums, out_a, out_b);
     return cuda_code(cudaGetLastError());
 }
 
 __global__ void owner_list_kernel(const int32_t* __restrict__ ncopies,
                                   const int32_t* __restrict__ entry_pos,
                                   const int32_t* __restrict__ owner_idx, int64_t n, int32_t* fown,
-                                  int32_t* fstart) {
+                                  int32_t* fstart, const int64_t* __restrict__ total) {
+    // total: copies (low half) and owners (high half) of the copy-count scan
+    if (blockIdx.x == 0 && threadIdx.x == 0) fstart[*total >> 32] = (int32_t)(*total & 0xffffffffll);
     for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x)
         if (ncopies[j] > 0) {
@@ -305,8 +329,9 @@ __global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t*
 // replace each copy's parent slot by the parent's position (0 = the owner).
 __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
                                   const int32_t* __restrict__ tmp, const int32_t* __restrict__ parent,
-                                  const int8_t* __restrict__ hop, int64_t n_owners,
+                                  const int8_t* __restrict__ hop, const int64_t* __restrict__ total,
                                   int32_t* __restrict__ fent, int* max_copies, int* err) {
+    const int64_t n_owners = *total >> 32;
     __shared__ int block_max;
     if (threadIdx.x == 0) block_max = 0;
     __syncthreads();
@@ -754,9 +779,11 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
 
 __global__ void owner_record_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
                                     const int32_t* __restrict__ fent, const int32_t* __restrict__ posA,
-                                    const int32_t* __restrict__ posB, int64_t n_owners,
+                                    const int32_t* __restrict__ posB,
+                                    const int64_t* __restrict__ total,
                                     int4* __restrict__ recA, int4* __restrict__ recB,
                                     int4* __restrict__ recC) {
+    const int64_t n_owners = *total >> 32;
     for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
          m += (int64_t)gridDim.x * blockDim.x) {
         const int s0 = fstart[m], k = fstart[m + 1] - s0;
@@ -838,15 +865,19 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     }
     pl->n_xflat_items = (int)items.size();
     HALO_TRY(dev_reserve(&pl->d_xflat_items, &pl->cap_xflat_items, (int64_t)items.size()));
-    // pinned staging: the item list, then a few words read back below
-    HALO_CUDA(cudaStreamSynchronize(st));  // the staging may grow: nothing in flight uses it
+    // pinned staging: the item list, then words read back at the end, after
+    // the descriptors that prepare_common may still be copying from its
+    // start; only a staging that must grow waits for the stream first
+    const size_t sp_bytes = ((pl->sp.size() * sizeof(SPDesc) + 15) & ~(size_t)15) + 64;
+    const size_t need = sp_bytes + items.size() * sizeof(int4) + 256;
+    if (pl->h_stage_cap < need) HALO_CUDA(cudaStreamSynchronize(st));
     char* stage = nullptr;
     {
         void* hs = nullptr;
-        HALO_TRY(host_stage(pl, items.size() * sizeof(int4) + 256, &hs));
-        stage = static_cast<char*>(hs);
+        HALO_TRY(host_stage(pl, need, &hs));
+        stage = static_cast<char*>(hs) + sp_bytes;
     }
-    int32_t* hw = reinterpret_cast<int32_t*>(stage + items.size() * sizeof(int4));  // 16 words
+    int64_t* hw = reinterpret_cast<int64_t*>(stage + items.size() * sizeof(int4));  // 8 words
     if (!items.empty()) {
         memcpy(stage, items.data(), items.size() * sizeof(int4));
         HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, stage, items.size() * sizeof(int4),
@@ -855,11 +886,19 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat,
                          std::max<int64_t>((int64_t)items.size() * kFlatChunk, 1)));
     HALO_TRY(dev_reserve(&pl->d_fent, &pl->cap_fent, H));
+    // owner tables sized by bounds (every halo slot is one copy of one owner:
+    // at most H owners, H / 4 with 4..11 copies, H / 12 with more), so that
+    // no count has to come back to the host before the end
+    HALO_TRY(dev_reserve(&pl->d_fown, &pl->cap_fown, H));
+    HALO_TRY(dev_reserve(&pl->d_fstart, &pl->cap_fstart, H + 1));
+    HALO_TRY(dev_reserve(&pl->d_frec[0], &pl->cap_frec[0], H));
+    HALO_TRY(dev_reserve(&pl->d_frec[1], &pl->cap_frec[1], 3 * (H / 4 + 1)));
+    HALO_TRY(dev_reserve(&pl->d_frec[2], &pl->cap_frec[2], H / 12 + 1));
 
     // scratch of the table build, carved from two pools kept in the plan
     const int64_t nsums = nl / kScanTile + 2;            // int64 tile sums + grand total
     const int64_t off_sums = (6 * nl + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
-    HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 8));
+    HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 16));
     HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
     int32_t* owner = pl->d_flat_pool32;
     int32_t* parent = owner + nl;
@@ -869,85 +908,65 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int32_t* owner_idx = flag + nl;
     int32_t* tmp = owner_idx + nl;
     int64_t* sums = reinterpret_cast<int64_t*>(pl->d_flat_pool32 + off_sums);
+    // misc: [0] largest copy list, [1] error; misc64: [0] copies | owners << 32,
+    // [1] class-A | class-B records << 32
     int32_t* misc = pl->d_flat_pool32 + off_sums + 2 * nsums;
+    int64_t* misc64 = reinterpret_cast<int64_t*>(misc + 8);
     int8_t* hop = pl->d_flat_pool8;
     int8_t* code = hop + nl;
-    int64_t* h64 = reinterpret_cast<int64_t*>(hw + 8);     // 8-byte aligned words read back
     int rc = HALO_OK;
     do {
         const int gb = blocks_for(nl, pl->num_sms);
+        const int gh = blocks_for(std::max<int64_t>(H, 1), pl->num_sms);
         for (int p = 0; p < P; p++) {
             const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
             chain_pulse_kernel<<<dim3(gx, nd), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, owner, parent,
                                                                   hop, code, P, p, pl->pulse_dim[p]);
         }
         if ((rc = cuda_code(cudaMemsetAsync(ncopies, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
+        if ((rc = cuda_code(cudaMemsetAsync(flag, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
+        if ((rc = cuda_code(cudaMemsetAsync(misc, 0, sizeof(int32_t) * 16, st))) != HALO_OK) break;
         if (!items.empty())
             xflat_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
                                                                        pl->d_xflat, ncopies);
         // entry offsets of every slot's copy list and the owner index of every
-        // slot with copies, in one pass; the grand total gives the owner count
-        if ((rc = pair_scan<0>(ncopies, nl, sums, entry_pos, owner_idx, st)) != HALO_OK) break;
-        const int64_t nb_l = (nl + kScanTile - 1) / kScanTile;
-        if ((rc = cuda_code(cudaMemcpyAsync(h64, sums + nb_l, sizeof(int64_t),
-                                            cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
-        if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
-        const int64_t n_owners = h64[0] >> 32;
-        if ((h64[0] & 0xffffffffll) != H) {  // every halo slot is one copy of one owner
-            rc = HALO_ECAPACITY;
+        // slot with copies, in one pass; the grand total (copies, owners)
+        // stays on the device
+        if ((rc = pair_scan<0>(ncopies, nl, nullptr, sums, entry_pos, owner_idx, misc64, st)) != HALO_OK)
             break;
-        }
-        pl->n_owners = n_owners;
-        if ((rc = dev_reserve(&pl->d_fown, &pl->cap_fown, n_owners)) != HALO_OK) break;
-        if ((rc = dev_reserve(&pl->d_fstart, &pl->cap_fstart, n_owners + 1)) != HALO_OK) break;
         owner_list_kernel<<<gb, kThreads, 0, st>>>(ncopies, entry_pos, owner_idx, nl, pl->d_fown,
-                                                   pl->d_fstart);
-        hw[2] = (int32_t)H;
-        if ((rc = cuda_code(cudaMemcpyAsync(pl->d_fstart + n_owners, hw + 2, sizeof(int32_t),
-                                            cudaMemcpyHostToDevice, st))) != HALO_OK) break;
-        if ((rc = cuda_code(cudaMemsetAsync(flag, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
+                                                   pl->d_fstart, misc64);
         if (!items.empty())
             owner_fill_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner,
                                                                             entry_pos, flag, tmp);
-        if ((rc = cuda_code(cudaMemsetAsync(misc, 0, sizeof(int32_t) * 4, st))) != HALO_OK) break;
         // record classes (A: <= 3 copies, B: 4..11, C: more): slots in each
         // class from one paired scan of the owners' copy counts
         int32_t* posA = entry_pos;  // scratch reuse: owner_fill has read entry_pos
         int32_t* posB = ncopies;    // and owner_list ncopies
-        if (n_owners > 0) {
-            owner_sort_kernel<<<blocks_for(n_owners, pl->num_sms), kThreads, 0, st>>>(
-                pl->d_fown, pl->d_fstart, tmp, parent, hop, n_owners, pl->d_fent, misc, misc + 1);
-            if ((rc = pair_scan<1>(pl->d_fstart, n_owners, sums, posA, posB, st)) != HALO_OK) break;
-            const int64_t nb_o = (n_owners + kScanTile - 1) / kScanTile;
-            if ((rc = cuda_code(cudaMemcpyAsync(h64 + 1, sums + nb_o, sizeof(int64_t),
-                                                cudaMemcpyDeviceToHost, st))) != HALO_OK) break;
-        } else {
-            h64[1] = 0;
-        }
-        int32_t* info = hw + 4;
-        if ((rc = cuda_code(cudaMemcpyAsync(info, misc, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost,
-                                            st))) != HALO_OK)
+        owner_sort_kernel<<<gh, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, tmp, parent, hop, misc64,
+                                                   pl->d_fent, misc, misc + 1);
+        if ((rc = pair_scan<1>(pl->d_fstart, std::max<int64_t>(H, 1), misc64, sums, posA, posB,
+                               misc64 + 1, st)) != HALO_OK)
+            break;
+        owner_record_kernel<<<gh, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB,
+                                                     misc64, pl->d_frec[0], pl->d_frec[1], pl->d_frec[2]);
+        // the one synchronisation: counts, largest list, error
+        if ((rc = cuda_code(cudaMemcpyAsync(hw, misc, 8 * sizeof(int32_t) + 2 * sizeof(int64_t),
+                                            cudaMemcpyDeviceToHost, st))) != HALO_OK)
             break;
         if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaGetLastError())) != HALO_OK) break;
-        if (info[1] != 0) {
+        const int32_t* info = reinterpret_cast<const int32_t*>(hw);
+        const int64_t tot_copies = hw[4] & 0xffffffffll, n_owners = hw[4] >> 32;
+        if (info[1] != 0 || tot_copies != H) {  // every halo slot is one copy of one owner
             rc = HALO_ECAPACITY;
             break;
         }
+        pl->n_owners = n_owners;
         pl->max_copies = info[0];
-        pl->n_rec[0] = h64[1] & 0xffffffffll;
-        pl->n_rec[1] = h64[1] >> 32;
+        pl->n_rec[0] = hw[5] & 0xffffffffll;
+        pl->n_rec[1] = hw[5] >> 32;
         pl->n_rec[2] = n_owners - pl->n_rec[0] - pl->n_rec[1];
-        if (n_owners > 0) {
-            if ((rc = dev_reserve(&pl->d_frec[0], &pl->cap_frec[0], pl->n_rec[0])) != HALO_OK) break;
-            if ((rc = dev_reserve(&pl->d_frec[1], &pl->cap_frec[1], 3 * pl->n_rec[1])) != HALO_OK) break;
-            if ((rc = dev_reserve(&pl->d_frec[2], &pl->cap_frec[2], pl->n_rec[2])) != HALO_OK) break;
-            owner_record_kernel<<<blocks_for(n_owners, pl->num_sms), kThreads, 0, st>>>(
-                pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB, n_owners, pl->d_frec[0],
-                pl->d_frec[1], pl->d_frec[2]);
-            if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
-            if ((rc = cuda_code(cudaGetLastError())) != HALO_OK) break;
-        }
     } while (false);
     if (rc != HALO_OK) return rc;
     pl->flat_ready = true;
