@@ -95,9 +95,11 @@ int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, 
     pl->trace_cap = 0;
     pl->flat_ready = false;  // the flattened tables describe the previous plan
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
+    halo::update_shard_first(pl);
     HALO_TRY(halo::prepare_common(pl, st));
     // each mode's own tables; the others are built when a mode is selected
-    if (pl->mode == HALO_MODE_FUSED) HALO_TRY(halo::prepare_fused(pl, st));
+    // (the sharded data plane runs on the FUSED work lists)
+    if (pl->mode == HALO_MODE_FUSED || pl->n_shards > 1) HALO_TRY(halo::prepare_fused(pl, st));
     if (pl->mode == HALO_MODE_FLAT) HALO_TRY(halo::prepare_flat(pl, st));
     if (pl->mode == HALO_MODE_STAGED) HALO_TRY(halo::prepare_staged(pl));
     pl->valid = true;
@@ -141,6 +143,7 @@ int halo_setup_ex(const float box[3], const int32_t grid[3], float rc, const flo
         // the fixed array of halo_exchange_x_noalloc gets its device address
         // here, so that call never loads or places anything itself
         if (rc_ == HALO_OK) rc_ = halo::noalloc_prepare();
+        if (rc_ == HALO_OK) rc_ = halo::set_shards(pl, 1);  // one shard: the dense buffer
         if (rc_ == HALO_OK) rc_ = do_build(pl, coords, domain_of_atom, n_atoms, stream);
     } catch (const std::bad_alloc&) {
         rc_ = HALO_ENOMEM;
@@ -277,6 +280,70 @@ int halo_exchange_f(halo_plan* pl, float* local_forces, void* stream) {
         case HALO_MODE_STAGED: return halo::launch_staged_f(pl, local_forces, as_stream(stream));
         default: return halo::launch_exchange_f(pl, local_forces, as_stream(stream));
     }
+}
+
+// ---- sharded data plane -------------------------------------------------------
+
+int halo_shard(halo_plan* pl, int32_t n_shards, void* stream) {
+    if (!pl || !pl->valid) return HALO_EINVAL;
+    DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
+    HALO_TRY(halo::set_shards(pl, n_shards));
+    // the work lists carry each item's shards
+    return halo::prepare_fused(pl, as_stream(stream));
+}
+
+int halo_shard_layout(const halo_plan* pl, int32_t shard, int32_t* first_domain, int32_t* n_domains,
+                      int64_t* first_slot, int64_t* n_local) {
+    if (!pl || !pl->valid || shard < 0 || shard >= pl->n_shards) return HALO_EINVAL;
+    if (first_domain) *first_domain = pl->shard_dom[shard];
+    if (n_domains) *n_domains = pl->shard_dom[shard + 1] - pl->shard_dom[shard];
+    if (first_slot) *first_slot = pl->shard_first[shard];
+    if (n_local) *n_local = pl->shard_first[shard + 1] - pl->shard_first[shard];
+    return HALO_OK;
+}
+
+namespace {
+bool shard_ptrs_ok(const halo_plan* pl, const void* const* p) {
+    if (!p) return false;
+    for (int k = 0; k < pl->n_shards; k++)
+        if (!p[k] || ((uintptr_t)p[k] & 3u)) return false;
+    return true;
+}
+}  // namespace
+
+int halo_load_home_sharded(const halo_plan* pl, const float* global_xyz, float* const* shard_local,
+                           void* stream) {
+    if (!pl || !global_xyz || !pl->valid || !shard_ptrs_ok(pl, (const void* const*)shard_local))
+        return HALO_EINVAL;
+    DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
+    return halo::launch_load_home_sharded(pl, global_xyz, shard_local, as_stream(stream));
+}
+
+int halo_store_home_sharded(const halo_plan* pl, const float* const* shard_local, float* global_xyz,
+                            void* stream) {
+    if (!pl || !global_xyz || !pl->valid || !shard_ptrs_ok(pl, (const void* const*)shard_local))
+        return HALO_EINVAL;
+    DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
+    return halo::launch_store_home_sharded(pl, shard_local, global_xyz, as_stream(stream));
+}
+
+int halo_exchange_x_sharded(halo_plan* pl, float* const* shard_coords, void* stream) {
+    if (!pl || !pl->valid || !pl->fused_ready || !shard_ptrs_ok(pl, (const void* const*)shard_coords))
+        return HALO_EINVAL;
+    DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
+    return halo::launch_exchange_x_sharded(pl, shard_coords, as_stream(stream));
+}
+
+int halo_exchange_f_sharded(halo_plan* pl, float* const* shard_forces, void* stream) {
+    if (!pl || !pl->valid || !pl->fused_ready || !shard_ptrs_ok(pl, (const void* const*)shard_forces))
+        return HALO_EINVAL;
+    DeviceGuard g(pl->dev);
+    if (!g.ok) return HALO_ECUDA;
+    return halo::launch_exchange_f_sharded(pl, shard_forces, as_stream(stream));
 }
 
 int halo_status(halo_plan* pl, void* stream) {

@@ -55,6 +55,20 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     return v;
 }
 
+// System scope: the sharded data plane, whose counters and buffers would sit
+// on different GPUs ("Redesigning GROMACS Halo Exchange ...", section 4,
+// memory ordering: the receiver's signal is a system-scope release store).
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <bool SYS>
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    return SYS ? ld_acquire_sys(p) : ld_acquire_gpu(p);
+}
+
 __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
     int v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -63,6 +77,23 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
 
 __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_release_sys_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.sys.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+template <bool SYS>
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+    if (SYS)
+        red_release_sys_add(p, v);
+    else
+        red_release_gpu_add(p, v);
+}
+
+// Dense slot g of shard k in the sharded data plane.
+__device__ __forceinline__ float* shard_slot(const ShardTable& t, int k, int64_t g) {
+    return t.ptr[k] + 3 * (g - t.first[k]);
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -96,15 +127,16 @@ __device__ __forceinline__ void trace_item(unsigned long long* trace, int item, 
 // Bounded wait until *c has reached target (modulo 2^32).  On timeout the
 // first waiter records where it gave up; every waiter gives up as soon as the
 // plan's error word is set.
+template <bool SYS>
 __device__ bool wait_count(const uint32_t* c, uint32_t target, int* err, long long timeout_ns,
                            int kernel, int flag) {
-    if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) return true;
+    if ((int32_t)(ld_acquire<SYS>(c) - target) >= 0) return true;
     const uint64_t t0 = global_timer_ns();
     unsigned ns = 8;
     for (;;) {
         __nanosleep(ns);
         if (ns < 128) ns <<= 1;
-        if ((int32_t)(ld_acquire_gpu(c) - target) >= 0) return true;
+        if ((int32_t)(ld_acquire<SYS>(c) - target) >= 0) return true;
         if (ld_relaxed_gpu(err) != 0) return false;
         if ((long long)(global_timer_ns() - t0) > timeout_ns) {
             if (atomicCAS(err, 0, HALO_ETIMEOUT) == 0) {
@@ -129,6 +161,7 @@ struct XArgs {
     int drop_flag;
     int64_t n_slots;  // local slots (checked in debug builds)
     unsigned long long* trace;  // optional: 4 words per item (see halo_set_trace)
+    ShardTable sh;    // sharded data plane only
 };
 
 struct FArgs {
@@ -143,6 +176,7 @@ struct FArgs {
     long long timeout_ns;
     unsigned long long* trace;
     int64_t n_slots;  // local slots (checked in debug builds)
+    ShardTable sh;    // sharded data plane only
 };
 
 constexpr int kWarps = kThreads / 32;
@@ -166,8 +200,10 @@ __device__ __forceinline__ WarpTicket decode_ticket(unsigned long long t, unsign
 // Coordinates: block-granular items of up to kThreads * E entries whose
 // destination is one contiguous halo range; the block stages it in shared
 // memory and one thread writes it with a single bulk copy.
-template <int E>
-__global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
+// SHARDED: the sharded data plane (sources and destinations in per-shard
+// buffers, system-scope signals); otherwise one dense buffer, gpu scope.
+template <int E, bool SHARDED>
+__global__ void __launch_bounds__(kThreads) pack_x_kernel(const __grid_constant__ XArgs a) {
     __shared__ __align__(128) float stage[3 * kThreads * E + 4];
     __shared__ unsigned long long s_ticket;
     __shared__ int s_go;
@@ -192,8 +228,8 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
         const XItem w = a.items[tk.item];
         const bool dependent = w.wait_mask != 0;
         const int32_t* map = a.maps + w.map_off;
-        const float* src = a.xyz + 3 * w.src_base;
-        float* dst = a.xyz + 3 * w.dst;
+        const float* src = SHARDED ? shard_slot(a.sh, w.src_shard, w.src_base) : a.xyz + 3 * w.src_base;
+        float* dst = SHARDED ? shard_slot(a.sh, w.dst_shard, w.dst) : a.xyz + 3 * w.dst;
         // index loads first: only the forwarded coordinates remain after a wait
         int idx[E];
         const bool dst_ok = w.len <= 0 || in_range(w.dst + w.len - 1, a.n_slots, a.err);
@@ -212,8 +248,8 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
                 int ok = 1;
                 for (uint64_t m = w.wait_mask; m && ok; m &= m - 1) {
                     const int c = w.wait_base + __ffsll((long long)m) - 1;
-                    ok = wait_count(a.arrived + c, tk.epoch * __ldg(a.target + c), a.err,
-                                    a.timeout_ns, 1, c);
+                    ok = wait_count<SHARDED>(a.arrived + c, tk.epoch * __ldg(a.target + c), a.err,
+                                             a.timeout_ns, 1, c);
                 }
                 s_go = ok;
             }
@@ -255,15 +291,15 @@ __global__ void __launch_bounds__(kThreads) pack_x_kernel(XArgs a) {
         __syncthreads();
         if (threadIdx.x == 0) {
             if (dst_ok) bulk_store_floats(dst, stage, 3 * w.len, true);
-            if (w.flag != a.drop_flag) red_release_gpu_add(a.arrived + w.flag, 1u);
+            if (w.flag != a.drop_flag) red_release_add<SHARDED>(a.arrived + w.flag, 1u);
             if (a.trace) trace_item(a.trace, tk.item, t_take, t_wait);
         }
         // the next iteration's barrier keeps the stage until the copy has read it
     }
 }
 
-template <int E>
-__global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
+template <int E, bool SHARDED>
+__global__ void __launch_bounds__(kThreads, 4) unpack_f_kernel(const __grid_constant__ FArgs a) {
     const int lane = threadIdx.x & 31;
     grid_launch_dependents();  // as in pack_x_kernel
     grid_dependency_wait();
@@ -292,27 +328,34 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
                                   in_range(sd[e].y, a.n_slots, a.err)))
                 sd[e] = make_int2(-1, -1);
         }
+        // halo sources in r's shard, destinations in s's shard (one buffer
+        // when not sharded)
+        const float* fr = SHARDED ? a.sh.ptr[w.r_shard] : a.f;
+        float* fs = SHARDED ? a.sh.ptr[w.s_shard] : a.f;
+        const int64_t r0 = SHARDED ? a.sh.first[w.r_shard] : 0;
+        const int64_t s0 = SHARDED ? a.sh.first[w.s_shard] : 0;
         if (w.ms | w.mr) {
             // warm L2 with the lines read after the wait (L2 is coherent, so
-            // the loads that follow the acquire still see the latest values)
+            // the loads that follow the acquire still see the latest values);
+            // sharded: only the destination lines, which are s's own
 #pragma unroll
             for (int e = 0; e < E; e++) {
                 if (sd[e].x >= 0) {
-                    prefetch_l2(a.f + 3 * (int64_t)sd[e].x);
-                    prefetch_l2(a.f + 3 * (int64_t)sd[e].y);
+                    if (!SHARDED) prefetch_l2(fr + 3 * ((int64_t)sd[e].x - r0));
+                    prefetch_l2(fs + 3 * ((int64_t)sd[e].y - s0));
                 }
             }
             int ok = 1;
             if (lane == 0) {
                 for (uint64_t m = w.ms; m && ok; m &= m - 1) {
                     const int c = w.s_base + __ffsll((long long)m) - 1;
-                    ok = wait_count(a.done + c, tk.epoch * __ldg(a.target + c), a.err,
-                                    a.timeout_ns, 2, c);
+                    ok = wait_count<SHARDED>(a.done + c, tk.epoch * __ldg(a.target + c), a.err,
+                                             a.timeout_ns, 2, c);
                 }
                 for (uint64_t m = w.mr; m && ok; m &= m - 1) {
                     const int c = w.r_base + __ffsll((long long)m) - 1;
-                    ok = wait_count(a.done + c, tk.epoch * __ldg(a.target + c), a.err,
-                                    a.timeout_ns, 2, c);
+                    ok = wait_count<SHARDED>(a.done + c, tk.epoch * __ldg(a.target + c), a.err,
+                                             a.timeout_ns, 2, c);
                 }
             }
             if (!__shfl_sync(kFull, ok, 0)) return;
@@ -322,8 +365,8 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
 #pragma unroll
         for (int e = 0; e < E; e++) {
             if (sd[e].x >= 0) {
-                const float* hp = a.f + 3 * (int64_t)sd[e].x;
-                const float* op = a.f + 3 * (int64_t)sd[e].y;
+                const float* hp = fr + 3 * ((int64_t)sd[e].x - r0);
+                const float* op = fs + 3 * ((int64_t)sd[e].y - s0);
                 h[e][0] = __ldcg(hp);
                 h[e][1] = __ldcg(hp + 1);
                 h[e][2] = __ldcg(hp + 2);
@@ -335,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
 #pragma unroll
         for (int e = 0; e < E; e++) {
             if (sd[e].x >= 0) {
-                float* op = a.f + 3 * (int64_t)sd[e].y;
+                float* op = fs + 3 * ((int64_t)sd[e].y - s0);
                 op[0] = o[e][0] + h[e][0];
                 op[1] = o[e][1] + h[e][1];
                 op[2] = o[e][2] + h[e][2];
@@ -344,7 +387,7 @@ __global__ void __launch_bounds__(kThreads) unpack_f_kernel(FArgs a) {
         // the warp's stores, then one gpu-scope release by the leader
         __syncwarp();
         if (lane == 0) {
-            red_release_gpu_add(a.done + w.flag, 1u);
+            red_release_add<SHARDED>(a.done + w.flag, 1u);
             if (a.trace) trace_item(a.trace, tk.item, t_take, t_wait);
         }
         next = __shfl_sync(kFull, next, 0);
@@ -457,6 +500,45 @@ __global__ void store_home_kernel(const int64_t* __restrict__ home_dst,
     }
 }
 
+// Sharded data plane: the shard of dense slot dd (shards are contiguous
+// ranges of dense slots).
+__device__ __forceinline__ float* shard_slot_of(const ShardTable& t, int n_shards, int64_t dd) {
+    int k = 0;
+    while (k + 1 < n_shards && dd >= t.first[k + 1]) k++;
+    return t.ptr[k] + 3 * (dd - t.first[k]);
+}
+
+__global__ void load_home_sharded_kernel(const int64_t* __restrict__ home_dst,
+                                         const int32_t* __restrict__ home_gid, int64_t n,
+                                         const float* __restrict__ g,
+                                         const __grid_constant__ ShardTable t, int n_shards,
+                                         int64_t n_slots, int* err) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t dd = home_dst[i], a = home_gid[i];
+        if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
+        float* q = shard_slot_of(t, n_shards, dd);
+        q[0] = g[3 * a + 0];
+        q[1] = g[3 * a + 1];
+        q[2] = g[3 * a + 2];
+    }
+}
+
+__global__ void store_home_sharded_kernel(const int64_t* __restrict__ home_dst,
+                                          const int32_t* __restrict__ home_gid, int64_t n,
+                                          const __grid_constant__ ShardTable t, int n_shards,
+                                          float* __restrict__ g, int64_t n_slots, int* err) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t dd = home_dst[i], a = home_gid[i];
+        if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
+        const float* q = shard_slot_of(t, n_shards, dd);
+        g[3 * a + 0] = q[0];
+        g[3 * a + 1] = q[1];
+        g[3 * a + 2] = q[2];
+    }
+}
+
 __global__ void home_gid_kernel(const int64_t* __restrict__ home_dst,
                                 const int32_t* __restrict__ home_gid, int64_t n,
                                 int32_t* __restrict__ out) {
@@ -482,6 +564,8 @@ struct ItemGen {
     const int32_t* nindep;          // independent force entries per (s, p)
     const uint64_t* recv_mask;      // per domain: pulses that delivered a nonempty slice
     int nd, P, CH, CHF;
+    int n_shards;
+    int shard_dom[kMaxShards + 1];  // shard k holds domains [shard_dom[k], shard_dom[k + 1])
     uint64_t fms[HALO_MAX_PULSES];  // force waits on s per pulse
     uint64_t fmr[HALO_MAX_PULSES];  // force waits on r per pulse
 };
@@ -491,6 +575,12 @@ __global__ void recv_mask_kernel(const SPDesc* __restrict__ sp, int nsp, uint64_
         const SPDesc d = sp[i];
         if (d.send > 0) atomicOr((unsigned long long*)(mask + d.r), 1ull << d.p);
     }
+}
+
+__device__ __forceinline__ int16_t shard_of(const ItemGen& a, int D) {
+    int k = 0;
+    while (k + 1 < a.n_shards && D >= a.shard_dom[k + 1]) k++;
+    return (int16_t)k;
 }
 
 // Group g of the coordinate list: p = g / (2 nd), dependent first, sender s.
@@ -554,7 +644,8 @@ __global__ void item_fill_kernel(ItemGen a, const int32_t* __restrict__ bx,
             w.len = min(a.CH, hi - st0);
             w.flag = d.r * a.P + d.p;
             w.wait_base = d.s * a.P;
-            w.pad = dep ? 1 : 0;
+            w.src_shard = shard_of(a, d.s);
+            w.dst_shard = shard_of(a, d.r);
             w.wait_mask = mask;
             w.shift[0] = d.shift[0];
             w.shift[1] = d.shift[1];
@@ -578,6 +669,9 @@ __global__ void item_fill_kernel(ItemGen a, const int32_t* __restrict__ bx,
             w.r_base = d.r * a.P;
             w.ms = waits ? a.fms[d.p] : 0ull;
             w.mr = waits ? a.fmr[d.p] : 0ull;
+            w.s_shard = shard_of(a, d.s);
+            w.r_shard = shard_of(a, d.r);
+            w.pad = 0;
             iff[bf[g] + c] = w;
         }
     }
@@ -612,8 +706,9 @@ int upload(T** d, int64_t* cap, const std::vector<T>& h, char* stage, size_t* of
 
 template <int E>
 int occupancy(int* blocks_x, int* blocks_f) {
-    HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_x, pack_x_kernel<E>, kThreads, 0));
-    HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_f, unpack_f_kernel<E>, kThreads, 0));
+    // the sharded variants have the same resources (checked by the build's register report)
+    HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_x, pack_x_kernel<E, false>, kThreads, 0));
+    HALO_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_f, unpack_f_kernel<E, false>, kThreads, 0));
     return HALO_OK;
 }
 
@@ -739,6 +834,8 @@ int prepare_fused(halo_plan* pl, cudaStream_t st) {
     a.P = P;
     a.CH = CH;
     a.CHF = CHF;
+    a.n_shards = pl->n_shards;
+    for (int k = 0; k <= kMaxShards; k++) a.shard_dom[k] = pl->shard_dom[k];
     for (int p = 0; p < HALO_MAX_PULSES; p++) a.fms[p] = a.fmr[p] = 0;
     // dependent force entries of (s, p) wait for (s, q) and (r, q), q > p,
     // whose index maps can touch the same slots: pulse 0 of a later dim (its
@@ -815,7 +912,7 @@ int launch_exchange_x(halo_plan* pl, float* xyz, cudaStream_t st) {
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
-    const cudaError_t e = launch_dependent(pack_x_kernel<4>, dim3(pl->grid_x), dim3(kThreads), st, a);
+    const cudaError_t e = launch_dependent(pack_x_kernel<4, false>, dim3(pl->grid_x), dim3(kThreads), st, a);
     if (e != cudaSuccess) return cuda_code(e);
     pl->launches_x++;
     return HALO_OK;
@@ -839,7 +936,7 @@ int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
     a.drop_flag = pl->drop_flag;
     a.trace = pl->trace;
     pl->drop_flag = -1;
-    const cudaError_t e = launch_dependent(pack_x_kernel<4>, dim3(pl->grid_x), dim3(kThreads), st, a);
+    const cudaError_t e = launch_dependent(pack_x_kernel<4, false>, dim3(pl->grid_x), dim3(kThreads), st, a);
     if (e != cudaSuccess) return cuda_code(e);
     pl->launches_x++;
     return HALO_OK;
@@ -861,7 +958,7 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
     a.timeout_ns = pl->wait_timeout_ns;
     a.n_slots = pl->n_local_total;
     a.trace = pl->trace ? pl->trace + 4 * (size_t)pl->n_items_x : nullptr;
-    const cudaError_t e = launch_dependent(unpack_f_kernel<4>, dim3(pl->grid_f), dim3(kThreads), st, a);
+    const cudaError_t e = launch_dependent(unpack_f_kernel<4, false>, dim3(pl->grid_f), dim3(kThreads), st, a);
     if (e != cudaSuccess) return cuda_code(e);
     pl->launches_f++;
     return HALO_OK;
@@ -892,6 +989,116 @@ int launch_local_to_global(const halo_plan* pl, int32_t* out, cudaStream_t st) {
         halo_gid_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, out,
                                                                    pl->P, p);
     }
+    return cuda_code(cudaGetLastError());
+}
+
+// ---- sharded data plane ------------------------------------------------------------
+// The pages put the domains of one system on several GPUs: a pulse whose
+// receiver sits on another GPU stores the packed coordinates into that GPU's
+// halo slice and signals it with a system-scope release ("Redesigning GROMACS
+// Halo Exchange ...", section 3, NVLink path; section 4, memory ordering), and
+// the force pass reads the remote halo forces back.  Here the plan's domains
+// are split into z-slabs (shards), each with its own buffer, and the FUSED
+// work lists carry every item's source and destination shard.  On one GPU
+// every shard's items run in one launch, in ticket order, so the waits between
+// shards resolve by the same induction as in the FUSED mode.
+
+int set_shards(halo_plan* pl, int n_shards) {
+    const int nz = pl->grid[2];
+    if (n_shards < 1 || n_shards > kMaxShards || n_shards > nz) return HALO_EINVAL;
+    const int layer = pl->grid[0] * pl->grid[1];
+    pl->n_shards = n_shards;
+    for (int k = 0; k <= kMaxShards; k++) {
+        const int kk = std::min(k, n_shards);
+        pl->shard_dom[k] = (int)(((int64_t)kk * nz / n_shards) * layer);
+    }
+    update_shard_first(pl);
+    return HALO_OK;
+}
+
+void update_shard_first(halo_plan* pl) {
+    for (int k = 0; k <= kMaxShards; k++) {
+        const int D = pl->shard_dom[std::min(k, pl->n_shards)];
+        pl->shard_first[k] = D < pl->n_dom && D < (int)pl->base.size() ? pl->base[D] : pl->n_local_total;
+    }
+}
+
+namespace {
+ShardTable shard_table(const halo_plan* pl, const float* const* ptrs) {
+    ShardTable t;
+    for (int k = 0; k < kMaxShards; k++) {
+        t.ptr[k] = k < pl->n_shards ? const_cast<float*>(ptrs[k]) : nullptr;
+        t.first[k] = pl->shard_first[k];
+    }
+    return t;
+}
+}  // namespace
+
+int launch_exchange_x_sharded(halo_plan* pl, float* const* shard_xyz, cudaStream_t st) {
+    if (!pl->fused_ready) return HALO_EINVAL;
+    if (pl->n_items_x == 0) return HALO_OK;
+    XArgs a;
+    a.xyz = nullptr;
+    a.maps = pl->d_maps;
+    a.items = pl->d_items_x;
+    a.target = pl->d_target;
+    a.arrived = pl->d_flags;
+    a.ticket = pl->d_tickets;
+    a.err = pl->d_err;
+    a.n_items = pl->n_items_x;
+    a.timeout_ns = pl->wait_timeout_ns;
+    a.n_slots = pl->n_local_total;
+    a.drop_flag = pl->drop_flag;
+    a.trace = pl->trace;
+    a.sh = shard_table(pl, shard_xyz);
+    pl->drop_flag = -1;
+    const cudaError_t e = launch_dependent(pack_x_kernel<4, true>, dim3(pl->grid_x), dim3(kThreads), st, a);
+    if (e != cudaSuccess) return cuda_code(e);
+    pl->launches_x++;
+    return HALO_OK;
+}
+
+int launch_exchange_f_sharded(halo_plan* pl, float* const* shard_f, cudaStream_t st) {
+    if (!pl->fused_ready) return HALO_EINVAL;
+    if (pl->n_items_f == 0) return HALO_OK;
+    const size_t nsp = (size_t)pl->n_dom * std::max(pl->P, 1);
+    FArgs a;
+    a.f = nullptr;
+    a.pairs = pl->d_fpairs;
+    a.items = pl->d_items_f;
+    a.target = pl->d_target + nsp;
+    a.done = pl->d_flags + nsp;
+    a.ticket = pl->d_tickets + 1;
+    a.err = pl->d_err;
+    a.n_items = pl->n_items_f;
+    a.timeout_ns = pl->wait_timeout_ns;
+    a.n_slots = pl->n_local_total;
+    a.trace = pl->trace ? pl->trace + 4 * (size_t)pl->n_items_x : nullptr;
+    a.sh = shard_table(pl, shard_f);
+    const cudaError_t e =
+        launch_dependent(unpack_f_kernel<4, true>, dim3(pl->grid_f), dim3(kThreads), st, a);
+    if (e != cudaSuccess) return cuda_code(e);
+    pl->launches_f++;
+    return HALO_OK;
+}
+
+int launch_load_home_sharded(const halo_plan* pl, const float* g, float* const* shard_local,
+                             cudaStream_t st) {
+    const int64_t n = pl->n_atoms;
+    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
+    load_home_sharded_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, g,
+                                                     shard_table(pl, shard_local), pl->n_shards,
+                                                     pl->n_local_total, pl->d_err);
+    return cuda_code(cudaGetLastError());
+}
+
+int launch_store_home_sharded(const halo_plan* pl, const float* const* shard_local, float* g,
+                              cudaStream_t st) {
+    const int64_t n = pl->n_atoms;
+    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
+    store_home_sharded_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n,
+                                                      shard_table(pl, shard_local), pl->n_shards, g,
+                                                      pl->n_local_total, pl->d_err);
     return cuda_code(cudaGetLastError());
 }
 

@@ -14,6 +14,15 @@ namespace halo {
 constexpr int kThreads = 256;          // threads per block of every kernel here
 constexpr int kHistTile = 1024;        // atoms per warp tile of the home partition
 constexpr int kScanTile = 2048;        // elements per block of the device scan
+constexpr int kMaxShards = HALO_MAX_SHARDS;
+
+// Sharded data plane: shard k holds the dense slots [first[k], first[k + 1])
+// in its own buffer ptr[k] (the domains of one z-slab), so dense slot g of
+// shard k lives at ptr[k] + 3 * (g - first[k]).
+struct ShardTable {
+    float* ptr[kMaxShards];
+    int64_t first[kMaxShards];
+};
 
 // Per (sender s, pulse p) description (host side, and the build-time kernels).
 struct SPDesc {
@@ -37,7 +46,8 @@ struct XItem {
     int32_t len;
     int32_t flag;        // counter released when done: arrived[r*P + p]
     int32_t wait_base;   // s*P: counters of the slices s received
-    int32_t pad;
+    int16_t src_shard;   // shard of s (the sender) and of r (the receiver)
+    int16_t dst_shard;
     uint64_t wait_mask;  // pulses q < p whose slices into s the entries reference
     float shift[3];
     int32_t pad2;
@@ -52,6 +62,9 @@ struct FItem {
     int32_t s_base;      // s*P
     int32_t r_base;      // r*P
     uint64_t ms, mr;     // later pulses to wait for, on s and on r (0 for independent)
+    int16_t s_shard;     // shard of s (destination slots) and of r (halo sources)
+    int16_t r_shard;
+    int32_t pad;
 };
 
 }  // namespace halo
@@ -133,6 +146,12 @@ struct halo_plan {
     size_t h_stage_cap = 0;
     int occ_x = 0, occ_f = 0;        // resident blocks per SM of the fused kernels (cached)
 
+    // sharded data plane: shard k holds the domains [shard_dom[k], shard_dom[k + 1])
+    // (a z-slab of the grid) and the dense slots [shard_first[k], shard_first[k + 1])
+    int n_shards = 1;
+    int shard_dom[halo::kMaxShards + 1] = {};
+    int64_t shard_first[halo::kMaxShards + 1] = {};
+
     // exchange mode (HALO_MODE_*) and the flattened exchange's tables
     int mode = 0;
     bool fused_ready = false;        // FUSED work lists built for the current plan
@@ -192,6 +211,17 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st);
 // (zeroed by the caller before the launch)
 int launch_exchange_x_scratch(halo_plan* pl, float* xyz, uint32_t* arrived,
                               unsigned long long* ticket, cudaStream_t st);
+// the sharded data plane: the FUSED kernels with per-shard buffers and
+// system-scope signals (every shard's work in one launch on this GPU)
+int launch_exchange_x_sharded(halo_plan* pl, float* const* shard_xyz, cudaStream_t st);
+int launch_exchange_f_sharded(halo_plan* pl, float* const* shard_f, cudaStream_t st);
+int launch_load_home_sharded(const halo_plan* pl, const float* g, float* const* shard_local,
+                             cudaStream_t st);
+int launch_store_home_sharded(const halo_plan* pl, const float* const* shard_local, float* g,
+                              cudaStream_t st);
+// shard_dom from the grid (z-slabs), shard_first from the plan's layout
+int set_shards(halo_plan* pl, int n_shards);
+void update_shard_first(halo_plan* pl);
 int launch_load_home(const halo_plan* pl, const float* g, float* local, cudaStream_t st);
 int launch_store_home(const halo_plan* pl, const float* local, float* g, cudaStream_t st);
 int launch_local_to_global(const halo_plan* pl, int32_t* out, cudaStream_t st);

@@ -24,6 +24,7 @@ OK, EINVAL, EPULSES, EDOMAIN, ECAPACITY, ECUDA, ETIMEOUT, EBOUNDS, ENOMEM, ESCRA
     0, -1, -2, -3, -4, -5, -6, -7, -8, -9)
 NOALLOC_MAX_COUNTERS = 16384
 MAX_PULSES = 64
+MAX_SHARDS = 8
 SETUP_PRUNE_CORNERS = 1
 MODE_FUSED, MODE_STEPWISE, MODE_FLAT, MODE_STAGED = 0, 1, 2, 3
 MODES = {"fused": MODE_FUSED, "stepwise": MODE_STEPWISE, "flat": MODE_FLAT, "staged": MODE_STAGED}
@@ -81,6 +82,12 @@ SIGNATURES = {
     "halo_set_mode": (ctypes.c_int, [_vp, _i32, _vp]),
     "halo_get_mode": (ctypes.c_int, [_vp, _P(_i32)]),
     "halo_work_items": (ctypes.c_int, [_vp, _P(_i32), _P(_i32), _P(_i32)]),
+    "halo_shard": (ctypes.c_int, [_vp, _i32, _vp]),
+    "halo_shard_layout": (ctypes.c_int, [_vp, _i32, _P(_i32), _P(_i32), _P(_i64), _P(_i64)]),
+    "halo_load_home_sharded": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "halo_store_home_sharded": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "halo_exchange_x_sharded": (ctypes.c_int, [_vp, _vp, _vp]),
+    "halo_exchange_f_sharded": (ctypes.c_int, [_vp, _vp, _vp]),
     "halo_destroy": (None, [_vp]),
     "halo_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -285,6 +292,63 @@ class HaloPlan:
             _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)), _stream_handle(stream)),
             "halo_store_home")
         return global_xyz
+
+    # ---- sharded data plane (include/halo.h: halo_shard ...) ------------------
+    def shard(self, n_shards: int, stream=None):
+        """halo_shard: split the domains into n_shards z-slabs, each with its
+        own buffer (kept across rebuilds)."""
+        _check(self._lib.halo_shard(self._h, int(n_shards), _stream_handle(stream)), "halo_shard")
+        self.n_shards = int(n_shards)
+
+    def shard_layout(self, k: int):
+        """halo_shard_layout: {first_domain, n_domains, first_slot, n_local} of shard k."""
+        fd, nd, fs, nl = _i32(), _i32(), _i64(), _i64()
+        _check(self._lib.halo_shard_layout(self._h, int(k), ctypes.byref(fd), ctypes.byref(nd),
+                                           ctypes.byref(fs), ctypes.byref(nl)), "halo_shard_layout")
+        return {"first_domain": fd.value, "n_domains": nd.value, "first_slot": fs.value,
+                "n_local": nl.value}
+
+    def _shard_ptrs(self, tensors):
+        import torch
+        n = getattr(self, "n_shards", 1)
+        if len(tensors) != n:
+            raise ValueError("expected %d shard buffers, got %d" % (n, len(tensors)))
+        ptrs = (ctypes.c_void_p * n)()
+        for k, t in enumerate(tensors):
+            ptrs[k] = _dev_ptr(t, torch.float32, (self.shard_layout(k)["n_local"], 3)).value
+        return ptrs
+
+    def shard_buffers(self):
+        """One zeroed (n_local x 3) fp32 buffer per shard."""
+        import torch
+        return [torch.zeros((self.shard_layout(k)["n_local"], 3), dtype=torch.float32, device="cuda")
+                for k in range(getattr(self, "n_shards", 1))]
+
+    def load_home_sharded(self, global_xyz, shards, stream=None):
+        import torch
+        _check(self._lib.halo_load_home_sharded(
+            self._h, _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)), self._shard_ptrs(shards),
+            _stream_handle(stream)), "halo_load_home_sharded")
+        return shards
+
+    def store_home_sharded(self, shards, global_xyz=None, stream=None):
+        import torch
+        if global_xyz is None:
+            global_xyz = torch.empty((self.n_atoms, 3), dtype=torch.float32, device="cuda")
+        _check(self._lib.halo_store_home_sharded(
+            self._h, self._shard_ptrs(shards), _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)),
+            _stream_handle(stream)), "halo_store_home_sharded")
+        return global_xyz
+
+    def exchange_x_sharded(self, shards, stream=None):
+        _check(self._lib.halo_exchange_x_sharded(self._h, self._shard_ptrs(shards),
+                                                 _stream_handle(stream)), "halo_exchange_x_sharded")
+        return shards
+
+    def exchange_f_sharded(self, shards, stream=None):
+        _check(self._lib.halo_exchange_f_sharded(self._h, self._shard_ptrs(shards),
+                                                 _stream_handle(stream)), "halo_exchange_f_sharded")
+        return shards
 
     def exchange_x(self, local_xyz, stream=None):
         import torch

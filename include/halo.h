@@ -72,6 +72,7 @@ extern "C" {
 #define HALO_MODE_STAGED 3   /* MPI-era baseline: pack, host wait, transfer, host wait per pulse */
 
 #define HALO_MAX_PULSES 64
+#define HALO_MAX_SHARDS 8
 #define HALO_MAX_DOMAINS 4096
 
 typedef struct halo_plan halo_plan; /* opaque; owns maps, metadata, flags, build buffers */
@@ -219,6 +220,47 @@ int halo_exchange_x_noalloc(halo_plan* plan, float* local_coords, void* stream);
  * Halo slots keep their (possibly forwarded-into) values.  Bit-identical to
  * the sequential order.  Asynchronous. */
 int halo_exchange_f(halo_plan* plan, float* local_forces, void* stream);
+
+/* ---- Sharded data plane ------------------------------------------------------
+ * The page "Redesigning GROMACS Halo Exchange ..." spreads the domains over
+ * several GPUs: a pulse whose receiver sits on another GPU stores the packed
+ * coordinates into that GPU's halo slice and signals it with a system-scope
+ * release (section 3, NVLink path; section 4, memory ordering), and the force
+ * pass reads the remote halo forces back (Algorithm 6).  These calls split a
+ * plan's domains into n_shards z-slabs, each with its own buffer, and run the
+ * FUSED exchanges across them with system-scope signals.  In one process on
+ * one GPU every shard's work runs in one launch per direction.
+ *
+ * Shard k holds the domains [first_domain, first_domain + n_domains) (domain
+ * id = ix + nx*(iy + ny*iz), so a z-slab is a contiguous id range), laid out
+ * as in the dense local array: domain by domain, [home | halo of pulse 0 | ...].
+ * Its buffer holds n_local x 3 fp32 (caller-owned); the dense slot g of the
+ * plan is slot g - first_slot of its shard's buffer.
+ *
+ * halo_shard: n_shards in [1, min(HALO_MAX_SHARDS, n_z)], shard k taking the
+ *   z layers [k*nz/n_shards, (k+1)*nz/n_shards).  Builds the FUSED work lists
+ *   with each item's source and destination shard (synchronises `stream`).
+ *   The partition persists across halo_rebuild (which then rebuilds those
+ *   lists whatever the mode).  HALO_EINVAL for a bad count.
+ * halo_shard_layout: shard k's domains and slots (host outputs, nullable).
+ * halo_load_home_sharded / halo_store_home_sharded: halo_load_home /
+ *   halo_store_home with the local array split into the shards' buffers.
+ * halo_exchange_x_sharded / halo_exchange_f_sharded: halo_exchange_x /
+ *   halo_exchange_f in HALO_MODE_FUSED on the shards' buffers (an array of
+ *   n_shards device pointers, host memory, read during the call): the same
+ *   result bit for bit, whatever the plan's mode.  HALO_EINVAL for a null or
+ *   misaligned buffer pointer or a plan without FUSED work lists.
+ *   Asynchronous; timeouts are reported by halo_status() as usual. */
+int halo_shard(halo_plan* plan, int32_t n_shards, void* stream);
+int halo_shard_layout(const halo_plan* plan, int32_t shard, int32_t* first_domain /*host*/,
+                      int32_t* n_domains /*host*/, int64_t* first_slot /*host*/,
+                      int64_t* n_local /*host*/);
+int halo_load_home_sharded(const halo_plan* plan, const float* global_xyz,
+                           float* const* shard_local /*host array of device pointers*/, void* stream);
+int halo_store_home_sharded(const halo_plan* plan, const float* const* shard_local /*host array*/,
+                            float* global_xyz, void* stream);
+int halo_exchange_x_sharded(halo_plan* plan, float* const* shard_coords /*host array*/, void* stream);
+int halo_exchange_f_sharded(halo_plan* plan, float* const* shard_forces /*host array*/, void* stream);
 
 /* Select how halo_exchange_x / halo_exchange_f run (HALO_MODE_*).
  *   FUSED: the pages' design (Algorithms 3-6): one launch per direction; the
