@@ -630,6 +630,47 @@ def stencil_case(device, stream, flush, iters, warmup):
     return res
 
 
+def shard_case(name, device, stream, steps, warmup, counts):
+    """The sharded data plane on this one GPU: the FUSED exchange on per-shard
+    buffers (z-slabs of domains, system-scope signals, every shard's work in
+    one launch) against the same exchange on one dense buffer; back to back
+    on one copy of the system (context: the shards' signalling cost, not a
+    multi-GPU number)."""
+    import ctypes
+    import torch
+    from domain_decomposition_halo_build_gb300 import halo
+    w, xyz, dom, x, plan, loc, f0 = setup_workload(name, device)
+    lib = halo.load_library()
+    h, st = plan.handle, ctypes.c_void_p(stream.cuda_stream)
+
+    def timed(fn):
+        for _ in range(max(warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / steps
+    plan.set_mode("fused")
+    px, pf = ctypes.c_void_p(loc.data_ptr()), ctypes.c_void_p(f0.data_ptr())
+    out = {"workload": name, "dense_fused_us_per_exchange":
+           timed(lambda: (lib.halo_exchange_x(h, px, st), lib.halo_exchange_f(h, pf, st)))}
+    for n in counts:
+        plan.shard(n)
+        xs = plan.load_home_sharded(x, plan.shard_buffers())
+        fs = plan.shard_buffers()
+        ax, af = plan._shard_ptrs(xs), plan._shard_ptrs(fs)
+        out["shards_%d_us_per_exchange" % n] = timed(
+            lambda: (lib.halo_exchange_x_sharded(h, ax, st), lib.halo_exchange_f_sharded(h, af, st)))
+        del xs, fs
+    assert plan.status() == 0
+    plan.close()
+    return out
+
+
 REBUILD_WORKLOAD = "water3M_8x8x8"
 
 
@@ -897,7 +938,7 @@ def main():
     traffic = recorded_traffic(dom_kernel, args.workload)
     alg_gbs = (BYTES_X + BYTES_F) * halo_slots / (step_ms * 1e-3) / 1e9
 
-    lat = pruned = warm = graph = all_configs = rebuild = stencil_res = overlap = None
+    lat = pruned = warm = graph = all_configs = rebuild = stencil_res = overlap = shards = None
     e2e_value = e2e_ms = h2d = d2h = e2e_serial_ms = None
     if not args.headline_only:
         # latency case: the multi-pulse system, every mode
@@ -957,6 +998,9 @@ def main():
         pruned.append(pruned_case(REBUILD_WORKLOAD, args.mode, device, stream, flush,
                                   min(args.steps, 300), args.warmup, rebuild["halo_slots"]))
         stencil_res = stencil_case(device, stream, flush, min(args.steps, 50), max(3, min(args.warmup, 5)))
+        shards = [shard_case(args.workload, device, stream, min(args.steps, 300), args.warmup, (2, 4)),
+                  shard_case(LATENCY_WORKLOAD, device, stream, min(args.steps, 300), args.warmup,
+                             (2, 4, 8))]
         overlap = [overlap_case(plan, loc, f0.clone(), min(args.steps, 300), args.warmup, flush, m, device,
                                 prio) for m in (args.mode, "fused") for prio in (0, -1)]
         plan.set_mode(args.mode)
@@ -1016,6 +1060,7 @@ def main():
             "rebuild_case": rebuild,
             "overlap_case": overlap,
             "stencil_case": stencil_res,
+            "shard_case": shards,
             "e2e": None if e2e_ms is None else {
                 "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_step": 1e3 * e2e_ms,
