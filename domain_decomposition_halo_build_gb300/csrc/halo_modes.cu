@@ -350,6 +350,47 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
             fent[s0] = v;
             continue;
         }
+        if (k <= 3) {
+            // two or three copies (most multi-copy owners): three compare-
+            // exchanges on (pulse descending, slot ascending)
+            int32_t nd3[3];
+            int hp3[3];
+#pragma unroll
+            for (int j = 0; j < 3; j++) {
+                nd3[j] = j < k ? tmp[s0 + j] : INT32_MAX;
+                hp3[j] = j < k ? (int)hop[nd3[j]] : -1000;
+            }
+            auto cx = [&](int a, int b) {
+                const bool swap = hp3[a] < hp3[b] || (hp3[a] == hp3[b] && nd3[a] > nd3[b]);
+                if (swap) {
+                    const int32_t tn = nd3[a];
+                    nd3[a] = nd3[b];
+                    nd3[b] = tn;
+                    const int th = hp3[a];
+                    hp3[a] = hp3[b];
+                    hp3[b] = th;
+                }
+            };
+            cx(0, 1);
+            cx(1, 2);
+            cx(0, 1);
+            const int32_t home = fown[m];
+#pragma unroll
+            for (int j = 0; j < 3; j++) {
+                if (j < k) {
+                    const int32_t ps = parent[nd3[j]];
+                    int pos = 0;
+                    if (ps != home) {
+#pragma unroll
+                        for (int q = 2; q > j; q--)
+                            if (q < k && nd3[q] == ps) pos = q + 1;
+                        if (pos == 0) atomicCAS(err, 0, HALO_ECAPACITY);  // parent not among the copies
+                    }
+                    fent[s0 + j] = nd3[j] | (pos << kNodeBits);
+                }
+            }
+            continue;
+        }
         if (k <= kSortRegs) {
             // the same order in registers: a fully unrolled exchange sort on
             // (pulse descending, slot ascending); unused places sort last
