@@ -192,6 +192,114 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
     }
 }
 
+// The same stable scatter through shared memory: the block first places its
+// tile's atoms in domain order in shared memory (warp by warp, 32 atoms at a
+// time, ranks from the warp match mask, so the order within a domain stays
+// the input order), then writes each domain's run of the tile contiguously.
+// The global stores then fill whole sectors; scattered one atom per domain,
+// each partly written sector had to be fetched from DRAM first.
+__host__ __device__ inline size_t staged_scatter_smem(int W, int nd) {
+    const size_t head = ((size_t)W * nd + 2 * (size_t)nd + 1) * sizeof(int32_t);
+    const size_t T = (size_t)W * kHistTile;
+    return ((head + 15) & ~(size_t)15) + T * (sizeof(float4) + sizeof(int32_t) + sizeof(int16_t));
+}
+
+__global__ void home_scatter_staged_kernel(const float* __restrict__ xyz,
+                                           const int32_t* __restrict__ dom, int64_t n, int nd,
+                                           int64_t nbt, const int32_t* __restrict__ offs,
+                                           const int32_t* __restrict__ wcounts,
+                                           int32_t* __restrict__ home_gid, float4* __restrict__ bxyz) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int W = blockDim.x >> 5;
+    const int T = W * kHistTile;
+    int32_t* wpos = reinterpret_cast<int32_t*>(smem);  // W * nd: next sorted position, per warp and domain
+    int32_t* lstart = wpos + (size_t)W * nd;           // nd + 1: first sorted position of each domain
+    int32_t* gstart = lstart + nd + 1;                 // nd: the domain run's first home-compact slot
+    const size_t head = ((size_t)W * nd + 2 * (size_t)nd + 1) * sizeof(int32_t);
+    float4* st_xyz = reinterpret_cast<float4*>(smem + ((head + 15) & ~(size_t)15));
+    int32_t* st_gid = reinterpret_cast<int32_t*>(st_xyz + T);
+    int16_t* st_dom = reinterpret_cast<int16_t*>(st_gid + T);
+    const int32_t* wc = wcounts + (int64_t)blockIdx.x * W * nd;
+    for (int d = threadIdx.x; d < nd; d += blockDim.x) {
+        int32_t t = 0;
+        for (int w = 0; w < W; w++) t += wc[(size_t)w * nd + d];
+        lstart[d] = t;
+        gstart[d] = offs[(int64_t)d * nbt + blockIdx.x];
+    }
+    __syncthreads();
+    // exclusive scan of the per-domain counts (the first warp, 32 at a time)
+    if (warp == 0) {
+        int32_t carry = 0;
+        for (int d0 = 0; d0 < nd; d0 += 32) {
+            const int d = d0 + lane;
+            const int32_t v = d < nd ? lstart[d] : 0;
+            int32_t x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(kFull, x, o);
+                if (lane >= o) x += y;
+            }
+            if (d < nd) lstart[d] = carry + x - v;
+            carry += __shfl_sync(kFull, x, 31);
+        }
+        if (lane == 0) lstart[nd] = carry;
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < nd; d += blockDim.x) {
+        int32_t acc = lstart[d];
+        for (int w = 0; w < W; w++) {
+            wpos[(size_t)w * nd + d] = acc;
+            acc += wc[(size_t)w * nd + d];
+        }
+    }
+    __syncthreads();
+    int32_t* run = wpos + (size_t)warp * nd;
+    const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * kHistTile;
+    const unsigned lt = lanemask_lt();
+    constexpr int U = 4;
+    for (int it = 0; it < kHistTile / 32; it += U) {
+        int d[U];
+        float c[U][3];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t a = a0 + (it + u) * 32 + lane;
+            d[u] = -1;
+            c[u][0] = c[u][1] = c[u][2] = 0.0f;
+            if (a < n) {
+                d[u] = __ldg(dom + a);
+                if (d[u] < 0 || d[u] >= nd) d[u] = -1;
+                c[u][0] = __ldg(xyz + 3 * a + 0);
+                c[u][1] = __ldg(xyz + 3 * a + 1);
+                c[u][2] = __ldg(xyz + 3 * a + 2);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t a = a0 + (it + u) * 32 + lane;
+            const unsigned peers = __match_any_sync(kFull, d[u]);
+            if (d[u] >= 0) {
+                const int pos = run[d[u]] + __popc(peers & lt);
+                st_xyz[pos] = make_float4(c[u][0], c[u][1], c[u][2], __int_as_float(0));
+                st_gid[pos] = (int32_t)a;
+                st_dom[pos] = (int16_t)d[u];
+            }
+            __syncwarp();
+            if (d[u] >= 0 && lane == __ffs(peers) - 1) run[d[u]] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // every domain's run of the tile, contiguous in the home-compact region
+    const int total = lstart[nd];
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int dd = st_dom[i];
+        const int64_t g = (int64_t)gstart[dd] + (i - lstart[dd]);
+        bxyz[g] = st_xyz[i];
+        home_gid[g] = st_gid[i];
+    }
+}
+
 // ---- generic int32 exclusive scan (three launches) ---------------------------------
 __global__ void scan_reduce_kernel(const int32_t* __restrict__ in, int64_t n,
                                    int32_t* __restrict__ sums) {
@@ -658,6 +766,20 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
     }
     pl->build_attempts = 0;
 
+    // the home scatter sorts each tile in shared memory where the tile and
+    // the per-domain tables fit (nd < 32768 for the int16 domain ids)
+    size_t staged_smem = 0;
+    {
+        int optin = 0;
+        HALO_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->dev));
+        const size_t need = staged_scatter_smem(wpb, nd);
+        if (nd < 32768 && need <= (size_t)optin) {
+            HALO_CUDA(cudaFuncSetAttribute(home_scatter_staged_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need));
+            staged_smem = need;
+        }
+    }
+
     const Meta m = meta_ptrs(pl->d_meta, nd, P);
     void* hstage = nullptr;
     HALO_TRY(host_stage(pl, mbytes, &hstage));
@@ -684,8 +806,14 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
                                                                   pl->d_counts, wcounts, m.flags);
         int32_t* offs = pl->d_counts + ncount;
         HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
-        home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
-            coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid, reinterpret_cast<float4*>(pl->d_bxyz));
+        if (staged_smem > 0)
+            home_scatter_staged_kernel<<<hist_blocks, wpb * 32, staged_smem, st>>>(
+                coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid,
+                reinterpret_cast<float4*>(pl->d_bxyz));
+        else
+            home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
+                coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid,
+                reinterpret_cast<float4*>(pl->d_bxyz));
         home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, nbt, n, nd, P, m);
         HALO_CUDA(cudaGetLastError());
         // 2. pulses in global order

@@ -11,6 +11,8 @@
  *     length per component (the slot's owner from halo_local_to_global);
  *   - with integer-valued forces the total force is conserved exactly and
  *     halo_store_home returns every atom's force in input order;
+ *   - the sharded data plane (4 z-slab shards, one buffer each) gives the
+ *     same coordinates and forces, shard by shard;
  *   - halo_status reports no device error; bad arguments are refused;
  *   - one fused stencil iteration equals a sweep followed by an exchange.
  * Prints "c abi ok" and returns 0 on success.
@@ -106,6 +108,43 @@ static int run_modes(void) {
     for (int m = 1; m < NM; m++) {
         CHECK(memcmp(loc[0], loc[m], sizeof(float) * 3 * nl) == 0, "coordinates differ between modes");
         CHECK(memcmp(fr[0], fr[m], sizeof(float) * 3 * nl) == 0, "forces differ between modes");
+    }
+
+    /* the sharded data plane: 4 shards, each its own buffer, laid out as its
+       part of the dense array */
+    {
+        enum { NS = 4 };
+        HL(halo_shard(plan, NS, NULL));
+        CHECK(halo_shard(plan, 9, NULL) == HALO_EINVAL, "shard count");
+        float* sx[NS];
+        float* sf[NS];
+        int64_t first[NS], cnt[NS], tot = 0;
+        for (int k = 0; k < NS; k++) {
+            int32_t fd, ndom;
+            HL(halo_shard_layout(plan, k, &fd, &ndom, &first[k], &cnt[k]));
+            CHECK(first[k] == tot && ndom == 16 && fd == 16 * k, "shard layout");
+            tot += cnt[k];
+            CU(cudaMalloc((void**)&sx[k], sizeof(float) * 3 * (cnt[k] > 0 ? cnt[k] : 1)));
+            CU(cudaMalloc((void**)&sf[k], sizeof(float) * 3 * (cnt[k] > 0 ? cnt[k] : 1)));
+            CU(cudaMemcpy(sf[k], f0 + 3 * first[k], sizeof(float) * 3 * cnt[k], cudaMemcpyHostToDevice));
+        }
+        CHECK(tot == nl, "shards tile the local layout");
+        HL(halo_load_home_sharded(plan, d_xyz, sx, NULL));
+        HL(halo_exchange_x_sharded(plan, sx, NULL));
+        HL(halo_exchange_f_sharded(plan, sf, NULL));
+        CHECK(halo_status(plan, NULL) == HALO_OK, "device error (sharded)");
+        float* hx = (float*)malloc(sizeof(float) * 3 * nl);
+        float* hf = (float*)malloc(sizeof(float) * 3 * nl);
+        for (int k = 0; k < NS; k++) {
+            CU(cudaMemcpy(hx + 3 * first[k], sx[k], sizeof(float) * 3 * cnt[k], cudaMemcpyDeviceToHost));
+            CU(cudaMemcpy(hf + 3 * first[k], sf[k], sizeof(float) * 3 * cnt[k], cudaMemcpyDeviceToHost));
+            CU(cudaFree(sx[k]));
+            CU(cudaFree(sf[k]));
+        }
+        CHECK(memcmp(hx, loc[0], sizeof(float) * 3 * nl) == 0, "sharded coordinates differ");
+        CHECK(memcmp(hf, fr[0], sizeof(float) * 3 * nl) == 0, "sharded forces differ");
+        free(hx);
+        free(hf);
     }
 
     /* halo coordinates = owner + 0 or L per component */
