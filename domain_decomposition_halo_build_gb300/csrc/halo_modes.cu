@@ -240,9 +240,11 @@ __global__ void __launch_bounds__(kThreads) pair_reduce_kernel(const int32_t* __
 }
 
 // Scans the nb tile sums in place and stores the grand total in sums[nb]
-// and, if given, in *total.
+// and, if given, in *total.  end (SRC 0): the owner list's end offset,
+// end[owners] = copies.
 __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ sums, int64_t n,
-                                                        const int64_t* n_dev, int64_t* total) {
+                                                        const int64_t* n_dev, int64_t* total,
+                                                        int32_t* end) {
     n = scan_count(n, n_dev);
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
     int64_t carry = 0;
@@ -257,19 +259,25 @@ __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ su
     if (threadIdx.x == 0) {
         sums[nb] = carry;
         if (total) *total = carry;
+        if (end) end[carry >> 32] = (int32_t)(carry & 0xffffffffll);
     }
 }
 
 // Down pass: each warp takes a contiguous run of kScanTile / warps elements
 // and walks it 32 at a time (coalesced loads and stores): a first walk sums
 // the run, the warp totals are scanned across the block, a second walk writes
-// the exclusive prefixes with a shuffle scan per 32 elements.
+// the exclusive prefixes with a shuffle scan per 32 elements.  SRC 0 also
+// writes the owner list: for a slot with copies, fown[its owner index] = the
+// slot and fstart[...] = its first entry (out_b, the owner indices, is then
+// not stored).
 template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __restrict__ in, int64_t n,
                                                              const int64_t* n_dev,
                                                              const int64_t* __restrict__ sums,
                                                              int32_t* __restrict__ out_a,
-                                                             int32_t* __restrict__ out_b) {
+                                                             int32_t* __restrict__ out_b,
+                                                             int32_t* __restrict__ fown,
+                                                             int32_t* __restrict__ fstart) {
     constexpr int kWarps = kThreads / 32;
     constexpr int R = kScanTile / kThreads;  // rounds of 32 per warp
     __shared__ int64_t wsum[kWarps];
@@ -303,7 +311,14 @@ __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __re
         const int64_t pre = carry + x - v[r];
         if (i < n) {
             out_a[i] = (int32_t)(pre & 0xffffffffll);
-            out_b[i] = (int32_t)(pre >> 32);
+            if (SRC == 0 && fown) {
+                if ((v[r] & 0xffffffffll) > 0) {
+                    fown[pre >> 32] = (int32_t)i;
+                    fstart[pre >> 32] = (int32_t)(pre & 0xffffffffll);
+                }
+            } else {
+                out_b[i] = (int32_t)(pre >> 32);
+            }
         }
         carry += __shfl_sync(kFull, x, 31);
     }
@@ -314,27 +329,15 @@ __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __re
 // scan_count (n is then the bound the grids are sized for).
 template <int SRC>
 int pair_scan(const int32_t* in, int64_t n, const int64_t* n_dev, int64_t* sums, int32_t* out_a,
-              int32_t* out_b, int64_t* total, cudaStream_t st) {
+              int32_t* out_b, int64_t* total, cudaStream_t st, int32_t* fown = nullptr,
+              int32_t* fstart = nullptr) {
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
     if (nb > 0) pair_reduce_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, n_dev, sums);
-    pair_top_kernel<<<1, 1024, 0, st>>>(sums, n, n_dev, total);
+    pair_top_kernel<<<1, 1024, 0, st>>>(sums, n, n_dev, total, fstart);
     if (nb > 0)
-        pair_down_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, n_dev, sums, out_a, out_b);
+        pair_down_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, n_dev, sums, out_a, out_b, fown,
+                                                                  fstart);
     return cuda_code(cudaGetLastError());
-}
-
-__global__ void owner_list_kernel(const int32_t* __restrict__ ncopies,
-                                  const int32_t* __restrict__ entry_pos,
-                                  const int32_t* __restrict__ owner_idx, int64_t n, int32_t* fown,
-                                  int32_t* fstart, const int64_t* __restrict__ total) {
-    // total: copies (low half) and owners (high half) of the copy-count scan
-    if (blockIdx.x == 0 && threadIdx.x == 0) fstart[*total >> 32] = (int32_t)(*total & 0xffffffffll);
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
-         j += (int64_t)gridDim.x * blockDim.x)
-        if (ncopies[j] > 0) {
-            fown[owner_idx[j]] = (int32_t)j;
-            fstart[owner_idx[j]] = entry_pos[j];
-        }
 }
 
 __global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
@@ -348,12 +351,35 @@ __global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t*
     }
 }
 
-// Per owner: order its copies by decreasing creating pulse (ties by slot) and
-// replace each copy's parent slot by the parent's position (0 = the owner).
+// Owner records (the force pass's tables): class A -- up to 3 copies, one
+// 16-byte record {home | k << 26, three entries}; class B -- up to 11 copies,
+// three 16-byte records; class C -- more copies, {header, first entry} into
+// the entry list.  An entry is node slot | parent position << 26.
+__device__ __forceinline__ void write_rec_a(int4* recA, int32_t hdr, const int32_t* e, int k) {
+    *recA = make_int4(hdr, e[0], k > 1 ? e[1] : 0, k > 2 ? e[2] : 0);
+}
+
+template <int N>
+__device__ __forceinline__ void write_rec_b(int4* recB, int32_t hdr, const int32_t (&e)[N], int k) {
+    int32_t w[11];
+#pragma unroll
+    for (int j = 0; j < 11; j++) w[j] = j < k && j < N ? e[j] : 0;
+    recB[0] = make_int4(hdr, w[0], w[1], w[2]);
+    recB[1] = make_int4(w[3], w[4], w[5], w[6]);
+    recB[2] = make_int4(w[7], w[8], w[9], w[10]);
+}
+
+// Per owner: order its copies by decreasing creating pulse (ties by slot),
+// replace each copy's parent slot by the parent's position (0 = the owner),
+// and write the owner's record at its class position (posA / posB from the
+// class scan; class C after them, with its entries in the entry list).
 __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
                                   const int32_t* __restrict__ tmp, const int32_t* __restrict__ parent,
                                   const int8_t* __restrict__ hop, const int64_t* __restrict__ total,
-                                  int32_t* __restrict__ fent, int* max_copies, int* err) {
+                                  const int32_t* __restrict__ posA, const int32_t* __restrict__ posB,
+                                  int4* __restrict__ recA, int4* __restrict__ recB,
+                                  int4* __restrict__ recC, int32_t* __restrict__ fent,
+                                  int* max_copies, int* err) {
     const int64_t n_owners = *total >> 32;
     __shared__ int block_max;
     if (threadIdx.x == 0) block_max = 0;
@@ -367,10 +393,11 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
             atomicCAS(err, 0, HALO_ECAPACITY);
             continue;
         }
+        const int32_t hdr = fown[m] | (k << kNodeBits);
         if (k == 1) {  // most owners: a single copy, received from the owner itself
             const int32_t v = tmp[s0];
             if (parent[v] != fown[m]) atomicCAS(err, 0, HALO_ECAPACITY);
-            fent[s0] = v;
+            recA[posA[m]] = make_int4(hdr, v, 0, 0);
             continue;
         }
         if (k <= 3) {
@@ -398,6 +425,7 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
             cx(1, 2);
             cx(0, 1);
             const int32_t home = fown[m];
+            int32_t e3[3] = {0, 0, 0};
 #pragma unroll
             for (int j = 0; j < 3; j++) {
                 if (j < k) {
@@ -409,9 +437,10 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
                             if (q < k && nd3[q] == ps) pos = q + 1;
                         if (pos == 0) atomicCAS(err, 0, HALO_ECAPACITY);  // parent not among the copies
                     }
-                    fent[s0 + j] = nd3[j] | (pos << kNodeBits);
+                    e3[j] = nd3[j] | (pos << kNodeBits);
                 }
             }
+            write_rec_a(recA + posA[m], hdr, e3, k);
             continue;
         }
         if (k <= kSortRegs) {
@@ -439,8 +468,10 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
                     }
                 }
             const int32_t home = fown[m];
+            int32_t e8[kSortRegs];
 #pragma unroll
             for (int j = 0; j < kSortRegs; j++) {
+                e8[j] = 0;
                 if (j < k) {
                     const int32_t ps = parent[nd8[j]];
                     int pos = 0;
@@ -450,9 +481,10 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
                             if (q < k && nd8[q] == ps) pos = q + 1;
                         if (pos == 0) atomicCAS(err, 0, HALO_ECAPACITY);  // parent not among the copies
                     }
-                    fent[s0 + j] = nd8[j] | (pos << kNodeBits);
+                    e8[j] = nd8[j] | (pos << kNodeBits);
                 }
             }
+            write_rec_b(recB + 3 * (int64_t)posB[m], hdr, e8, k);  // 4..8 copies: class B
             continue;
         }
         int32_t node[kMaxCopies];
@@ -481,7 +513,15 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
                     }
                 if (pos == 0) atomicCAS(err, 0, HALO_ECAPACITY);  // parent not among the copies
             }
-            fent[s0 + j] = node[j] | (pos << kNodeBits);
+            node[j] = node[j] | (pos << kNodeBits);  // the entry, in place
+        }
+        if (k <= 11) {
+            int32_t e11[11];
+            for (int j = 0; j < 11; j++) e11[j] = j < k ? node[j] : 0;
+            write_rec_b(recB + 3 * (int64_t)posB[m], hdr, e11, k);
+        } else {
+            for (int j = 0; j < k; j++) fent[s0 + j] = node[j];
+            recC[m - posA[m] - posB[m]] = make_int4(hdr, s0, 0, 0);  // class-C owners before m
         }
     }
     atomicMax(&block_max, my_max);
@@ -838,32 +878,6 @@ __global__ void __launch_bounds__(kThreads) flat_f_kernel(float* f, const int4* 
 }
 
 
-__global__ void owner_record_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
-                                    const int32_t* __restrict__ fent, const int32_t* __restrict__ posA,
-                                    const int32_t* __restrict__ posB,
-                                    const int64_t* __restrict__ total,
-                                    int4* __restrict__ recA, int4* __restrict__ recB,
-                                    int4* __restrict__ recC) {
-    const int64_t n_owners = *total >> 32;
-    for (int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; m < n_owners;
-         m += (int64_t)gridDim.x * blockDim.x) {
-        const int s0 = fstart[m], k = fstart[m + 1] - s0;
-        const int32_t hdr = fown[m] | (k << kNodeBits);
-        int32_t e[11] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-        for (int j = 0; j < k && j < 11; j++) e[j] = fent[s0 + j];
-        if (k <= 3) {
-            recA[posA[m]] = make_int4(hdr, e[0], e[1], e[2]);
-        } else if (k <= 11) {
-            recB[3 * (int64_t)posB[m]] = make_int4(hdr, e[0], e[1], e[2]);
-            recB[3 * (int64_t)posB[m] + 1] = make_int4(e[3], e[4], e[5], e[6]);
-            recB[3 * (int64_t)posB[m] + 2] = make_int4(e[7], e[8], e[9], e[10]);
-        } else {
-            const int64_t c = m - posA[m] - posB[m];  // class-C owners before m
-            recC[c] = make_int4(hdr, s0, 0, 0);
-        }
-    }
-}
-
 int blocks_for(int64_t n, int num_sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>((n + kThreads - 1) / kThreads,
                                                        (int64_t)num_sms * 16));
@@ -958,7 +972,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
 
     // scratch of the table build, carved from two pools kept in the plan
     const int64_t nsums = nl / kScanTile + 2;            // int64 tile sums + grand total
-    const int64_t off_sums = (6 * nl + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
+    const int64_t off_sums = (5 * nl + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
     HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 16));
     HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
     int32_t* owner = pl->d_flat_pool32;
@@ -966,8 +980,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int32_t* ncopies = parent + nl;
     int32_t* entry_pos = ncopies + nl;
     int32_t* flag = entry_pos + nl;
-    int32_t* owner_idx = flag + nl;
-    int32_t* tmp = owner_idx + nl;
+    int32_t* tmp = flag + nl;
     int64_t* sums = reinterpret_cast<int64_t*>(pl->d_flat_pool32 + off_sums);
     // misc: [0] largest copy list, [1] error; misc64: [0] copies | owners << 32,
     // [1] class-A | class-B records << 32
@@ -977,7 +990,6 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int8_t* code = hop + nl;
     int rc = HALO_OK;
     do {
-        const int gb = blocks_for(nl, pl->num_sms);
         const int gh = blocks_for(std::max<int64_t>(H, 1), pl->num_sms);
         for (int p = 0; p < P; p++) {
             const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
@@ -990,27 +1002,26 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if (!items.empty())
             xflat_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
                                                                        pl->d_xflat, ncopies);
-        // entry offsets of every slot's copy list and the owner index of every
-        // slot with copies, in one pass; the grand total (copies, owners)
+        // entry offsets of every slot's copy list and, from the same scan,
+        // the owner list (fown, fstart); the grand total (copies, owners)
         // stays on the device
-        if ((rc = pair_scan<0>(ncopies, nl, nullptr, sums, entry_pos, owner_idx, misc64, st)) != HALO_OK)
+        if ((rc = pair_scan<0>(ncopies, nl, nullptr, sums, entry_pos, nullptr, misc64, st, pl->d_fown,
+                               pl->d_fstart)) != HALO_OK)
             break;
-        owner_list_kernel<<<gb, kThreads, 0, st>>>(ncopies, entry_pos, owner_idx, nl, pl->d_fown,
-                                                   pl->d_fstart, misc64);
         if (!items.empty())
             owner_fill_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner,
                                                                             entry_pos, flag, tmp);
-        // record classes (A: <= 3 copies, B: 4..11, C: more): slots in each
-        // class from one paired scan of the owners' copy counts
+        // record classes (A: <= 3 copies, B: 4..11, C: more): positions in
+        // each class from one paired scan of the owners' copy counts, then the
+        // sort writes every owner's record there
         int32_t* posA = entry_pos;  // scratch reuse: owner_fill has read entry_pos
-        int32_t* posB = ncopies;    // and owner_list ncopies
-        owner_sort_kernel<<<gh, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, tmp, parent, hop, misc64,
-                                                   pl->d_fent, misc, misc + 1);
+        int32_t* posB = ncopies;    // and the copy-count scan ncopies
         if ((rc = pair_scan<1>(pl->d_fstart, std::max<int64_t>(H, 1), misc64, sums, posA, posB,
                                misc64 + 1, st)) != HALO_OK)
             break;
-        owner_record_kernel<<<gh, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, pl->d_fent, posA, posB,
-                                                     misc64, pl->d_frec[0], pl->d_frec[1], pl->d_frec[2]);
+        owner_sort_kernel<<<gh, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, tmp, parent, hop, misc64,
+                                                   posA, posB, pl->d_frec[0], pl->d_frec[1],
+                                                   pl->d_frec[2], pl->d_fent, misc, misc + 1);
         // the one synchronisation: counts, largest list, error
         if ((rc = cuda_code(cudaMemcpyAsync(hw, misc, 8 * sizeof(int32_t) + 2 * sizeof(int64_t),
                                             cudaMemcpyDeviceToHost, st))) != HALO_OK)
