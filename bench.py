@@ -219,7 +219,9 @@ def setup_replicas(name, device, l2_multiple=4, prune=False):
 
 def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=None, settle_s=0.0):
     """K back-to-back steps through the C ABI, step i on replica i mod R; one
-    CUDA event pair around all K.  which: "xf" (the step), "x" or "f" (one direction alone).
+    CUDA event pair around all K (a device-side delay ahead of the start event
+    keeps the host's issue latency out of it).  which: "xf" (the step), "x" or
+    "f" (one direction alone).
     With a clock sampler, sampling starts before the warm-up, and the warm-up
     runs for at least settle_s seconds of the same steps, so that the samples
     show the clocks under this load even when the timed region itself is far
@@ -256,6 +258,11 @@ def time_rotated(reps, steps, warmup, stream, which="xf", sampler=None, barrier=
     torch.cuda.synchronize()
     l0 = sum(sum(p.launch_counts()) for p, _, _ in reps)
     t0 = time.perf_counter()
+    # a device-side delay ahead of the start event (torch's spin kernel, about
+    # 100 us, outside the timed region): the first steps are queued while it
+    # runs, so the event pair times the K steps' GPU work back to back rather
+    # than the host's issue latency for the first one
+    torch.cuda._sleep(200000)
     e0.record(stream)
     for i in range(steps):
         run(i)
