@@ -669,7 +669,7 @@ def shard_case(name, device, stream, steps, warmup, counts):
         plan.shard(n)
         xs = plan.load_home_sharded(x, plan.shard_buffers())
         fs = plan.shard_buffers()
-        ax, af = plan._shard_ptrs(xs), plan._shard_ptrs(fs)
+        ax, af = plan.shard_ptrs(xs), plan.shard_ptrs(fs)
         out["shards_%d_us_per_exchange" % n] = timed(
             lambda: (lib.halo_exchange_x_sharded(h, ax, st), lib.halo_exchange_f_sharded(h, af, st)))
         del xs, fs

@@ -99,7 +99,7 @@ int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, 
     HALO_TRY(halo::prepare_common(pl, st));
     // each mode's own tables; the others are built when a mode is selected
     // (the sharded data plane runs on the FUSED work lists)
-    if (pl->mode == HALO_MODE_FUSED || pl->n_shards > 1) HALO_TRY(halo::prepare_fused(pl, st));
+    if (pl->mode == HALO_MODE_FUSED || pl->shard_lists) HALO_TRY(halo::prepare_fused(pl, st));
     if (pl->mode == HALO_MODE_FLAT) HALO_TRY(halo::prepare_flat(pl, st));
     if (pl->mode == HALO_MODE_STAGED) HALO_TRY(halo::prepare_staged(pl));
     pl->valid = true;
@@ -289,6 +289,7 @@ int halo_shard(halo_plan* pl, int32_t n_shards, void* stream) {
     DeviceGuard g(pl->dev);
     if (!g.ok) return HALO_ECUDA;
     HALO_TRY(halo::set_shards(pl, n_shards));
+    pl->shard_lists = true;
     // the work lists carry each item's shards
     return halo::prepare_fused(pl, as_stream(stream));
 }

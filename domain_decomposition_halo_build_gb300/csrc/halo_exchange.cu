@@ -384,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 4) unpack_f_kernel(const __grid_cons
                 op[2] = o[e][2] + h[e][2];
             }
         }
-        // the warp's stores, then one gpu-scope release by the leader
+        // the warp's stores, then one release by the leader (gpu scope; system
+        // scope on the sharded data plane)
         __syncwarp();
         if (lane == 0) {
             red_release_add<SHARDED>(a.done + w.flag, 1u);

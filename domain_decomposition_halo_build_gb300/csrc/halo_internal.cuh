@@ -149,6 +149,7 @@ struct halo_plan {
     // sharded data plane: shard k holds the domains [shard_dom[k], shard_dom[k + 1])
     // (a z-slab of the grid) and the dense slots [shard_first[k], shard_first[k + 1])
     int n_shards = 1;
+    bool shard_lists = false;        // halo_shard was called: rebuilds keep the FUSED work lists
     int shard_dom[halo::kMaxShards + 1] = {};
     int64_t shard_first[halo::kMaxShards + 1] = {};
 

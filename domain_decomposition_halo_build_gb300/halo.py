@@ -211,6 +211,7 @@ class HaloPlan:
         self._lib = load_library()
         flags = SETUP_PRUNE_CORNERS if prune else 0
         self._h = halo_setup_ex(box, grid, rc, coords, domain_of_atom, flags, stream)
+        self.n_shards = 1
         self._refresh()
 
     def _refresh(self):
@@ -308,9 +309,13 @@ class HaloPlan:
         return {"first_domain": fd.value, "n_domains": nd.value, "first_slot": fs.value,
                 "n_local": nl.value}
 
-    def _shard_ptrs(self, tensors):
+    def shard_ptrs(self, tensors):
+        """The host array of shard buffer pointers that the sharded calls take,
+        each buffer checked against its shard's layout.  Valid until the next
+        rebuild or halo_shard; a loop may build it once and call the library
+        with it directly."""
         import torch
-        n = getattr(self, "n_shards", 1)
+        n = self.n_shards
         if len(tensors) != n:
             raise ValueError("expected %d shard buffers, got %d" % (n, len(tensors)))
         ptrs = (ctypes.c_void_p * n)()
@@ -322,12 +327,12 @@ class HaloPlan:
         """One zeroed (n_local x 3) fp32 buffer per shard."""
         import torch
         return [torch.zeros((self.shard_layout(k)["n_local"], 3), dtype=torch.float32, device="cuda")
-                for k in range(getattr(self, "n_shards", 1))]
+                for k in range(self.n_shards)]
 
     def load_home_sharded(self, global_xyz, shards, stream=None):
         import torch
         _check(self._lib.halo_load_home_sharded(
-            self._h, _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)), self._shard_ptrs(shards),
+            self._h, _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)), self.shard_ptrs(shards),
             _stream_handle(stream)), "halo_load_home_sharded")
         return shards
 
@@ -336,17 +341,17 @@ class HaloPlan:
         if global_xyz is None:
             global_xyz = torch.empty((self.n_atoms, 3), dtype=torch.float32, device="cuda")
         _check(self._lib.halo_store_home_sharded(
-            self._h, self._shard_ptrs(shards), _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)),
+            self._h, self.shard_ptrs(shards), _dev_ptr(global_xyz, torch.float32, (self.n_atoms, 3)),
             _stream_handle(stream)), "halo_store_home_sharded")
         return global_xyz
 
     def exchange_x_sharded(self, shards, stream=None):
-        _check(self._lib.halo_exchange_x_sharded(self._h, self._shard_ptrs(shards),
+        _check(self._lib.halo_exchange_x_sharded(self._h, self.shard_ptrs(shards),
                                                  _stream_handle(stream)), "halo_exchange_x_sharded")
         return shards
 
     def exchange_f_sharded(self, shards, stream=None):
-        _check(self._lib.halo_exchange_f_sharded(self._h, self._shard_ptrs(shards),
+        _check(self._lib.halo_exchange_f_sharded(self._h, self.shard_ptrs(shards),
                                                  _stream_handle(stream)), "halo_exchange_f_sharded")
         return shards
 

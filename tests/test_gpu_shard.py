@@ -96,7 +96,8 @@ def test_sharded_and_dense_calls_interleave():
         plan.close()
 
 
-def test_sharding_survives_rebuild_and_pruning():
+@pytest.mark.parametrize("n", [1, 2])
+def test_sharding_survives_rebuild_and_pruning(n):
     import torch
     w = synth.WORKLOADS["water24k_2x4x8"]
     xyz, dom = synth.system(w)
@@ -106,7 +107,7 @@ def test_sharding_survives_rebuild_and_pruning():
     plan = halo.HaloPlan(w.box, w.grid, w.rc, x, d, prune=True)
     try:
         plan.set_mode("flat")          # the sharded calls run on their own work lists
-        plan.shard(2)
+        plan.shard(n)
         x2, d2 = synth.displaced(xyz, w.box, w.grid, 1)
         plan.rebuild(torch.from_numpy(x2).cuda(), torch.from_numpy(d2).cuda())
         o = oracle.Oracle(w.box, w.grid, w.rc, x2, d2, prune=True)
