@@ -94,7 +94,12 @@ int do_build(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n, 
     pl->trace = nullptr;  // item counts change with the plan: the caller re-arms tracing
     pl->trace_cap = 0;
     pl->flat_ready = false;  // the flattened tables describe the previous plan
+    pl->flat_chains_ready = false;
     HALO_TRY(halo::build_plan(pl, coords, dom, n, st));
+    // FLAT: the forwarding chains need only the device's descriptors and the
+    // sizes, so the GPU runs them while the host builds its copy of the
+    // descriptors below
+    if (pl->mode == HALO_MODE_FLAT) HALO_TRY(halo::launch_flat_chains(pl, st));
     halo::update_shard_first(pl);
     HALO_TRY(halo::prepare_common(pl, st));
     // each mode's own tables; the others are built when a mode is selected

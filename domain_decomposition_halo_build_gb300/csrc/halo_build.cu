@@ -13,13 +13,13 @@
 //
 // Device pipeline (one stream, one host synchronisation at the end):
 //   1. home partition: a histogram of domain ids per block tile (per-warp
-//      shared histograms), exclusive scan, stable scatter (warp match +
-//      running per-domain counters) -> every domain's home atoms in input
-//      order, in a home-compact region;
+//      shared histograms), exclusive scan, stable scatter (each tile ranked in
+//      shared memory: warp match + running per-domain counters) -> every
+//      domain's home atoms in input order, in a home-compact region;
 //   2. per pulse: count kernel (predicate per candidate, with the optional
-//      corner test), scan kernel (block offsets, sizes, receiver offsets),
-//      write kernel (stable block-wide ballot compaction -> ascending index
-//      map + the new halo coordinates);
+//      corner test), scan kernel (unit offsets, sizes, receiver offsets),
+//      write kernel (stable warp ballot compaction -> ascending index map +
+//      the new halo coordinates);
 //   3. finalize: dense bases, home slot -> dense slot map; one D2H copy of the
 //      metadata.
 // Index maps hold domain-relative local indices, so the dense relayout touches
@@ -85,26 +85,27 @@ __device__ __forceinline__ int cell_of(int D, int d, int nx, int ny) {
 
 
 // ---- 1. home partition ------------------------------------------------------------
-// A block of W warps covers the block tile b of W * kHistTile atoms; warp w
-// its sub-tile [(b*W + w)*kHistTile, ... + kHistTile).  Each warp counts its
-// sub-tile into its own shared histogram (shared-memory atomics); the block
-// writes one count per domain, counts[D*nbt + b] (domain-major, so one
-// exclusive scan gives every (domain, block tile) start), and every warp's
-// counts, wcounts[(b*W + w)*nd + D] (contiguous per block, for the scatter).
+// A block of W warps covers the block tile b of W * wtile atoms; warp w its
+// sub-tile [(b*W + w)*wtile, ... + wtile) (wtile a multiple of 128).  Each
+// warp counts its sub-tile into its own shared histogram (shared-memory
+// atomics); the block writes one count per domain, counts[D*nbt + b]
+// (domain-major, so one exclusive scan gives every (domain, block tile)
+// start), and, if wcounts is given, every warp's counts,
+// wcounts[(b*W + w)*nd + D] (contiguous per block, for the direct scatter).
 __global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int nd, int64_t nbt,
-                                 int32_t* __restrict__ counts, int32_t* __restrict__ wcounts,
-                                 int64_t* __restrict__ flags) {
+                                 int wtile, int32_t* __restrict__ counts,
+                                 int32_t* __restrict__ wcounts, int64_t* __restrict__ flags) {
     extern __shared__ int32_t sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int W = blockDim.x >> 5;
     int32_t* h = sh + (size_t)warp * nd;
     for (int i = lane; i < nd; i += 32) h[i] = 0;
     __syncwarp();
-    const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * kHistTile;
+    const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * wtile;
     bool bad = false;
-    // eight coalesced loads in flight per lane, then their counts
-    constexpr int U = 8;
-    for (int it = 0; it < kHistTile / 32; it += U) {
+    // four coalesced loads in flight per lane, then their counts
+    constexpr int U = 4;
+    for (int it = 0; it < wtile / 32; it += U) {
         int d[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
@@ -122,8 +123,10 @@ __global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int
     }
     if (bad) flags[1] = 1;
     __syncthreads();
-    int32_t* wc = wcounts + (int64_t)blockIdx.x * W * nd;
-    for (int i = threadIdx.x; i < W * nd; i += blockDim.x) wc[i] = sh[i];
+    if (wcounts) {
+        int32_t* wc = wcounts + (int64_t)blockIdx.x * W * nd;
+        for (int i = threadIdx.x; i < W * nd; i += blockDim.x) wc[i] = sh[i];
+    }
     for (int d = threadIdx.x; d < nd; d += blockDim.x) {
         int32_t t = 0;
         for (int w = 0; w < W; w++) t += sh[(size_t)w * nd + d];
@@ -192,43 +195,80 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
     }
 }
 
-// The same stable scatter through shared memory: the block first places its
-// tile's atoms in domain order in shared memory (warp by warp, 32 atoms at a
-// time, ranks from the warp match mask, so the order within a domain stays
-// the input order), then writes each domain's run of the tile contiguously.
-// The global stores then fill whole sectors; scattered one atom per domain,
-// each partly written sector had to be fetched from DRAM first.
-__host__ __device__ inline size_t staged_scatter_smem(int W, int nd) {
-    const size_t head = ((size_t)W * nd + 2 * (size_t)nd + 1) * sizeof(int32_t);
-    const size_t T = (size_t)W * kHistTile;
-    return ((head + 15) & ~(size_t)15) + T * (sizeof(float4) + sizeof(int32_t) + sizeof(int16_t));
+// The stable scatter with the block's whole tile in shared memory.  Block b
+// copies its T atoms' coordinates and domain ids into shared memory (16-byte
+// asynchronous copies where the tile is 16-byte aligned, so every copy is in
+// flight at once), counts them per warp sub-tile, ranks them (per-domain tile
+// starts, then each warp's atoms in input order, 32 at a time, ranks among
+// equal ids from the warp match mask) and writes every domain's run of the
+// tile contiguously, from its scanned start tstart[b*nd + D] (the exclusive
+// scan of the hist kernel's domain-major counts, stored tile-major).  Several
+// blocks fit on an SM, so one block's copies overlap another's ranking.
+__host__ __device__ inline size_t tile_scatter_head(int W, int nd) {
+    return ((((size_t)W * nd + 2 * (size_t)nd + 1) * sizeof(int32_t)) + 15) & ~(size_t)15;
+}
+__host__ __device__ inline size_t tile_scatter_smem(int W, int nd, int T) {
+    // raw coordinates, raw domain ids, sorted position -> tile index
+    return tile_scatter_head(W, nd) + (size_t)T * (3 * sizeof(float) + sizeof(int32_t) + sizeof(int16_t));
 }
 
-__global__ void home_scatter_staged_kernel(const float* __restrict__ xyz,
-                                           const int32_t* __restrict__ dom, int64_t n, int nd,
-                                           int64_t nbt, const int32_t* __restrict__ offs,
-                                           const int32_t* __restrict__ wcounts,
-                                           int32_t* __restrict__ home_gid, float4* __restrict__ bxyz) {
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads) home_scatter_tile_kernel(
+    const float* __restrict__ xyz, const int32_t* __restrict__ dom, int64_t n, int nd, int T,
+    int vec, const int32_t* __restrict__ tstart, int32_t* __restrict__ home_gid,
+    float4* __restrict__ bxyz) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int W = blockDim.x >> 5;
-    const int T = W * kHistTile;
-    int32_t* wpos = reinterpret_cast<int32_t*>(smem);  // W * nd: next sorted position, per warp and domain
-    int32_t* lstart = wpos + (size_t)W * nd;           // nd + 1: first sorted position of each domain
-    int32_t* gstart = lstart + nd + 1;                 // nd: the domain run's first home-compact slot
-    const size_t head = ((size_t)W * nd + 2 * (size_t)nd + 1) * sizeof(int32_t);
-    float4* st_xyz = reinterpret_cast<float4*>(smem + ((head + 15) & ~(size_t)15));
-    int32_t* st_gid = reinterpret_cast<int32_t*>(st_xyz + T);
-    int16_t* st_dom = reinterpret_cast<int16_t*>(st_gid + T);
-    const int32_t* wc = wcounts + (int64_t)blockIdx.x * W * nd;
-    for (int d = threadIdx.x; d < nd; d += blockDim.x) {
-        int32_t t = 0;
-        for (int w = 0; w < W; w++) t += wc[(size_t)w * nd + d];
-        lstart[d] = t;
-        gstart[d] = offs[(int64_t)d * nbt + blockIdx.x];
+    constexpr int W = kThreads / 32;
+    int32_t* whist = reinterpret_cast<int32_t*>(smem);  // W * nd: per warp and domain
+    int32_t* lstart = whist + (size_t)W * nd;           // nd + 1: tile start of each domain
+    int32_t* gstart = lstart + nd + 1;                  // nd: the domain run's first home slot
+    float* rx = reinterpret_cast<float*>(smem + tile_scatter_head(W, nd));
+    int32_t* rd = reinterpret_cast<int32_t*>(rx + 3 * (size_t)T);
+    int16_t* perm = reinterpret_cast<int16_t*>(rd + T);
+    const int64_t a0 = (int64_t)blockIdx.x * T;
+    const int cnt = (int)min((int64_t)T, n - a0);
+    const float* gx = xyz + 3 * a0;
+    const int32_t* gd = dom + a0;
+    // 1. the raw tile into shared memory
+    const int nf = 3 * cnt;
+    int vf = 0, vd = 0;
+    if (vec) {
+        vf = nf >> 2;
+        vd = cnt >> 2;
+        for (int i = threadIdx.x; i < vf; i += kThreads) cp_async16(rx + 4 * i, gx + 4 * i);
+        for (int i = threadIdx.x; i < vd; i += kThreads) cp_async16(rd + 4 * i, gd + 4 * i);
+    }
+    for (int i = 4 * vf + threadIdx.x; i < nf; i += kThreads) rx[i] = __ldg(gx + i);
+    for (int i = 4 * vd + threadIdx.x; i < cnt; i += kThreads) rd[i] = __ldg(gd + i);
+    for (int d = threadIdx.x; d < nd; d += kThreads) gstart[d] = tstart[(int64_t)blockIdx.x * nd + d];
+    for (int i = threadIdx.x; i < W * nd; i += kThreads) whist[i] = 0;
+    if (vec) asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    // 2. per-warp counts of the warp's sub-tile
+    const int S = T / W;
+    const int i0 = warp * S;
+    for (int i = i0 + lane; i < i0 + S; i += 32) {
+        if (i >= cnt) break;
+        const int d = rd[i];
+        if (d >= 0 && d < nd) atomicAdd(&whist[(size_t)warp * nd + d], 1);
     }
     __syncthreads();
-    // exclusive scan of the per-domain counts (the first warp, 32 at a time)
+    // 3. tile count per domain; each warp's start within its domain's run
+    for (int d = threadIdx.x; d < nd; d += kThreads) {
+        int32_t acc = 0;
+        for (int w = 0; w < W; w++) {
+            const int32_t c = whist[(size_t)w * nd + d];
+            whist[(size_t)w * nd + d] = acc;
+            acc += c;
+        }
+        lstart[d] = acc;
+    }
+    __syncthreads();
     if (warp == 0) {
         int32_t carry = 0;
         for (int d0 = 0; d0 < nd; d0 += 32) {
@@ -246,57 +286,33 @@ __global__ void home_scatter_staged_kernel(const float* __restrict__ xyz,
         if (lane == 0) lstart[nd] = carry;
     }
     __syncthreads();
-    for (int d = threadIdx.x; d < nd; d += blockDim.x) {
-        int32_t acc = lstart[d];
-        for (int w = 0; w < W; w++) {
-            wpos[(size_t)w * nd + d] = acc;
-            acc += wc[(size_t)w * nd + d];
-        }
+    for (int d = threadIdx.x; d < nd; d += kThreads) {
+        const int32_t l = lstart[d];
+        for (int w = 0; w < W; w++) whist[(size_t)w * nd + d] += l;
     }
     __syncthreads();
-    int32_t* run = wpos + (size_t)warp * nd;
-    const int64_t a0 = ((int64_t)blockIdx.x * W + warp) * kHistTile;
+    // 4. rank: each warp places its atoms in input order
     const unsigned lt = lanemask_lt();
-    constexpr int U = 4;
-    for (int it = 0; it < kHistTile / 32; it += U) {
-        int d[U];
-        float c[U][3];
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int64_t a = a0 + (it + u) * 32 + lane;
-            d[u] = -1;
-            c[u][0] = c[u][1] = c[u][2] = 0.0f;
-            if (a < n) {
-                d[u] = __ldg(dom + a);
-                if (d[u] < 0 || d[u] >= nd) d[u] = -1;
-                c[u][0] = __ldg(xyz + 3 * a + 0);
-                c[u][1] = __ldg(xyz + 3 * a + 1);
-                c[u][2] = __ldg(xyz + 3 * a + 2);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int64_t a = a0 + (it + u) * 32 + lane;
-            const unsigned peers = __match_any_sync(kFull, d[u]);
-            if (d[u] >= 0) {
-                const int pos = run[d[u]] + __popc(peers & lt);
-                st_xyz[pos] = make_float4(c[u][0], c[u][1], c[u][2], __int_as_float(0));
-                st_gid[pos] = (int32_t)a;
-                st_dom[pos] = (int16_t)d[u];
-            }
-            __syncwarp();
-            if (d[u] >= 0 && lane == __ffs(peers) - 1) run[d[u]] += __popc(peers);
-            __syncwarp();
-        }
+    int32_t* run = whist + (size_t)warp * nd;
+    for (int r = 0; r < S; r += 32) {
+        const int i = i0 + r + lane;
+        int d = i < cnt ? rd[i] : -1;
+        if (d >= nd) d = -1;
+        const unsigned peers = __match_any_sync(kFull, d);
+        if (d >= 0) perm[run[d] + __popc(peers & lt)] = (int16_t)i;
+        __syncwarp();
+        if (d >= 0 && lane == __ffs(peers) - 1) run[d] += __popc(peers);
+        __syncwarp();
     }
     __syncthreads();
-    // every domain's run of the tile, contiguous in the home-compact region
+    // 5. every domain's run of the tile, contiguous in the home-compact region
     const int total = lstart[nd];
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-        const int dd = st_dom[i];
-        const int64_t g = (int64_t)gstart[dd] + (i - lstart[dd]);
-        bxyz[g] = st_xyz[i];
-        home_gid[g] = st_gid[i];
+    for (int j = threadIdx.x; j < total; j += kThreads) {
+        const int i = perm[j];
+        const int d = rd[i];
+        const int64_t g = (int64_t)gstart[d] + (j - lstart[d]);
+        bxyz[g] = make_float4(rx[3 * i], rx[3 * i + 1], rx[3 * i + 2], __int_as_float(0));
+        home_gid[g] = (int32_t)(a0 + i);
     }
 }
 
@@ -326,9 +342,12 @@ __global__ void scan_top_kernel(int32_t* __restrict__ sums, int64_t nb) {
     }
 }
 
+// rows > 0: the input is rows-major within cols groups (i = c * rows + r), and
+// the output is stored transposed, out[r * cols + c].
 __global__ void __launch_bounds__(kThreads) scan_down_kernel(const int32_t* __restrict__ in,
                                                              int32_t* __restrict__ out, int64_t n,
-                                                             const int32_t* __restrict__ sums) {
+                                                             const int32_t* __restrict__ sums,
+                                                             int64_t rows, int64_t cols) {
     // each warp walks a contiguous run of the tile 32 elements at a time
     // (coalesced), a shuffle scan per 32, warp totals scanned across the block
     constexpr int kWarps = kThreads / 32;
@@ -359,17 +378,19 @@ __global__ void __launch_bounds__(kThreads) scan_down_kernel(const int32_t* __re
             if (lane >= o) x += y;
         }
         const int64_t i = r0 + r * 32 + lane;
-        if (i < n) out[i] = (int32_t)(carry + x - v[r]);
+        if (i < n) out[rows > 0 ? (i % rows) * cols + i / rows : i] = (int32_t)(carry + x - v[r]);
         carry += __shfl_sync(kFull, x, 31);
     }
 }
 
 // Per-domain home counts and starts from the scanned tile offsets; pulse state init.
-__global__ void home_meta_kernel(const int32_t* __restrict__ offs, int64_t ntiles, int64_t n,
+// offs[D * dstride] is domain D's first home slot (the scanned start of its
+// first tile).
+__global__ void home_meta_kernel(const int32_t* __restrict__ offs, int64_t dstride, int64_t n,
                                  int nd, int P, Meta m) {
     for (int D = blockIdx.x * blockDim.x + threadIdx.x; D < nd; D += gridDim.x * blockDim.x) {
-        const int64_t h0 = offs[(int64_t)D * ntiles];
-        const int64_t h1 = (D + 1 < nd) ? offs[(int64_t)(D + 1) * ntiles] : n;
+        const int64_t h0 = offs[(int64_t)D * dstride];
+        const int64_t h1 = (D + 1 < nd) ? offs[(int64_t)(D + 1) * dstride] : n;
         m.hstart[D] = h0;
         m.n_home[D] = h1 - h0;
         m.own_off[(int64_t)D * (P + 1)] = h1 - h0;
@@ -444,63 +465,77 @@ __device__ __forceinline__ void load_locator(Locator& L, const PulseArgs& a, int
     __syncthreads();
 }
 
-__device__ __forceinline__ void sub_range(const Locator& L, const PulseArgs& a, int b,
-                                          int64_t* lo, int64_t* hi) {
+// Warp-granular work: block b of sender s has kPulseWarps warps, and warp w
+// takes unit u = b * kPulseWarps + w of the B * kPulseWarps contiguous, equal
+// parts of the candidate range (so the units, in order, cover it in order).
+constexpr int kPulseWarps = kThreads / 32;
+
+__device__ __forceinline__ void unit_range(const Locator& L, const PulseArgs& a, int u,
+                                           int64_t* lo, int64_t* hi) {
     const int64_t c0 = (a.k == 0) ? 0 : L.oo[a.p - 1];
     const int64_t c1 = L.oo[a.p];
     const int64_t len = c1 - c0;
-    *lo = c0 + len * b / a.B;
-    *hi = c0 + len * (b + 1) / a.B;
+    const int64_t units = (int64_t)a.B * kPulseWarps;
+    *lo = c0 + len * u / units;
+    *hi = c0 + len * (u + 1) / units;
 }
 
+// Is candidate slot v (coordinates, forwarding dims in w) sent by this pulse?
+__device__ __forceinline__ bool pulse_selects(const PulseArgs& a, const int cell[3], float thr,
+                                              const float4& v) {
+    const float vd = a.d == 0 ? v.x : (a.d == 1 ? v.y : v.z);
+    if (!(vd < thr)) return false;
+    if (!a.prune) return true;
+    const float c[3] = {v.x, v.y, v.z};
+    return corner_within(a, cell, c, (unsigned)__float_as_int(v.w));
+}
+
+// Per unit: how many candidates the pulse sends, and how many of them are
+// home atoms (the split).  Each warp counts its unit 32 candidates at a time,
+// U rounds' loads in flight.
 __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
     __shared__ Locator L;
-    const int s = blockIdx.y, b = blockIdx.x;
+    const int s = blockIdx.y;
     load_locator(L, a, s);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int u0 = blockIdx.x * kPulseWarps + w;
     const int cs = cell_of(s, a.d, a.nx, a.ny);
     const float thr = a.thr[cs];
     const int cell[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
     int64_t lo, hi;
-    sub_range(L, a, b, &lo, &hi);
+    unit_range(L, a, u0, &lo, &hi);
     const int64_t nh = L.oo[0];
-    int64_t c = 0, ch = 0;
-    // four candidates per thread and step, their loads issued together
-    constexpr int U = 4;
-    for (int64_t i0 = lo + threadIdx.x; i0 < hi; i0 += U * kThreads) {
-        float4 slot[U];
+    int c = 0, ch = 0;
+    constexpr int U = 8;
+    for (int64_t t0 = lo; t0 < hi; t0 += U * 32) {
+        float4 v[U];
         bool in[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            const int64_t i = i0 + u * kThreads;
+            const int64_t i = t0 + u * 32 + lane;
             const int64_t pos = i < hi ? locate(L, a.p, i) : -1;
             in[u] = pos >= 0 && pos < a.cap;
-            slot[u] = in[u] ? a.bxyz[pos] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            v[u] = in[u] ? a.bxyz[pos] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            if (!in[u]) continue;
-            const float vd = a.d == 0 ? slot[u].x : (a.d == 1 ? slot[u].y : slot[u].z);
-            if (vd < thr) {
-                if (a.prune) {
-                    const float v[3] = {slot[u].x, slot[u].y, slot[u].z};
-                    if (!corner_within(a, cell, v, (unsigned)__float_as_int(slot[u].w))) continue;
-                }
-                c++;
-                if (i0 + u * kThreads < nh) ch++;
-            }
+            const bool sel = in[u] && pulse_selects(a, cell, thr, v[u]);
+            const unsigned bal = __ballot_sync(kFull, sel);
+            c += __popc(bal);
+            const int64_t i0 = t0 + u * 32;  // the round's first candidate
+            if (i0 < nh) ch += __popc(bal & (nh - i0 >= 32 ? kFull : ((1u << (nh - i0)) - 1u)));
         }
     }
-    int64_t tc, th;
-    block_exclusive_scan<kThreads>(c, &tc);
-    block_exclusive_scan<kThreads>(ch, &th);
-    if (threadIdx.x == 0) {
-        a.cnt[(int64_t)s * a.B + b] = (int32_t)tc;
-        a.cnt_home[(int64_t)s * a.B + b] = (int32_t)th;
+    if (lane == 0) {
+        const int64_t q = (int64_t)s * a.B * kPulseWarps + u0;
+        a.cnt[q] = c;
+        a.cnt_home[q] = ch;
     }
 }
 
 __global__ void __launch_bounds__(1024) pulse_scan_kernel(PulseArgs a) {
-    const int64_t M = (int64_t)a.nd * a.B;
+    const int64_t per = (int64_t)a.B * kPulseWarps;  // units per sender
+    const int64_t M = (int64_t)a.nd * per;
     int64_t carry = 0;
     for (int64_t b0 = 0; b0 < M; b0 += 1024) {
         const int64_t i = b0 + threadIdx.x;
@@ -514,11 +549,11 @@ __global__ void __launch_bounds__(1024) pulse_scan_kernel(PulseArgs a) {
     const int64_t R = a.m.region[a.p];
     for (int s = threadIdx.x; s < a.nd; s += blockDim.x) {
         int64_t snd = 0, spl = 0;
-        for (int b = 0; b < a.B; b++) {
-            snd += a.cnt[(int64_t)s * a.B + b];
-            spl += a.cnt_home[(int64_t)s * a.B + b];
+        for (int64_t u = 0; u < per; u++) {
+            snd += a.cnt[(int64_t)s * per + u];
+            spl += a.cnt_home[(int64_t)s * per + u];
         }
-        const int64_t G = a.blk_off[(int64_t)s * a.B];
+        const int64_t G = a.blk_off[(int64_t)s * per];
         const int64_t sp = (int64_t)s * a.P + a.p;
         a.m.send[sp] = snd;
         a.m.split[sp] = spl;
@@ -537,70 +572,50 @@ __global__ void __launch_bounds__(1024) pulse_scan_kernel(PulseArgs a) {
     }
 }
 
+// Each warp writes its unit's sent candidates from the unit's scanned offset
+// on, in candidate order (ranks from the round's ballot): no block barrier.
 __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
-    constexpr int U = 4;  // tiles of kThreads candidates per step
     __shared__ Locator L;
-    __shared__ int wcnt[U][kThreads / 32];
-    const int s = blockIdx.y, b = blockIdx.x;
+    const int s = blockIdx.y;
     load_locator(L, a, s);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int u0 = blockIdx.x * kPulseWarps + w;
     const int cs = cell_of(s, a.d, a.nx, a.ny);
     const float thr = a.thr[cs];
     const int cell[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
     float sh[3] = {0.0f, 0.0f, 0.0f};
     if (cs == 0) sh[a.d] = a.Ld;
     int64_t lo, hi;
-    sub_range(L, a, b, &lo, &hi);
-    int64_t out = a.m.region[a.p] + a.blk_off[(int64_t)s * a.B + b];
+    unit_range(L, a, u0, &lo, &hi);
+    int64_t out = a.m.region[a.p] + a.blk_off[(int64_t)s * a.B * kPulseWarps + u0];
     const unsigned lt = lanemask_lt();
-    // U consecutive tiles per step: every candidate's load is issued first,
-    // then the tiles are compacted in order (one barrier pair per step)
-    for (int64_t t0 = lo; t0 < hi; t0 += U * kThreads) {
-        float4 slot[U];
-        bool sel[U];
-        unsigned bal[U];
+    const unsigned bit = 1u << a.d;
+    constexpr int U = 8;
+    for (int64_t t0 = lo; t0 < hi; t0 += U * 32) {
+        float4 v[U];
+        bool in[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            const int64_t i = t0 + u * kThreads + threadIdx.x;
+            const int64_t i = t0 + u * 32 + lane;
             const int64_t pos = i < hi ? locate(L, a.p, i) : -1;
-            sel[u] = pos >= 0 && pos < a.cap;
-            slot[u] = sel[u] ? a.bxyz[pos] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            in[u] = pos >= 0 && pos < a.cap;
+            v[u] = in[u] ? a.bxyz[pos] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            if (sel[u]) {
-                const float vd = a.d == 0 ? slot[u].x : (a.d == 1 ? slot[u].y : slot[u].z);
-                sel[u] = vd < thr;
-                if (sel[u] && a.prune) {
-                    const float v[3] = {slot[u].x, slot[u].y, slot[u].z};
-                    sel[u] = corner_within(a, cell, v, (unsigned)__float_as_int(slot[u].w));
-                }
-            }
-            bal[u] = __ballot_sync(kFull, sel[u]);
-            if (lane == 0) wcnt[u][warp] = __popc(bal[u]);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            int before = 0, total = 0;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; w++) {
-                const int c = wcnt[u][w];
-                before += (w < warp) ? c : 0;
-                total += c;
-            }
-            if (sel[u]) {
-                const int64_t o = out + before + __popc(bal[u] & lt);
+            const bool sel = in[u] && pulse_selects(a, cell, thr, v[u]);
+            const unsigned bal = __ballot_sync(kFull, sel);
+            if (sel) {
+                const int64_t o = out + __popc(bal & lt);
                 if (o >= a.N && o < a.cap) {
-                    const unsigned m = (unsigned)__float_as_int(slot[u].w);
-                    a.maps[o - a.N] = (int32_t)(t0 + u * kThreads + threadIdx.x);
-                    a.bxyz[o] = make_float4(slot[u].x + sh[0], slot[u].y + sh[1], slot[u].z + sh[2],
-                                            __int_as_float((int)(m | (1u << a.d))));
+                    const unsigned m = (unsigned)__float_as_int(v[u].w);
+                    a.maps[o - a.N] = (int32_t)(t0 + u * 32 + lane);
+                    a.bxyz[o] = make_float4(v[u].x + sh[0], v[u].y + sh[1], v[u].z + sh[2],
+                                            __int_as_float((int)(m | bit)));
                 }
             }
-            out += total;
+            out += __popc(bal);
         }
-        __syncthreads();
     }
 }
 
@@ -615,6 +630,43 @@ __global__ void __launch_bounds__(1024) finalize_kernel(Meta m, int nd, int P) {
         if (D < nd) m.base[D] = carry + pre;
         carry += tot;
     }
+}
+
+// Pulse descriptors on the device, from the metadata: the fields of the
+// host's copy of the plan (map offset, sender base, the halo slice's first
+// dense slot in the receiver, sizes, the shift across the periodic boundary),
+// so the kernels that read them can run before the host has its own copy.
+struct SPArgs {
+    int8_t dim[HALO_MAX_PULSES];
+    float box[3];
+    int nx, ny, nz, nd, P;
+    int64_t n;
+};
+
+__global__ void sp_kernel(Meta m, SPArgs a, SPDesc* __restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)a.nd * a.P) return;
+    const int s = (int)(i / a.P), p = (int)(i % a.P);
+    const int d = a.dim[p];
+    const int g[3] = {a.nx, a.ny, a.nz};
+    int c[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
+    const bool wrap = c[d] == 0;
+    c[d] = (c[d] - 1 + g[d]) % g[d];
+    const int r = c[0] + a.nx * (c[1] + a.ny * c[2]);
+    SPDesc x;
+    x.map_off = m.map_pos[i] - a.n;
+    x.src_base = m.base[s];
+    x.dst = m.base[r] + m.own_off[(int64_t)r * (a.P + 1) + p];
+    x.send = (int32_t)m.send[i];
+    x.split = (int32_t)m.split[i];
+    x.s = s;
+    x.r = r;
+    x.p = p;
+    x.pad = 0;
+    x.shift[0] = x.shift[1] = x.shift[2] = 0.0f;
+    if (wrap) x.shift[d] = a.box[d];
+    x.pad2 = 0.0f;
+    out[i] = x;
 }
 
 __global__ void home_dst_kernel(Meta m, int64_t* __restrict__ home_dst) {
@@ -635,12 +687,12 @@ int grow(float** p, int64_t* cap_have, int64_t need_slots) {
 }  // namespace
 
 int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
-                          cudaStream_t st) {
+                          cudaStream_t st, int64_t rows, int64_t cols) {
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
     if (nb == 0) return HALO_OK;
     scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, n, tmp);
     scan_top_kernel<<<1, 1024, 0, st>>>(tmp, nb);
-    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp);
+    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp, rows, cols);
     return cuda_code(cudaGetLastError());
 }
 
@@ -665,12 +717,37 @@ void free_build(halo_plan* pl) {
 int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n,
                cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
-    const int64_t ntiles = (n + kHistTile - 1) / kHistTile;
-    // home partition: W warps per block (their histograms share 48 KB of
-    // shared memory), one block tile of W * kHistTile atoms per block
-    const int wpb = (int)std::min<int64_t>(8, std::max<int64_t>(1, (48 * 1024) / ((int64_t)nd * 4)));
+    // home partition.  Tiled: blocks of kThreads / 32 warps over tiles of T
+    // atoms, each tile ranked in shared memory by the scatter; T is the
+    // largest of 8192 .. 1024 with two scatter blocks per SM (the per-warp
+    // histograms of 8 warps must fit 48 KB).  Measured on the 3M-atom
+    // system (T = 4096): rebuild 0.59 ms against 0.60 at T = 2048 (three
+    // blocks per SM) and 0.60 at T = 8192 (one).  Otherwise the direct
+    // scatter: W warps per block (their histograms share 48 KB of shared
+    // memory), one block tile of W * kHistTile atoms per block.
+    int tileT = 0;
+    size_t tile_smem = 0;
+    if ((size_t)(kThreads / 32) * nd * sizeof(int32_t) <= 48 * 1024 && nd < 32768) {
+        int optin = 0, per_sm = 0;
+        HALO_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->dev));
+        HALO_CUDA(cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, pl->dev));
+        for (int T : {8192, 4096, 2048, 1024}) {
+            const size_t need = tile_scatter_smem(kThreads / 32, nd, T);
+            if (need <= (size_t)optin && 2 * (need + 1024) <= (size_t)per_sm) {
+                tileT = T;
+                tile_smem = need;
+                break;
+            }
+        }
+        if (tileT > 0)
+            HALO_CUDA(cudaFuncSetAttribute(home_scatter_tile_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem));
+    }
+    const int wpb = tileT > 0 ? kThreads / 32
+                              : (int)std::min<int64_t>(8, std::max<int64_t>(1, (48 * 1024) / ((int64_t)nd * 4)));
+    const int wtile = tileT > 0 ? tileT / wpb : kHistTile;
     const size_t hist_smem = (size_t)wpb * nd * sizeof(int32_t);
-    const int64_t nbt = (ntiles + wpb - 1) / wpb;
+    const int64_t nbt = (n + (int64_t)wpb * wtile - 1) / ((int64_t)wpb * wtile);
     const unsigned hist_blocks = (unsigned)std::max<int64_t>(nbt, 1);
 
     // --- buffers that depend on N
@@ -683,9 +760,9 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         pl->n_alloc_atoms = n;
     }
     const int64_t ncount = (int64_t)nd * nbt;
-    // block-tile counts, their scanned offsets, then every warp's counts
-    // (block-major: [block tile][warp][domain]) for the scatter
-    const int64_t nwc = (int64_t)nd * nbt * wpb;
+    // block-tile counts, their scanned offsets, then (direct scatter) every
+    // warp's counts (block-major: [block tile][warp][domain])
+    const int64_t nwc = tileT > 0 ? 0 : (int64_t)nd * nbt * wpb;
     if (2 * ncount + nwc > pl->counts_cap) {
         dev_free(pl->d_counts);
         pl->counts_cap = 0;
@@ -715,7 +792,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         B = std::min<int64_t>(B, 64);
         if (B != pl->build_blocks_per_domain || !pl->d_pulse_scratch) {
             dev_free(pl->d_pulse_scratch);
-            HALO_TRY(dev_alloc(&pl->d_pulse_scratch, (size_t)3 * nd * B));
+            HALO_TRY(dev_alloc(&pl->d_pulse_scratch, (size_t)3 * nd * B * kPulseWarps));
             pl->build_blocks_per_domain = (int)B;
         }
     }
@@ -766,21 +843,18 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
     }
     pl->build_attempts = 0;
 
-    // the home scatter sorts each tile in shared memory where the tile and
-    // the per-domain tables fit (nd < 32768 for the int16 domain ids)
-    size_t staged_smem = 0;
-    {
-        int optin = 0;
-        HALO_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->dev));
-        const size_t need = staged_scatter_smem(wpb, nd);
-        if (nd < 32768 && need <= (size_t)optin) {
-            HALO_CUDA(cudaFuncSetAttribute(home_scatter_staged_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need));
-            staged_smem = need;
-        }
-    }
 
     const Meta m = meta_ptrs(pl->d_meta, nd, P);
+    HALO_TRY(dev_reserve(&pl->d_sp, &pl->cap_sp, (int64_t)nd * P));
+    SPArgs spa;
+    for (int p = 0; p < HALO_MAX_PULSES; p++) spa.dim[p] = (int8_t)(p < P ? pl->pulse_dim[p] : 0);
+    for (int d = 0; d < 3; d++) spa.box[d] = pl->box[d];
+    spa.nx = pl->grid[0];
+    spa.ny = pl->grid[1];
+    spa.nz = pl->grid[2];
+    spa.nd = nd;
+    spa.P = P;
+    spa.n = n;
     void* hstage = nullptr;
     HALO_TRY(host_stage(pl, mbytes, &hstage));
     int64_t* hm = static_cast<int64_t*>(hstage);
@@ -801,20 +875,25 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         }
         HALO_CUDA(cudaMemsetAsync(pl->d_meta, 0, mbytes, st));
         // 1. home partition
-        int32_t* wcounts = pl->d_counts + 2 * ncount;
-        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(dom, n, nd, nbt,
+        int32_t* wcounts = tileT > 0 ? nullptr : pl->d_counts + 2 * ncount;
+        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(dom, n, nd, nbt, wtile,
                                                                   pl->d_counts, wcounts, m.flags);
         int32_t* offs = pl->d_counts + ncount;
-        HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
-        if (staged_smem > 0)
-            home_scatter_staged_kernel<<<hist_blocks, wpb * 32, staged_smem, st>>>(
-                coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid,
+        if (tileT > 0) {
+            // tile starts stored tile-major, so each scatter block reads its
+            // domains' starts contiguously
+            HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st, nbt, nd));
+            const int vec = ((uintptr_t)coords % 16 == 0 && (uintptr_t)dom % 16 == 0) ? 1 : 0;
+            home_scatter_tile_kernel<<<hist_blocks, kThreads, tile_smem, st>>>(
+                coords, dom, n, nd, tileT, vec, offs, pl->d_home_gid,
                 reinterpret_cast<float4*>(pl->d_bxyz));
-        else
+        } else {
+            HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
             home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
                 coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid,
                 reinterpret_cast<float4*>(pl->d_bxyz));
-        home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, nbt, n, nd, P, m);
+        }
+        home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, tileT > 0 ? 1 : nbt, n, nd, P, m);
         HALO_CUDA(cudaGetLastError());
         // 2. pulses in global order
         for (int p = 0; p < P; p++) {
@@ -825,8 +904,8 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
             a.cap = pl->cap_slots;
             a.m = m;
             a.cnt = pl->d_pulse_scratch;
-            a.cnt_home = pl->d_pulse_scratch + (size_t)nd * B;
-            a.blk_off = pl->d_pulse_scratch + (size_t)2 * nd * B;
+            a.cnt_home = pl->d_pulse_scratch + (size_t)nd * B * kPulseWarps;
+            a.blk_off = pl->d_pulse_scratch + (size_t)2 * nd * B * kPulseWarps;
             a.thr = pl->d_thr + (size_t)p * nmax;
             a.nd = nd;
             a.P = P;
@@ -850,6 +929,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         // 3. dense layout
         finalize_kernel<<<1, 1024, 0, st>>>(m, nd, P);
         home_dst_kernel<<<nd, 256, 0, st>>>(m, pl->d_home_dst);
+        if (nd * P > 0) sp_kernel<<<(unsigned)((nd * P + 255) / 256), 256, 0, st>>>(m, spa, pl->d_sp);
         HALO_CUDA(cudaGetLastError());
         HALO_CUDA(cudaMemcpyAsync(hm, pl->d_meta, mbytes, cudaMemcpyDeviceToHost, st));
         HALO_CUDA(cudaStreamSynchronize(st));
@@ -877,10 +957,13 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
             pl->own_off[(size_t)D * (P + 1) + q] = (int32_t)h.own_off[(size_t)D * (P + 1) + q];
         tot += pl->n_local[D];
     }
+    pl->max_chunks.assign((size_t)std::max(P, 1), 0);
     for (size_t i = 0; i < (size_t)nd * P; i++) {
         pl->send[i] = (int32_t)h.send[i];
         pl->split[i] = (int32_t)h.split[i];
         pl->map_off[i] = h.map_pos[i] - n;
+        const int p = (int)(i % P);
+        pl->max_chunks[p] = std::max(pl->max_chunks[p], (pl->send[i] + kThreads - 1) / kThreads);
     }
     pl->n_local_total = tot;
     pl->n_halo_total = tot - n;

@@ -685,26 +685,6 @@ int grid_cells(const halo_plan* pl, int D, int c[3]) {
     return 0;
 }
 
-// Bytes of pinned staging a vector needs (16-byte granules).
-template <class T>
-size_t stage_bytes(const std::vector<T>& h) {
-    return (h.size() * sizeof(T) + 15) & ~(size_t)15;
-}
-
-// Copy `h` to the device buffer through the pinned staging at *off (the
-// staging must stay untouched until the stream has passed the copy).
-template <class T>
-int upload(T** d, int64_t* cap, const std::vector<T>& h, char* stage, size_t* off,
-           cudaStream_t st) {
-    HALO_TRY(dev_reserve(d, cap, (int64_t)h.size()));
-    if (h.empty()) return HALO_OK;
-    char* src = stage + *off;
-    memcpy(src, h.data(), h.size() * sizeof(T));
-    *off += stage_bytes(h);
-    HALO_CUDA(cudaMemcpyAsync(*d, src, h.size() * sizeof(T), cudaMemcpyHostToDevice, st));
-    return HALO_OK;
-}
-
 template <int E>
 int occupancy(int* blocks_x, int* blocks_f) {
     // the sharded variants have the same resources (checked by the build's register report)
@@ -754,9 +734,9 @@ int prepare_common(halo_plan* pl, cudaStream_t st) {
     pl->entries_per_thread = E;
     pl->chunk = kThreads * E;
 
-    // per (s, p) descriptors
+    // the host's copy of the per (s, p) descriptors (the build wrote the
+    // device's, and the largest chunk counts)
     pl->sp.assign((size_t)nd * P, SPDesc{});
-    pl->max_chunks.assign((size_t)std::max(P, 1), 0);
     for (int s = 0; s < nd; s++) {
         int c[3];
         grid_cells(pl, s, c);
@@ -777,17 +757,8 @@ int prepare_common(halo_plan* pl, cudaStream_t st) {
             x.p = p;
             x.shift[0] = x.shift[1] = x.shift[2] = 0.0f;
             if (c[d] == 0) x.shift[d] = pl->box[d];
-            pl->max_chunks[p] = std::max(pl->max_chunks[p], (x.send + kThreads - 1) / kThreads);
         }
     }
-    char* stage = nullptr;
-    size_t off = 0;
-    {
-        void* hs = nullptr;
-        HALO_TRY(host_stage(pl, stage_bytes(pl->sp) + 64, &hs));
-        stage = static_cast<char*>(hs);
-    }
-    HALO_TRY(upload(&pl->d_sp, &pl->cap_sp, pl->sp, stage, &off, st));
     if (!pl->d_err) HALO_TRY(dev_alloc(&pl->d_err, 8));
     HALO_CUDA(cudaMemsetAsync(pl->d_err, 0, sizeof(int) * 8, st));
     return HALO_OK;
@@ -801,13 +772,13 @@ int prepare_fused(halo_plan* pl, cudaStream_t st) {
     const int E = pl->entries_per_thread;
     const int CHF = 32 * E;
     const int CH = pl->chunk;
-    // four words read back below, in the pinned staging after the descriptors
-    // (which prepare_common reserved; an upload of them may still be in flight)
+    // four words read back below, in the pinned staging (no copy from it is
+    // in flight: every build step that uses it synchronises before returning)
     int32_t* h_tot = nullptr;
     {
         void* hs = nullptr;
-        HALO_TRY(host_stage(pl, stage_bytes(pl->sp) + 64, &hs));
-        h_tot = reinterpret_cast<int32_t*>(static_cast<char*>(hs) + stage_bytes(pl->sp));
+        HALO_TRY(host_stage(pl, 64, &hs));
+        h_tot = static_cast<int32_t*>(hs);
     }
 
     // force-entry classification on the device: last pulse adding into each

@@ -150,6 +150,7 @@ struct halo_plan {
     // (a z-slab of the grid) and the dense slots [shard_first[k], shard_first[k + 1])
     int n_shards = 1;
     bool shard_lists = false;        // halo_shard was called: rebuilds keep the FUSED work lists
+    bool flat_chains_ready = false;  // the FLAT forwarding chains of this build are launched
     int shard_dom[halo::kMaxShards + 1] = {};
     int64_t shard_first[halo::kMaxShards + 1] = {};
 
@@ -187,11 +188,17 @@ namespace halo {
 int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n_atoms,
                cudaStream_t st);
 
+// scratch tmp: ceil(n / kScanTile) ints.  rows > 0: the input is n / rows
+// groups of rows entries (i = c * rows + r) and out is stored transposed,
+// out[r * cols + c].
 int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
-                          cudaStream_t st);  // scratch tmp: ceil(n / kScanTile) ints
+                          cudaStream_t st, int64_t rows = 0, int64_t cols = 0);
 
 // halo_modes.cu: one launch per pulse, and the flattened exchange
 int prepare_flat(halo_plan* pl, cudaStream_t st);
+// The FLAT forwarding chains alone (device descriptors and sizes known); prepare_flat
+// launches them itself unless this ran first in the same build.
+int launch_flat_chains(halo_plan* pl, cudaStream_t st);
 void free_flat(halo_plan* pl);
 int launch_stepwise_x(halo_plan* pl, float* xyz, cudaStream_t st);
 int launch_stepwise_f(halo_plan* pl, float* f, cudaStream_t st);

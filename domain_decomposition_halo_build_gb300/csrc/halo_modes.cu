@@ -908,10 +908,55 @@ void free_flat(halo_plan* pl) {
     pl->max_copies = 0;
 }
 
+namespace {
+// Scratch of the FLAT table build, carved from two pools kept in the plan.
+struct FlatScratch {
+    int32_t *owner, *parent, *ncopies, *entry_pos, *flag, *tmp;
+    int64_t* sums;    // int64 tile sums + grand total
+    int32_t* misc;    // [0] largest copy list, [1] error
+    int64_t* misc64;  // [0] copies | owners << 32, [1] class-A | class-B records << 32
+    int8_t *hop, *code;
+};
+
+int flat_scratch(halo_plan* pl, FlatScratch* f) {
+    const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
+    const int64_t nsums = nl / kScanTile + 2;
+    const int64_t off_sums = (5 * nl + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
+    HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 16));
+    HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
+    f->owner = pl->d_flat_pool32;
+    f->parent = f->owner + nl;
+    f->ncopies = f->parent + nl;
+    f->entry_pos = f->ncopies + nl;
+    f->flag = f->entry_pos + nl;
+    f->tmp = f->flag + nl;
+    f->sums = reinterpret_cast<int64_t*>(pl->d_flat_pool32 + off_sums);
+    f->misc = pl->d_flat_pool32 + off_sums + 2 * nsums;
+    f->misc64 = reinterpret_cast<int64_t*>(f->misc + 8);
+    f->hop = pl->d_flat_pool8;
+    f->code = f->hop + nl;
+    return HALO_OK;
+}
+}  // namespace
+
+int launch_flat_chains(halo_plan* pl, cudaStream_t st) {
+    if (pl->n_local_total >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
+    FlatScratch f;
+    HALO_TRY(flat_scratch(pl, &f));
+    for (int p = 0; p < pl->P; p++) {
+        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+        chain_pulse_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(
+            pl->d_sp, pl->d_maps, f.owner, f.parent, f.hop, f.code, pl->P, p, pl->pulse_dim[p]);
+    }
+    HALO_CUDA(cudaGetLastError());
+    pl->flat_chains_ready = true;
+    return HALO_OK;
+}
+
 int prepare_flat(halo_plan* pl, cudaStream_t st) {
     pl->flat_ready = false;  // buffers are kept (grow-only) across rebuilds
     const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
-    const int nd = pl->n_dom, P = pl->P;
+    const int nd = pl->n_dom;
     if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
     // coordinate items: halo range of every domain, in chunks of kXT * E
     // slots.  E = 2 unless that needs more than two waves of resident blocks,
@@ -930,36 +975,12 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     // item b = {table offset b * kFlatChunk, first halo slot, count}: the
     // table is padded to whole chunks so a block can address its entries
     // from its index alone
-    std::vector<int4> items;
-    for (int D = 0; D < nd; D++) {
-        const int64_t d0 = pl->base[D] + pl->n_home[D];
-        const int64_t nh = (int64_t)pl->n_local[D] - pl->n_home[D];
-        for (int64_t i = 0; i < nh; i += kFlatChunk)
-            items.push_back(make_int4((int)(items.size() * kFlatChunk), (int)(d0 + i),
-                                      (int)std::min<int64_t>(kFlatChunk, nh - i), 0));
-    }
-    pl->n_xflat_items = (int)items.size();
-    HALO_TRY(dev_reserve(&pl->d_xflat_items, &pl->cap_xflat_items, (int64_t)items.size()));
-    // pinned staging: the item list, then words read back at the end, after
-    // the descriptors that prepare_common may still be copying from its
-    // start; only a staging that must grow waits for the stream first
-    const size_t sp_bytes = ((pl->sp.size() * sizeof(SPDesc) + 15) & ~(size_t)15) + 64;
-    const size_t need = sp_bytes + items.size() * sizeof(int4) + 256;
-    if (pl->h_stage_cap < need) HALO_CUDA(cudaStreamSynchronize(st));
-    char* stage = nullptr;
-    {
-        void* hs = nullptr;
-        HALO_TRY(host_stage(pl, need, &hs));
-        stage = static_cast<char*>(hs) + sp_bytes;
-    }
-    int64_t* hw = reinterpret_cast<int64_t*>(stage + items.size() * sizeof(int4));  // 8 words
-    if (!items.empty()) {
-        memcpy(stage, items.data(), items.size() * sizeof(int4));
-        HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, stage, items.size() * sizeof(int4),
-                                  cudaMemcpyHostToDevice, st));
-    }
-    HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat,
-                         std::max<int64_t>((int64_t)items.size() * kFlatChunk, 1)));
+    int64_t n_items = 0;
+    for (int D = 0; D < nd; D++)
+        n_items += ((int64_t)pl->n_local[D] - pl->n_home[D] + kFlatChunk - 1) / kFlatChunk;
+    pl->n_xflat_items = (int)n_items;
+    HALO_TRY(dev_reserve(&pl->d_xflat_items, &pl->cap_xflat_items, n_items));
+    HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat, std::max<int64_t>(n_items * kFlatChunk, 1)));
     HALO_TRY(dev_reserve(&pl->d_fent, &pl->cap_fent, H));
     // owner tables sized by bounds (every halo slot is one copy of one owner:
     // at most H owners, H / 4 with 4..11 copies, H / 12 with more), so that
@@ -970,37 +991,60 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     HALO_TRY(dev_reserve(&pl->d_frec[1], &pl->cap_frec[1], 3 * (H / 4 + 1)));
     HALO_TRY(dev_reserve(&pl->d_frec[2], &pl->cap_frec[2], H / 12 + 1));
 
-    // scratch of the table build, carved from two pools kept in the plan
-    const int64_t nsums = nl / kScanTile + 2;            // int64 tile sums + grand total
-    const int64_t off_sums = (5 * nl + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
-    HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 16));
-    HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
-    int32_t* owner = pl->d_flat_pool32;
-    int32_t* parent = owner + nl;
-    int32_t* ncopies = parent + nl;
-    int32_t* entry_pos = ncopies + nl;
-    int32_t* flag = entry_pos + nl;
-    int32_t* tmp = flag + nl;
-    int64_t* sums = reinterpret_cast<int64_t*>(pl->d_flat_pool32 + off_sums);
-    // misc: [0] largest copy list, [1] error; misc64: [0] copies | owners << 32,
-    // [1] class-A | class-B records << 32
-    int32_t* misc = pl->d_flat_pool32 + off_sums + 2 * nsums;
-    int64_t* misc64 = reinterpret_cast<int64_t*>(misc + 8);
-    int8_t* hop = pl->d_flat_pool8;
-    int8_t* code = hop + nl;
+    FlatScratch f;
+    HALO_TRY(flat_scratch(pl, &f));
+    int32_t* owner = f.owner;
+    int32_t* parent = f.parent;
+    int32_t* ncopies = f.ncopies;
+    int32_t* entry_pos = f.entry_pos;
+    int32_t* flag = f.flag;
+    int32_t* tmp = f.tmp;
+    int64_t* sums = f.sums;
+    int32_t* misc = f.misc;
+    int64_t* misc64 = f.misc64;
+    int8_t* hop = f.hop;
+    int8_t* code = f.code;
+
+    // the forwarding chains need only the pulse descriptors: a rebuild
+    // launches them as soon as the sizes are known (before the host's own
+    // copy of the plan is built), else they are launched here, and run while
+    // the host writes the item list below
+    if (!pl->flat_chains_ready) HALO_TRY(launch_flat_chains(pl, st));
+    pl->flat_chains_ready = false;
+
+    // pinned staging: the item list, then words read back at the end (a
+    // staging that must grow waits for the stream first)
+    const size_t need = (size_t)n_items * sizeof(int4) + 256;
+    if (pl->h_stage_cap < need) HALO_CUDA(cudaStreamSynchronize(st));
+    char* stage = nullptr;
+    {
+        void* hs = nullptr;
+        HALO_TRY(host_stage(pl, need, &hs));
+        stage = static_cast<char*>(hs);
+    }
+    int4* hitems = reinterpret_cast<int4*>(stage);
+    {
+        int64_t b = 0;
+        for (int D = 0; D < nd; D++) {
+            const int64_t d0 = pl->base[D] + pl->n_home[D];
+            const int64_t nh = (int64_t)pl->n_local[D] - pl->n_home[D];
+            for (int64_t i = 0; i < nh; i += kFlatChunk, b++)
+                hitems[b] = make_int4((int)(b * kFlatChunk), (int)(d0 + i),
+                                      (int)std::min<int64_t>(kFlatChunk, nh - i), 0);
+        }
+    }
+    int64_t* hw = reinterpret_cast<int64_t*>(stage + (size_t)n_items * sizeof(int4));  // 8 words
+    if (n_items > 0)
+        HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, hitems, (size_t)n_items * sizeof(int4),
+                                  cudaMemcpyHostToDevice, st));
     int rc = HALO_OK;
     do {
         const int gh = blocks_for(std::max<int64_t>(H, 1), pl->num_sms);
-        for (int p = 0; p < P; p++) {
-            const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
-            chain_pulse_kernel<<<dim3(gx, nd), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, owner, parent,
-                                                                  hop, code, P, p, pl->pulse_dim[p]);
-        }
         if ((rc = cuda_code(cudaMemsetAsync(ncopies, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaMemsetAsync(flag, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaMemsetAsync(misc, 0, sizeof(int32_t) * 16, st))) != HALO_OK) break;
-        if (!items.empty())
-            xflat_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
+        if (n_items > 0)
+            xflat_kernel<<<(unsigned)n_items, kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
                                                                        pl->d_xflat, ncopies);
         // entry offsets of every slot's copy list and, from the same scan,
         // the owner list (fown, fstart); the grand total (copies, owners)
@@ -1008,8 +1052,8 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if ((rc = pair_scan<0>(ncopies, nl, nullptr, sums, entry_pos, nullptr, misc64, st, pl->d_fown,
                                pl->d_fstart)) != HALO_OK)
             break;
-        if (!items.empty())
-            owner_fill_kernel<<<(unsigned)items.size(), kThreads, 0, st>>>(pl->d_xflat_items, owner,
+        if (n_items > 0)
+            owner_fill_kernel<<<(unsigned)n_items, kThreads, 0, st>>>(pl->d_xflat_items, owner,
                                                                             entry_pos, flag, tmp);
         // record classes (A: <= 3 copies, B: 4..11, C: more): positions in
         // each class from one paired scan of the owners' copy counts, then the

@@ -254,6 +254,32 @@ def test_empty_domains_and_skewed_load():
         g.close()
 
 
+@pytest.mark.parametrize("name", ["water24k_2x4x8", "water48k_2x2x2"])
+def test_unaligned_inputs(name):
+    """Coordinates and domain ids that start 12 and 4 bytes past a 16-byte
+    boundary (views one atom into larger arrays): the home partition copies
+    its tiles with plain loads instead of 16-byte copies."""
+    import torch
+    w = synth.WORKLOADS[name]
+    xyz, dom = synth.system(w)
+    o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+    g = gpu_plan(w.box, w.grid, w.rc, xyz, dom)
+    try:
+        xs = torch.zeros((len(xyz) + 1, 3), dtype=torch.float32, device="cuda")
+        ds = torch.zeros(len(dom) + 1, dtype=torch.int32, device="cuda")
+        xs[1:] = torch.from_numpy(xyz)
+        ds[1:] = torch.from_numpy(dom)
+        x, d = xs[1:], ds[1:]
+        assert x.data_ptr() % 16 != 0 and d.data_ptr() % 16 != 0
+        g.plan.rebuild(x, d)
+        g._sync()
+        compare_plans(g, o)
+        g.plan.set_mode("flat")
+        compare_exchanges(g, o, xyz)
+    finally:
+        g.close()
+
+
 def test_setup_errors():
     import torch
     from domain_decomposition_halo_build_gb300 import halo
