@@ -17,11 +17,11 @@
 //      shared memory: warp match + running per-domain counters) -> every
 //      domain's home atoms in input order, in a home-compact region;
 //   2. per pulse: count kernel (predicate per candidate, with the optional
-//      corner test), scan kernel (unit offsets, sizes, receiver offsets),
-//      write kernel (stable warp ballot compaction -> ascending index map +
+//      corner test; its last block scans the unit counts into offsets, sizes
+//      and receiver offsets), write kernel (stable warp ballot compaction -> ascending index map +
 //      the new halo coordinates);
-//   3. finalize: dense bases, home slot -> dense slot map; one D2H copy of the
-//      metadata.
+//   3. finalize: dense bases, pulse descriptors, home slot -> dense slot map;
+//      one D2H copy of the metadata.
 // Index maps hold domain-relative local indices, so the dense relayout touches
 // none of them.
 #include <math.h>
@@ -88,12 +88,13 @@ __device__ __forceinline__ int cell_of(int D, int d, int nx, int ny) {
 // A block of W warps covers the block tile b of W * wtile atoms; warp w its
 // sub-tile [(b*W + w)*wtile, ... + wtile) (wtile a multiple of 128).  Each
 // warp counts its sub-tile into its own shared histogram (shared-memory
-// atomics); the block writes one count per domain, counts[D*nbt + b]
-// (domain-major, so one exclusive scan gives every (domain, block tile)
-// start), and, if wcounts is given, every warp's counts,
-// wcounts[(b*W + w)*nd + D] (contiguous per block, for the direct scatter).
+// atomics); the block writes one count per domain: tile-major,
+// counts[b*nd + D] (tiled scatter), or domain-major, counts[D*nbt + b], so
+// that one exclusive scan gives every (domain, block tile) start, and then,
+// if wcounts is given, every warp's counts, wcounts[(b*W + w)*nd + D]
+// (contiguous per block, for the direct scatter).
 __global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int nd, int64_t nbt,
-                                 int wtile, int32_t* __restrict__ counts,
+                                 int wtile, int tile_major, int32_t* __restrict__ counts,
                                  int32_t* __restrict__ wcounts, int64_t* __restrict__ flags) {
     extern __shared__ int32_t sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -130,7 +131,7 @@ __global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int
     for (int d = threadIdx.x; d < nd; d += blockDim.x) {
         int32_t t = 0;
         for (int w = 0; w < W; w++) t += sh[(size_t)w * nd + d];
-        counts[(int64_t)d * nbt + blockIdx.x] = t;
+        counts[tile_major ? (int64_t)blockIdx.x * nd + d : (int64_t)d * nbt + blockIdx.x] = t;
     }
 }
 
@@ -201,9 +202,9 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
 // flight at once), counts them per warp sub-tile, ranks them (per-domain tile
 // starts, then each warp's atoms in input order, 32 at a time, ranks among
 // equal ids from the warp match mask) and writes every domain's run of the
-// tile contiguously, from its scanned start tstart[b*nd + D] (the exclusive
-// scan of the hist kernel's domain-major counts, stored tile-major).  Several
-// blocks fit on an SM, so one block's copies overlap another's ranking.
+// tile contiguously, from hstart[D] + pre[b*nd + D] (the column prefixes of
+// the tile-major counts).  Several blocks fit on an SM, so one block's copies
+// overlap another's ranking.
 __host__ __device__ inline size_t tile_scatter_head(int W, int nd) {
     return ((((size_t)W * nd + 2 * (size_t)nd + 1) * sizeof(int32_t)) + 15) & ~(size_t)15;
 }
@@ -212,18 +213,91 @@ __host__ __device__ inline size_t tile_scatter_smem(int W, int nd, int T) {
     return tile_scatter_head(W, nd) + (size_t)T * (3 * sizeof(float) + sizeof(int32_t) + sizeof(int16_t));
 }
 
+// Column prefixes of the tile-major counts: for domain d (a lane of a strip
+// of 32 domains) and tile b, pre[b*nd + d] = the count of d's atoms in tiles
+// before b; the warps of a block split the tiles into 32 contiguous ranges.
+// Column totals are the home counts n_home[d].  The last block to finish
+// (an atomic ticket in flags[2], zeroed with the metadata) scans them: every
+// domain's first home slot hstart[d], own_off[d][0] = n_home[d], region[0].
+__global__ void __launch_bounds__(1024) home_colscan_kernel(const int32_t* __restrict__ counts,
+                                                            int64_t nbt, int nd, int P, int64_t n,
+                                                            int32_t* __restrict__ pre, Meta m) {
+    __shared__ int32_t part[32][33];
+    __shared__ int last;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int d = blockIdx.x * 32 + lane;
+    const int64_t b0 = nbt * w / 32, b1 = nbt * (w + 1) / 32;
+    int32_t s = 0;
+    if (d < nd) {
+        int64_t b = b0;
+        for (; b + 4 <= b1; b += 4) {
+            const int32_t c0 = counts[b * nd + d], c1 = counts[(b + 1) * nd + d];
+            const int32_t c2 = counts[(b + 2) * nd + d], c3 = counts[(b + 3) * nd + d];
+            s += (c0 + c1) + (c2 + c3);
+        }
+        for (; b < b1; b++) s += counts[b * nd + d];
+    }
+    part[w][lane] = s;
+    __syncthreads();
+    int32_t acc = 0, tot = 0;
+    for (int q = 0; q < 32; q++) {
+        const int32_t v = part[q][lane];
+        acc += q < w ? v : 0;
+        tot += v;
+    }
+    if (d < nd) {
+        int64_t b = b0;
+        for (; b + 4 <= b1; b += 4) {  // four loads in flight, then their prefixes
+            const int32_t c0 = counts[b * nd + d], c1 = counts[(b + 1) * nd + d];
+            const int32_t c2 = counts[(b + 2) * nd + d], c3 = counts[(b + 3) * nd + d];
+            pre[b * nd + d] = acc;
+            pre[(b + 1) * nd + d] = acc + c0;
+            pre[(b + 2) * nd + d] = acc + c0 + c1;
+            pre[(b + 3) * nd + d] = acc + c0 + c1 + c2;
+            acc += (c0 + c1) + (c2 + c3);
+        }
+        for (; b < b1; b++) {
+            pre[b * nd + d] = acc;
+            acc += counts[b * nd + d];
+        }
+        if (w == 0) m.n_home[d] = tot;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        last = atomicAdd(reinterpret_cast<unsigned long long*>(m.flags + 2), 1ull) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    int64_t carry = 0;
+    for (int D0 = 0; D0 < nd; D0 += 1024) {
+        const int D = D0 + threadIdx.x;
+        const int64_t v = D < nd ? __ldcg(m.n_home + D) : 0;
+        int64_t t;
+        const int64_t p0 = block_exclusive_scan<1024>(v, &t);
+        if (D < nd) {
+            m.hstart[D] = carry + p0;
+            m.own_off[(int64_t)D * (P + 1)] = v;
+        }
+        carry += t;
+    }
+    if (threadIdx.x == 0) m.region[0] = n;
+}
+
+constexpr int kScatterThreads = 512;  // threads (16 warp sub-tiles) per tiled scatter block
+
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads) home_scatter_tile_kernel(
+__global__ void __launch_bounds__(kScatterThreads) home_scatter_tile_kernel(
     const float* __restrict__ xyz, const int32_t* __restrict__ dom, int64_t n, int nd, int T,
-    int vec, const int32_t* __restrict__ tstart, int32_t* __restrict__ home_gid,
-    float4* __restrict__ bxyz) {
+    int vec, const int32_t* __restrict__ pre, const int64_t* __restrict__ hstart,
+    int32_t* __restrict__ home_gid, float4* __restrict__ bxyz) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int W = kThreads / 32;
+    constexpr int W = kScatterThreads / 32;
     int32_t* whist = reinterpret_cast<int32_t*>(smem);  // W * nd: per warp and domain
     int32_t* lstart = whist + (size_t)W * nd;           // nd + 1: tile start of each domain
     int32_t* gstart = lstart + nd + 1;                  // nd: the domain run's first home slot
@@ -240,13 +314,14 @@ __global__ void __launch_bounds__(kThreads) home_scatter_tile_kernel(
     if (vec) {
         vf = nf >> 2;
         vd = cnt >> 2;
-        for (int i = threadIdx.x; i < vf; i += kThreads) cp_async16(rx + 4 * i, gx + 4 * i);
-        for (int i = threadIdx.x; i < vd; i += kThreads) cp_async16(rd + 4 * i, gd + 4 * i);
+        for (int i = threadIdx.x; i < vf; i += kScatterThreads) cp_async16(rx + 4 * i, gx + 4 * i);
+        for (int i = threadIdx.x; i < vd; i += kScatterThreads) cp_async16(rd + 4 * i, gd + 4 * i);
     }
-    for (int i = 4 * vf + threadIdx.x; i < nf; i += kThreads) rx[i] = __ldg(gx + i);
-    for (int i = 4 * vd + threadIdx.x; i < cnt; i += kThreads) rd[i] = __ldg(gd + i);
-    for (int d = threadIdx.x; d < nd; d += kThreads) gstart[d] = tstart[(int64_t)blockIdx.x * nd + d];
-    for (int i = threadIdx.x; i < W * nd; i += kThreads) whist[i] = 0;
+    for (int i = 4 * vf + threadIdx.x; i < nf; i += kScatterThreads) rx[i] = __ldg(gx + i);
+    for (int i = 4 * vd + threadIdx.x; i < cnt; i += kScatterThreads) rd[i] = __ldg(gd + i);
+    for (int d = threadIdx.x; d < nd; d += kScatterThreads)
+        gstart[d] = (int32_t)hstart[d] + pre[(int64_t)blockIdx.x * nd + d];
+    for (int i = threadIdx.x; i < W * nd; i += kScatterThreads) whist[i] = 0;
     if (vec) asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // 2. per-warp counts of the warp's sub-tile
@@ -259,7 +334,7 @@ __global__ void __launch_bounds__(kThreads) home_scatter_tile_kernel(
     }
     __syncthreads();
     // 3. tile count per domain; each warp's start within its domain's run
-    for (int d = threadIdx.x; d < nd; d += kThreads) {
+    for (int d = threadIdx.x; d < nd; d += kScatterThreads) {
         int32_t acc = 0;
         for (int w = 0; w < W; w++) {
             const int32_t c = whist[(size_t)w * nd + d];
@@ -286,7 +361,7 @@ __global__ void __launch_bounds__(kThreads) home_scatter_tile_kernel(
         if (lane == 0) lstart[nd] = carry;
     }
     __syncthreads();
-    for (int d = threadIdx.x; d < nd; d += kThreads) {
+    for (int d = threadIdx.x; d < nd; d += kScatterThreads) {
         const int32_t l = lstart[d];
         for (int w = 0; w < W; w++) whist[(size_t)w * nd + d] += l;
     }
@@ -307,7 +382,7 @@ __global__ void __launch_bounds__(kThreads) home_scatter_tile_kernel(
     __syncthreads();
     // 5. every domain's run of the tile, contiguous in the home-compact region
     const int total = lstart[nd];
-    for (int j = threadIdx.x; j < total; j += kThreads) {
+    for (int j = threadIdx.x; j < total; j += kScatterThreads) {
         const int i = perm[j];
         const int d = rd[i];
         const int64_t g = (int64_t)gstart[d] + (j - lstart[d]);
@@ -342,12 +417,9 @@ __global__ void scan_top_kernel(int32_t* __restrict__ sums, int64_t nb) {
     }
 }
 
-// rows > 0: the input is rows-major within cols groups (i = c * rows + r), and
-// the output is stored transposed, out[r * cols + c].
 __global__ void __launch_bounds__(kThreads) scan_down_kernel(const int32_t* __restrict__ in,
                                                              int32_t* __restrict__ out, int64_t n,
-                                                             const int32_t* __restrict__ sums,
-                                                             int64_t rows, int64_t cols) {
+                                                             const int32_t* __restrict__ sums) {
     // each warp walks a contiguous run of the tile 32 elements at a time
     // (coalesced), a shuffle scan per 32, warp totals scanned across the block
     constexpr int kWarps = kThreads / 32;
@@ -378,19 +450,17 @@ __global__ void __launch_bounds__(kThreads) scan_down_kernel(const int32_t* __re
             if (lane >= o) x += y;
         }
         const int64_t i = r0 + r * 32 + lane;
-        if (i < n) out[rows > 0 ? (i % rows) * cols + i / rows : i] = (int32_t)(carry + x - v[r]);
+        if (i < n) out[i] = (int32_t)(carry + x - v[r]);
         carry += __shfl_sync(kFull, x, 31);
     }
 }
 
 // Per-domain home counts and starts from the scanned tile offsets; pulse state init.
-// offs[D * dstride] is domain D's first home slot (the scanned start of its
-// first tile).
-__global__ void home_meta_kernel(const int32_t* __restrict__ offs, int64_t dstride, int64_t n,
+__global__ void home_meta_kernel(const int32_t* __restrict__ offs, int64_t ntiles, int64_t n,
                                  int nd, int P, Meta m) {
     for (int D = blockIdx.x * blockDim.x + threadIdx.x; D < nd; D += gridDim.x * blockDim.x) {
-        const int64_t h0 = offs[(int64_t)D * dstride];
-        const int64_t h1 = (D + 1 < nd) ? offs[(int64_t)(D + 1) * dstride] : n;
+        const int64_t h0 = offs[(int64_t)D * ntiles];
+        const int64_t h1 = (D + 1 < nd) ? offs[(int64_t)(D + 1) * ntiles] : n;
         m.hstart[D] = h0;
         m.n_home[D] = h1 - h0;
         m.own_off[(int64_t)D * (P + 1)] = h1 - h0;
@@ -408,9 +478,10 @@ struct PulseArgs {
     int64_t N;
     int64_t cap;    // slots of bxyz
     Meta m;
-    int32_t* cnt;
-    int32_t* cnt_home;
-    int32_t* blk_off;
+    int32_t* cnt;        // per warp unit: sent candidates
+    int32_t* cntb;       // per block: sent candidates
+    int32_t* cntb_home;  // per block: sent home atoms
+    int32_t* blk_off;    // per block: output offset in the pulse's region
     const float* thr;  // thresholds of this pulse, by sender cell along d
     int nd, P, p, d, k, B;
     int nx, ny, nz;
@@ -490,9 +561,77 @@ __device__ __forceinline__ bool pulse_selects(const PulseArgs& a, const int cell
     return corner_within(a, cell, c, (unsigned)__float_as_int(v.w));
 }
 
+// Output offsets of the pulse from the block counts, run by the last count
+// block: blk_off[s*B + b] = the exclusive prefix of the block counts over all
+// senders' blocks (relative to the pulse's region); per sender s its send
+// size, split and output start; the receiver's slice position and local
+// offsets.  Rounds of whole senders, eight block counts per thread; counts
+// are read through L2 (other blocks wrote them in this launch).
+constexpr int kOffsetSenders = 1024;  // senders per round of pulse_offsets
+
+__device__ void pulse_offsets(const PulseArgs& a, int32_t* dsnd, int32_t* dspl) {
+    constexpr int EPT = 8;
+    const int64_t B = a.B;
+    const int64_t dpr = min((int64_t)kOffsetSenders, max((int64_t)1, EPT * kThreads / B));
+    const int64_t R = a.m.region[a.p];
+    int64_t carry = 0;
+    for (int64_t s0 = 0; s0 < a.nd; s0 += dpr) {
+        const int64_t ns = min(dpr, (int64_t)a.nd - s0);
+        const int64_t e0 = s0 * B, e1 = (s0 + ns) * B;  // this round's entries
+        const int64_t i0 = e0 + EPT * threadIdx.x;
+        for (int64_t j = threadIdx.x; j < dpr; j += kThreads) dsnd[j] = dspl[j] = 0;
+        int32_t c[EPT], h[EPT];
+        int64_t cs = 0;
+#pragma unroll
+        for (int k = 0; k < EPT; k++) {
+            const bool in = i0 + k < e1;
+            c[k] = in ? __ldcg(a.cntb + i0 + k) : 0;
+            h[k] = in ? __ldcg(a.cntb_home + i0 + k) : 0;
+            cs += c[k];
+        }
+        __syncthreads();
+        int64_t tot;
+        int64_t run = carry + block_exclusive_scan<kThreads>(cs, &tot);
+#pragma unroll
+        for (int k = 0; k < EPT; k++) {
+            if (i0 + k < e1) {
+                a.blk_off[i0 + k] = (int32_t)run;
+                const int64_t j = (i0 + k) / B - s0;
+                atomicAdd(&dsnd[j], c[k]);
+                atomicAdd(&dspl[j], h[k]);
+            }
+            run += c[k];
+        }
+        __syncthreads();
+        for (int64_t j = threadIdx.x; j < ns; j += kThreads) {
+            const int s = (int)(s0 + j);
+            const int64_t snd = dsnd[j], spl = dspl[j];
+            const int64_t G = a.blk_off[(int64_t)s * B];
+            const int64_t sp = (int64_t)s * a.P + a.p;
+            a.m.send[sp] = snd;
+            a.m.split[sp] = spl;
+            a.m.map_pos[sp] = R + G;
+            int cc[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
+            const int nd_d = a.d == 0 ? a.nx : (a.d == 1 ? a.ny : a.nz);
+            cc[a.d] = (cc[a.d] - 1 + nd_d) % nd_d;
+            const int r = cc[0] + a.nx * (cc[1] + a.ny * cc[2]);
+            a.m.recv_pos[(int64_t)r * a.P + a.p] = R + G;
+            a.m.own_off[(int64_t)r * (a.P + 1) + a.p + 1] =
+                a.m.own_off[(int64_t)r * (a.P + 1) + a.p] + snd;
+        }
+        carry += tot;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        a.m.region[a.p + 1] = R + carry;
+        if (R + carry > a.cap) a.m.flags[0] = 1;
+    }
+}
+
 // Per unit: how many candidates the pulse sends, and how many of them are
 // home atoms (the split).  Each warp counts its unit 32 candidates at a time,
-// U rounds' loads in flight.
+// U rounds' loads in flight.  The last block to finish (an atomic ticket in
+// flags[3], reset for the next pulse) computes the offsets.
 __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
     __shared__ Locator L;
     const int s = blockIdx.y;
@@ -526,50 +665,34 @@ __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
             if (i0 < nh) ch += __popc(bal & (nh - i0 >= 32 ? kFull : ((1u << (nh - i0)) - 1u)));
         }
     }
+    // per warp (its offset within the block, for the write kernel) and per
+    // block (for the offsets)
+    __shared__ int32_t wc[kPulseWarps], wh[kPulseWarps];
+    __shared__ int32_t dsnd[kOffsetSenders], dspl[kOffsetSenders];
+    __shared__ int last;
     if (lane == 0) {
-        const int64_t q = (int64_t)s * a.B * kPulseWarps + u0;
-        a.cnt[q] = c;
-        a.cnt_home[q] = ch;
-    }
-}
-
-__global__ void __launch_bounds__(1024) pulse_scan_kernel(PulseArgs a) {
-    const int64_t per = (int64_t)a.B * kPulseWarps;  // units per sender
-    const int64_t M = (int64_t)a.nd * per;
-    int64_t carry = 0;
-    for (int64_t b0 = 0; b0 < M; b0 += 1024) {
-        const int64_t i = b0 + threadIdx.x;
-        const int64_t v = i < M ? a.cnt[i] : 0;
-        int64_t tot;
-        const int64_t pre = block_exclusive_scan<1024>(v, &tot);
-        if (i < M) a.blk_off[i] = (int32_t)(carry + pre);
-        carry += tot;
+        a.cnt[(int64_t)s * a.B * kPulseWarps + u0] = c;
+        wc[w] = c;
+        wh[w] = ch;
     }
     __syncthreads();
-    const int64_t R = a.m.region[a.p];
-    for (int s = threadIdx.x; s < a.nd; s += blockDim.x) {
-        int64_t snd = 0, spl = 0;
-        for (int64_t u = 0; u < per; u++) {
-            snd += a.cnt[(int64_t)s * per + u];
-            spl += a.cnt_home[(int64_t)s * per + u];
-        }
-        const int64_t G = a.blk_off[(int64_t)s * per];
-        const int64_t sp = (int64_t)s * a.P + a.p;
-        a.m.send[sp] = snd;
-        a.m.split[sp] = spl;
-        a.m.map_pos[sp] = R + G;
-        int c[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
-        const int nd_d = a.d == 0 ? a.nx : (a.d == 1 ? a.ny : a.nz);
-        c[a.d] = (c[a.d] - 1 + nd_d) % nd_d;
-        const int r = c[0] + a.nx * (c[1] + a.ny * c[2]);
-        a.m.recv_pos[(int64_t)r * a.P + a.p] = R + G;
-        a.m.own_off[(int64_t)r * (a.P + 1) + a.p + 1] =
-            a.m.own_off[(int64_t)r * (a.P + 1) + a.p] + snd;
-    }
     if (threadIdx.x == 0) {
-        a.m.region[a.p + 1] = R + carry;
-        if (R + carry > a.cap) a.m.flags[0] = 1;
+        int32_t tc = 0, th = 0;
+        for (int q = 0; q < kPulseWarps; q++) {
+            tc += wc[q];
+            th += wh[q];
+        }
+        a.cntb[(int64_t)s * a.B + blockIdx.x] = tc;
+        a.cntb_home[(int64_t)s * a.B + blockIdx.x] = th;
+        __threadfence();
+        unsigned long long* ticket = reinterpret_cast<unsigned long long*>(a.m.flags + 3);
+        last = atomicAdd(ticket, 1ull) == (unsigned long long)gridDim.x * gridDim.y - 1;
+        if (last) *ticket = 0;
     }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    pulse_offsets(a, dsnd, dspl);
 }
 
 // Each warp writes its unit's sent candidates from the unit's scanned offset
@@ -587,7 +710,12 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
     if (cs == 0) sh[a.d] = a.Ld;
     int64_t lo, hi;
     unit_range(L, a, u0, &lo, &hi);
-    int64_t out = a.m.region[a.p] + a.blk_off[(int64_t)s * a.B * kPulseWarps + u0];
+    int64_t out = a.m.region[a.p] + a.blk_off[(int64_t)s * a.B + blockIdx.x];
+    {
+        const int32_t* wcnt = a.cnt + ((int64_t)s * a.B + blockIdx.x) * kPulseWarps;
+        const int32_t v = lane < w ? wcnt[lane] : 0;
+        out += __reduce_add_sync(kFull, (unsigned)v);
+    }
     const unsigned lt = lanemask_lt();
     const unsigned bit = 1u << a.d;
     constexpr int U = 8;
@@ -620,6 +748,19 @@ __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
 }
 
 // ---- 3. finalize -----------------------------------------------------------------
+// Pulse descriptors on the device, from the metadata: the fields of the
+// host's copy of the plan (map offset, sender base, the halo slice's first
+// dense slot in the receiver, sizes, the shift across the periodic boundary),
+// so the kernels that read them can run before the host has its own copy.
+struct SPArgs {
+    int8_t dim[HALO_MAX_PULSES];
+    float box[3];
+    int nx, ny, nz, nd, P;
+    int64_t n;
+};
+
+// One block: every domain's first dense slot (exclusive scan of the local
+// counts).
 __global__ void __launch_bounds__(1024) finalize_kernel(Meta m, int nd, int P) {
     int64_t carry = 0;
     for (int D0 = 0; D0 < nd; D0 += 1024) {
@@ -632,47 +773,38 @@ __global__ void __launch_bounds__(1024) finalize_kernel(Meta m, int nd, int P) {
     }
 }
 
-// Pulse descriptors on the device, from the metadata: the fields of the
-// host's copy of the plan (map offset, sender base, the halo slice's first
-// dense slot in the receiver, sizes, the shift across the periodic boundary),
-// so the kernels that read them can run before the host has its own copy.
-struct SPArgs {
-    int8_t dim[HALO_MAX_PULSES];
-    float box[3];
-    int nx, ny, nz, nd, P;
-    int64_t n;
-};
-
-__global__ void sp_kernel(Meta m, SPArgs a, SPDesc* __restrict__ out) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)a.nd * a.P) return;
-    const int s = (int)(i / a.P), p = (int)(i % a.P);
-    const int d = a.dim[p];
-    const int g[3] = {a.nx, a.ny, a.nz};
-    int c[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
-    const bool wrap = c[d] == 0;
-    c[d] = (c[d] - 1 + g[d]) % g[d];
-    const int r = c[0] + a.nx * (c[1] + a.ny * c[2]);
-    SPDesc x;
-    x.map_off = m.map_pos[i] - a.n;
-    x.src_base = m.base[s];
-    x.dst = m.base[r] + m.own_off[(int64_t)r * (a.P + 1) + p];
-    x.send = (int32_t)m.send[i];
-    x.split = (int32_t)m.split[i];
-    x.s = s;
-    x.r = r;
-    x.p = p;
-    x.pad = 0;
-    x.shift[0] = x.shift[1] = x.shift[2] = 0.0f;
-    if (wrap) x.shift[d] = a.box[d];
-    x.pad2 = 0.0f;
-    out[i] = x;
-}
-
-__global__ void home_dst_kernel(Meta m, int64_t* __restrict__ home_dst) {
+// Block D: the dense slot of each of D's home-compact slots, and D's pulse
+// descriptors (as sender).
+__global__ void home_dst_kernel(Meta m, int64_t* __restrict__ home_dst, SPArgs a,
+                                SPDesc* __restrict__ out) {
     const int D = blockIdx.x;
     const int64_t h0 = m.hstart[D], nh = m.n_home[D], b = m.base[D];
     for (int64_t j = threadIdx.x; j < nh; j += blockDim.x) home_dst[h0 + j] = b + j;
+    const int P = a.P;
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int s = D;
+        const int64_t i = (int64_t)s * P + p;
+        const int d = a.dim[p];
+        const int g[3] = {a.nx, a.ny, a.nz};
+        int c[3] = {s % a.nx, (s / a.nx) % a.ny, s / (a.nx * a.ny)};
+        const bool wrap = c[d] == 0;
+        c[d] = (c[d] - 1 + g[d]) % g[d];
+        const int r = c[0] + a.nx * (c[1] + a.ny * c[2]);
+        SPDesc x;
+        x.map_off = m.map_pos[i] - a.n;
+        x.src_base = b;
+        x.dst = m.base[r] + m.own_off[(int64_t)r * (P + 1) + p];
+        x.send = (int32_t)m.send[i];
+        x.split = (int32_t)m.split[i];
+        x.s = s;
+        x.r = r;
+        x.p = p;
+        x.pad = 0;
+        x.shift[0] = x.shift[1] = x.shift[2] = 0.0f;
+        if (wrap) x.shift[d] = a.box[d];
+        x.pad2 = 0.0f;
+        out[i] = x;
+    }
 }
 
 int grow(float** p, int64_t* cap_have, int64_t need_slots) {
@@ -687,12 +819,12 @@ int grow(float** p, int64_t* cap_have, int64_t need_slots) {
 }  // namespace
 
 int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
-                          cudaStream_t st, int64_t rows, int64_t cols) {
+                          cudaStream_t st) {
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
     if (nb == 0) return HALO_OK;
     scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, n, tmp);
     scan_top_kernel<<<1, 1024, 0, st>>>(tmp, nb);
-    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp, rows, cols);
+    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp);
     return cuda_code(cudaGetLastError());
 }
 
@@ -714,25 +846,31 @@ void free_build(halo_plan* pl) {
     pl->meta_bytes = 0;
 }
 
+DomainTables domain_tables(const halo_plan* pl) {
+    const Meta m = meta_ptrs(pl->d_meta, pl->n_dom, pl->P);
+    return DomainTables{m.n_home, m.base, m.own_off};
+}
+
 int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n,
                cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
-    // home partition.  Tiled: blocks of kThreads / 32 warps over tiles of T
-    // atoms, each tile ranked in shared memory by the scatter; T is the
+    // home partition.  Tiled: tiles of T atoms, each ranked in shared memory
+    // by a scatter block of kScatterThreads / 32 warp sub-tiles; T is the
     // largest of 8192 .. 1024 with two scatter blocks per SM (the per-warp
-    // histograms of 8 warps must fit 48 KB).  Measured on the 3M-atom
-    // system (T = 4096): rebuild 0.59 ms against 0.60 at T = 2048 (three
-    // blocks per SM) and 0.60 at T = 8192 (one).  Otherwise the direct
+    // histograms must fit 48 KB).  Measured on the 3M-atom system (T = 4096,
+    // 256 threads): rebuild 0.59 ms against 0.60 at T = 2048 (three blocks
+    // per SM) and 0.60 at T = 8192 (one); 512 threads, 5 us less.  Otherwise
+    // the direct
     // scatter: W warps per block (their histograms share 48 KB of shared
     // memory), one block tile of W * kHistTile atoms per block.
     int tileT = 0;
     size_t tile_smem = 0;
-    if ((size_t)(kThreads / 32) * nd * sizeof(int32_t) <= 48 * 1024 && nd < 32768) {
+    if ((size_t)(kScatterThreads / 32) * nd * sizeof(int32_t) <= 48 * 1024 && nd < 32768) {
         int optin = 0, per_sm = 0;
         HALO_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->dev));
         HALO_CUDA(cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, pl->dev));
         for (int T : {8192, 4096, 2048, 1024}) {
-            const size_t need = tile_scatter_smem(kThreads / 32, nd, T);
+            const size_t need = tile_scatter_smem(kScatterThreads / 32, nd, T);
             if (need <= (size_t)optin && 2 * (need + 1024) <= (size_t)per_sm) {
                 tileT = T;
                 tile_smem = need;
@@ -792,7 +930,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         B = std::min<int64_t>(B, 64);
         if (B != pl->build_blocks_per_domain || !pl->d_pulse_scratch) {
             dev_free(pl->d_pulse_scratch);
-            HALO_TRY(dev_alloc(&pl->d_pulse_scratch, (size_t)3 * nd * B * kPulseWarps));
+            HALO_TRY(dev_alloc(&pl->d_pulse_scratch, (size_t)nd * B * (kPulseWarps + 3)));
             pl->build_blocks_per_domain = (int)B;
         }
     }
@@ -876,24 +1014,25 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         HALO_CUDA(cudaMemsetAsync(pl->d_meta, 0, mbytes, st));
         // 1. home partition
         int32_t* wcounts = tileT > 0 ? nullptr : pl->d_counts + 2 * ncount;
-        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(dom, n, nd, nbt, wtile,
-                                                                  pl->d_counts, wcounts, m.flags);
+        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
+            dom, n, nd, nbt, wtile, tileT > 0 ? 1 : 0, pl->d_counts, wcounts, m.flags);
         int32_t* offs = pl->d_counts + ncount;
         if (tileT > 0) {
-            // tile starts stored tile-major, so each scatter block reads its
-            // domains' starts contiguously
-            HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st, nbt, nd));
+            // column prefixes (tile-major, so each scatter block reads its
+            // domains' starts contiguously) and the per-domain home metadata
+            home_colscan_kernel<<<(unsigned)((nd + 31) / 32), 1024, 0, st>>>(pl->d_counts, nbt, nd, P, n,
+                                                                            offs, m);
             const int vec = ((uintptr_t)coords % 16 == 0 && (uintptr_t)dom % 16 == 0) ? 1 : 0;
-            home_scatter_tile_kernel<<<hist_blocks, kThreads, tile_smem, st>>>(
-                coords, dom, n, nd, tileT, vec, offs, pl->d_home_gid,
+            home_scatter_tile_kernel<<<hist_blocks, kScatterThreads, tile_smem, st>>>(
+                coords, dom, n, nd, tileT, vec, offs, m.hstart, pl->d_home_gid,
                 reinterpret_cast<float4*>(pl->d_bxyz));
         } else {
             HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
             home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
                 coords, dom, n, nd, nbt, offs, wcounts, pl->d_home_gid,
                 reinterpret_cast<float4*>(pl->d_bxyz));
+            home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, nbt, n, nd, P, m);
         }
-        home_meta_kernel<<<(nd + 255) / 256, 256, 0, st>>>(offs, tileT > 0 ? 1 : nbt, n, nd, P, m);
         HALO_CUDA(cudaGetLastError());
         // 2. pulses in global order
         for (int p = 0; p < P; p++) {
@@ -904,8 +1043,9 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
             a.cap = pl->cap_slots;
             a.m = m;
             a.cnt = pl->d_pulse_scratch;
-            a.cnt_home = pl->d_pulse_scratch + (size_t)nd * B * kPulseWarps;
-            a.blk_off = pl->d_pulse_scratch + (size_t)2 * nd * B * kPulseWarps;
+            a.cntb = a.cnt + (size_t)nd * B * kPulseWarps;
+            a.cntb_home = a.cntb + (size_t)nd * B;
+            a.blk_off = a.cntb_home + (size_t)nd * B;
             a.thr = pl->d_thr + (size_t)p * nmax;
             a.nd = nd;
             a.P = P;
@@ -923,13 +1063,11 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
             a.faces = pl->d_faces;
             dim3 g((unsigned)B, (unsigned)nd);
             pulse_count_kernel<<<g, kThreads, 0, st>>>(a);
-            pulse_scan_kernel<<<1, 1024, 0, st>>>(a);
             pulse_write_kernel<<<g, kThreads, 0, st>>>(a);
         }
         // 3. dense layout
         finalize_kernel<<<1, 1024, 0, st>>>(m, nd, P);
-        home_dst_kernel<<<nd, 256, 0, st>>>(m, pl->d_home_dst);
-        if (nd * P > 0) sp_kernel<<<(unsigned)((nd * P + 255) / 256), 256, 0, st>>>(m, spa, pl->d_sp);
+        home_dst_kernel<<<nd, 256, 0, st>>>(m, pl->d_home_dst, spa, pl->d_sp);
         HALO_CUDA(cudaGetLastError());
         HALO_CUDA(cudaMemcpyAsync(hm, pl->d_meta, mbytes, cudaMemcpyDeviceToHost, st));
         HALO_CUDA(cudaStreamSynchronize(st));

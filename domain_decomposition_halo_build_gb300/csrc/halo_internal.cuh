@@ -185,14 +185,20 @@ struct halo_plan {
 namespace halo {
 
 // halo_build.cu
+// The plan's per-domain tables on the device (valid while the plan is):
+// n_home[D], base[D] (first dense slot), own_off[D * (P + 1) + q] (first
+// local index of each received slice; q = P: the domain's local count).
+struct DomainTables {
+    const int64_t* n_home;
+    const int64_t* base;
+    const int64_t* own_off;
+};
+DomainTables domain_tables(const halo_plan* pl);
 int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n_atoms,
                cudaStream_t st);
 
-// scratch tmp: ceil(n / kScanTile) ints.  rows > 0: the input is n / rows
-// groups of rows entries (i = c * rows + r) and out is stored transposed,
-// out[r * cols + c].
 int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp,
-                          cudaStream_t st, int64_t rows = 0, int64_t cols = 0);
+                          cudaStream_t st);  // scratch tmp: ceil(n / kScanTile) ints
 
 // halo_modes.cu: one launch per pulse, and the flattened exchange
 int prepare_flat(halo_plan* pl, cudaStream_t st);

@@ -188,16 +188,53 @@ __global__ void chain_pulse_kernel(const SPDesc* __restrict__ sp, const int32_t*
     }
 }
 
-// Coordinate table over halo slots; also counts the copies of every owner.
+// The coordinate kernel's work items: domain D's halo range in chunks of
+// `chunk` slots, numbered in domain order; item b = {b * chunk (its table
+// offset), first halo slot, count}.  One block: 1024 domains per round, their
+// first items from a block scan, then a warp per domain writes its items.
+__global__ void __launch_bounds__(1024) xflat_items_kernel(DomainTables t, int nd, int P, int chunk,
+                                                           int4* __restrict__ items) {
+    __shared__ int64_t sfirst[1024], snh[1024], sd0[1024];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t carry = 0;
+    for (int D0 = 0; D0 < nd; D0 += 1024) {
+        const int D = D0 + threadIdx.x;
+        int64_t nh = 0, d0 = 0;
+        if (D < nd) {
+            nh = t.own_off[(int64_t)D * (P + 1) + P] - t.n_home[D];
+            d0 = t.base[D] + t.n_home[D];
+        }
+        int64_t tot;
+        const int64_t pre = block_exclusive_scan<1024>((nh + chunk - 1) / chunk, &tot);
+        sfirst[threadIdx.x] = carry + pre;
+        snh[threadIdx.x] = nh;
+        sd0[threadIdx.x] = d0;
+        __syncthreads();
+        for (int j = warp; j < 1024 && D0 + j < nd; j += 32) {
+            const int64_t nhj = snh[j], f = sfirst[j], dj = sd0[j];
+            for (int64_t k = lane; k * chunk < nhj; k += 32) {
+                const int64_t b = f + k;
+                items[b] = make_int4((int)(b * chunk), (int)(dj + k * chunk),
+                                     (int)min((int64_t)chunk, nhj - k * chunk), 0);
+            }
+        }
+        carry += tot;
+        __syncthreads();
+    }
+}
+
+// Coordinate table over halo slots; also counts the copies of every owner,
+// and keeps each halo slot's rank among its owner's copies (the counter's
+// value before its increment) for owner_fill_kernel.
 __global__ void xflat_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
                              const int8_t* __restrict__ code, int32_t* __restrict__ xflat,
-                             int32_t* __restrict__ ncopies) {
+                             int32_t* __restrict__ ncopies, int32_t* __restrict__ rank) {
     const int4 it = items[blockIdx.x];
     for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
         const int64_t j = (int64_t)it.y + i;
         const int32_t o = owner[j];
         xflat[(int64_t)it.x + i] = o | ((int32_t)code[j] << 29);
-        atomicAdd(ncopies + o, 1);
+        rank[j] = atomicAdd(ncopies + o, 1);
     }
 }
 
@@ -224,19 +261,55 @@ __device__ __forceinline__ int64_t scan_count(int64_t n, const int64_t* n_dev) {
     return n_dev ? (*n_dev >> 32) : n;
 }
 
+// Elements i .. i + 7 of a pair scan (pair_value), 0 past n; i is a multiple
+// of 8 and `in` 16-byte aligned, so a whole group is two 16-byte loads (SRC 1
+// also reads in[i + 8]).
+template <int SRC>
+__device__ __forceinline__ void pair_load8(const int32_t* __restrict__ in, int64_t i, int64_t n,
+                                           int64_t v[8]) {
+    if (i + 8 <= n) {
+        const int4 x0 = *reinterpret_cast<const int4*>(in + i);
+        const int4 x1 = *reinterpret_cast<const int4*>(in + i + 4);
+        const int32_t e[9] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, SRC == 1 ? in[i + 8] : 0};
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            if (SRC == 0) {
+                v[k] = (int64_t)e[k] | ((int64_t)(e[k] > 0 ? 1 : 0) << 32);
+            } else {
+                const int32_t c = e[k + 1] - e[k];
+                v[k] = (int64_t)(c <= 3 ? 1 : 0) | ((int64_t)(c > 3 && c <= 11 ? 1 : 0) << 32);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; k++) v[k] = i + k < n ? pair_value<SRC>(in, i + k) : 0;
+    }
+}
+
+// Tile sums: thread t of block b sums elements b * kScanTile + 8t .. + 7.
 template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_reduce_kernel(const int32_t* __restrict__ in,
                                                                int64_t n, const int64_t* n_dev,
                                                                int64_t* __restrict__ sums) {
+    static_assert(kScanTile == 8 * kThreads, "eight elements per thread");
+    __shared__ int64_t ws[kThreads / 32];
     n = scan_count(n, n_dev);
     const int64_t b0 = (int64_t)blockIdx.x * kScanTile;
     if (b0 >= n) return;
+    int64_t v[8];
+    pair_load8<SRC>(in, b0 + 8 * threadIdx.x, n, v);
     int64_t s = 0;
-    for (int j = threadIdx.x; j < kScanTile; j += kThreads)
-        if (b0 + j < n) s += pair_value<SRC>(in, b0 + j);
-    int64_t tot;
-    block_exclusive_scan<kThreads>(s, &tot);
-    if (threadIdx.x == 0) sums[blockIdx.x] = tot;
+#pragma unroll
+    for (int k = 0; k < 8; k++) s += v[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t t = 0;
+        for (int w = 0; w < kThreads / 32; w++) t += ws[w];
+        sums[blockIdx.x] = t;
+    }
 }
 
 // Scans the nb tile sums in place and stores the grand total in sums[nb]
@@ -263,13 +336,12 @@ __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ su
     }
 }
 
-// Down pass: each warp takes a contiguous run of kScanTile / warps elements
-// and walks it 32 at a time (coalesced loads and stores): a first walk sums
-// the run, the warp totals are scanned across the block, a second walk writes
-// the exclusive prefixes with a shuffle scan per 32 elements.  SRC 0 also
-// writes the owner list: for a slot with copies, fown[its owner index] = the
-// slot and fstart[...] = its first entry (out_b, the owner indices, is then
-// not stored).
+// Down pass: thread t of block b takes elements b * kScanTile + 8t .. + 7
+// (two 16-byte loads), one block scan of the thread sums gives its first
+// prefix, and it writes its eight exclusive prefixes.  SRC 0 also writes the
+// owner list: for a slot with copies, fown[its owner index] = the slot and
+// fstart[...] = its first entry (out_b, the owner indices, is then not
+// stored).
 template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __restrict__ in, int64_t n,
                                                              const int64_t* n_dev,
@@ -278,49 +350,44 @@ __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __re
                                                              int32_t* __restrict__ out_b,
                                                              int32_t* __restrict__ fown,
                                                              int32_t* __restrict__ fstart) {
-    constexpr int kWarps = kThreads / 32;
-    constexpr int R = kScanTile / kThreads;  // rounds of 32 per warp
-    __shared__ int64_t wsum[kWarps];
     n = scan_count(n, n_dev);
-    if ((int64_t)blockIdx.x * kScanTile >= n) return;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t r0 = (int64_t)blockIdx.x * kScanTile + (int64_t)w * 32 * R;
-    int64_t v[R];
-    int64_t s = 0;
+    const int64_t b0 = (int64_t)blockIdx.x * kScanTile;
+    if (b0 >= n) return;
+    const int64_t i0 = b0 + 8 * threadIdx.x;
+    int64_t v[8];
+    pair_load8<SRC>(in, i0, n, v);
+    int64_t t = 0;
 #pragma unroll
-    for (int r = 0; r < R; r++) {
-        const int64_t i = r0 + r * 32 + lane;
-        v[r] = i < n ? pair_value<SRC>(in, i) : 0;
-        s += v[r];
-    }
+    for (int k = 0; k < 8; k++) t += v[k];
+    int64_t tot;
+    int64_t run = sums[blockIdx.x] + block_exclusive_scan<kThreads>(t, &tot);
+    int32_t a[8], bb[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-    if (lane == 0) wsum[w] = s;
-    __syncthreads();
-    int64_t carry = sums[blockIdx.x];
-    for (int q = 0; q < w; q++) carry += wsum[q];
-#pragma unroll
-    for (int r = 0; r < R; r++) {
-        int64_t x = v[r];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t y = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += y;
+    for (int k = 0; k < 8; k++) {
+        a[k] = (int32_t)(run & 0xffffffffll);
+        bb[k] = (int32_t)(run >> 32);
+        if (SRC == 0 && fown && (v[k] & 0xffffffffll) > 0 && i0 + k < n) {
+            fown[bb[k]] = (int32_t)(i0 + k);
+            fstart[bb[k]] = a[k];
         }
-        const int64_t i = r0 + r * 32 + lane;
-        const int64_t pre = carry + x - v[r];
-        if (i < n) {
-            out_a[i] = (int32_t)(pre & 0xffffffffll);
-            if (SRC == 0 && fown) {
-                if ((v[r] & 0xffffffffll) > 0) {
-                    fown[pre >> 32] = (int32_t)i;
-                    fstart[pre >> 32] = (int32_t)(pre & 0xffffffffll);
-                }
-            } else {
-                out_b[i] = (int32_t)(pre >> 32);
+        run += v[k];
+    }
+    const bool write_b = !(SRC == 0 && fown);
+    if (i0 + 8 <= n) {
+        *reinterpret_cast<int4*>(out_a + i0) = make_int4(a[0], a[1], a[2], a[3]);
+        *reinterpret_cast<int4*>(out_a + i0 + 4) = make_int4(a[4], a[5], a[6], a[7]);
+        if (write_b) {
+            *reinterpret_cast<int4*>(out_b + i0) = make_int4(bb[0], bb[1], bb[2], bb[3]);
+            *reinterpret_cast<int4*>(out_b + i0 + 4) = make_int4(bb[4], bb[5], bb[6], bb[7]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            if (i0 + k < n) {
+                out_a[i0 + k] = a[k];
+                if (write_b) out_b[i0 + k] = bb[k];
             }
         }
-        carry += __shfl_sync(kFull, x, 31);
     }
 }
 
@@ -340,14 +407,14 @@ int pair_scan(const int32_t* in, int64_t n, const int64_t* n_dev, int64_t* sums,
     return cuda_code(cudaGetLastError());
 }
 
+// Every halo slot into its owner's copy list, at the rank xflat_kernel took.
 __global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
-                                  const int32_t* __restrict__ entry_pos, int32_t* fillc,
-                                  int32_t* __restrict__ tmp) {
+                                  const int32_t* __restrict__ entry_pos,
+                                  const int32_t* __restrict__ rank, int32_t* __restrict__ tmp) {
     const int4 it = items[blockIdx.x];
     for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
         const int64_t j = (int64_t)it.y + i;
-        const int32_t o = owner[j];
-        tmp[entry_pos[o] + atomicAdd(fillc + o, 1)] = (int32_t)j;
+        tmp[entry_pos[owner[j]] + rank[j]] = (int32_t)j;
     }
 }
 
@@ -373,13 +440,15 @@ __device__ __forceinline__ void write_rec_b(int4* recB, int32_t hdr, const int32
 // replace each copy's parent slot by the parent's position (0 = the owner),
 // and write the owner's record at its class position (posA / posB from the
 // class scan; class C after them, with its entries in the entry list).
+// Owners of up to three copies (class A, nearly all) are done here; the
+// others are listed (listB[posB[m]], listC[class-C rank]) for
+// owner_sort_bc_kernel, so that no warp here runs the longer sorts.
 __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
                                   const int32_t* __restrict__ tmp, const int32_t* __restrict__ parent,
                                   const int8_t* __restrict__ hop, const int64_t* __restrict__ total,
                                   const int32_t* __restrict__ posA, const int32_t* __restrict__ posB,
-                                  int4* __restrict__ recA, int4* __restrict__ recB,
-                                  int4* __restrict__ recC, int32_t* __restrict__ fent,
-                                  int* max_copies, int* err) {
+                                  int4* __restrict__ recA, int32_t* __restrict__ listB,
+                                  int32_t* __restrict__ listC, int* max_copies, int* err) {
     const int64_t n_owners = *total >> 32;
     __shared__ int block_max;
     if (threadIdx.x == 0) block_max = 0;
@@ -389,10 +458,7 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
          m += (int64_t)gridDim.x * blockDim.x) {
         const int s0 = fstart[m], k = fstart[m + 1] - s0;
         my_max = max(my_max, k);
-        if (k > kMaxCopies) {
-            atomicCAS(err, 0, HALO_ECAPACITY);
-            continue;
-        }
+        if (k > kMaxCopies) atomicCAS(err, 0, HALO_ECAPACITY);  // listed below, skipped there
         const int32_t hdr = fown[m] | (k << kNodeBits);
         if (k == 1) {  // most owners: a single copy, received from the owner itself
             const int32_t v = tmp[s0];
@@ -443,6 +509,35 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
             write_rec_a(recA + posA[m], hdr, e3, k);
             continue;
         }
+        if (k <= 11)
+            listB[posB[m]] = (int32_t)m;
+        else
+            listC[m - posA[m] - posB[m]] = (int32_t)m;  // class-C owners before m
+    }
+    atomicMax(&block_max, my_max);
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(max_copies, block_max);
+}
+
+// The owners of four or more copies (classes B and C), from the lists
+// owner_sort_kernel wrote: counts[0] = copies | owners << 32, counts[1] =
+// class A | class B << 32.
+__global__ void owner_sort_bc_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
+                                     const int32_t* __restrict__ tmp, const int32_t* __restrict__ parent,
+                                     const int8_t* __restrict__ hop, const int64_t* __restrict__ counts,
+                                     const int32_t* __restrict__ posA, const int32_t* __restrict__ posB,
+                                     const int32_t* __restrict__ listB, const int32_t* __restrict__ listC,
+                                     int4* __restrict__ recB, int4* __restrict__ recC,
+                                     int32_t* __restrict__ fent, int* err) {
+    const int64_t n_owners = counts[0] >> 32;
+    const int64_t n_a = counts[1] & 0xffffffffll, n_b = counts[1] >> 32;
+    const int64_t n_bc = n_owners - n_a;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n_bc;
+         q += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = q < n_b ? listB[q] : listC[q - n_b];
+        const int s0 = fstart[m], k = fstart[m + 1] - s0;
+        if (k > kMaxCopies) continue;  // reported by owner_sort_kernel
+        const int32_t hdr = fown[m] | (k << kNodeBits);
         if (k <= kSortRegs) {
             // the same order in registers: a fully unrolled exchange sort on
             // (pulse descending, slot ascending); unused places sort last
@@ -524,9 +619,6 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
             recC[m - posA[m] - posB[m]] = make_int4(hdr, s0, 0, 0);  // class-C owners before m
         }
     }
-    atomicMax(&block_max, my_max);
-    __syncthreads();
-    if (threadIdx.x == 0) atomicMax(max_copies, block_max);
 }
 
 // ---- flat: the exchanges ------------------------------------------------------------
@@ -911,7 +1003,7 @@ void free_flat(halo_plan* pl) {
 namespace {
 // Scratch of the FLAT table build, carved from two pools kept in the plan.
 struct FlatScratch {
-    int32_t *owner, *parent, *ncopies, *entry_pos, *flag, *tmp;
+    int32_t *owner, *parent, *ncopies, *entry_pos, *rank, *tmp;
     int64_t* sums;    // int64 tile sums + grand total
     int32_t* misc;    // [0] largest copy list, [1] error
     int64_t* misc64;  // [0] copies | owners << 32, [1] class-A | class-B records << 32
@@ -920,16 +1012,19 @@ struct FlatScratch {
 
 int flat_scratch(halo_plan* pl, FlatScratch* f) {
     const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
+    // int32 arrays start on 16-byte boundaries (the scans load and store them
+    // 16 bytes at a time)
+    const int64_t nl4 = (nl + 3) & ~(int64_t)3;
     const int64_t nsums = nl / kScanTile + 2;
-    const int64_t off_sums = (5 * nl + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
+    const int64_t off_sums = (5 * nl4 + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
     HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 16));
     HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
     f->owner = pl->d_flat_pool32;
-    f->parent = f->owner + nl;
-    f->ncopies = f->parent + nl;
-    f->entry_pos = f->ncopies + nl;
-    f->flag = f->entry_pos + nl;
-    f->tmp = f->flag + nl;
+    f->parent = f->owner + nl4;
+    f->ncopies = f->parent + nl4;
+    f->entry_pos = f->ncopies + nl4;
+    f->rank = f->entry_pos + nl4;
+    f->tmp = f->rank + nl4;
     f->sums = reinterpret_cast<int64_t*>(pl->d_flat_pool32 + off_sums);
     f->misc = pl->d_flat_pool32 + off_sums + 2 * nsums;
     f->misc64 = reinterpret_cast<int64_t*>(f->misc + 8);
@@ -974,7 +1069,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     const int kFlatChunk = kXT * E;
     // item b = {table offset b * kFlatChunk, first halo slot, count}: the
     // table is padded to whole chunks so a block can address its entries
-    // from its index alone
+    // from its index alone (the items are written on the device below)
     int64_t n_items = 0;
     for (int D = 0; D < nd; D++)
         n_items += ((int64_t)pl->n_local[D] - pl->n_home[D] + kFlatChunk - 1) / kFlatChunk;
@@ -997,7 +1092,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int32_t* parent = f.parent;
     int32_t* ncopies = f.ncopies;
     int32_t* entry_pos = f.entry_pos;
-    int32_t* flag = f.flag;
+    int32_t* rank = f.rank;
     int32_t* tmp = f.tmp;
     int64_t* sums = f.sums;
     int32_t* misc = f.misc;
@@ -1007,45 +1102,28 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
 
     // the forwarding chains need only the pulse descriptors: a rebuild
     // launches them as soon as the sizes are known (before the host's own
-    // copy of the plan is built), else they are launched here, and run while
-    // the host writes the item list below
+    // copy of the plan is built), else they are launched here
     if (!pl->flat_chains_ready) HALO_TRY(launch_flat_chains(pl, st));
     pl->flat_chains_ready = false;
 
-    // pinned staging: the item list, then words read back at the end (a
-    // staging that must grow waits for the stream first)
-    const size_t need = (size_t)n_items * sizeof(int4) + 256;
-    if (pl->h_stage_cap < need) HALO_CUDA(cudaStreamSynchronize(st));
-    char* stage = nullptr;
+    if (n_items > 0)
+        xflat_items_kernel<<<1, 1024, 0, st>>>(domain_tables(pl), nd, pl->P, kFlatChunk,
+                                               pl->d_xflat_items);
+    // pinned staging: words read back at the end
+    int64_t* hw = nullptr;
     {
         void* hs = nullptr;
-        HALO_TRY(host_stage(pl, need, &hs));
-        stage = static_cast<char*>(hs);
+        HALO_TRY(host_stage(pl, 256, &hs));
+        hw = static_cast<int64_t*>(hs);  // 8 words
     }
-    int4* hitems = reinterpret_cast<int4*>(stage);
-    {
-        int64_t b = 0;
-        for (int D = 0; D < nd; D++) {
-            const int64_t d0 = pl->base[D] + pl->n_home[D];
-            const int64_t nh = (int64_t)pl->n_local[D] - pl->n_home[D];
-            for (int64_t i = 0; i < nh; i += kFlatChunk, b++)
-                hitems[b] = make_int4((int)(b * kFlatChunk), (int)(d0 + i),
-                                      (int)std::min<int64_t>(kFlatChunk, nh - i), 0);
-        }
-    }
-    int64_t* hw = reinterpret_cast<int64_t*>(stage + (size_t)n_items * sizeof(int4));  // 8 words
-    if (n_items > 0)
-        HALO_CUDA(cudaMemcpyAsync(pl->d_xflat_items, hitems, (size_t)n_items * sizeof(int4),
-                                  cudaMemcpyHostToDevice, st));
     int rc = HALO_OK;
     do {
         const int gh = blocks_for(std::max<int64_t>(H, 1), pl->num_sms);
         if ((rc = cuda_code(cudaMemsetAsync(ncopies, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
-        if ((rc = cuda_code(cudaMemsetAsync(flag, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
         if ((rc = cuda_code(cudaMemsetAsync(misc, 0, sizeof(int32_t) * 16, st))) != HALO_OK) break;
         if (n_items > 0)
             xflat_kernel<<<(unsigned)n_items, kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
-                                                                       pl->d_xflat, ncopies);
+                                                                       pl->d_xflat, ncopies, rank);
         // entry offsets of every slot's copy list and, from the same scan,
         // the owner list (fown, fstart); the grand total (copies, owners)
         // stays on the device
@@ -1054,7 +1132,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
             break;
         if (n_items > 0)
             owner_fill_kernel<<<(unsigned)n_items, kThreads, 0, st>>>(pl->d_xflat_items, owner,
-                                                                            entry_pos, flag, tmp);
+                                                                            entry_pos, rank, tmp);
         // record classes (A: <= 3 copies, B: 4..11, C: more): positions in
         // each class from one paired scan of the owners' copy counts, then the
         // sort writes every owner's record there
@@ -1063,9 +1141,16 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         if ((rc = pair_scan<1>(pl->d_fstart, std::max<int64_t>(H, 1), misc64, sums, posA, posB,
                                misc64 + 1, st)) != HALO_OK)
             break;
+        // class A here; classes B and C (listed in the ranks' place: owner_fill
+        // has read them) in a second pass
+        int32_t* listB = rank;
+        int32_t* listC = rank + (H / 4 + 1);
         owner_sort_kernel<<<gh, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, tmp, parent, hop, misc64,
-                                                   posA, posB, pl->d_frec[0], pl->d_frec[1],
-                                                   pl->d_frec[2], pl->d_fent, misc, misc + 1);
+                                                   posA, posB, pl->d_frec[0], listB, listC, misc,
+                                                   misc + 1);
+        owner_sort_bc_kernel<<<blocks_for(H / 4 + 1, pl->num_sms), kThreads, 0, st>>>(
+            pl->d_fown, pl->d_fstart, tmp, parent, hop, misc64, posA, posB, listB, listC,
+            pl->d_frec[1], pl->d_frec[2], pl->d_fent, misc + 1);
         // the one synchronisation: counts, largest list, error
         if ((rc = cuda_code(cudaMemcpyAsync(hw, misc, 8 * sizeof(int32_t) + 2 * sizeof(int64_t),
                                             cudaMemcpyDeviceToHost, st))) != HALO_OK)
