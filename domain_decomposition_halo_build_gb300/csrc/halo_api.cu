@@ -84,6 +84,7 @@ void destroy_plan(halo_plan* pl) {
         halo::free_build(pl);
         if (pl->h_stage) cudaFreeHost(pl->h_stage);
         pl->h_stage = nullptr;
+        pl->h_stage_dev = nullptr;
     }
     delete pl;
 }

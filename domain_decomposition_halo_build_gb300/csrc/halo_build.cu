@@ -96,6 +96,8 @@ __device__ __forceinline__ int cell_of(int D, int d, int nx, int ny) {
 __global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int nd, int64_t nbt,
                                  int wtile, int tile_major, int32_t* __restrict__ counts,
                                  int32_t* __restrict__ wcounts, int64_t* __restrict__ flags) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     extern __shared__ int32_t sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int W = blockDim.x >> 5;
@@ -222,6 +224,8 @@ __host__ __device__ inline size_t tile_scatter_smem(int W, int nd, int T) {
 __global__ void __launch_bounds__(1024) home_colscan_kernel(const int32_t* __restrict__ counts,
                                                             int64_t nbt, int nd, int P, int64_t n,
                                                             int32_t* __restrict__ pre, Meta m) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     __shared__ int32_t part[32][33];
     __shared__ int last;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -295,6 +299,8 @@ __global__ void __launch_bounds__(kScatterThreads) home_scatter_tile_kernel(
     const float* __restrict__ xyz, const int32_t* __restrict__ dom, int64_t n, int nd, int T,
     int vec, const int32_t* __restrict__ pre, const int64_t* __restrict__ hstart,
     int32_t* __restrict__ home_gid, float4* __restrict__ bxyz) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int W = kScatterThreads / 32;
@@ -633,6 +639,8 @@ __device__ void pulse_offsets(const PulseArgs& a, int32_t* dsnd, int32_t* dspl) 
 // U rounds' loads in flight.  The last block to finish (an atomic ticket in
 // flags[3], reset for the next pulse) computes the offsets.
 __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     __shared__ Locator L;
     const int s = blockIdx.y;
     load_locator(L, a, s);
@@ -698,6 +706,8 @@ __global__ void __launch_bounds__(kThreads) pulse_count_kernel(PulseArgs a) {
 // Each warp writes its unit's sent candidates from the unit's scanned offset
 // on, in candidate order (ranks from the round's ballot): no block barrier.
 __global__ void __launch_bounds__(kThreads) pulse_write_kernel(PulseArgs a) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     __shared__ Locator L;
     const int s = blockIdx.y;
     load_locator(L, a, s);
@@ -762,6 +772,8 @@ struct SPArgs {
 // One block: every domain's first dense slot (exclusive scan of the local
 // counts).
 __global__ void __launch_bounds__(1024) finalize_kernel(Meta m, int nd, int P) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     int64_t carry = 0;
     for (int D0 = 0; D0 < nd; D0 += 1024) {
         const int D = D0 + threadIdx.x;
@@ -773,11 +785,19 @@ __global__ void __launch_bounds__(1024) finalize_kernel(Meta m, int nd, int P) {
     }
 }
 
-// Block D: the dense slot of each of D's home-compact slots, and D's pulse
-// descriptors (as sender).
+// Block D: the dense slot of each of D's home-compact slots, D's pulse
+// descriptors (as sender) and, if host_meta is given (the host's mapped
+// staging), its share of the metadata words for the host.
 __global__ void home_dst_kernel(Meta m, int64_t* __restrict__ home_dst, SPArgs a,
-                                SPDesc* __restrict__ out) {
+                                SPDesc* __restrict__ out, const int64_t* __restrict__ meta,
+                                int64_t meta_words, int64_t* __restrict__ host_meta) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const int D = blockIdx.x;
+    if (host_meta) {
+        const int64_t w0 = meta_words * D / gridDim.x, w1 = meta_words * (D + 1) / gridDim.x;
+        for (int64_t q = w0 + threadIdx.x; q < w1; q += blockDim.x) host_meta[q] = meta[q];
+    }
     const int64_t h0 = m.hstart[D], nh = m.n_home[D], b = m.base[D];
     for (int64_t j = threadIdx.x; j < nh; j += blockDim.x) home_dst[h0 + j] = b + j;
     const int P = a.P;
@@ -1014,18 +1034,20 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         HALO_CUDA(cudaMemsetAsync(pl->d_meta, 0, mbytes, st));
         // 1. home partition
         int32_t* wcounts = tileT > 0 ? nullptr : pl->d_counts + 2 * ncount;
-        home_hist_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
-            dom, n, nd, nbt, wtile, tileT > 0 ? 1 : 0, pl->d_counts, wcounts, m.flags);
+        HALO_CUDA(launch_dependent_shm(home_hist_kernel, dim3(hist_blocks), dim3(wpb * 32), hist_smem, st,
+                                       dom, n, nd, nbt, wtile, tileT > 0 ? 1 : 0, pl->d_counts, wcounts,
+                                       m.flags));
         int32_t* offs = pl->d_counts + ncount;
         if (tileT > 0) {
             // column prefixes (tile-major, so each scatter block reads its
             // domains' starts contiguously) and the per-domain home metadata
-            home_colscan_kernel<<<(unsigned)((nd + 31) / 32), 1024, 0, st>>>(pl->d_counts, nbt, nd, P, n,
-                                                                            offs, m);
+            HALO_CUDA(launch_dependent_shm(home_colscan_kernel, dim3((unsigned)((nd + 31) / 32)), dim3(1024),
+                                           0, st, (const int32_t*)pl->d_counts, nbt, nd, P, n, offs, m));
             const int vec = ((uintptr_t)coords % 16 == 0 && (uintptr_t)dom % 16 == 0) ? 1 : 0;
-            home_scatter_tile_kernel<<<hist_blocks, kScatterThreads, tile_smem, st>>>(
-                coords, dom, n, nd, tileT, vec, offs, m.hstart, pl->d_home_gid,
-                reinterpret_cast<float4*>(pl->d_bxyz));
+            HALO_CUDA(launch_dependent_shm(home_scatter_tile_kernel, dim3(hist_blocks), dim3(kScatterThreads),
+                                           tile_smem, st, coords, dom, n, nd, tileT, vec,
+                                           (const int32_t*)offs, (const int64_t*)m.hstart, pl->d_home_gid,
+                                           reinterpret_cast<float4*>(pl->d_bxyz)));
         } else {
             HALO_TRY(device_exclusive_scan(pl->d_counts, offs, ncount, pl->d_scan_tmp, st));
             home_scatter_kernel<<<hist_blocks, wpb * 32, hist_smem, st>>>(
@@ -1062,14 +1084,19 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
             a.rc2 = (double)pl->rc * (double)pl->rc;
             a.faces = pl->d_faces;
             dim3 g((unsigned)B, (unsigned)nd);
-            pulse_count_kernel<<<g, kThreads, 0, st>>>(a);
-            pulse_write_kernel<<<g, kThreads, 0, st>>>(a);
+            HALO_CUDA(launch_dependent_shm(pulse_count_kernel, g, dim3(kThreads), 0, st, a));
+            HALO_CUDA(launch_dependent_shm(pulse_write_kernel, g, dim3(kThreads), 0, st, a));
         }
         // 3. dense layout
-        finalize_kernel<<<1, 1024, 0, st>>>(m, nd, P);
-        home_dst_kernel<<<nd, 256, 0, st>>>(m, pl->d_home_dst, spa, pl->d_sp);
+        HALO_CUDA(launch_dependent_shm(finalize_kernel, dim3(1), dim3(1024), 0, st, m, nd, P));
+        // the metadata comes back through the mapped staging (written by the
+        // home slot kernel), else with a copy
+        int64_t* host_meta = static_cast<int64_t*>(pl->h_stage_dev);
+        HALO_CUDA(launch_dependent_shm(home_dst_kernel, dim3(nd), dim3(256), 0, st, m, pl->d_home_dst, spa,
+                                       pl->d_sp, reinterpret_cast<const int64_t*>(pl->d_meta),
+                                       (int64_t)(mbytes / sizeof(int64_t)), host_meta));
         HALO_CUDA(cudaGetLastError());
-        HALO_CUDA(cudaMemcpyAsync(hm, pl->d_meta, mbytes, cudaMemcpyDeviceToHost, st));
+        if (!host_meta) HALO_CUDA(cudaMemcpyAsync(hm, pl->d_meta, mbytes, cudaMemcpyDeviceToHost, st));
         HALO_CUDA(cudaStreamSynchronize(st));
         if (h.flags[1]) return HALO_EDOMAIN;
         if (!h.flags[0]) break;

@@ -144,6 +144,7 @@ struct halo_plan {
     // pinned host staging for the build's host<->device copies (grow-only)
     void* h_stage = nullptr;
     size_t h_stage_cap = 0;
+    void* h_stage_dev = nullptr;     // its device address (mapped), or null: copied with the copy engine
     int occ_x = 0, occ_f = 0;        // resident blocks per SM of the fused kernels (cached)
 
     // sharded data plane: shard k holds the domains [shard_dom[k], shard_dom[k + 1])
@@ -270,6 +271,25 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 bl
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The same with dynamic shared memory: the build's kernels, each of which
+// starts with grid_launch_dependents() and grid_dependency_wait(), so the
+// next kernel's launch overlaps the end of the one before.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_dependent_shm(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                        cudaStream_t st, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <class T>
 inline int dev_alloc(T** p, size_t count) {
     *p = nullptr;
@@ -311,13 +331,19 @@ inline int host_stage(halo_plan* pl, size_t bytes, void** out) {
         if (pl->h_stage) cudaFreeHost(pl->h_stage);
         pl->h_stage = nullptr;
         pl->h_stage_cap = 0;
+        pl->h_stage_dev = nullptr;
         const size_t want = bytes + bytes / 4 + 4096;
-        if (cudaMallocHost(&pl->h_stage, want) != cudaSuccess) {
+        if (cudaHostAlloc(&pl->h_stage, want, cudaHostAllocMapped) != cudaSuccess) {
             (void)cudaGetLastError();
             pl->h_stage = nullptr;
             return HALO_ENOMEM;
         }
         pl->h_stage_cap = want;
+        // kernels write the words the host reads back straight into it
+        if (cudaHostGetDevicePointer(&pl->h_stage_dev, pl->h_stage, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            pl->h_stage_dev = nullptr;
+        }
     }
     *out = pl->h_stage;
     return HALO_OK;

@@ -167,12 +167,21 @@ __global__ void staged_unpack_f_kernel(const SPDesc* __restrict__ sp, const int3
 // ---- flat: build-time composition of the chains -------------------------------
 
 // Pulse p, in ascending order: every received slot inherits its source's owner
-// and boundary crossings, and remembers its source (parent) and pulse.
+// and boundary crossings, and remembers its source (parent) and pulse.  It
+// also writes its coordinate-table entry (owner | crossings << 29, at
+// xbase[receiver] + slot) and counts its owner's copies, keeping its rank
+// among them (the counter's value before its increment).
 __global__ void chain_pulse_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
                                    int32_t* owner, int32_t* parent, int8_t* hop, int8_t* code,
-                                   int P, int p, int dim) {
+                                   const int32_t* __restrict__ xbase, int32_t* __restrict__ xflat,
+                                   int32_t* ncopies, int32_t* __restrict__ rank, int P, int p,
+                                   int dim) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
+    if (d.send <= 0) return;
     const int8_t bit = d.shift[dim] != 0.0f ? (int8_t)(1 << dim) : (int8_t)0;
+    const int64_t xb = xbase[d.r];
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x) {
         const int64_t h = d.dst + i;
         const int64_t src = d.src_base + maps[d.map_off + i];
@@ -181,19 +190,28 @@ __global__ void chain_pulse_kernel(const SPDesc* __restrict__ sp, const int32_t*
         // Home slots' entries of these arrays are never read, so nothing
         // initialises them.
         const bool home = i < d.split;
-        owner[h] = home ? (int32_t)src : owner[src];
+        const int32_t o = home ? (int32_t)src : owner[src];
+        const int8_t c = (int8_t)((home ? 0 : code[src]) | bit);
+        owner[h] = o;
         parent[h] = (int32_t)src;
         hop[h] = (int8_t)p;
-        code[h] = (int8_t)((home ? 0 : code[src]) | bit);
+        code[h] = c;
+        xflat[xb + h] = o | ((int32_t)c << 29);
+        rank[h] = atomicAdd(ncopies + o, 1);
     }
 }
 
 // The coordinate kernel's work items: domain D's halo range in chunks of
 // `chunk` slots, numbered in domain order; item b = {b * chunk (its table
-// offset), first halo slot, count}.  One block: 1024 domains per round, their
-// first items from a block scan, then a warp per domain writes its items.
+// offset), first halo slot, count}; xbase[D] = the table offset of D's halo
+// slot 0 minus the slot (halo slot h of D sits at xbase[D] + h).  One block:
+// 1024 domains per round, their first items from a block scan, then a warp
+// per domain writes its items.
 __global__ void __launch_bounds__(1024) xflat_items_kernel(DomainTables t, int nd, int P, int chunk,
-                                                           int4* __restrict__ items) {
+                                                           int4* __restrict__ items,
+                                                           int32_t* __restrict__ xbase) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     __shared__ int64_t sfirst[1024], snh[1024], sd0[1024];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t carry = 0;
@@ -209,6 +227,7 @@ __global__ void __launch_bounds__(1024) xflat_items_kernel(DomainTables t, int n
         sfirst[threadIdx.x] = carry + pre;
         snh[threadIdx.x] = nh;
         sd0[threadIdx.x] = d0;
+        if (D < nd) xbase[D] = (int32_t)((carry + pre) * chunk - d0);  // table offset - first halo slot
         __syncthreads();
         for (int j = warp; j < 1024 && D0 + j < nd; j += 32) {
             const int64_t nhj = snh[j], f = sfirst[j], dj = sd0[j];
@@ -220,21 +239,6 @@ __global__ void __launch_bounds__(1024) xflat_items_kernel(DomainTables t, int n
         }
         carry += tot;
         __syncthreads();
-    }
-}
-
-// Coordinate table over halo slots; also counts the copies of every owner,
-// and keeps each halo slot's rank among its owner's copies (the counter's
-// value before its increment) for owner_fill_kernel.
-__global__ void xflat_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
-                             const int8_t* __restrict__ code, int32_t* __restrict__ xflat,
-                             int32_t* __restrict__ ncopies, int32_t* __restrict__ rank) {
-    const int4 it = items[blockIdx.x];
-    for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
-        const int64_t j = (int64_t)it.y + i;
-        const int32_t o = owner[j];
-        xflat[(int64_t)it.x + i] = o | ((int32_t)code[j] << 29);
-        rank[j] = atomicAdd(ncopies + o, 1);
     }
 }
 
@@ -291,6 +295,8 @@ template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_reduce_kernel(const int32_t* __restrict__ in,
                                                                int64_t n, const int64_t* n_dev,
                                                                int64_t* __restrict__ sums) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     static_assert(kScanTile == 8 * kThreads, "eight elements per thread");
     __shared__ int64_t ws[kThreads / 32];
     n = scan_count(n, n_dev);
@@ -318,6 +324,8 @@ __global__ void __launch_bounds__(kThreads) pair_reduce_kernel(const int32_t* __
 __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ sums, int64_t n,
                                                         const int64_t* n_dev, int64_t* total,
                                                         int32_t* end) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     n = scan_count(n, n_dev);
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
     int64_t carry = 0;
@@ -350,6 +358,8 @@ __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __re
                                                              int32_t* __restrict__ out_b,
                                                              int32_t* __restrict__ fown,
                                                              int32_t* __restrict__ fstart) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     n = scan_count(n, n_dev);
     const int64_t b0 = (int64_t)blockIdx.x * kScanTile;
     if (b0 >= n) return;
@@ -399,18 +409,23 @@ int pair_scan(const int32_t* in, int64_t n, const int64_t* n_dev, int64_t* sums,
               int32_t* out_b, int64_t* total, cudaStream_t st, int32_t* fown = nullptr,
               int32_t* fstart = nullptr) {
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
-    if (nb > 0) pair_reduce_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, n_dev, sums);
-    pair_top_kernel<<<1, 1024, 0, st>>>(sums, n, n_dev, total, fstart);
     if (nb > 0)
-        pair_down_kernel<SRC><<<(unsigned)nb, kThreads, 0, st>>>(in, n, n_dev, sums, out_a, out_b, fown,
-                                                                  fstart);
-    return cuda_code(cudaGetLastError());
+        HALO_CUDA(launch_dependent_shm(pair_reduce_kernel<SRC>, dim3((unsigned)nb), dim3(kThreads), 0, st,
+                                       in, n, n_dev, sums));
+    HALO_CUDA(launch_dependent_shm(pair_top_kernel, dim3(1), dim3(1024), 0, st, sums, n, n_dev, total,
+                                   fstart));
+    if (nb > 0)
+        HALO_CUDA(launch_dependent_shm(pair_down_kernel<SRC>, dim3((unsigned)nb), dim3(kThreads), 0, st,
+                                       in, n, n_dev, (const int64_t*)sums, out_a, out_b, fown, fstart));
+    return HALO_OK;
 }
 
 // Every halo slot into its owner's copy list, at the rank xflat_kernel took.
 __global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
                                   const int32_t* __restrict__ entry_pos,
                                   const int32_t* __restrict__ rank, int32_t* __restrict__ tmp) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const int4 it = items[blockIdx.x];
     for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
         const int64_t j = (int64_t)it.y + i;
@@ -449,6 +464,8 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
                                   const int32_t* __restrict__ posA, const int32_t* __restrict__ posB,
                                   int4* __restrict__ recA, int32_t* __restrict__ listB,
                                   int32_t* __restrict__ listC, int* max_copies, int* err) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const int64_t n_owners = *total >> 32;
     __shared__ int block_max;
     if (threadIdx.x == 0) block_max = 0;
@@ -521,14 +538,19 @@ __global__ void owner_sort_kernel(const int32_t* __restrict__ fown, const int32_
 
 // The owners of four or more copies (classes B and C), from the lists
 // owner_sort_kernel wrote: counts[0] = copies | owners << 32, counts[1] =
-// class A | class B << 32.
+// class A | class B << 32.  If host_out is given (the host's mapped
+// staging), the last block to finish (ticket in misc[2]) copies the build's
+// summary words misc[0 .. 11] there.
 __global__ void owner_sort_bc_kernel(const int32_t* __restrict__ fown, const int32_t* __restrict__ fstart,
                                      const int32_t* __restrict__ tmp, const int32_t* __restrict__ parent,
                                      const int8_t* __restrict__ hop, const int64_t* __restrict__ counts,
                                      const int32_t* __restrict__ posA, const int32_t* __restrict__ posB,
                                      const int32_t* __restrict__ listB, const int32_t* __restrict__ listC,
                                      int4* __restrict__ recB, int4* __restrict__ recC,
-                                     int32_t* __restrict__ fent, int* err) {
+                                     int32_t* __restrict__ fent, int* err, int32_t* misc,
+                                     int32_t* __restrict__ host_out) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const int64_t n_owners = counts[0] >> 32;
     const int64_t n_a = counts[1] & 0xffffffffll, n_b = counts[1] >> 32;
     const int64_t n_bc = n_owners - n_a;
@@ -617,6 +639,17 @@ __global__ void owner_sort_bc_kernel(const int32_t* __restrict__ fown, const int
         } else {
             for (int j = 0; j < k; j++) fent[s0 + j] = node[j];
             recC[m - posA[m] - posB[m]] = make_int4(hdr, s0, 0, 0);  // class-C owners before m
+        }
+    }
+    if (host_out) {
+        __shared__ int last;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last = atomicAdd(misc + 2, 1) == (int)gridDim.x - 1;
+        __syncthreads();
+        if (last) {
+            __threadfence();
+            if (threadIdx.x < 12) host_out[threadIdx.x] = __ldcg(misc + threadIdx.x);
         }
     }
 }
@@ -1004,6 +1037,7 @@ namespace {
 // Scratch of the FLAT table build, carved from two pools kept in the plan.
 struct FlatScratch {
     int32_t *owner, *parent, *ncopies, *entry_pos, *rank, *tmp;
+    int32_t* xbase;   // per domain: coordinate-table offset of halo slot 0, minus the slot
     int64_t* sums;    // int64 tile sums + grand total
     int32_t* misc;    // [0] largest copy list, [1] error
     int64_t* misc64;  // [0] copies | owners << 32, [1] class-A | class-B records << 32
@@ -1016,7 +1050,8 @@ int flat_scratch(halo_plan* pl, FlatScratch* f) {
     // 16 bytes at a time)
     const int64_t nl4 = (nl + 3) & ~(int64_t)3;
     const int64_t nsums = nl / kScanTile + 2;
-    const int64_t off_sums = (5 * nl4 + std::max<int64_t>(H, 1) + 1) & ~(int64_t)1;  // 8-byte aligned
+    const int64_t off_xbase = 5 * nl4 + ((std::max<int64_t>(H, 1) + 1 + 3) & ~(int64_t)3);
+    const int64_t off_sums = (off_xbase + pl->n_dom + 1) & ~(int64_t)1;  // 8-byte aligned
     HALO_TRY(dev_reserve(&pl->d_flat_pool32, &pl->cap_pool32, off_sums + 2 * nsums + 16));
     HALO_TRY(dev_reserve(&pl->d_flat_pool8, &pl->cap_pool8, 2 * nl));
     f->owner = pl->d_flat_pool32;
@@ -1025,6 +1060,7 @@ int flat_scratch(halo_plan* pl, FlatScratch* f) {
     f->entry_pos = f->ncopies + nl4;
     f->rank = f->entry_pos + nl4;
     f->tmp = f->rank + nl4;
+    f->xbase = pl->d_flat_pool32 + off_xbase;
     f->sums = reinterpret_cast<int64_t*>(pl->d_flat_pool32 + off_sums);
     f->misc = pl->d_flat_pool32 + off_sums + 2 * nsums;
     f->misc64 = reinterpret_cast<int64_t*>(f->misc + 8);
@@ -1035,24 +1071,8 @@ int flat_scratch(halo_plan* pl, FlatScratch* f) {
 }  // namespace
 
 int launch_flat_chains(halo_plan* pl, cudaStream_t st) {
-    if (pl->n_local_total >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
-    FlatScratch f;
-    HALO_TRY(flat_scratch(pl, &f));
-    for (int p = 0; p < pl->P; p++) {
-        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
-        chain_pulse_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(
-            pl->d_sp, pl->d_maps, f.owner, f.parent, f.hop, f.code, pl->P, p, pl->pulse_dim[p]);
-    }
-    HALO_CUDA(cudaGetLastError());
-    pl->flat_chains_ready = true;
-    return HALO_OK;
-}
-
-int prepare_flat(halo_plan* pl, cudaStream_t st) {
-    pl->flat_ready = false;  // buffers are kept (grow-only) across rebuilds
-    const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
     const int nd = pl->n_dom;
-    if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
+    if (pl->n_local_total >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
     // coordinate items: halo range of every domain, in chunks of kXT * E
     // slots.  E = 2 unless that needs more than two waves of resident blocks,
     // then 3 (measured, x + f back to back, 128-thread blocks: the 1M-atom
@@ -1069,13 +1089,43 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     const int kFlatChunk = kXT * E;
     // item b = {table offset b * kFlatChunk, first halo slot, count}: the
     // table is padded to whole chunks so a block can address its entries
-    // from its index alone (the items are written on the device below)
+    // from its index alone (the items are written on the device)
     int64_t n_items = 0;
     for (int D = 0; D < nd; D++)
         n_items += ((int64_t)pl->n_local[D] - pl->n_home[D] + kFlatChunk - 1) / kFlatChunk;
     pl->n_xflat_items = (int)n_items;
     HALO_TRY(dev_reserve(&pl->d_xflat_items, &pl->cap_xflat_items, n_items));
     HALO_TRY(dev_reserve(&pl->d_xflat, &pl->cap_xflat, std::max<int64_t>(n_items * kFlatChunk, 1)));
+    FlatScratch f;
+    HALO_TRY(flat_scratch(pl, &f));
+    HALO_CUDA(cudaMemsetAsync(f.ncopies, 0, sizeof(int32_t) * pl->n_local_total, st));
+    HALO_CUDA(cudaMemsetAsync(f.misc, 0, sizeof(int32_t) * 16, st));
+    if (n_items > 0)
+        HALO_CUDA(launch_dependent_shm(xflat_items_kernel, dim3(1), dim3(1024), 0, st, domain_tables(pl), nd,
+                                       pl->P, kFlatChunk, pl->d_xflat_items, f.xbase));
+    for (int p = 0; p < pl->P; p++) {
+        const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
+        HALO_CUDA(launch_dependent_shm(chain_pulse_kernel, dim3(gx, nd), dim3(kThreads), 0, st,
+                                       (const SPDesc*)pl->d_sp, (const int32_t*)pl->d_maps, f.owner,
+                                       f.parent, f.hop, f.code, (const int32_t*)f.xbase, pl->d_xflat,
+                                       f.ncopies, f.rank, pl->P, p, (int)pl->pulse_dim[p]));
+    }
+    HALO_CUDA(cudaGetLastError());
+    pl->flat_chains_ready = true;
+    return HALO_OK;
+}
+
+int prepare_flat(halo_plan* pl, cudaStream_t st) {
+    pl->flat_ready = false;  // buffers are kept (grow-only) across rebuilds
+    const int64_t nl = pl->n_local_total, H = pl->n_halo_total;
+    if (nl >= ((int64_t)1 << kNodeBits)) return HALO_ECAPACITY;
+    // the coordinate items, the forwarding chains and the coordinate table
+    // need only the pulse descriptors and the sizes: a rebuild launches them
+    // as soon as those are known (before the host's own copy of the plan is
+    // built), else they are launched here
+    if (!pl->flat_chains_ready) HALO_TRY(launch_flat_chains(pl, st));
+    pl->flat_chains_ready = false;
+    const int64_t n_items = pl->n_xflat_items;
     HALO_TRY(dev_reserve(&pl->d_fent, &pl->cap_fent, H));
     // owner tables sized by bounds (every halo slot is one copy of one owner:
     // at most H owners, H / 4 with 4..11 copies, H / 12 with more), so that
@@ -1098,17 +1148,7 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int32_t* misc = f.misc;
     int64_t* misc64 = f.misc64;
     int8_t* hop = f.hop;
-    int8_t* code = f.code;
 
-    // the forwarding chains need only the pulse descriptors: a rebuild
-    // launches them as soon as the sizes are known (before the host's own
-    // copy of the plan is built), else they are launched here
-    if (!pl->flat_chains_ready) HALO_TRY(launch_flat_chains(pl, st));
-    pl->flat_chains_ready = false;
-
-    if (n_items > 0)
-        xflat_items_kernel<<<1, 1024, 0, st>>>(domain_tables(pl), nd, pl->P, kFlatChunk,
-                                               pl->d_xflat_items);
     // pinned staging: words read back at the end
     int64_t* hw = nullptr;
     {
@@ -1119,11 +1159,6 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
     int rc = HALO_OK;
     do {
         const int gh = blocks_for(std::max<int64_t>(H, 1), pl->num_sms);
-        if ((rc = cuda_code(cudaMemsetAsync(ncopies, 0, sizeof(int32_t) * nl, st))) != HALO_OK) break;
-        if ((rc = cuda_code(cudaMemsetAsync(misc, 0, sizeof(int32_t) * 16, st))) != HALO_OK) break;
-        if (n_items > 0)
-            xflat_kernel<<<(unsigned)n_items, kThreads, 0, st>>>(pl->d_xflat_items, owner, code,
-                                                                       pl->d_xflat, ncopies, rank);
         // entry offsets of every slot's copy list and, from the same scan,
         // the owner list (fown, fstart); the grand total (copies, owners)
         // stays on the device
@@ -1131,8 +1166,11 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
                                pl->d_fstart)) != HALO_OK)
             break;
         if (n_items > 0)
-            owner_fill_kernel<<<(unsigned)n_items, kThreads, 0, st>>>(pl->d_xflat_items, owner,
-                                                                            entry_pos, rank, tmp);
+            if ((rc = cuda_code(launch_dependent_shm(owner_fill_kernel, dim3((unsigned)n_items), dim3(kThreads),
+                                                     0, st, (const int4*)pl->d_xflat_items,
+                                                     (const int32_t*)owner, (const int32_t*)entry_pos,
+                                                     (const int32_t*)rank, tmp))) != HALO_OK)
+                break;
         // record classes (A: <= 3 copies, B: 4..11, C: more): positions in
         // each class from one paired scan of the owners' copy counts, then the
         // sort writes every owner's record there
@@ -1145,14 +1183,26 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
         // has read them) in a second pass
         int32_t* listB = rank;
         int32_t* listC = rank + (H / 4 + 1);
-        owner_sort_kernel<<<gh, kThreads, 0, st>>>(pl->d_fown, pl->d_fstart, tmp, parent, hop, misc64,
-                                                   posA, posB, pl->d_frec[0], listB, listC, misc,
-                                                   misc + 1);
-        owner_sort_bc_kernel<<<blocks_for(H / 4 + 1, pl->num_sms), kThreads, 0, st>>>(
-            pl->d_fown, pl->d_fstart, tmp, parent, hop, misc64, posA, posB, listB, listC,
-            pl->d_frec[1], pl->d_frec[2], pl->d_fent, misc + 1);
+        if ((rc = cuda_code(launch_dependent_shm(
+                 owner_sort_kernel, dim3(gh), dim3(kThreads), 0, st, (const int32_t*)pl->d_fown,
+                 (const int32_t*)pl->d_fstart, (const int32_t*)tmp, (const int32_t*)parent,
+                 (const int8_t*)hop, (const int64_t*)misc64, (const int32_t*)posA, (const int32_t*)posB,
+                 pl->d_frec[0], listB, listC, misc, misc + 1))) != HALO_OK)
+            break;
+        // the summary words come back through the mapped staging (written by
+        // the last sort block), else with a copy
+        int32_t* host_out = static_cast<int32_t*>(pl->h_stage_dev);
+        if ((rc = cuda_code(launch_dependent_shm(
+                 owner_sort_bc_kernel, dim3(blocks_for(H / 4 + 1, pl->num_sms)), dim3(kThreads), 0, st,
+                 (const int32_t*)pl->d_fown, (const int32_t*)pl->d_fstart, (const int32_t*)tmp,
+                 (const int32_t*)parent, (const int8_t*)hop, (const int64_t*)misc64,
+                 (const int32_t*)posA, (const int32_t*)posB, (const int32_t*)listB,
+                 (const int32_t*)listC, pl->d_frec[1], pl->d_frec[2], pl->d_fent, misc + 1, misc,
+                 host_out))) != HALO_OK)
+            break;
         // the one synchronisation: counts, largest list, error
-        if ((rc = cuda_code(cudaMemcpyAsync(hw, misc, 8 * sizeof(int32_t) + 2 * sizeof(int64_t),
+        if (!host_out &&
+            (rc = cuda_code(cudaMemcpyAsync(hw, misc, 8 * sizeof(int32_t) + 2 * sizeof(int64_t),
                                             cudaMemcpyDeviceToHost, st))) != HALO_OK)
             break;
         if ((rc = cuda_code(cudaStreamSynchronize(st))) != HALO_OK) break;
