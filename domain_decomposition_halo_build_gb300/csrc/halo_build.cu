@@ -400,6 +400,8 @@ __global__ void __launch_bounds__(kScatterThreads) home_scatter_tile_kernel(
 // ---- generic int32 exclusive scan (three launches) ---------------------------------
 __global__ void scan_reduce_kernel(const int32_t* __restrict__ in, int64_t n,
                                    int32_t* __restrict__ sums) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const int64_t b0 = (int64_t)blockIdx.x * kScanTile;
     int64_t s = 0;
     for (int j = threadIdx.x; j < kScanTile; j += kThreads) {
@@ -412,6 +414,8 @@ __global__ void scan_reduce_kernel(const int32_t* __restrict__ in, int64_t n,
 }
 
 __global__ void scan_top_kernel(int32_t* __restrict__ sums, int64_t nb) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     int64_t carry = 0;
     for (int64_t b = 0; b < nb; b += 1024) {
         const int64_t i = b + threadIdx.x;
@@ -426,6 +430,8 @@ __global__ void scan_top_kernel(int32_t* __restrict__ sums, int64_t nb) {
 __global__ void __launch_bounds__(kThreads) scan_down_kernel(const int32_t* __restrict__ in,
                                                              int32_t* __restrict__ out, int64_t n,
                                                              const int32_t* __restrict__ sums) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     // each warp walks a contiguous run of the tile 32 elements at a time
     // (coalesced), a shuffle scan per 32, warp totals scanned across the block
     constexpr int kWarps = kThreads / 32;
@@ -842,10 +848,11 @@ int device_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int32_t* t
                           cudaStream_t st) {
     const int64_t nb = (n + kScanTile - 1) / kScanTile;
     if (nb == 0) return HALO_OK;
-    scan_reduce_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, n, tmp);
-    scan_top_kernel<<<1, 1024, 0, st>>>(tmp, nb);
-    scan_down_kernel<<<(unsigned)nb, kThreads, 0, st>>>(in, out, n, tmp);
-    return cuda_code(cudaGetLastError());
+    HALO_CUDA(launch_dependent_shm(scan_reduce_kernel, dim3((unsigned)nb), dim3(kThreads), 0, st, in, n, tmp));
+    HALO_CUDA(launch_dependent_shm(scan_top_kernel, dim3(1), dim3(1024), 0, st, tmp, nb));
+    HALO_CUDA(launch_dependent_shm(scan_down_kernel, dim3((unsigned)nb), dim3(kThreads), 0, st, in, out, n,
+                                   (const int32_t*)tmp));
+    return HALO_OK;
 }
 
 void free_build(halo_plan* pl) {

@@ -401,6 +401,8 @@ __global__ void __launch_bounds__(kThreads, 4) unpack_f_kernel(const __grid_cons
 // launched in ascending order; within one pulse a slot appears at most once).
 __global__ void mark_kernel(const SPDesc* __restrict__ sp, const int32_t* __restrict__ maps,
                             int8_t* __restrict__ wmax, int P, int p) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const SPDesc d = sp[(int64_t)blockIdx.y * P + p];
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d.send; i += gridDim.x * blockDim.x)
         wmax[d.src_base + maps[d.map_off + i]] = (int8_t)p;
@@ -413,6 +415,8 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(const SPDesc* __rest
                                                             const int8_t* __restrict__ wmax,
                                                             int2* __restrict__ pairs,
                                                             int32_t* __restrict__ nindep) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     __shared__ int wi[kThreads / 32], wd[kThreads / 32];
     __shared__ int s_tot;
     const SPDesc d = sp[blockIdx.x];
@@ -572,6 +576,8 @@ struct ItemGen {
 };
 
 __global__ void recv_mask_kernel(const SPDesc* __restrict__ sp, int nsp, uint64_t* mask) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nsp; i += gridDim.x * blockDim.x) {
         const SPDesc d = sp[i];
         if (d.send > 0) atomicOr((unsigned long long*)(mask + d.r), 1ull << d.p);
@@ -605,6 +611,8 @@ __device__ __forceinline__ void f_group(const ItemGen& a, int g, int* sp, int* l
 }
 
 __global__ void item_count_kernel(ItemGen a, int32_t* cx, int32_t* cf, uint32_t* target) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const int ng = 2 * a.P * a.nd;
     for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < ng; g += gridDim.x * blockDim.x) {
         int sp, lo, hi;
@@ -627,6 +635,8 @@ __global__ void item_count_kernel(ItemGen a, int32_t* cx, int32_t* cf, uint32_t*
 __global__ void item_fill_kernel(ItemGen a, const int32_t* __restrict__ bx,
                                  const int32_t* __restrict__ bf, XItem* __restrict__ ix,
                                  FItem* __restrict__ iff) {
+    grid_launch_dependents();  // the next kernel may start; it waits for this one
+    grid_dependency_wait();
     const int g = blockIdx.x;
     int sp, lo, hi;
     bool dep;
@@ -764,6 +774,21 @@ int prepare_common(halo_plan* pl, cudaStream_t st) {
     return HALO_OK;
 }
 
+namespace {
+// The work-list totals for the host: items = the last group's offset plus its
+// count, coordinate and force lists, into the host's mapped staging.
+__global__ void item_totals_kernel(const int32_t* __restrict__ bx, const int32_t* __restrict__ cx,
+                                   const int32_t* __restrict__ bf, const int32_t* __restrict__ cf, int ng,
+                                   int32_t* __restrict__ out) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        out[0] = bx[ng - 1] + cx[ng - 1];
+        out[1] = bf[ng - 1] + cf[ng - 1];
+    }
+}
+}  // namespace
+
 int prepare_fused(halo_plan* pl, cudaStream_t st) {
     const int nd = pl->n_dom, P = pl->P;
     pl->trace = nullptr;  // item counts change: the caller re-arms tracing
@@ -772,8 +797,9 @@ int prepare_fused(halo_plan* pl, cudaStream_t st) {
     const int E = pl->entries_per_thread;
     const int CHF = 32 * E;
     const int CH = pl->chunk;
-    // four words read back below, in the pinned staging (no copy from it is
-    // in flight: every build step that uses it synchronises before returning)
+    // the two list totals read back below, in the pinned staging (no copy
+    // from it is in flight: every build step that uses it synchronises
+    // before returning)
     int32_t* h_tot = nullptr;
     {
         void* hs = nullptr;
@@ -790,11 +816,13 @@ int prepare_fused(halo_plan* pl, cudaStream_t st) {
         HALO_CUDA(cudaMemsetAsync(pl->d_wmax, 0xff, (size_t)pl->n_local_total, st));
         for (int p = 0; p < P; p++) {
             const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
-            mark_kernel<<<dim3(gx, nd), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, pl->d_wmax, P, p);
+            HALO_CUDA(launch_dependent_shm(mark_kernel, dim3(gx, nd), dim3(kThreads), 0, st,
+                                           (const SPDesc*)pl->d_sp, (const int32_t*)pl->d_maps, pl->d_wmax,
+                                           P, p));
         }
-        classify_kernel<<<(unsigned)(nd * P), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, pl->d_wmax,
-                                                                  pl->d_fpairs, pl->d_nindep);
-        HALO_CUDA(cudaGetLastError());
+        HALO_CUDA(launch_dependent_shm(classify_kernel, dim3((unsigned)(nd * P)), dim3(kThreads), 0, st,
+                                       (const SPDesc*)pl->d_sp, (const int32_t*)pl->d_maps,
+                                       (const int8_t*)pl->d_wmax, pl->d_fpairs, pl->d_nindep));
     }
 
     // work lists on the device: chunk counts per group, scans, fill
@@ -835,34 +863,48 @@ int prepare_fused(halo_plan* pl, cudaStream_t st) {
     HALO_TRY(dev_reserve(&pl->d_items_x, &pl->cap_items_x, ub_x));
     HALO_TRY(dev_reserve(&pl->d_items_f, &pl->cap_items_f, ub_f));
     a.recv_mask = pl->d_recv_mask;
-    h_tot[0] = h_tot[1] = h_tot[2] = h_tot[3] = 0;
-    if (ng > 0) {
-        HALO_CUDA(cudaMemsetAsync(pl->d_recv_mask, 0, sizeof(uint64_t) * nd, st));
-        recv_mask_kernel<<<(unsigned)((nsp + 255) / 256), 256, 0, st>>>(pl->d_sp, (int)nsp,
-                                                                         pl->d_recv_mask);
-        item_count_kernel<<<(unsigned)((ng + 255) / 256), 256, 0, st>>>(a, cx, cf, pl->d_target);
-        HALO_TRY(device_exclusive_scan(cx, bx, ng, sct, st));
-        HALO_TRY(device_exclusive_scan(cf, bf, ng, sct, st));
-        item_fill_kernel<<<(unsigned)ng, 128, 0, st>>>(a, bx, bf, pl->d_items_x, pl->d_items_f);
-        HALO_CUDA(cudaGetLastError());
-        HALO_CUDA(cudaMemcpyAsync(h_tot, bx + ng - 1, 4, cudaMemcpyDeviceToHost, st));
-        HALO_CUDA(cudaMemcpyAsync(h_tot + 1, cx + ng - 1, 4, cudaMemcpyDeviceToHost, st));
-        HALO_CUDA(cudaMemcpyAsync(h_tot + 2, bf + ng - 1, 4, cudaMemcpyDeviceToHost, st));
-        HALO_CUDA(cudaMemcpyAsync(h_tot + 3, cf + ng - 1, 4, cudaMemcpyDeviceToHost, st));
-    }
-    HALO_CUDA(cudaStreamSynchronize(st));
-    pl->n_items_x = h_tot[0] + h_tot[1];
-    pl->n_items_f = h_tot[2] + h_tot[3];
+    // the exchanges' signal counters and tickets, cleared before the one
+    // synchronisation
     HALO_TRY(dev_reserve(&pl->d_flags, &pl->cap_flags, (int64_t)(2 * nsp)));
     if (!pl->d_tickets) HALO_TRY(dev_alloc(&pl->d_tickets, 2));
+    h_tot[0] = h_tot[1] = 0;
+    if (ng > 0) {
+        HALO_CUDA(cudaMemsetAsync(pl->d_recv_mask, 0, sizeof(uint64_t) * nd, st));
+        HALO_CUDA(launch_dependent_shm(recv_mask_kernel, dim3((unsigned)((nsp + 255) / 256)), dim3(256), 0, st,
+                                       (const SPDesc*)pl->d_sp, (int)nsp, pl->d_recv_mask));
+        HALO_CUDA(launch_dependent_shm(item_count_kernel, dim3((unsigned)((ng + 255) / 256)), dim3(256), 0,
+                                       st, a, cx, cf, pl->d_target));
+        HALO_TRY(device_exclusive_scan(cx, bx, ng, sct, st));
+        HALO_TRY(device_exclusive_scan(cf, bf, ng, sct, st));
+        HALO_CUDA(launch_dependent_shm(item_fill_kernel, dim3((unsigned)ng), dim3(128), 0, st, a,
+                                       (const int32_t*)bx, (const int32_t*)bf, pl->d_items_x,
+                                       pl->d_items_f));
+        // the totals come back through the mapped staging, else with copies
+        if (pl->h_stage_dev) {
+            HALO_CUDA(launch_dependent_shm(item_totals_kernel, dim3(1), dim3(32), 0, st, (const int32_t*)bx,
+                                           (const int32_t*)cx, (const int32_t*)bf, (const int32_t*)cf, ng,
+                                           static_cast<int32_t*>(pl->h_stage_dev)));
+        } else {
+            HALO_CUDA(cudaMemcpyAsync(h_tot + 2, bx + ng - 1, 4, cudaMemcpyDeviceToHost, st));
+            HALO_CUDA(cudaMemcpyAsync(h_tot + 3, cx + ng - 1, 4, cudaMemcpyDeviceToHost, st));
+            HALO_CUDA(cudaMemcpyAsync(h_tot + 4, bf + ng - 1, 4, cudaMemcpyDeviceToHost, st));
+            HALO_CUDA(cudaMemcpyAsync(h_tot + 5, cf + ng - 1, 4, cudaMemcpyDeviceToHost, st));
+        }
+    }
+    HALO_TRY(reset_flags(pl, st));
+    HALO_CUDA(cudaStreamSynchronize(st));
+    if (ng > 0 && !pl->h_stage_dev) {
+        h_tot[0] = h_tot[2] + h_tot[3];
+        h_tot[1] = h_tot[4] + h_tot[5];
+    }
+    pl->n_items_x = h_tot[0];
+    pl->n_items_f = h_tot[1];
     if (pl->occ_x <= 0 || pl->occ_f <= 0) HALO_TRY(occupancy<4>(&pl->occ_x, &pl->occ_f));
     pl->grid_x = (int)std::max<int64_t>(
         1, std::min<int64_t>(pl->n_items_x, (int64_t)pl->num_sms * std::max(pl->occ_x, 1)));
     pl->grid_f = (int)std::max<int64_t>(
         1, std::min<int64_t>((pl->n_items_f + kWarps - 1) / kWarps,
                              (int64_t)pl->num_sms * std::max(pl->occ_f, 1)));
-    HALO_TRY(reset_flags(pl, st));
-    HALO_CUDA(cudaStreamSynchronize(st));
     pl->fused_ready = true;
     return HALO_OK;
 }

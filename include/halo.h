@@ -38,8 +38,9 @@
  *
  * Pointers are DEVICE pointers unless marked (host).  `stream` is a
  * cudaStream_t passed as void* (NULL = legacy default stream).  Exchanges are
- * asynchronous on `stream`; halo_setup / halo_rebuild synchronise `stream` once
- * to read the sizes back.  A plan is used by one stream at a time.  Every call
+ * asynchronous on `stream`; halo_setup / halo_rebuild synchronise `stream` to
+ * read the sizes back and return with all the work they queued on it done.
+ * A plan is used by one stream at a time.  Every call
  * returns HALO_OK or a negative error code; no exception crosses the ABI.
  * Errors met by a kernel (a bounded wait that gave up) are sticky in the plan
  * and are returned, and cleared, by halo_status().
