@@ -420,7 +420,7 @@ int pair_scan(const int32_t* in, int64_t n, const int64_t* n_dev, int64_t* sums,
     return HALO_OK;
 }
 
-// Every halo slot into its owner's copy list, at the rank xflat_kernel took.
+// Every halo slot into its owner's copy list, at the rank chain_pulse_kernel took.
 __global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
                                   const int32_t* __restrict__ entry_pos,
                                   const int32_t* __restrict__ rank, int32_t* __restrict__ tmp) {
