@@ -84,6 +84,20 @@ __device__ __forceinline__ int cell_of(int D, int d, int nx, int ny) {
 }
 
 
+// The lanes of the warp whose domain id equals this lane's (valid lanes only;
+// an invalid lane's result is not used): one ballot per bit of the id, so
+// the cost is fixed (nbits + 1 ballots) where the match instruction's grows
+// with the number of distinct ids among the 32 lanes.
+__device__ __forceinline__ unsigned same_domain_lanes(int d, bool valid, int nbits) {
+    unsigned m = __ballot_sync(kFull, valid);
+    for (int b = 0; b < nbits; b++) {
+        const bool bit = ((d >> b) & 1) != 0;
+        const unsigned bb = __ballot_sync(kFull, bit);
+        m &= bit ? bb : ~bb;
+    }
+    return m;
+}
+
 // ---- 1. home partition ------------------------------------------------------------
 // A block of W warps covers the block tile b of W * wtile atoms; warp w its
 // sub-tile [(b*W + w)*wtile, ... + wtile) (wtile a multiple of 128).  Each
@@ -140,12 +154,13 @@ __global__ void home_hist_kernel(const int32_t* __restrict__ dom, int64_t n, int
 // Stable scatter: every warp's start per domain is its block tile's start
 // plus the counts of the warps before it; then each warp visits its atoms in
 // input order, and within 32 atoms the rank among equal domain ids comes from
-// the warp match mask.
+// the lanes with the same id (same_domain_lanes).
 __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t* __restrict__ dom,
                                     int64_t n, int nd, int64_t nbt,
                                     const int32_t* __restrict__ offs,
                                     const int32_t* __restrict__ wcounts,
                                     int32_t* __restrict__ home_gid, float4* __restrict__ bxyz) {
+    const int nbits = 32 - __clz(max(nd - 1, 0));  // bits of a domain id
     extern __shared__ int32_t sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int W = blockDim.x >> 5;
@@ -184,7 +199,7 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
 #pragma unroll
         for (int u = 0; u < U; u++) {
             const int64_t a = a0 + (it + u) * 32 + lane;
-            const unsigned peers = __match_any_sync(kFull, d[u]);
+            const unsigned peers = same_domain_lanes(d[u], d[u] >= 0, nbits);
             if (d[u] >= 0) {
                 const int64_t pos = (int64_t)run[d[u]] + __popc(peers & lt);
                 home_gid[pos] = (int32_t)a;
@@ -203,7 +218,7 @@ __global__ void home_scatter_kernel(const float* __restrict__ xyz, const int32_t
 // asynchronous copies where the tile is 16-byte aligned, so every copy is in
 // flight at once), counts them per warp sub-tile, ranks them (per-domain tile
 // starts, then each warp's atoms in input order, 32 at a time, ranks among
-// equal ids from the warp match mask) and writes every domain's run of the
+// equal ids from same_domain_lanes) and writes every domain's run of the
 // tile contiguously, from hstart[D] + pre[b*nd + D] (the column prefixes of
 // the tile-major counts).  Several blocks fit on an SM, so one block's copies
 // overlap another's ranking.
@@ -301,6 +316,7 @@ __global__ void __launch_bounds__(kScatterThreads) home_scatter_tile_kernel(
     int32_t* __restrict__ home_gid, float4* __restrict__ bxyz) {
     grid_launch_dependents();  // the next kernel may start; it waits for this one
     grid_dependency_wait();
+    const int nbits = 32 - __clz(max(nd - 1, 0));  // bits of a domain id
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int W = kScatterThreads / 32;
@@ -350,21 +366,16 @@ __global__ void __launch_bounds__(kScatterThreads) home_scatter_tile_kernel(
         lstart[d] = acc;
     }
     __syncthreads();
-    if (warp == 0) {
-        int32_t carry = 0;
-        for (int d0 = 0; d0 < nd; d0 += 32) {
-            const int d = d0 + lane;
-            const int32_t v = d < nd ? lstart[d] : 0;
-            int32_t x = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t y = __shfl_up_sync(kFull, x, o);
-                if (lane >= o) x += y;
-            }
-            if (d < nd) lstart[d] = carry + x - v;
-            carry += __shfl_sync(kFull, x, 31);
-        }
-        if (lane == 0) lstart[nd] = carry;
+    {
+        // exclusive scan of the tile counts over the domains, two per thread
+        // (the tiled path has nd <= 2 * kScatterThreads)
+        const int d0 = 2 * threadIdx.x;
+        const int32_t v0 = d0 < nd ? lstart[d0] : 0, v1 = d0 + 1 < nd ? lstart[d0 + 1] : 0;
+        int64_t tot;
+        const int64_t pre = block_exclusive_scan<kScatterThreads>(v0 + v1, &tot);
+        if (d0 < nd) lstart[d0] = (int32_t)pre;
+        if (d0 + 1 < nd) lstart[d0 + 1] = (int32_t)(pre + v0);
+        if (threadIdx.x == 0) lstart[nd] = (int32_t)tot;
     }
     __syncthreads();
     for (int d = threadIdx.x; d < nd; d += kScatterThreads) {
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(kScatterThreads) home_scatter_tile_kernel(
         const int i = i0 + r + lane;
         int d = i < cnt ? rd[i] : -1;
         if (d >= nd) d = -1;
-        const unsigned peers = __match_any_sync(kFull, d);
+        const unsigned peers = same_domain_lanes(d, d >= 0, nbits);
         if (d >= 0) perm[run[d] + __popc(peers & lt)] = (int16_t)i;
         __syncwarp();
         if (d >= 0 && lane == __ffs(peers) - 1) run[d] += __popc(peers);
@@ -884,7 +895,8 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
     // home partition.  Tiled: tiles of T atoms, each ranked in shared memory
     // by a scatter block of kScatterThreads / 32 warp sub-tiles; T is the
     // largest of 8192 .. 1024 with two scatter blocks per SM (the per-warp
-    // histograms must fit 48 KB).  Measured on the 3M-atom system (T = 4096,
+    // histograms must fit 48 KB, and a block scans the domains two per
+    // thread).  Measured on the 3M-atom system (T = 4096,
     // 256 threads): rebuild 0.59 ms against 0.60 at T = 2048 (three blocks
     // per SM) and 0.60 at T = 8192 (one); 512 threads, 5 us less.  Otherwise
     // the direct
@@ -892,7 +904,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
     // memory), one block tile of W * kHistTile atoms per block.
     int tileT = 0;
     size_t tile_smem = 0;
-    if ((size_t)(kScatterThreads / 32) * nd * sizeof(int32_t) <= 48 * 1024 && nd < 32768) {
+    if ((size_t)(kScatterThreads / 32) * nd * sizeof(int32_t) <= 48 * 1024 && nd <= 2 * kScatterThreads) {
         int optin = 0, per_sm = 0;
         HALO_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->dev));
         HALO_CUDA(cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, pl->dev));
