@@ -204,41 +204,50 @@ __global__ void chain_pulse_kernel(const SPDesc* __restrict__ sp, const int32_t*
 // The coordinate kernel's work items: domain D's halo range in chunks of
 // `chunk` slots, numbered in domain order; item b = {b * chunk (its table
 // offset), first halo slot, count}; xbase[D] = the table offset of D's halo
-// slot 0 minus the slot (halo slot h of D sits at xbase[D] + h).  One block:
-// 1024 domains per round, their first items from a block scan, then a warp
-// per domain writes its items.
+// slot 0 minus the slot (halo slot h of D sits at xbase[D] + h).  Block g
+// takes domains [32g, 32g + 32): it sums the item counts of the domains
+// before them (every block for itself: a few hundred L2 loads), warp 0 scans
+// its 32, and warp w writes domain 32g + w's items.
 __global__ void __launch_bounds__(1024) xflat_items_kernel(DomainTables t, int nd, int P, int chunk,
                                                            int4* __restrict__ items,
                                                            int32_t* __restrict__ xbase) {
     grid_launch_dependents();  // the next kernel may start; it waits for this one
     grid_dependency_wait();
-    __shared__ int64_t sfirst[1024], snh[1024], sd0[1024];
+    __shared__ int64_t sfirst[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g0 = blockIdx.x * 32;
+    auto count = [&](int D) -> int64_t {
+        const int64_t nh = t.own_off[(int64_t)D * (P + 1) + P] - t.n_home[D];
+        return (nh + chunk - 1) / chunk;
+    };
     int64_t carry = 0;
-    for (int D0 = 0; D0 < nd; D0 += 1024) {
+    for (int D0 = 0; D0 < g0; D0 += 1024) {
         const int D = D0 + threadIdx.x;
-        int64_t nh = 0, d0 = 0;
-        if (D < nd) {
-            nh = t.own_off[(int64_t)D * (P + 1) + P] - t.n_home[D];
-            d0 = t.base[D] + t.n_home[D];
-        }
         int64_t tot;
-        const int64_t pre = block_exclusive_scan<1024>((nh + chunk - 1) / chunk, &tot);
-        sfirst[threadIdx.x] = carry + pre;
-        snh[threadIdx.x] = nh;
-        sd0[threadIdx.x] = d0;
-        if (D < nd) xbase[D] = (int32_t)((carry + pre) * chunk - d0);  // table offset - first halo slot
-        __syncthreads();
-        for (int j = warp; j < 1024 && D0 + j < nd; j += 32) {
-            const int64_t nhj = snh[j], f = sfirst[j], dj = sd0[j];
-            for (int64_t k = lane; k * chunk < nhj; k += 32) {
-                const int64_t b = f + k;
-                items[b] = make_int4((int)(b * chunk), (int)(dj + k * chunk),
-                                     (int)min((int64_t)chunk, nhj - k * chunk), 0);
-            }
-        }
+        block_exclusive_scan<1024>(D < g0 ? count(D) : 0, &tot);
         carry += tot;
-        __syncthreads();
+    }
+    if (warp == 0) {
+        const int D = g0 + lane;
+        const int64_t c = D < nd ? count(D) : 0;
+        int64_t x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        sfirst[lane] = carry + x - c;
+    }
+    __syncthreads();
+    const int D = g0 + warp;
+    if (D >= nd) return;
+    const int64_t nh = t.own_off[(int64_t)D * (P + 1) + P] - t.n_home[D];
+    const int64_t d0 = t.base[D] + t.n_home[D];
+    const int64_t f = sfirst[warp];
+    if (lane == 0) xbase[D] = (int32_t)(f * chunk - d0);  // table offset - first halo slot
+    for (int64_t k = lane; k * chunk < nh; k += 32) {
+        const int64_t b = f + k;
+        items[b] = make_int4((int)(b * chunk), (int)(d0 + k * chunk), (int)min((int64_t)chunk, nh - k * chunk), 0);
     }
 }
 
@@ -349,7 +358,7 @@ __global__ void __launch_bounds__(1024) pair_top_kernel(int64_t* __restrict__ su
 // prefix, and it writes its eight exclusive prefixes.  SRC 0 also writes the
 // owner list: for a slot with copies, fown[its owner index] = the slot and
 // fstart[...] = its first entry (out_b, the owner indices, is then not
-// stored).
+// stored), through shared memory.
 template <int SRC>
 __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __restrict__ in, int64_t n,
                                                              const int64_t* n_dev,
@@ -370,17 +379,31 @@ __global__ void __launch_bounds__(kThreads) pair_down_kernel(const int32_t* __re
 #pragma unroll
     for (int k = 0; k < 8; k++) t += v[k];
     int64_t tot;
-    int64_t run = sums[blockIdx.x] + block_exclusive_scan<kThreads>(t, &tot);
+    const int64_t first = sums[blockIdx.x];
+    int64_t run = first + block_exclusive_scan<kThreads>(t, &tot);
+    // SRC 0: the block's owners take the contiguous owner indices from
+    // first >> 32 on; they are staged in shared memory and written out
+    // coalesced
+    __shared__ int32_t s_own[SRC == 0 ? kScanTile : 1], s_start[SRC == 0 ? kScanTile : 1];
+    const int32_t own0 = (int32_t)(first >> 32);
     int32_t a[8], bb[8];
 #pragma unroll
     for (int k = 0; k < 8; k++) {
         a[k] = (int32_t)(run & 0xffffffffll);
         bb[k] = (int32_t)(run >> 32);
         if (SRC == 0 && fown && (v[k] & 0xffffffffll) > 0 && i0 + k < n) {
-            fown[bb[k]] = (int32_t)(i0 + k);
-            fstart[bb[k]] = a[k];
+            s_own[bb[k] - own0] = (int32_t)(i0 + k);
+            s_start[bb[k] - own0] = a[k];
         }
         run += v[k];
+    }
+    if (SRC == 0 && fown) {
+        __syncthreads();
+        const int n_own = (int)(tot >> 32);  // owners in this block's tile
+        for (int j = threadIdx.x; j < n_own; j += kThreads) {
+            fown[own0 + j] = s_own[j];
+            fstart[own0 + j] = s_start[j];
+        }
     }
     const bool write_b = !(SRC == 0 && fown);
     if (i0 + 8 <= n) {
@@ -420,16 +443,21 @@ int pair_scan(const int32_t* in, int64_t n, const int64_t* n_dev, int64_t* sums,
     return HALO_OK;
 }
 
-// Every halo slot into its owner's copy list, at the rank chain_pulse_kernel took.
-__global__ void owner_fill_kernel(const int4* __restrict__ items, const int32_t* __restrict__ owner,
+// Every halo slot into its owner's copy list, at the rank chain_pulse_kernel
+// took.  The blocks stride over the coordinate items (a block per item
+// would launch one short block per 256-384 slots).
+__global__ void owner_fill_kernel(const int4* __restrict__ items, int n_items,
+                                  const int32_t* __restrict__ owner,
                                   const int32_t* __restrict__ entry_pos,
                                   const int32_t* __restrict__ rank, int32_t* __restrict__ tmp) {
     grid_launch_dependents();  // the next kernel may start; it waits for this one
     grid_dependency_wait();
-    const int4 it = items[blockIdx.x];
-    for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
-        const int64_t j = (int64_t)it.y + i;
-        tmp[entry_pos[owner[j]] + rank[j]] = (int32_t)j;
+    for (int b = blockIdx.x; b < n_items; b += gridDim.x) {
+        const int4 it = items[b];
+        for (int i = threadIdx.x; i < it.z; i += blockDim.x) {
+            const int64_t j = (int64_t)it.y + i;
+            tmp[entry_pos[owner[j]] + rank[j]] = (int32_t)j;
+        }
     }
 }
 
@@ -1101,8 +1129,8 @@ int launch_flat_chains(halo_plan* pl, cudaStream_t st) {
     HALO_CUDA(cudaMemsetAsync(f.ncopies, 0, sizeof(int32_t) * pl->n_local_total, st));
     HALO_CUDA(cudaMemsetAsync(f.misc, 0, sizeof(int32_t) * 16, st));
     if (n_items > 0)
-        HALO_CUDA(launch_dependent_shm(xflat_items_kernel, dim3(1), dim3(1024), 0, st, domain_tables(pl), nd,
-                                       pl->P, kFlatChunk, pl->d_xflat_items, f.xbase));
+        HALO_CUDA(launch_dependent_shm(xflat_items_kernel, dim3((unsigned)((nd + 31) / 32)), dim3(1024), 0, st,
+                                       domain_tables(pl), nd, pl->P, kFlatChunk, pl->d_xflat_items, f.xbase));
     for (int p = 0; p < pl->P; p++) {
         const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
         HALO_CUDA(launch_dependent_shm(chain_pulse_kernel, dim3(gx, nd), dim3(kThreads), 0, st,
@@ -1166,10 +1194,10 @@ int prepare_flat(halo_plan* pl, cudaStream_t st) {
                                pl->d_fstart)) != HALO_OK)
             break;
         if (n_items > 0)
-            if ((rc = cuda_code(launch_dependent_shm(owner_fill_kernel, dim3((unsigned)n_items), dim3(kThreads),
-                                                     0, st, (const int4*)pl->d_xflat_items,
-                                                     (const int32_t*)owner, (const int32_t*)entry_pos,
-                                                     (const int32_t*)rank, tmp))) != HALO_OK)
+            if ((rc = cuda_code(launch_dependent_shm(
+                     owner_fill_kernel, dim3((unsigned)std::min<int64_t>(n_items, 8 * (int64_t)pl->num_sms)),
+                     dim3(kThreads), 0, st, (const int4*)pl->d_xflat_items, (int)n_items,
+                     (const int32_t*)owner, (const int32_t*)entry_pos, (const int32_t*)rank, tmp))) != HALO_OK)
                 break;
         // record classes (A: <= 3 copies, B: 4..11, C: more): positions in
         // each class from one paired scan of the owners' copy counts, then the
