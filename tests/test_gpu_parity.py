@@ -219,6 +219,7 @@ EDGE = [
     ((5.0, 4.0, 3.0), (5, 4, 3), 0.9, 20000, 6),     # rectangular box, odd grid
     ((6.0, 6.0, 6.0), (3, 3, 3), 0.05, 2000, 7),     # almost nothing sent
     ((8.0, 8.0, 8.0), (16, 16, 16), 1.4, 40000, 8),  # 4096 domains, 3 pulses per dim
+    ((10.0, 8.0, 8.0), (10, 8, 8), 0.9, 30000, 9),   # 640 domains: 2048-atom partition tiles
 ]
 
 
