@@ -253,27 +253,11 @@ inline int cuda_code(cudaError_t e) { return e == cudaSuccess ? HALO_OK : HALO_E
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while its predecessor in the stream drains, and holds back every access to
-// exchanged data until grid_dependency_wait() (kernels of the flat and
-// stepwise modes).
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
-                                    Args... args) {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-// The same with dynamic shared memory: the build's kernels, each of which
-// starts with grid_launch_dependents() and grid_dependency_wait(), so the
-// next kernel's launch overlaps the end of the one before.
+// data an earlier kernel wrote until grid_dependency_wait() (the exchange
+// kernels of the flat and stepwise modes, and every kernel of the build,
+// each of which starts with grid_launch_dependents() and
+// grid_dependency_wait(), so the next kernel's launch overlaps the end of the
+// one before).  smem: dynamic shared memory bytes.
 template <class... KArgs, class... Args>
 inline cudaError_t launch_dependent_shm(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                         cudaStream_t st, Args... args) {
@@ -288,6 +272,12 @@ inline cudaError_t launch_dependent_shm(void (*kernel)(KArgs...), dim3 grid, dim
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                                    Args... args) {
+    return launch_dependent_shm(kernel, grid, block, 0, st, args...);
 }
 
 template <class T>
