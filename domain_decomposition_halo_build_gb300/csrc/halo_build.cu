@@ -20,8 +20,8 @@
 //      corner test; its last block scans the unit counts into offsets, sizes
 //      and receiver offsets), write kernel (stable warp ballot compaction -> ascending index map +
 //      the new halo coordinates);
-//   3. finalize: dense bases, pulse descriptors, home slot -> dense slot map;
-//      one D2H copy of the metadata.
+//   3. finalize: dense bases, pulse descriptors; the metadata back to the
+//      host.
 // Index maps hold domain-relative local indices, so the dense relayout touches
 // none of them.
 #include <math.h>
@@ -802,12 +802,11 @@ __global__ void __launch_bounds__(1024) finalize_kernel(Meta m, int nd, int P) {
     }
 }
 
-// Block D: the dense slot of each of D's home-compact slots, D's pulse
-// descriptors (as sender) and, if host_meta is given (the host's mapped
-// staging), its share of the metadata words for the host.
-__global__ void home_dst_kernel(Meta m, int64_t* __restrict__ home_dst, SPArgs a,
-                                SPDesc* __restrict__ out, const int64_t* __restrict__ meta,
-                                int64_t meta_words, int64_t* __restrict__ host_meta) {
+// Block D: D's pulse descriptors (as sender) and, if host_meta is given (the
+// host's mapped staging), its share of the metadata words for the host.
+__global__ void sp_meta_kernel(Meta m, SPArgs a, SPDesc* __restrict__ out,
+                               const int64_t* __restrict__ meta, int64_t meta_words,
+                               int64_t* __restrict__ host_meta) {
     grid_launch_dependents();  // the next kernel may start; it waits for this one
     grid_dependency_wait();
     const int D = blockIdx.x;
@@ -815,8 +814,7 @@ __global__ void home_dst_kernel(Meta m, int64_t* __restrict__ home_dst, SPArgs a
         const int64_t w0 = meta_words * D / gridDim.x, w1 = meta_words * (D + 1) / gridDim.x;
         for (int64_t q = w0 + threadIdx.x; q < w1; q += blockDim.x) host_meta[q] = meta[q];
     }
-    const int64_t h0 = m.hstart[D], nh = m.n_home[D], b = m.base[D];
-    for (int64_t j = threadIdx.x; j < nh; j += blockDim.x) home_dst[h0 + j] = b + j;
+    const int64_t b = m.base[D];
     const int P = a.P;
     for (int p = threadIdx.x; p < P; p += blockDim.x) {
         const int s = D;
@@ -870,7 +868,6 @@ void free_build(halo_plan* pl) {
     dev_free(pl->d_bxyz);
     dev_free(pl->d_maps);
     dev_free(pl->d_home_gid);
-    dev_free(pl->d_home_dst);
     dev_free(pl->d_counts);
     dev_free(pl->d_scan_tmp);
     dev_free(pl->d_meta);
@@ -886,7 +883,7 @@ void free_build(halo_plan* pl) {
 
 DomainTables domain_tables(const halo_plan* pl) {
     const Meta m = meta_ptrs(pl->d_meta, pl->n_dom, pl->P);
-    return DomainTables{m.n_home, m.base, m.own_off};
+    return DomainTables{m.n_home, m.hstart, m.base, m.own_off};
 }
 
 int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n,
@@ -930,10 +927,8 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
     // --- buffers that depend on N
     if (n > pl->n_alloc_atoms) {
         dev_free(pl->d_home_gid);
-        dev_free(pl->d_home_dst);
         pl->n_alloc_atoms = 0;
         HALO_TRY(dev_alloc(&pl->d_home_gid, (size_t)n));
-        HALO_TRY(dev_alloc(&pl->d_home_dst, (size_t)n));
         pl->n_alloc_atoms = n;
     }
     const int64_t ncount = (int64_t)nd * nbt;
@@ -1111,7 +1106,7 @@ int build_plan(halo_plan* pl, const float* coords, const int32_t* dom, int64_t n
         // the metadata comes back through the mapped staging (written by the
         // home slot kernel), else with a copy
         int64_t* host_meta = static_cast<int64_t*>(pl->h_stage_dev);
-        HALO_CUDA(launch_dependent_shm(home_dst_kernel, dim3(nd), dim3(256), 0, st, m, pl->d_home_dst, spa,
+        HALO_CUDA(launch_dependent_shm(sp_meta_kernel, dim3(nd), dim3(256), 0, st, m, spa,
                                        pl->d_sp, reinterpret_cast<const int64_t*>(pl->d_meta),
                                        (int64_t)(mbytes / sizeof(int64_t)), host_meta));
         HALO_CUDA(cudaGetLastError());

@@ -475,13 +475,17 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(const SPDesc* __rest
     }
 }
 
-__global__ void load_home_kernel(const int64_t* __restrict__ home_dst,
-                                 const int32_t* __restrict__ home_gid, int64_t n,
+// Home atoms: block (x, D) takes domain D's home atoms j = x * blockDim +
+// thread, striding by gridDim.x * blockDim; atom home_gid[hstart[D] + j]
+// (the home partition) sits at dense slot base[D] + j.
+__global__ void load_home_kernel(DomainTables t, const int32_t* __restrict__ home_gid, int64_t n,
                                  const float* __restrict__ g, float* __restrict__ local,
                                  int64_t n_slots, int* err) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t dd = home_dst[i], a = home_gid[i];
+    const int D = blockIdx.y;
+    const int64_t h0 = t.hstart[D], nh = t.n_home[D], b = t.base[D];
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nh;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t dd = b + j, a = home_gid[h0 + j];
         if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
         local[3 * dd + 0] = g[3 * a + 0];
         local[3 * dd + 1] = g[3 * a + 1];
@@ -489,15 +493,14 @@ __global__ void load_home_kernel(const int64_t* __restrict__ home_dst,
     }
 }
 
-// global[atom] = local[its home slot]: every atom has exactly one home slot,
-// so the writes are disjoint
-__global__ void store_home_kernel(const int64_t* __restrict__ home_dst,
-                                  const int32_t* __restrict__ home_gid, int64_t n,
+__global__ void store_home_kernel(DomainTables t, const int32_t* __restrict__ home_gid, int64_t n,
                                   const float* __restrict__ local, float* __restrict__ g,
                                   int64_t n_slots, int* err) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t dd = home_dst[i], a = home_gid[i];
+    const int D = blockIdx.y;
+    const int64_t h0 = t.hstart[D], nh = t.n_home[D], b = t.base[D];
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nh;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t dd = b + j, a = home_gid[h0 + j];
         if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
         g[3 * a + 0] = local[3 * dd + 0];
         g[3 * a + 1] = local[3 * dd + 1];
@@ -505,51 +508,57 @@ __global__ void store_home_kernel(const int64_t* __restrict__ home_dst,
     }
 }
 
-// Sharded data plane: the shard of dense slot dd (shards are contiguous
-// ranges of dense slots).
-__device__ __forceinline__ float* shard_slot_of(const ShardTable& t, int n_shards, int64_t dd) {
+// Sharded data plane: the shard holding dense slot dd (shards are contiguous
+// ranges of dense slots, so a domain lies in one).
+__device__ __forceinline__ int shard_of_slot(const ShardTable& t, int n_shards, int64_t dd) {
     int k = 0;
     while (k + 1 < n_shards && dd >= t.first[k + 1]) k++;
-    return t.ptr[k] + 3 * (dd - t.first[k]);
+    return k;
 }
 
-__global__ void load_home_sharded_kernel(const int64_t* __restrict__ home_dst,
-                                         const int32_t* __restrict__ home_gid, int64_t n,
-                                         const float* __restrict__ g,
-                                         const __grid_constant__ ShardTable t, int n_shards,
+__global__ void load_home_sharded_kernel(DomainTables t, const int32_t* __restrict__ home_gid,
+                                         int64_t n, const float* __restrict__ g,
+                                         const __grid_constant__ ShardTable sh, int n_shards,
                                          int64_t n_slots, int* err) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t dd = home_dst[i], a = home_gid[i];
+    const int D = blockIdx.y;
+    const int64_t h0 = t.hstart[D], nh = t.n_home[D], b = t.base[D];
+    const int k = shard_of_slot(sh, n_shards, b);
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nh;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t dd = b + j, a = home_gid[h0 + j];
         if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
-        float* q = shard_slot_of(t, n_shards, dd);
+        float* q = sh.ptr[k] + 3 * (dd - sh.first[k]);
         q[0] = g[3 * a + 0];
         q[1] = g[3 * a + 1];
         q[2] = g[3 * a + 2];
     }
 }
 
-__global__ void store_home_sharded_kernel(const int64_t* __restrict__ home_dst,
-                                          const int32_t* __restrict__ home_gid, int64_t n,
-                                          const __grid_constant__ ShardTable t, int n_shards,
-                                          float* __restrict__ g, int64_t n_slots, int* err) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t dd = home_dst[i], a = home_gid[i];
+__global__ void store_home_sharded_kernel(DomainTables t, const int32_t* __restrict__ home_gid,
+                                          int64_t n, const __grid_constant__ ShardTable sh,
+                                          int n_shards, float* __restrict__ g, int64_t n_slots,
+                                          int* err) {
+    const int D = blockIdx.y;
+    const int64_t h0 = t.hstart[D], nh = t.n_home[D], b = t.base[D];
+    const int k = shard_of_slot(sh, n_shards, b);
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nh;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t dd = b + j, a = home_gid[h0 + j];
         if (!in_range(dd, n_slots, err) || !in_range(a, n, err)) continue;
-        const float* q = shard_slot_of(t, n_shards, dd);
+        const float* q = sh.ptr[k] + 3 * (dd - sh.first[k]);
         g[3 * a + 0] = q[0];
         g[3 * a + 1] = q[1];
         g[3 * a + 2] = q[2];
     }
 }
 
-__global__ void home_gid_kernel(const int64_t* __restrict__ home_dst,
-                                const int32_t* __restrict__ home_gid, int64_t n,
+__global__ void home_gid_kernel(DomainTables t, const int32_t* __restrict__ home_gid,
                                 int32_t* __restrict__ out) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x)
-        out[home_dst[i]] = home_gid[i];
+    const int D = blockIdx.y;
+    const int64_t h0 = t.hstart[D], nh = t.n_home[D], b = t.base[D];
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nh;
+         j += (int64_t)gridDim.x * blockDim.x)
+        out[b + j] = home_gid[h0 + j];
 }
 
 // Owner id of every halo slot of one pulse.
@@ -744,6 +753,11 @@ int prepare_common(halo_plan* pl, cudaStream_t st) {
     pl->entries_per_thread = E;
     pl->chunk = kThreads * E;
 
+    // the home load / store kernels: blocks per domain so that the largest
+    // domain's threads take about four atoms each
+    int64_t max_home = 1;
+    for (int D = 0; D < nd; D++) max_home = std::max<int64_t>(max_home, pl->n_home[D]);
+    pl->home_grid_x = (int)std::min<int64_t>((max_home + 1023) / 1024, 65535);
     // the host's copy of the per (s, p) descriptors (the build wrote the
     // device's, and the largest chunk counts)
     pl->sp.assign((size_t)nd * P, SPDesc{});
@@ -979,25 +993,20 @@ int launch_exchange_f(halo_plan* pl, float* f, cudaStream_t st) {
 }
 
 int launch_store_home(const halo_plan* pl, const float* local, float* g, cudaStream_t st) {
-    const int64_t n = pl->n_atoms;
-    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
-    store_home_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, local, g,
-                                              pl->n_local_total, pl->d_err);
+    store_home_kernel<<<dim3(pl->home_grid_x, pl->n_dom), 256, 0, st>>>(
+        domain_tables(pl), pl->d_home_gid, pl->n_atoms, local, g, pl->n_local_total, pl->d_err);
     return cuda_code(cudaGetLastError());
 }
 
 int launch_load_home(const halo_plan* pl, const float* g, float* local, cudaStream_t st) {
-    const int64_t n = pl->n_atoms;
-    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
-    load_home_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, g, local,
-                                             pl->n_local_total, pl->d_err);
+    load_home_kernel<<<dim3(pl->home_grid_x, pl->n_dom), 256, 0, st>>>(
+        domain_tables(pl), pl->d_home_gid, pl->n_atoms, g, local, pl->n_local_total, pl->d_err);
     return cuda_code(cudaGetLastError());
 }
 
 int launch_local_to_global(const halo_plan* pl, int32_t* out, cudaStream_t st) {
-    const int64_t n = pl->n_atoms;
-    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
-    home_gid_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, out);
+    home_gid_kernel<<<dim3(pl->home_grid_x, pl->n_dom), 256, 0, st>>>(domain_tables(pl), pl->d_home_gid,
+                                                                       out);
     for (int p = 0; p < pl->P; p++) {
         const unsigned gx = (unsigned)std::min(std::max(pl->max_chunks[p], 1), 1024);
         halo_gid_kernel<<<dim3(gx, pl->n_dom), kThreads, 0, st>>>(pl->d_sp, pl->d_maps, out,
@@ -1098,21 +1107,17 @@ int launch_exchange_f_sharded(halo_plan* pl, float* const* shard_f, cudaStream_t
 
 int launch_load_home_sharded(const halo_plan* pl, const float* g, float* const* shard_local,
                              cudaStream_t st) {
-    const int64_t n = pl->n_atoms;
-    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
-    load_home_sharded_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n, g,
-                                                     shard_table(pl, shard_local), pl->n_shards,
-                                                     pl->n_local_total, pl->d_err);
+    load_home_sharded_kernel<<<dim3(pl->home_grid_x, pl->n_dom), 256, 0, st>>>(
+        domain_tables(pl), pl->d_home_gid, pl->n_atoms, g, shard_table(pl, shard_local), pl->n_shards,
+        pl->n_local_total, pl->d_err);
     return cuda_code(cudaGetLastError());
 }
 
 int launch_store_home_sharded(const halo_plan* pl, const float* const* shard_local, float* g,
                               cudaStream_t st) {
-    const int64_t n = pl->n_atoms;
-    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)pl->num_sms * 8);
-    store_home_sharded_kernel<<<blocks, 256, 0, st>>>(pl->d_home_dst, pl->d_home_gid, n,
-                                                      shard_table(pl, shard_local), pl->n_shards, g,
-                                                      pl->n_local_total, pl->d_err);
+    store_home_sharded_kernel<<<dim3(pl->home_grid_x, pl->n_dom), 256, 0, st>>>(
+        domain_tables(pl), pl->d_home_gid, pl->n_atoms, shard_table(pl, shard_local), pl->n_shards, g,
+        pl->n_local_total, pl->d_err);
     return cuda_code(cudaGetLastError());
 }
 

@@ -96,7 +96,6 @@ struct halo_plan {
     int64_t cap_slots = 0;          // capacity of d_bxyz in slots (and of d_maps)
     int32_t* d_maps = nullptr;      // index maps, (pulse, sender) order
     int32_t* d_home_gid = nullptr;  // global id of each home-compact slot
-    int64_t* d_home_dst = nullptr;  // dense slot of each home-compact slot
     int64_t n_alloc_atoms = 0;
     int32_t* d_counts = nullptr;    // home partition tile counts (and scan output)
     int64_t counts_cap = 0;
@@ -152,6 +151,7 @@ struct halo_plan {
     int n_shards = 1;
     bool shard_lists = false;        // halo_shard was called: rebuilds keep the FUSED work lists
     bool flat_chains_ready = false;  // the FLAT forwarding chains of this build are launched
+    int home_grid_x = 1;             // blocks per domain of the home load / store kernels
     int shard_dom[halo::kMaxShards + 1] = {};
     int64_t shard_first[halo::kMaxShards + 1] = {};
 
@@ -187,10 +187,13 @@ namespace halo {
 
 // halo_build.cu
 // The plan's per-domain tables on the device (valid while the plan is):
-// n_home[D], base[D] (first dense slot), own_off[D * (P + 1) + q] (first
-// local index of each received slice; q = P: the domain's local count).
+// n_home[D], hstart[D] (first home-compact slot: D's home atoms in the build's
+// home partition, whose ids home_gid holds), base[D] (first dense slot),
+// own_off[D * (P + 1) + q] (first local index of each received slice; q = P:
+// the domain's local count).
 struct DomainTables {
     const int64_t* n_home;
+    const int64_t* hstart;
     const int64_t* base;
     const int64_t* own_off;
 };
