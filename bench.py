@@ -865,6 +865,9 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the context legs (latency, pruning, configurations, rebuild, graph, "
                          "overlap, stencil, end-to-end): for short profiling runs")
+    ap.add_argument("--rebuild-only", action="store_true",
+                    help="run only the 3M-atom rebuild leg and print its result: for profiling "
+                         "the build")
     args = ap.parse_args()
     if args.impl == "reference":
         if args.steps == 20000 and "--steps" not in sys.argv:
@@ -889,6 +892,12 @@ def main():
         __graft_entry__.build()
     stream = torch.cuda.current_stream(device)
     barrier = (lambda: dist.barrier()) if dist else None
+    if args.rebuild_only:
+        flush, _ = make_flush(device)
+        r = rebuild_case(device, stream, flush, min(args.steps, 300), args.warmup)
+        if rank == 0:
+            print(json.dumps({"rebuild_case": r}))
+        return
 
     w, xyz, dom, x, reps, f0, rep_bytes = setup_replicas(args.workload, device)
     plan, loc, _ = reps[0]
