@@ -139,6 +139,7 @@ int halo_setup_ex(const float box[3], const int32_t grid[3], float rc, const flo
         const double ms = atof(env);
         if (ms > 0.0 && isfinite(ms)) pl->wait_timeout_ns = (long long)(ms * 1e6);
     }
+    if (const char* env = getenv("HALO_STAGE_COPIES")) pl->stage_copies = env[0] != '\0' && strcmp(env, "0") != 0;
     try {
         rc_ = check_problem(box, grid, rc, pl);
         if (rc_ == HALO_OK && cudaGetDevice(&pl->dev) != cudaSuccess) rc_ = HALO_ECUDA;

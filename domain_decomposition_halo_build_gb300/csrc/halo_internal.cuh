@@ -144,6 +144,7 @@ struct halo_plan {
     void* h_stage = nullptr;
     size_t h_stage_cap = 0;
     void* h_stage_dev = nullptr;     // its device address (mapped), or null: copied with the copy engine
+    bool stage_copies = false;       // never map the staging (HALO_STAGE_COPIES at setup)
     int occ_x = 0, occ_f = 0;        // resident blocks per SM of the fused kernels (cached)
 
     // sharded data plane: shard k holds the domains [shard_dom[k], shard_dom[k + 1])
@@ -333,7 +334,7 @@ inline int host_stage(halo_plan* pl, size_t bytes, void** out) {
         }
         pl->h_stage_cap = want;
         // kernels write the words the host reads back straight into it
-        if (cudaHostGetDevicePointer(&pl->h_stage_dev, pl->h_stage, 0) != cudaSuccess) {
+        if (pl->stage_copies || cudaHostGetDevicePointer(&pl->h_stage_dev, pl->h_stage, 0) != cudaSuccess) {
             (void)cudaGetLastError();
             pl->h_stage_dev = nullptr;
         }

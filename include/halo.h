@@ -307,6 +307,12 @@ int halo_debug_set_build_capacity(halo_plan* plan, int64_t slots);
  * variable holds a positive number at halo_setup. */
 int halo_set_wait_timeout(halo_plan* plan, double seconds);
 
+/* The words a setup or rebuild reads back (sizes, counts, errors) are written
+ * by its last kernels straight into the plan's pinned host staging, mapped
+ * into the device's address space.  Where that staging cannot be mapped, or
+ * when the environment variable HALO_STAGE_COPIES is set (not "0") at
+ * halo_setup, they are copied back instead; the results are the same. */
+
 /* Test hook: in the next halo_exchange_x, the producer of (domain, pulse)
  * skips its completion signal, so its consumers' waits run out and the kernel
  * reports HALO_ETIMEOUT through halo_status().  (-1, -1) disarms. */

@@ -281,6 +281,29 @@ def test_unaligned_inputs(name):
         g.close()
 
 
+def test_copied_readbacks(monkeypatch):
+    """With HALO_STAGE_COPIES set at setup the build's readbacks are copied
+    instead of written into mapped host memory by the last kernels: the same
+    plan, tables and exchanges, through a rebuild, in FUSED and FLAT mode."""
+    monkeypatch.setenv("HALO_STAGE_COPIES", "1")
+    w = synth.WORKLOADS["water24k_2x4x8"]
+    xyz, dom = synth.system(w)
+    g = gpu_plan(w.box, w.grid, w.rc, xyz, dom)
+    try:
+        o = oracle.Oracle(w.box, w.grid, w.rc, xyz, dom)
+        compare_plans(g, o)
+        compare_exchanges(g, o, xyz)                  # FUSED (the default)
+        g.plan.set_mode("flat")
+        compare_exchanges(g, o, xyz)
+        x2, d2 = synth.displaced(xyz, w.box, w.grid, 3)
+        g.rebuild(x2, d2)
+        o2 = oracle.Oracle(w.box, w.grid, w.rc, x2, d2)
+        compare_plans(g, o2)
+        compare_exchanges(g, o2, x2)
+    finally:
+        g.close()
+
+
 def test_setup_errors():
     import torch
     from domain_decomposition_halo_build_gb300 import halo
